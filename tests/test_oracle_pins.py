@@ -1,0 +1,467 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test checks the oracle (``oracle/``) against a value fixed by the pages
+or by mathematics: a hand-worked example (``tests/golden``), brute-force
+enumeration, a closed form (the cumulative-sum formula for locations), a
+library routine (NumPy stable sort, SciPy softmax, torch's bf16 rounding,
+a dense one-hot einsum in float64), conservation invariants, adjoint
+identities and finite differences.  Each is chosen so that a plausible slip
+in the oracle (off-by-one location, k-major instead of token-order priority,
+a missing gate, a transposed operand, a wrong sign) fails at least one.
+
+Sources: DeepSpeed #8195 "MoE dispatch: fix silent Tutel + TP corruption,
+speed up native and Tutel paths" (changes 1 and 3, Testing); DeepSpeed #8213
+"Add an opt-in DeepEP transport for the AutoEP expert all-to-all"
+(description; review thread on weighted combine and router gradients).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from combine_moe_topk_gb300 import workloads as W
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |v| (8 significant bits)."""
+    a = np.abs(v)
+    e = np.floor(np.log2(np.maximum(a, 2.0**-126)))
+    return 2.0 ** (e - 7)
+
+
+# ------------------------------------------------------------------ golden --
+
+def test_hand_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "hand_worked_s4_e3_k2.json")))
+    logits = np.array(g["logits"], np.float32)
+    k = g["k"]
+    idx, gate = oracle.topk_gate(logits, k, renorm=1)
+    assert idx.tolist() == g["idx"]
+    np.testing.assert_allclose(gate, np.array(g["gate_renorm"]), rtol=1e-7)
+    idx0, gate0 = oracle.topk_gate(logits, k, renorm=0)
+    assert idx0.tolist() == g["idx"]
+    np.testing.assert_allclose(gate0, np.array(g["gate_full_softmax"]), rtol=1e-7)
+
+    cap = g["capacity"]
+    L = oracle.layout(idx, e=3, capacity=cap["c"], R=3)
+    assert L["loc"].tolist() == g["loc"]
+    assert L["raw_counts"].tolist() == g["raw_counts"]
+    assert L["drop"].tolist() == cap["drop"]
+    assert L["counts"].tolist() == cap["counts"]
+    assert L["offsets"].tolist() == cap["offsets"]
+    assert L["row"].tolist() == cap["row"]
+    assert L["token_in_rank"].tolist() == cap["token_in_rank_R3"]
+    assert L["rank_counts"].tolist() == cap["rank_counts_R3"]
+
+    dl = g["dropless"]
+    L = oracle.layout(idx, e=3, capacity=0, R=3)
+    assert L["loc"].tolist() == g["loc"]
+    assert L["drop"].sum() == 0
+    assert L["counts"].tolist() == dl["counts"]
+    assert L["offsets"].tolist() == dl["offsets"]
+    assert L["row"].tolist() == dl["row"]
+    assert L["token_in_rank"].tolist() == dl["token_in_rank_R3"]
+    assert L["rank_counts"].tolist() == dl["rank_counts_R3"]
+
+
+# -------------------------------------------------------------------- bf16 --
+
+def test_bf16_rounding_matches_torch():
+    rng = np.random.default_rng(1)
+    vals = [0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, 3.3895313892515355e38, 3.4e38, -3.4e38,
+            1e-40, -1e-40, 1.17549435e-38, 2.0**-133]
+    # exact ties: the low 16 bits are 0x8000, with the kept lsb even and odd
+    for hi in (0x3F80, 0x3F81, 0xBF80, 0xBF81, 0x7F7F, 0x0001, 0x0080):
+        vals.append(np.array([(hi << 16) | 0x8000], np.uint32).view(np.float32)[0])
+        vals.append(np.array([(hi << 16) | 0x7FFF], np.uint32).view(np.float32)[0])
+        vals.append(np.array([(hi << 16) | 0x8001], np.uint32).view(np.float32)[0])
+    vals += list(rng.standard_normal(3000).astype(np.float32))
+    vals += list((rng.standard_normal(2000) * 1e30).astype(np.float32))
+    vals += list(rng.integers(0, 2**32, 3000, dtype=np.uint64).astype(np.uint32).view(np.float32))
+    f = np.array(vals, np.float32)
+    ref = bf16_bits(torch.from_numpy(f).to(torch.bfloat16))
+    got = np.array([oracle.f32_to_bf16(float(v)) for v in f], np.uint16)
+    nan = np.isnan(f)
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+    assert np.all(np.isnan(bits_to_f64(got[nan])))
+    # widening is exact
+    for b in rng.integers(0, 2**16, 2000):
+        v = oracle.bf16_to_f32(int(b))
+        w = float(torch.tensor([int(b)], dtype=torch.int32).to(torch.int16).view(torch.bfloat16).float())
+        assert (math.isnan(v) and math.isnan(w)) or v == w
+
+
+# -------------------------------------------------------------------- gate --
+
+@pytest.mark.parametrize("s,e,k", [(64, 8, 2), (50, 128, 8), (33, 64, 6), (20, 5, 5), (40, 256, 16), (7, 1, 1)])
+def test_topk_matches_stable_sort(s, e, k):
+    rng = np.random.default_rng(s * 1000 + e)
+    logits = rng.standard_normal((s, e)).astype(np.float32)
+    # plant ties, including +0.0 against -0.0
+    logits[0, : min(e, 4)] = 0.5
+    if e >= 3:
+        logits[1, 0], logits[1, 2] = -0.0, 0.0
+        logits[1, 1] = -1.0
+    logits[2 % s] = np.round(logits[2 % s])
+    idx, gate = oracle.topk_gate(logits, k)
+    ref = np.argsort(-logits, axis=1, kind="stable")[:, :k]
+    np.testing.assert_array_equal(idx, ref)
+
+
+def test_topk_brute_force_tiny():
+    rng = np.random.default_rng(7)
+    for _ in range(200):
+        e = int(rng.integers(1, 9))
+        k = int(rng.integers(1, e + 1))
+        l = rng.integers(-2, 3, size=e).astype(np.float32)  # many ties
+        idx, _ = oracle.topk_gate(l[None], k)
+        # enumerate: best k under (value desc, index asc)
+        order = sorted(range(e), key=lambda j: (-float(l[j]), j))
+        assert idx[0].tolist() == order[:k]
+
+
+@pytest.mark.parametrize("renorm", [0, 1])
+def test_gates_match_scipy_softmax(renorm):
+    rng = np.random.default_rng(11 + renorm)
+    s, e, k = 300, 64, 6
+    logits = (rng.standard_normal((s, e)) * 3).astype(np.float32)
+    idx, gate = oracle.topk_gate(logits, k, renorm=renorm)
+    l64 = logits.astype(np.float64)
+    if renorm:
+        ref = scipy.special.softmax(np.take_along_axis(l64, idx, 1), axis=1)
+    else:
+        ref = np.take_along_axis(scipy.special.softmax(l64, axis=1), idx, 1)
+    # the oracle rounds once from double: at most one float ulp away
+    np.testing.assert_array_less(np.abs(gate - ref.astype(np.float32)), np.spacing(np.abs(ref.astype(np.float32))) * 1.01)
+    if renorm:
+        np.testing.assert_allclose(gate.astype(np.float64).sum(1), 1.0, atol=1e-6)
+    assert np.all(np.diff(gate, axis=1) <= 0), "gates follow the descending logits"
+
+
+def test_gates_special_cases():
+    # all logits equal: ties to the lower index; gates 1/k (renorm) or 1/e
+    l = np.full((3, 8), 0.25, np.float32)
+    idx, g = oracle.topk_gate(l, 3, renorm=1)
+    assert idx.tolist() == [[0, 1, 2]] * 3
+    np.testing.assert_allclose(g, 1 / 3, rtol=1e-7)
+    _, g0 = oracle.topk_gate(l, 3, renorm=0)
+    np.testing.assert_allclose(g0, 1 / 8, rtol=1e-7)
+    # k = e without renormalisation is the full softmax, sorted
+    rng = np.random.default_rng(3)
+    l = rng.standard_normal((5, 7)).astype(np.float32)
+    idx, g = oracle.topk_gate(l, 7, renorm=0)
+    ref = scipy.special.softmax(l.astype(np.float64), axis=1)
+    np.testing.assert_allclose(g, np.take_along_axis(ref, idx, 1), rtol=2e-7)
+    # k = 1 with renorm gives weight exactly one
+    _, g1 = oracle.topk_gate(l, 1, renorm=1)
+    assert np.all(g1 == 1.0)
+
+
+def test_gate_rejects_nonfinite():
+    l = np.zeros((2, 4), np.float32)
+    l[1, 2] = np.nan
+    with pytest.raises(oracle.OracleError):
+        oracle.topk_gate(l, 2)
+    l[1, 2] = np.inf
+    with pytest.raises(oracle.OracleError):
+        oracle.topk_gate(l, 2)
+
+
+# ------------------------------------------------------------------ layout --
+
+def brute_layout(idx, e, capacity):
+    s, k = idx.shape
+    loc = np.zeros_like(idx)
+    for t in range(s):
+        for j in range(k):
+            x = idx[t, j]
+            loc[t, j] = sum(1 for t2 in range(t) for j2 in range(k) if idx[t2, j2] == x)
+    return loc
+
+
+def cumsum_locations(idx, e):
+    """The pages' formula: location = cumulative sum (over tokens) of the
+    one-hot expert mask, minus one, read at each route."""
+    s, k = idx.shape
+    mask = np.zeros((s, e), np.int64)
+    np.put_along_axis(mask, idx.astype(np.int64), 1, axis=1)
+    cum = np.cumsum(mask, axis=0) - 1
+    return np.take_along_axis(cum, idx.astype(np.int64), 1).astype(np.int32)
+
+
+@pytest.mark.parametrize("s,e,k,cap", [(40, 8, 2, 0), (40, 8, 2, 6), (30, 16, 4, 5), (25, 6, 6, 3), (1, 4, 2, 1), (0, 4, 2, 0)])
+def test_layout_brute_force(s, e, k, cap):
+    idx = W.random_routes(s, e, k, seed=s + e).numpy() if s else np.zeros((0, k), np.int32)
+    L = oracle.layout(idx, e, cap)
+    np.testing.assert_array_equal(L["loc"], brute_layout(idx, e, cap))
+    if s:
+        np.testing.assert_array_equal(L["loc"], cumsum_locations(idx, e))
+
+
+def check_invariants(idx, e, cap, L):
+    s, k = idx.shape
+    loc, row, drop = L["loc"], L["row"], L["drop"].astype(bool)
+    raw, counts, off = L["raw_counts"], L["counts"], L["offsets"]
+    rows = e * cap if cap else s * k
+    assert raw.sum() == s * k
+    np.testing.assert_array_equal(raw, np.bincount(idx.ravel(), minlength=e))
+    assert counts.sum() == s * k - drop.sum()
+    kept = row[~drop]
+    assert len(np.unique(kept)) == len(kept), "every kept route owns a unique row"
+    assert np.all((kept >= 0) & (kept < rows))
+    assert np.all(row[drop] == -1)
+    if cap:
+        assert np.all(counts <= cap)
+        np.testing.assert_array_equal(drop, loc >= cap)
+        np.testing.assert_array_equal(counts, np.minimum(raw, cap))
+    else:
+        assert not drop.any()
+        assert off[0] == 0 and off[-1] == rows
+        np.testing.assert_array_equal(np.diff(off), counts)
+    # slots fill in token order within each expert
+    for x in range(e):
+        t_of = np.nonzero((idx == x).any(1))[0]
+        locs = loc[idx == x]  # row-major order = token order
+        np.testing.assert_array_equal(locs, np.arange(len(t_of)))
+        if not cap:
+            np.testing.assert_array_equal(row[idx == x], off[x] + np.arange(len(t_of)))
+
+
+@pytest.mark.parametrize("name", ["tiny-capacity", "mixtral-dropless", "fine-grained-skewed", "gshard-capacity"])
+def test_layout_invariants_on_workload_routing(name):
+    w = W.WORKLOADS[name]
+    w = w.replace(s=min(w.s, 4096))
+    cap = w.capacity if w.capacity == 0 else max(1, (w.capacity * w.s) // W.WORKLOADS[name].s)
+    logits = W.make_logits(w).numpy()
+    idx, _ = oracle.topk_gate(logits, w.k)
+    L = oracle.layout(idx, w.e, cap, R=w.R)
+    check_invariants(idx, w.e, cap, L)
+    np.testing.assert_array_equal(L["loc"], cumsum_locations(idx, w.e))
+
+
+@pytest.mark.parametrize("cap,R", [(0, 4), (3, 4), (0, 1), (2, 8), (0, 8)])
+def test_dedup_brute_force(cap, R):
+    s, e, k = 60, 16, 4
+    idx = W.random_routes(s, e, k, seed=5).numpy()
+    L = oracle.layout(idx, e, cap, R=R)
+    per = e // R
+    tir = np.zeros((s, R), np.uint8)
+    for t in range(s):
+        for j in range(k):
+            if not L["drop"][t, j]:
+                tir[t, idx[t, j] // per] = 1
+    np.testing.assert_array_equal(L["token_in_rank"], tir)
+    np.testing.assert_array_equal(L["rank_counts"], tir.sum(0))
+    u = int((~L["drop"].astype(bool)).any(1).sum())
+    assert u <= L["rank_counts"].sum() <= s * min(k, R)
+    for r in range(R):
+        assert L["rank_counts"][r] <= L["counts"][r * per:(r + 1) * per].sum()
+
+
+def test_layout_rejects_bad_routes():
+    with pytest.raises(oracle.OracleError):
+        oracle.layout(np.array([[0, 4]], np.int32), e=4)
+    with pytest.raises(oracle.OracleError):
+        oracle.layout(np.array([[1, 1]], np.int32), e=4)
+    with pytest.raises(oracle.OracleError):
+        oracle.layout(np.array([[-1, 1]], np.int32), e=4)
+
+
+# ------------------------------------------------------- dispatch / combine --
+
+def dense_masks(idx, L, e, cap, gate):
+    """One-hot [s, rows] route mask and its gate-weighted twin, float64.
+    With capacity this is the [s, e, c] mask of the dense einsum path,
+    flattened over (e, c)."""
+    s, k = idx.shape
+    rows = e * cap if cap else s * k
+    mask = np.zeros((s, rows))
+    gm = np.zeros((s, rows))
+    for t in range(s):
+        for j in range(k):
+            if not L["drop"][t, j]:
+                x, l = int(idx[t, j]), int(L["loc"][t, j])
+                r = x * cap + l if cap else int(L["offsets"][x]) + l
+                mask[t, r] = 1.0
+                gm[t, r] = float(gate[t, j])
+    return mask, gm
+
+
+def to64(a):
+    return bits_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+def draw(shape, dtype, rng):
+    v = rng.standard_normal(shape).astype(np.float32)
+    return bf16_bits(torch.from_numpy(v).to(torch.bfloat16)) if dtype == "bf16" else v
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("s,e,k,cap", [(48, 8, 2, 10), (48, 8, 2, 0), (40, 16, 4, 0), (37, 6, 3, 4)])
+def test_dispatch_combine_match_dense_einsum(dtype, s, e, k, cap):
+    rng = np.random.default_rng(s + 100 * e + cap)
+    m = 24
+    idx = W.random_routes(s, e, k, seed=s + e).numpy()
+    gate = (rng.random((s, k)) + 0.05).astype(np.float32)
+    L = oracle.layout(idx, e, cap)
+    rows = L["rows"]
+    x = draw((s, m), dtype, rng)
+    y = draw((rows, m), dtype, rng)
+    mask, gm = dense_masks(idx, L, e, cap, gate)
+    if cap:
+        # the [s, e, c] einsum of the dense path, written with torch
+        mask3 = torch.from_numpy(mask.reshape(s, e, cap))
+        Xd = torch.einsum("sec,sm->ecm", mask3, torch.from_numpy(to64(x))).reshape(rows, m).numpy()
+        gm3 = torch.from_numpy(gm.reshape(s, e, cap))
+        outd = torch.einsum("sec,ecm->sm", gm3, torch.from_numpy(to64(y)).reshape(e, cap, m)).numpy()
+    else:
+        Xd = mask.T @ to64(x)
+        outd = gm @ to64(y)
+
+    X = oracle.dispatch(L["row"], x, rows)
+    np.testing.assert_array_equal(to64(X), Xd)  # a copy: exact
+
+    out = oracle.combine(L["row"], gate, y)
+    scale = np.abs(gm) @ np.abs(to64(y))
+    err = np.abs(to64(out) - outd)
+    if dtype == "f32":
+        assert np.all(err <= 1e-6 * scale + 1e-30)
+    else:
+        assert np.all(err <= bf16_ulp(outd) + 1e-30)
+    # the weights are applied: the unweighted sum is different
+    unweighted = mask @ to64(y)
+    assert np.abs(unweighted - outd).max() > 1e-2
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cap", [0, 5])
+def test_backward_adjoints_and_finite_difference(dtype, cap):
+    rng = np.random.default_rng(21 + cap)
+    s, e, k, m = 40, 8, 3, 16
+    idx = W.random_routes(s, e, k, seed=9).numpy()
+    gate = (rng.random((s, k)) + 0.05).astype(np.float32)
+    L = oracle.layout(idx, e, cap)
+    rows = L["rows"]
+    x = draw((s, m), dtype, rng)
+    y = draw((rows, m), dtype, rng)
+    dout = draw((s, m), dtype, rng)
+    dXin = draw((rows, m), dtype, rng)
+    mask, gm = dense_masks(idx, L, e, cap, gate)
+    tol = 1e-6 if dtype == "f32" else 1e-2
+
+    # <dispatch(x), dX> = <x, dispatch_bwd(dX)>
+    X = to64(oracle.dispatch(L["row"], x, rows))
+    dx = to64(oracle.dispatch_bwd(L["row"], dXin))
+    lhs, rhs = np.sum(X * to64(dXin)), np.sum(to64(x) * dx)
+    assert abs(lhs - rhs) <= tol * np.sum(np.abs(mask.T @ np.abs(to64(x))) * np.abs(to64(dXin)))
+    # dispatch_bwd is the unit-weight combine: the transpose of the dispatch mask
+    ref = mask @ to64(dXin)
+    if dtype == "f32":
+        assert np.all(np.abs(dx - ref) <= 1e-6 * (mask @ np.abs(to64(dXin))) + 1e-30)
+    else:
+        assert np.all(np.abs(dx - ref) <= bf16_ulp(ref) + 1e-30)
+
+    # <combine(y), dout> = <y, dY>
+    dY, dgate = oracle.combine_bwd(L["row"], gate, dout, y)
+    out = gm @ to64(y)
+    lhs = np.sum(out * to64(dout))
+    rhs = np.sum(to64(y) * to64(dY))
+    assert abs(lhs - rhs) <= tol * np.sum(np.abs(gm) @ np.abs(to64(y)) * np.abs(to64(dout)))
+    # dY is the gate-scaled scatter of dout; untouched rows are zero
+    dYd = gm.T @ to64(dout)
+    err = np.abs(to64(dY) - dYd)
+    assert np.all(err <= (1e-6 * np.abs(dYd) if dtype == "f32" else bf16_ulp(dYd)) + 1e-30)
+    assert np.all(to64(dY)[mask.sum(0) == 0] == 0)
+
+    # dgate is the derivative of <combine(y, gate), dout> in each gate (central difference, float64)
+    y64, d64 = to64(y), to64(dout)
+
+    def loss(g):
+        _, gmm = dense_masks(idx, L, e, cap, g)
+        return np.sum((gmm @ y64) * d64)
+
+    h = 1e-3
+    for t, j in [(0, 0), (3, 1), (s - 1, k - 1), (17, 2)]:
+        gp, gn = gate.astype(np.float64).copy(), gate.astype(np.float64).copy()
+        gp[t, j] += h
+        gn[t, j] -= h
+        fd = (loss(gp) - loss(gn)) / (2 * h)
+        scale = np.sum(np.abs(d64[t])) * np.abs(y64).max() + 1e-30
+        if L["drop"][t, j]:
+            assert dgate[t, j] == 0.0 and abs(fd) < 1e-9
+        else:
+            assert abs(dgate[t, j] - fd) <= 1e-6 * scale
+
+
+def test_identity_expert_returns_input():
+    """Dropless, gates renormalised to one, y = dispatch(x): combine gives x back."""
+    rng = np.random.default_rng(4)
+    s, e, k, m = 64, 16, 4, 32
+    logits = rng.standard_normal((s, e)).astype(np.float32)
+    idx, gate = oracle.topk_gate(logits, k, renorm=1)
+    L = oracle.layout(idx, e, 0)
+    for dtype in ("f32", "bf16"):
+        x = draw((s, m), dtype, rng)
+        X = oracle.dispatch(L["row"], x, L["rows"])
+        out = oracle.combine(L["row"], gate, X)
+        if dtype == "f32":
+            np.testing.assert_allclose(out, x, rtol=1e-6, atol=1e-30)
+        else:
+            np.testing.assert_array_equal(out, x)
+
+
+def test_fully_dropped_token_gives_zero():
+    idx = np.array([[0, 1], [0, 1], [0, 1]], np.int32)
+    L = oracle.layout(idx, e=2, capacity=1)
+    assert L["drop"].tolist() == [[0, 0], [1, 1], [1, 1]]
+    y = np.arange(2 * 1 * 4, dtype=np.float32).reshape(2, 4) + 1
+    gate = np.full((3, 2), 0.5, np.float32)
+    out = oracle.combine(L["row"], gate, y)
+    assert np.all(out[1:] == 0) and np.all(out[0] == 0.5 * (y[0] + y[1]))
+    dY, dg = oracle.combine_bwd(L["row"], gate, np.ones((3, 4), np.float32), y)
+    assert np.all(dg[1:] == 0)
+
+
+def test_combine_accumulates_in_fp32_k_order():
+    """Three routes whose fp32 sum depends on the order: the definition
+    (fmaf in route order, starting from +0) fixes the bits."""
+    y = np.array([[1.0], [2.0**-24], [2.0**-24]], np.float32)
+    row = np.array([[0, 1, 2]], np.int32)
+    g = np.ones((1, 3), np.float32)
+    out = oracle.combine(row, g, y)
+    # 1 + 2^-24 rounds to 1 (tie to even), twice: order 0,1,2 gives exactly 1
+    assert out[0, 0] == np.float32(1.0)
+    out2 = oracle.combine(np.array([[1, 2, 0]], np.int32), g, y)
+    assert out2[0, 0] == np.float32(1.0 + 2.0**-23)
+
+
+def test_threads_do_not_change_results():
+    rng = np.random.default_rng(8)
+    s, e, k, m = 200, 16, 4, 64
+    logits = rng.standard_normal((s, e)).astype(np.float32)
+    y = rng.standard_normal((s * k, m)).astype(np.float32)
+    outs = []
+    for n in (1, 4):
+        oracle.set_threads(n)
+        idx, gate = oracle.topk_gate(logits, k)
+        L = oracle.layout(idx, e)
+        outs.append((idx, gate, oracle.combine(L["row"], gate, y)))
+    oracle.set_threads(1)
+    for a, b in zip(outs[0], outs[1]):
+        np.testing.assert_array_equal(a, b)
