@@ -1,0 +1,304 @@
+"""ctypes binding of ``libmoe_gb300.so`` (C ABI in ``include/moe_gb300.h``).
+
+Argument marshalling only: every step of the token path runs in the CUDA
+library.  PyTorch supplies device memory (outputs are allocated with
+``torch.empty`` when the caller does not pass them) and the current CUDA
+stream.  The functions keep the C names; tensors replace (pointer, size)
+pairs.  Every non-OK status raises ``MoEError``; if the shared library is
+missing the first call raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
+
+MOE_OK = 0
+STATUS = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_DTYPE",
+    4: "MOE_ERR_HANDLE_MISMATCH", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_OOM", 7: "MOE_ERR_TIMEOUT",
+    8: "MOE_ERR_NONFINITE", 9: "MOE_ERR_BAD_ROUTE",
+}
+MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
+MOE_DEV_NONFINITE, MOE_DEV_BAD_ROUTE, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4
+KERNELS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd"]
+KERNEL_ID = {n: i for i, n in enumerate(KERNELS)}
+
+# every entry point the header declares (checked by the CPU test-suite)
+EXPORTS = [
+    "moe_topk_gate", "moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_combine_bwd",
+    "moe_dispatch_bwd", "moe_handle_info", "moe_handle_status", "moe_handle_destroy", "moe_capacity",
+    "moe_status_string", "moe_last_error", "moe_launch_count", "moe_debug_hold_layout_tile",
+]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        super().__init__(f"{where}: {self.name}" + (f" ({detail})" if detail else ""))
+
+
+class LayoutInfo(ctypes.Structure):
+    _fields_ = [("s", ctypes.c_int32), ("e", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("capacity", ctypes.c_int32), ("R", ctypes.c_int32), ("rows", ctypes.c_int32),
+                ("device", ctypes.c_int32)] + [
+        (n, ctypes.c_void_p) for n in ("idx", "loc", "row", "drop", "raw_counts", "counts", "offsets",
+                                       "token_in_rank", "rank_counts", "status")]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                               "g.build()\"` (nvcc, sm_103a); there is no CPU fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
+        sig = {
+            "moe_topk_gate": [P, I, I, I, I, P, P, P, P],
+            "moe_dispatch_layout": [P, I, I, I, I, I, P, ctypes.POINTER(P)],
+            "moe_dispatch": [P, I, I, I, I, P, P, P],
+            "moe_combine": [P, I, I, I, I, P, P, P, P],
+            "moe_combine_bwd": [P, I, I, I, I, P, P, P, P, P, P],
+            "moe_dispatch_bwd": [P, I, I, I, I, P, P, P],
+            "moe_handle_info": [P, ctypes.POINTER(LayoutInfo)],
+            "moe_handle_status": [P, P, ctypes.POINTER(ctypes.c_int32)],
+            "moe_handle_destroy": [P],
+            "moe_debug_hold_layout_tile": [I, I],
+        }
+        for name, args in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = I
+        L.moe_capacity.argtypes = [ctypes.c_double, I, I, I]
+        L.moe_capacity.restype = I
+        L.moe_status_string.argtypes = [I]
+        L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_last_error.argtypes = []
+        L.moe_last_error.restype = ctypes.c_char_p
+        L.moe_launch_count.argtypes = [I]
+        L.moe_launch_count.restype = U
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, where: str):
+    if rc != MOE_OK:
+        detail = lib().moe_last_error().decode(errors="replace")
+        raise MoEError(rc, where, detail)
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the MoE library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return MOE_F32
+    if t.dtype == torch.bfloat16:
+        return MOE_BF16
+    if t.dtype == torch.float16:
+        return MOE_F16
+    return -1
+
+
+# ------------------------------------------------------------------ handle --
+
+class _DeviceArray:
+    """A read-only CUDA array view of handle memory (``__cuda_array_interface__``)."""
+
+    def __init__(self, owner, ptr: int, shape: tuple, typestr: str):
+        self._owner = owner  # keeps the handle (and its memory) alive
+        self.__cuda_array_interface__ = {
+            "shape": shape, "typestr": typestr, "data": (ptr or 0, True), "version": 3, "strides": None,
+            "stream": None,
+        }
+
+
+class Handle:
+    """Owns a ``moe_handle``; destroys it when garbage-collected."""
+
+    def __init__(self, raw: ctypes.c_void_p, device: torch.device):
+        self._raw = raw
+        self.device = device
+        info = LayoutInfo()
+        _check(lib().moe_handle_info(raw, ctypes.byref(info)), "moe_handle_info")
+        self.info = info
+        self.s, self.e, self.k = info.s, info.e, info.k
+        self.capacity, self.R, self.rows = info.capacity, info.R, info.rows
+
+    @property
+    def raw(self):
+        if self._raw is None:
+            raise MoEError(4, "handle", "destroyed")
+        return self._raw
+
+    def _view(self, name: str, shape: tuple, typestr: str) -> torch.Tensor:
+        ptr = getattr(self.info, name)
+        if not ptr or 0 in shape:
+            dt = {"<i4": torch.int32, "|u1": torch.uint8}[typestr]
+            return torch.empty(shape, dtype=dt, device=self.device)
+        return torch.as_tensor(_DeviceArray(self, ptr, shape, typestr), device=self.device)
+
+    # device arrays of the layout (views of handle memory, valid while the handle lives)
+    def idx(self): return self._view("idx", (self.s, self.k), "<i4")
+    def loc(self): return self._view("loc", (self.s, self.k), "<i4")
+    def row(self): return self._view("row", (self.s, self.k), "<i4")
+    def drop(self): return self._view("drop", (self.s, self.k), "|u1")
+    def raw_counts(self): return self._view("raw_counts", (self.e,), "<i4")
+    def counts(self): return self._view("counts", (self.e,), "<i4")
+    def offsets(self): return self._view("offsets", (self.e + 1,), "<i4")
+    def token_in_rank(self): return self._view("token_in_rank", (self.s, self.R), "|u1")
+    def rank_counts(self): return self._view("rank_counts", (self.R,), "<i4")
+
+    def status(self) -> int:
+        """Synchronise and read the device status word (MOE_DEV_* bits)."""
+        v = ctypes.c_int32(0)
+        _check(lib().moe_handle_status(self.raw, _stream(self.device), ctypes.byref(v)), "moe_handle_status")
+        return v.value
+
+    def destroy(self):
+        if self._raw is not None:
+            raw, self._raw = self._raw, None
+            with torch.cuda.device(self.device):
+                _check(lib().moe_handle_destroy(raw), "moe_handle_destroy")
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------- entry points --
+
+def moe_capacity(capacity_factor: float, s: int, k: int, e: int) -> int:
+    return lib().moe_capacity(float(capacity_factor), int(s), int(k), int(e))
+
+
+def moe_launch_count(kernel: str | int) -> int:
+    return lib().moe_launch_count(KERNEL_ID.get(kernel, kernel) if isinstance(kernel, str) else kernel)
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def moe_debug_hold_layout_tile(tile: int, timeout_ms: int = 200):
+    _check(lib().moe_debug_hold_layout_tile(int(tile), int(timeout_ms)), "moe_debug_hold_layout_tile")
+
+
+def moe_topk_gate(logits: torch.Tensor, k: int, renorm: int = 1, topk_idx: torch.Tensor | None = None,
+                  topk_gate: torch.Tensor | None = None, device_status: torch.Tensor | None = None):
+    """logits f32 [s,e] -> (idx i32 [s,k], gate f32 [s,k])."""
+    if logits.dim() != 2:
+        raise ValueError("logits must be [s, e]")
+    s, e = logits.shape
+    if logits.dtype != torch.float32:
+        raise MoEError(3, "moe_topk_gate", "logits must be float32")
+    dev = logits.device
+    if topk_idx is None:
+        topk_idx = torch.empty(s, k, dtype=torch.int32, device=dev)
+    if topk_gate is None:
+        topk_gate = torch.empty(s, k, dtype=torch.float32, device=dev)
+    rc = lib().moe_topk_gate(_ptr(logits), s, e, int(k), int(renorm), _ptr(topk_idx), _ptr(topk_gate),
+                             _ptr(device_status), _stream(dev))
+    _check(rc, "moe_topk_gate")
+    return topk_idx, topk_gate
+
+
+def moe_dispatch_layout(topk_idx: torch.Tensor, e: int, capacity: int = 0, num_virtual_ranks: int = 0) -> Handle:
+    """topk_idx i32 [s,k] -> Handle (counts, locations, rows, drops, dedup counts)."""
+    if topk_idx.dim() != 2 or topk_idx.dtype != torch.int32:
+        raise ValueError("topk_idx must be int32 [s, k]")
+    s, k = topk_idx.shape
+    raw = ctypes.c_void_p()
+    dev = topk_idx.device
+    rc = lib().moe_dispatch_layout(_ptr(topk_idx), s, int(e), k, int(capacity), int(num_virtual_ranks),
+                                   _stream(dev), ctypes.byref(raw))
+    _check(rc, "moe_dispatch_layout")
+    return Handle(raw, dev)
+
+
+def _rows2(t: torch.Tensor, name: str) -> tuple[int, int]:
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    return t.shape[0], t.shape[1]
+
+
+def moe_dispatch(h: Handle, x: torch.Tensor, X: torch.Tensor | None = None) -> torch.Tensor:
+    """x [s,m] -> X [rows,m]."""
+    s, m = _rows2(x, "x")
+    if X is None:
+        X = torch.empty(h.rows, m, dtype=x.dtype, device=x.device)
+    rows, mX = _rows2(X, "X")
+    if mX != m or X.dtype != x.dtype:
+        raise MoEError(1, "moe_dispatch", "x and X disagree in width or dtype")
+    _check(lib().moe_dispatch(h.raw, s, rows, m, _dtype(x), _ptr(x), _ptr(X), _stream(x.device)), "moe_dispatch")
+    return X
+
+
+def moe_combine(h: Handle, y: torch.Tensor, gate: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """y [rows,m], gate f32 [s,k] -> out [s,m]."""
+    rows, m = _rows2(y, "y")
+    if gate.dtype != torch.float32 or gate.shape != (h.s, h.k):
+        raise MoEError(1, "moe_combine", "gate must be float32 [s, k]")
+    if out is None:
+        out = torch.empty(h.s, m, dtype=y.dtype, device=y.device)
+    s, mo = _rows2(out, "out")
+    if mo != m or out.dtype != y.dtype:
+        raise MoEError(1, "moe_combine", "y and out disagree in width or dtype")
+    _check(lib().moe_combine(h.raw, s, rows, m, _dtype(y), _ptr(y), _ptr(gate), _ptr(out), _stream(y.device)),
+           "moe_combine")
+    return out
+
+
+def moe_combine_bwd(h: Handle, dout: torch.Tensor, gate: torch.Tensor, y: torch.Tensor,
+                    dY: torch.Tensor | None = None, dgate: torch.Tensor | None = None):
+    """dout [s,m], gate f32 [s,k], y [rows,m] -> (dY [rows,m], dgate f32 [s,k])."""
+    s, m = _rows2(dout, "dout")
+    rows, my = _rows2(y, "y")
+    if my != m or y.dtype != dout.dtype:
+        raise MoEError(1, "moe_combine_bwd", "dout and y disagree in width or dtype")
+    if gate.dtype != torch.float32 or gate.shape != (h.s, h.k):
+        raise MoEError(1, "moe_combine_bwd", "gate must be float32 [s, k]")
+    if dY is None:
+        dY = torch.empty(rows, m, dtype=dout.dtype, device=dout.device)
+    if dgate is None:
+        dgate = torch.empty(h.s, h.k, dtype=torch.float32, device=dout.device)
+    if dY.shape != (rows, m) or dY.dtype != dout.dtype or dgate.shape != (h.s, h.k):
+        raise MoEError(1, "moe_combine_bwd", "output shapes")
+    rc = lib().moe_combine_bwd(h.raw, s, rows, m, _dtype(dout), _ptr(dout), _ptr(gate), _ptr(y), _ptr(dY),
+                               _ptr(dgate), _stream(dout.device))
+    _check(rc, "moe_combine_bwd")
+    return dY, dgate
+
+
+def moe_dispatch_bwd(h: Handle, dX: torch.Tensor, dx: torch.Tensor | None = None) -> torch.Tensor:
+    """dX [rows,m] -> dx [s,m]."""
+    rows, m = _rows2(dX, "dX")
+    if dx is None:
+        dx = torch.empty(h.s, m, dtype=dX.dtype, device=dX.device)
+    s, mx = _rows2(dx, "dx")
+    if mx != m or dx.dtype != dX.dtype:
+        raise MoEError(1, "moe_dispatch_bwd", "dX and dx disagree in width or dtype")
+    _check(lib().moe_dispatch_bwd(h.raw, s, rows, m, _dtype(dX), _ptr(dX), _ptr(dx), _stream(dX.device)),
+           "moe_dispatch_bwd")
+    return dx

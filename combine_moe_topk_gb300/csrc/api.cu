@@ -1,0 +1,485 @@
+// api.cu -- the C ABI of libmoe_gb300 (declared in include/moe_gb300.h):
+// host-side validation, the layout handle and its stream-ordered memory,
+// launch counters, and the calls into the kernel launchers.
+//
+// Validation runs entirely on the host and before the first CUDA call of an
+// entry point, so a rejected call enqueues nothing (and works without a GPU).
+#include <cuda_runtime.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+#include <string>
+#include <unordered_set>
+
+#include "../../include/moe_gb300.h"
+#include "internal.h"
+
+namespace moe {
+int layout_blocks_per_sm();
+}
+
+struct moe_handle_s {
+  int device;
+  cudaStream_t stream;
+  int s, e, k, capacity, R, rows;
+  void* blob;
+  size_t blob_bytes;
+  moe::LayoutOut out;
+  moe::LayoutPlan plan;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches[MOE_KERNEL_COUNT];
+std::mutex g_mu;
+std::unordered_set<const moe_handle_s*> g_live;  // handles not yet destroyed
+int g_hold_tile = -1;                            // test hook, see moe_debug_hold_layout_tile
+long long g_hold_timeout_ns = 0;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 16;
+constexpr int kMaxR = 64;
+constexpr long long kDefaultTimeoutNs = 2000000000LL;  // bounded device waits: 2 s
+
+moe_status fail(moe_status st, const std::string& why) {
+  g_last_error = why;
+  return st;
+}
+
+moe_status cuda_fail(cudaError_t err, const char* where) {
+  g_last_error = std::string(where) + ": " + cudaGetErrorString(err);
+  return err == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-only checks of a payload row: dtype and 16-byte row length.
+moe_status check_payload(moe_dtype dt, int m, long long* row_bytes) {
+  if (dt == MOE_F16) return fail(MOE_ERR_DTYPE, "fp16 activations are not supported; use bf16 or fp32");
+  if (dt != MOE_F32 && dt != MOE_BF16) return fail(MOE_ERR_DTYPE, "unknown dtype");
+  if (m < 1) return fail(MOE_ERR_INVALID_ARG, "m must be >= 1");
+  const long long rb = (long long)m * (dt == MOE_F32 ? 4 : 2);
+  if (rb % 16 != 0) return fail(MOE_ERR_INVALID_ARG, "a payload row (m * element size) must be a multiple of 16 bytes");
+  *row_bytes = rb;
+  return MOE_OK;
+}
+
+moe_status check_ptr(const void* p, const char* name, bool may_be_null = false) {
+  if (!p) {
+    if (may_be_null) return MOE_OK;
+    return fail(MOE_ERR_INVALID_ARG, std::string(name) + " is NULL");
+  }
+  if (!aligned16(p)) return fail(MOE_ERR_INVALID_ARG, std::string(name) + " is not 16-byte aligned");
+  return MOE_OK;
+}
+
+// Device residency: a pointer the kernels can dereference on `device`.
+moe_status check_device_ptr(const void* p, const char* name, int device) {
+  if (!p) return MOE_OK;
+  cudaPointerAttributes a;
+  cudaError_t err = cudaPointerGetAttributes(&a, p);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MOE_ERR_INVALID_ARG, std::string(name) + ": not a CUDA pointer");
+  }
+  if (a.type == cudaMemoryTypeManaged) return MOE_OK;
+  if (a.type != cudaMemoryTypeDevice)
+    return fail(MOE_ERR_INVALID_ARG, std::string(name) + " is not device memory");
+  if (a.device != device)
+    return fail(MOE_ERR_INVALID_ARG, std::string(name) + " lives on another device");
+  return MOE_OK;
+}
+
+#define MOE_TRY(expr)               \
+  do {                              \
+    moe_status _st = (expr);        \
+    if (_st != MOE_OK) return _st;  \
+  } while (0)
+
+moe_status live_handle(moe_handle h) {
+  if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_live.count(h)) return fail(MOE_ERR_HANDLE_MISMATCH, "handle is unknown or destroyed");
+  return MOE_OK;
+}
+
+moe_status check_shape(moe_handle h, int s, int rows) {
+  if (s != h->s)
+    return fail(MOE_ERR_HANDLE_MISMATCH, "token count " + std::to_string(s) + " differs from the handle's " + std::to_string(h->s));
+  if (rows != h->rows)
+    return fail(MOE_ERR_HANDLE_MISMATCH, "row count " + std::to_string(rows) + " differs from the handle's " + std::to_string(h->rows));
+  return MOE_OK;
+}
+
+moe_status current_device(int* dev) {
+  cudaError_t err = cudaGetDevice(dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  if (*dev < 0 || *dev >= kMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "device ordinal too large");
+  return MOE_OK;
+}
+
+moe_status handle_device(moe_handle h) {
+  int dev = 0;
+  MOE_TRY(current_device(&dev));
+  if (dev != h->device) return fail(MOE_ERR_HANDLE_MISMATCH, "the current device is not the handle's device");
+  return MOE_OK;
+}
+
+// ---- per-device state --------------------------------------------------------
+
+std::once_flag g_dev_once[kMaxDevices];
+moe::DeviceInfo g_dev_info[kMaxDevices];
+cudaMemPool_t g_pool[kMaxDevices];
+cudaError_t g_dev_err[kMaxDevices];
+
+void init_device(int dev) {
+  moe::DeviceInfo& di = g_dev_info[dev];
+  cudaError_t err = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err == cudaSuccess)
+    err = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (err == cudaSuccess) di.layout_blocks_per_sm = moe::layout_blocks_per_sm();
+  if (err == cudaSuccess) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    err = cudaMemPoolCreate(&g_pool[dev], &props);
+    if (err == cudaSuccess) {
+      // keep freed blocks in the pool: handles are built and destroyed per step
+      uint64_t keep = UINT64_MAX;
+      err = cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+    }
+  }
+  g_dev_err[dev] = err;
+}
+
+moe_status device_state(int dev, const moe::DeviceInfo** di) {
+  std::call_once(g_dev_once[dev], init_device, dev);
+  if (g_dev_err[dev] != cudaSuccess) return cuda_fail(g_dev_err[dev], "device initialisation");
+  *di = &g_dev_info[dev];
+  return MOE_OK;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+namespace moe {
+const DeviceInfo& device_info(int device) { return g_dev_info[device]; }
+}  // namespace moe
+
+extern "C" {
+
+const char* moe_status_string(moe_status st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_DTYPE: return "unsupported dtype (fp32 and bf16 only)";
+    case MOE_ERR_HANDLE_MISMATCH: return "handle mismatch";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_OOM: return "out of device memory";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_NONFINITE: return "non-finite logit";
+    case MOE_ERR_BAD_ROUTE: return "expert id out of range or repeated in a token";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t moe_launch_count(int kernel_id) {
+  if (kernel_id < 0 || kernel_id >= MOE_KERNEL_COUNT) return 0;
+  return g_launches[kernel_id].load();
+}
+
+int moe_capacity(double capacity_factor, int s, int k, int e) {
+  if (!(capacity_factor > 0.0) || !std::isfinite(capacity_factor) || s < 0 || k < 1 || e < 1) return 0;
+  const double c = std::ceil(capacity_factor * (double)s * (double)k / (double)e);
+  if (c > 2147483647.0) return 0;
+  return (int)c;
+}
+
+moe_status moe_debug_hold_layout_tile(int tile, int timeout_ms) {
+  if (timeout_ms < 1 || timeout_ms > 10000) return fail(MOE_ERR_INVALID_ARG, "timeout_ms must be in [1, 10000]");
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_hold_tile = tile < 0 ? -1 : tile;
+  g_hold_timeout_ns = (long long)timeout_ms * 1000000LL;
+  return MOE_OK;
+}
+
+moe_status moe_topk_gate(const float* logits, int s, int e, int k, int renorm, int32_t* topk_idx,
+                         float* topk_gate, int32_t* device_status, void* stream) {
+  if (s < 0 || e < 1 || e > kMaxE || k < 1 || k > e || k > kMaxK)
+    return fail(MOE_ERR_INVALID_ARG, "need s >= 0, 1 <= e <= 256, 1 <= k <= min(e, 16)");
+  if ((long long)s * k > 2147483647LL) return fail(MOE_ERR_INVALID_ARG, "s*k must be < 2^31");
+  if (renorm != 0 && renorm != 1) return fail(MOE_ERR_INVALID_ARG, "renorm must be 0 or 1");
+  if (s == 0) return MOE_OK;
+  MOE_TRY(check_ptr(logits, "logits"));
+  MOE_TRY(check_ptr(topk_idx, "topk_idx"));
+  MOE_TRY(check_ptr(topk_gate, "topk_gate"));
+  if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u))
+    return fail(MOE_ERR_INVALID_ARG, "device_status is not 4-byte aligned");
+  int dev = 0;
+  MOE_TRY(current_device(&dev));
+  MOE_TRY(check_device_ptr(logits, "logits", dev));
+  MOE_TRY(check_device_ptr(topk_idx, "topk_idx", dev));
+  MOE_TRY(check_device_ptr(topk_gate, "topk_gate", dev));
+  MOE_TRY(check_device_ptr(device_status, "device_status", dev));
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(dev, &di));
+  cudaError_t err = moe::launch_topk_gate(logits, s, e, k, renorm, topk_idx, topk_gate, device_status,
+                                          *di, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "topk_gate launch");
+  g_launches[MOE_KERNEL_TOPK_GATE]++;
+  return MOE_OK;
+}
+
+moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity,
+                               int num_virtual_ranks, void* stream, moe_handle* out) {
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  const int R = num_virtual_ranks;
+  if (s < 0 || e < 1 || e > kMaxE || k < 1 || k > e || k > kMaxK)
+    return fail(MOE_ERR_INVALID_ARG, "need s >= 0, 1 <= e <= 256, 1 <= k <= min(e, 16)");
+  if (capacity < 0) return fail(MOE_ERR_INVALID_ARG, "capacity must be >= 0 (0 = dropless)");
+  if (R < 0 || R > kMaxR || (R > 0 && e % R != 0))
+    return fail(MOE_ERR_INVALID_ARG, "num_virtual_ranks must be in [0, 64] and divide e");
+  const long long routes = (long long)s * k;
+  const long long rows = capacity > 0 ? (long long)e * capacity : routes;
+  if (routes > 2147483647LL || rows > 2147483647LL)
+    return fail(MOE_ERR_INVALID_ARG, "s*k and the row count must be < 2^31");
+  if (s > 0) MOE_TRY(check_ptr(topk_idx, "topk_idx"));
+
+  int dev = 0;
+  MOE_TRY(current_device(&dev));
+  if (s > 0) MOE_TRY(check_device_ptr(topk_idx, "topk_idx", dev));
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(dev, &di));
+
+  moe_handle_s* h = new moe_handle_s();
+  h->device = dev;
+  h->stream = static_cast<cudaStream_t>(stream);
+  h->s = s;
+  h->e = e;
+  h->k = k;
+  h->capacity = capacity;
+  h->R = R;
+  h->rows = (int)rows;
+  h->plan = moe::plan_layout(s, *di);
+
+  // one blob: [zeroed: status, rank_counts, look-back words] then the rest
+  const size_t A = 256;
+  size_t off = 0;
+  const size_t o_status = off; off = align_up(off + 4, A);
+  const size_t o_rank = off;   off = align_up(off + 4 * (size_t)(R > 0 ? R : 1), A);
+  const size_t o_lb = off;     off = align_up(off + 8 * (size_t)h->plan.tiles * e, A);
+  const size_t zero_bytes = off;
+  const size_t o_idx = off;    off = align_up(off + 4 * (size_t)routes, A);
+  const size_t o_loc = off;    off = align_up(off + 4 * (size_t)routes, A);
+  const size_t o_row = off;    off = align_up(off + 4 * (size_t)routes, A);
+  const size_t o_drop = off;   off = align_up(off + (size_t)routes, A);
+  const size_t o_raw = off;    off = align_up(off + 4 * (size_t)e, A);
+  const size_t o_cnt = off;    off = align_up(off + 4 * (size_t)e, A);
+  const size_t o_off = off;    off = align_up(off + 4 * (size_t)(e + 1), A);
+  const size_t o_tir = off;    off = align_up(off + (size_t)s * (R > 0 ? R : 0) + 1, A);
+  h->blob_bytes = off;
+
+  cudaError_t err = cudaMallocFromPoolAsync(&h->blob, h->blob_bytes, g_pool[dev], h->stream);
+  if (err != cudaSuccess) {
+    delete h;
+    return cuda_fail(err, "handle allocation");
+  }
+  char* base = static_cast<char*>(h->blob);
+  h->out.status = reinterpret_cast<int32_t*>(base + o_status);
+  h->out.rank_counts = R > 0 ? reinterpret_cast<int32_t*>(base + o_rank) : nullptr;
+  h->out.lookback = reinterpret_cast<unsigned long long*>(base + o_lb);
+  h->out.idx = reinterpret_cast<int32_t*>(base + o_idx);
+  h->out.loc = reinterpret_cast<int32_t*>(base + o_loc);
+  h->out.row = reinterpret_cast<int32_t*>(base + o_row);
+  h->out.drop = reinterpret_cast<uint8_t*>(base + o_drop);
+  h->out.raw_counts = reinterpret_cast<int32_t*>(base + o_raw);
+  h->out.counts = reinterpret_cast<int32_t*>(base + o_cnt);
+  h->out.offsets = reinterpret_cast<int32_t*>(base + o_off);
+  h->out.token_in_rank = R > 0 ? reinterpret_cast<uint8_t*>(base + o_tir) : nullptr;
+
+  err = cudaMemsetAsync(base, 0, zero_bytes, h->stream);
+  int hold = -1;
+  long long timeout_ns = kDefaultTimeoutNs;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_hold_tile >= 0 && g_hold_tile < h->plan.tiles) {
+      hold = g_hold_tile;
+      timeout_ns = g_hold_timeout_ns;
+      g_hold_tile = -1;
+    }
+  }
+  if (err == cudaSuccess)
+    err = moe::launch_layout(topk_idx, s, e, k, capacity, R, h->plan, h->out, hold, timeout_ns,
+                             h->stream);
+  if (err != cudaSuccess) {
+    cudaFreeAsync(h->blob, h->stream);
+    delete h;
+    return cuda_fail(err, "layout launch");
+  }
+  g_launches[MOE_KERNEL_LAYOUT]++;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_live.insert(h);
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+moe_status moe_handle_info(moe_handle h, moe_layout_info* info) {
+  MOE_TRY(live_handle(h));
+  if (!info) return fail(MOE_ERR_INVALID_ARG, "info is NULL");
+  info->s = h->s;
+  info->e = h->e;
+  info->k = h->k;
+  info->capacity = h->capacity;
+  info->R = h->R;
+  info->rows = h->rows;
+  info->device = h->device;
+  info->idx = h->out.idx;
+  info->loc = h->out.loc;
+  info->row = h->out.row;
+  info->drop = h->out.drop;
+  info->raw_counts = h->out.raw_counts;
+  info->counts = h->out.counts;
+  info->offsets = h->out.offsets;
+  info->token_in_rank = h->out.token_in_rank;
+  info->rank_counts = h->out.rank_counts;
+  info->status = h->out.status;
+  return MOE_OK;
+}
+
+moe_status moe_handle_status(moe_handle h, void* stream, int32_t* device_status) {
+  MOE_TRY(live_handle(h));
+  if (!device_status) return fail(MOE_ERR_INVALID_ARG, "device_status is NULL");
+  MOE_TRY(handle_device(h));
+  cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (err == cudaSuccess) err = cudaStreamSynchronize(h->stream);
+  if (err == cudaSuccess)
+    err = cudaMemcpy(device_status, h->out.status, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (err != cudaSuccess) return cuda_fail(err, "reading the handle status");
+  return MOE_OK;
+}
+
+moe_status moe_handle_destroy(moe_handle h) {
+  if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_live.erase(h)) return fail(MOE_ERR_HANDLE_MISMATCH, "handle is unknown or destroyed");
+  }
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != h->device) cudaSetDevice(h->device);
+  cudaError_t err = cudaFreeAsync(h->blob, h->stream);
+  if (prev >= 0 && prev != h->device) cudaSetDevice(prev);
+  delete h;
+  if (err != cudaSuccess) return cuda_fail(err, "handle free");
+  return MOE_OK;
+}
+
+moe_status moe_dispatch(moe_handle h, int s, int rows, int m, moe_dtype dtype, const void* x,
+                        void* X, void* stream) {
+  MOE_TRY(live_handle(h));
+  MOE_TRY(check_shape(h, s, rows));
+  long long rb = 0;
+  MOE_TRY(check_payload(dtype, m, &rb));
+  if (s > 0) MOE_TRY(check_ptr(x, "x"));
+  if (rows > 0) MOE_TRY(check_ptr(X, "X"));
+  MOE_TRY(handle_device(h));
+  if (s > 0) MOE_TRY(check_device_ptr(x, "x", h->device));
+  if (rows > 0) MOE_TRY(check_device_ptr(X, "X", h->device));
+  if (rows == 0) return MOE_OK;
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(h->device, &di));
+  cudaError_t err = moe::launch_dispatch(h->out.row, h->out.counts, s, h->k, h->e, h->capacity, x, X,
+                                         rb, h->out.status, *di, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "dispatch launch");
+  g_launches[MOE_KERNEL_DISPATCH]++;
+  return MOE_OK;
+}
+
+moe_status moe_combine(moe_handle h, int s, int rows, int m, moe_dtype dtype, const void* y,
+                       const float* gate, void* out, void* stream) {
+  MOE_TRY(live_handle(h));
+  MOE_TRY(check_shape(h, s, rows));
+  long long rb = 0;
+  MOE_TRY(check_payload(dtype, m, &rb));
+  if (s == 0) return MOE_OK;
+  if (rows > 0) MOE_TRY(check_ptr(y, "y"));
+  MOE_TRY(check_ptr(gate, "gate"));
+  MOE_TRY(check_ptr(out, "out"));
+  MOE_TRY(handle_device(h));
+  if (rows > 0) MOE_TRY(check_device_ptr(y, "y", h->device));
+  MOE_TRY(check_device_ptr(gate, "gate", h->device));
+  MOE_TRY(check_device_ptr(out, "out", h->device));
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(h->device, &di));
+  cudaError_t err = moe::launch_combine(h->out.row, gate, s, h->k, m, dtype == MOE_F32 ? 0 : 1, y, out,
+                                        *di, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "combine launch");
+  g_launches[MOE_KERNEL_COMBINE]++;
+  return MOE_OK;
+}
+
+moe_status moe_combine_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype, const void* dout,
+                           const float* gate, const void* y, void* dY, float* dgate, void* stream) {
+  MOE_TRY(live_handle(h));
+  MOE_TRY(check_shape(h, s, rows));
+  long long rb = 0;
+  MOE_TRY(check_payload(dtype, m, &rb));
+  if (s == 0 && rows == 0) return MOE_OK;
+  if (s > 0) {
+    MOE_TRY(check_ptr(dout, "dout"));
+    MOE_TRY(check_ptr(gate, "gate"));
+    MOE_TRY(check_ptr(dgate, "dgate"));
+  }
+  if (rows > 0) {
+    MOE_TRY(check_ptr(y, "y"));
+    MOE_TRY(check_ptr(dY, "dY"));
+  }
+  MOE_TRY(handle_device(h));
+  const void* ptrs[5] = {dout, gate, y, dY, dgate};
+  const char* names[5] = {"dout", "gate", "y", "dY", "dgate"};
+  for (int i = 0; i < 5; ++i) MOE_TRY(check_device_ptr(ptrs[i], names[i], h->device));
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(h->device, &di));
+  cudaError_t err = moe::launch_combine_bwd(h->out.row, h->out.counts, gate, s, h->k, h->e, h->capacity,
+                                            m, dtype == MOE_F32 ? 0 : 1, dout, y, dY, dgate, *di,
+                                            static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "combine_bwd launch");
+  g_launches[MOE_KERNEL_COMBINE_BWD]++;
+  return MOE_OK;
+}
+
+moe_status moe_dispatch_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype, const void* dX,
+                            void* dx, void* stream) {
+  MOE_TRY(live_handle(h));
+  MOE_TRY(check_shape(h, s, rows));
+  long long rb = 0;
+  MOE_TRY(check_payload(dtype, m, &rb));
+  if (s == 0) return MOE_OK;
+  if (rows > 0) MOE_TRY(check_ptr(dX, "dX"));
+  MOE_TRY(check_ptr(dx, "dx"));
+  MOE_TRY(handle_device(h));
+  if (rows > 0) MOE_TRY(check_device_ptr(dX, "dX", h->device));
+  MOE_TRY(check_device_ptr(dx, "dx", h->device));
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(h->device, &di));
+  cudaError_t err = moe::launch_combine(h->out.row, nullptr, s, h->k, m, dtype == MOE_F32 ? 0 : 1, dX, dx,
+                                        *di, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "dispatch_bwd launch");
+  g_launches[MOE_KERNEL_DISPATCH_BWD]++;
+  return MOE_OK;
+}
+
+}  // extern "C"

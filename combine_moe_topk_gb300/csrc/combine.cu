@@ -1,0 +1,265 @@
+// combine.cu -- the weighted combine, its unit-weight twin (the backward of
+// dispatch) and the combine backward (a gate-scaled dispatch plus the gate
+// gradient).  One warp per token, 16-byte vector loads, fp32 accumulation.
+//
+// DeepSpeed #8195 "MoE dispatch: fix silent Tutel + TP corruption, speed up
+// native and Tutel paths", change 3: combine is a gather through the slots
+// and accumulates in fp32 (as the einsum it replaces did inside the matmul).
+// DeepSpeed #8213 "Add an opt-in DeepEP transport for the AutoEP expert
+// all-to-all": description -- the gradient of a combine is a dispatch and the
+// gradient of a dispatch is a combine; review thread -- the routing weights
+// must be applied to each expert row, and their gradient must reach the
+// router gate.
+//
+// Accumulation order is fixed: acc starts at +0.0f and takes one fmaf per
+// kept route in route order, so the result does not depend on the launch
+// shape.  The gate gradient sums dout*y per lane in element order, then a
+// butterfly across the warp: also launch-shape independent.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+// Route rows and gates of token t, broadcast from lanes 0..k-1.
+template <int KMAX, bool WEIGHTED>
+__device__ __forceinline__ void token_routes(const int32_t* __restrict__ row,
+                                             const float* __restrict__ gate, int t, int k,
+                                             int lane, int (&r)[KMAX], float (&g)[KMAX]) {
+  const int rl = lane < k ? __ldg(row + (size_t)t * k + lane) : -1;
+  const float gl = (WEIGHTED && lane < k) ? __ldg(gate + (size_t)t * k + lane) : 1.0f;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    r[j] = __shfl_sync(0xffffffffu, rl, j);
+    g[j] = __shfl_sync(0xffffffffu, gl, j);
+  }
+}
+
+template <typename T, int KMAX, int UNR, bool WEIGHTED>
+__global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __restrict__ row,
+                                                           const float* __restrict__ gate, int s,
+                                                           int k, int nvec,
+                                                           const uint4* __restrict__ y,
+                                                           uint4* __restrict__ out) {
+  constexpr int N = Vec<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < s; t += warps) {
+    int r[KMAX];
+    float g[KMAX];
+    token_routes<KMAX, WEIGHTED>(row, gate, t, k, lane, r, g);
+    uint4* o = out + (size_t)t * nvec;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * UNR) {
+      uint4 val[KMAX][UNR];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (r[j] >= 0) {
+          const uint4* src = y + (size_t)r[j] * nvec;
+#pragma unroll
+          for (int u = 0; u < UNR; ++u) {
+            const int v = v0 + 32 * u;
+            if (v < nvec) val[j][u] = ld_stream(src + v);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int v = v0 + 32 * u;
+        if (v >= nvec) break;
+        float acc[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          if (r[j] >= 0) {
+            float f[N];
+            Vec<T>::to_float(val[j][u], f);
+#pragma unroll
+            for (int i = 0; i < N; ++i) acc[i] = __fmaf_rn(g[j], f[i], acc[i]);
+          }
+        }
+        st_stream(o + v, Vec<T>::from_float(acc));
+      }
+    }
+  }
+}
+
+template <typename T, int KMAX, int UNR>
+__global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
+    const int32_t* __restrict__ row, const int32_t* __restrict__ counts,
+    const float* __restrict__ gate, int s, int k, int e, int capacity, int nvec,
+    const uint4* __restrict__ dout, const uint4* __restrict__ y, uint4* __restrict__ dY,
+    float* __restrict__ dgate) {
+  constexpr int N = Vec<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  for (int t = gw; t < s; t += warps) {
+    int r[KMAX];
+    float g[KMAX];
+    token_routes<KMAX, true>(row, gate, t, k, lane, r, g);
+    float dot[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) dot[j] = 0.0f;
+    const uint4* d = dout + (size_t)t * nvec;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * UNR) {
+      uint4 dv[UNR];
+      uint4 yv[KMAX][UNR];
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < nvec) dv[u] = ld_stream(d + v);
+      }
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (r[j] >= 0) {
+          const uint4* src = y + (size_t)r[j] * nvec;
+#pragma unroll
+          for (int u = 0; u < UNR; ++u) {
+            const int v = v0 + 32 * u;
+            if (v < nvec) yv[j][u] = ld_stream(src + v);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int v = v0 + 32 * u;
+        if (v >= nvec) break;
+        float df[N];
+        Vec<T>::to_float(dv[u], df);
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          if (r[j] >= 0) {
+            float yf[N], p[N];
+            Vec<T>::to_float(yv[j][u], yf);
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+              dot[j] = __fmaf_rn(df[i], yf[i], dot[j]);
+              p[i] = __fmul_rn(g[j], df[i]);
+            }
+            st_stream(dY + (size_t)r[j] * nvec + v, Vec<T>::from_float(p));
+          }
+        }
+      }
+    }
+    float mine = 0.0f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      float v = dot[j];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == j) mine = v;
+    }
+    if (lane < k) dgate[(size_t)t * k + lane] = mine;
+  }
+
+  // capacity mode: slots no kept route owns get zero gradient
+  if (capacity > 0) {
+    const long long E = (long long)e * capacity;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (long long rr = gw; rr < E; rr += warps) {
+      const int x = (int)(rr / capacity);
+      const int slot = (int)(rr - (long long)x * capacity);
+      if (slot < __ldg(counts + x)) continue;
+      uint4* dst = dY + (size_t)rr * nvec;
+      for (int v = lane; v < nvec; v += 32) st_stream(dst + v, z);
+    }
+  }
+}
+
+template <typename K>
+int occupancy(K kern) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, 0) != cudaSuccess) return 1;
+  return n;
+}
+
+int grid_for(long long warps_wanted, const DeviceInfo& di, int blocks_per_sm) {
+  long long blocks = (warps_wanted * 32 + kThreads - 1) / kThreads;
+  const long long cap = (long long)di.sms * (blocks_per_sm > 0 ? blocks_per_sm : 1);
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return (int)blocks;
+}
+
+template <typename T, int KMAX>
+cudaError_t combine_t(const int32_t* row, const float* gate, int s, int k, int m, const void* y,
+                      void* out, const DeviceInfo& di, cudaStream_t st) {
+  constexpr int UNR = KMAX <= 2 ? 4 : (KMAX <= 4 ? 2 : 1);
+  const int nvec = m / Vec<T>::N;
+  if (gate) {
+    auto kern = combine_kernel<T, KMAX, UNR, true>;
+    static const int bps = occupancy(kern);
+    kern<<<grid_for(s, di, bps), kThreads, 0, st>>>(row, gate, s, k, nvec,
+                                                    static_cast<const uint4*>(y),
+                                                    static_cast<uint4*>(out));
+  } else {
+    auto kern = combine_kernel<T, KMAX, UNR, false>;
+    static const int bps = occupancy(kern);
+    kern<<<grid_for(s, di, bps), kThreads, 0, st>>>(row, nullptr, s, k, nvec,
+                                                    static_cast<const uint4*>(y),
+                                                    static_cast<uint4*>(out));
+  }
+  return cudaGetLastError();
+}
+
+template <typename T, int KMAX>
+cudaError_t combine_bwd_t(const int32_t* row, const int32_t* counts, const float* gate, int s,
+                          int k, int e, int capacity, int m, const void* dout, const void* y,
+                          void* dY, float* dgate, const DeviceInfo& di, cudaStream_t st) {
+  constexpr int UNR = KMAX <= 2 ? 4 : (KMAX <= 4 ? 2 : 1);
+  const int nvec = m / Vec<T>::N;
+  auto kern = combine_bwd_kernel<T, KMAX, UNR>;
+  static const int bps = occupancy(kern);
+  long long warps = s;
+  if (capacity > 0 && (long long)e * capacity > warps) warps = (long long)e * capacity;
+  kern<<<grid_for(warps, di, bps), kThreads, 0, st>>>(
+      row, counts, gate, s, k, e, capacity, nvec, static_cast<const uint4*>(dout),
+      static_cast<const uint4*>(y), static_cast<uint4*>(dY), dgate);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t combine_k(const int32_t* row, const float* gate, int s, int k, int m, const void* y,
+                      void* out, const DeviceInfo& di, cudaStream_t st) {
+  if (k <= 2) return combine_t<T, 2>(row, gate, s, k, m, y, out, di, st);
+  if (k <= 4) return combine_t<T, 4>(row, gate, s, k, m, y, out, di, st);
+  if (k <= 8) return combine_t<T, 8>(row, gate, s, k, m, y, out, di, st);
+  return combine_t<T, 16>(row, gate, s, k, m, y, out, di, st);
+}
+
+template <typename T>
+cudaError_t combine_bwd_k(const int32_t* row, const int32_t* counts, const float* gate, int s,
+                          int k, int e, int capacity, int m, const void* dout, const void* y,
+                          void* dY, float* dgate, const DeviceInfo& di, cudaStream_t st) {
+  if (k <= 2)
+    return combine_bwd_t<T, 2>(row, counts, gate, s, k, e, capacity, m, dout, y, dY, dgate, di, st);
+  if (k <= 4)
+    return combine_bwd_t<T, 4>(row, counts, gate, s, k, e, capacity, m, dout, y, dY, dgate, di, st);
+  if (k <= 8)
+    return combine_bwd_t<T, 8>(row, counts, gate, s, k, e, capacity, m, dout, y, dY, dgate, di, st);
+  return combine_bwd_t<T, 16>(row, counts, gate, s, k, e, capacity, m, dout, y, dY, dgate, di, st);
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const int32_t* row, const float* gate, int s, int k, int m, int dtype,
+                           const void* y, void* out, const DeviceInfo& di, cudaStream_t st) {
+  if (dtype == 0) return combine_k<float>(row, gate, s, k, m, y, out, di, st);
+  return combine_k<__nv_bfloat16>(row, gate, s, k, m, y, out, di, st);
+}
+
+cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const float* gate, int s,
+                               int k, int e, int capacity, int m, int dtype, const void* dout,
+                               const void* y, void* dY, float* dgate, const DeviceInfo& di,
+                               cudaStream_t st) {
+  if (dtype == 0)
+    return combine_bwd_k<float>(row, counts, gate, s, k, e, capacity, m, dout, y, dY, dgate, di, st);
+  return combine_bwd_k<__nv_bfloat16>(row, counts, gate, s, k, e, capacity, m, dout, y, dY, dgate,
+                                      di, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,62 @@
+// internal.h -- host-side launchers of the kernels, called by api.cu after
+// argument validation.  Each returns the cudaError_t of its launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+struct DeviceInfo {
+  int sms = 0;                 // streaming multiprocessors
+  int layout_blocks_per_sm = 0;
+  int max_smem_optin = 0;      // bytes of dynamic shared memory a block may opt into
+};
+
+const DeviceInfo& device_info(int device);
+
+// --- gate ---------------------------------------------------------------
+cudaError_t launch_topk_gate(const float* logits, int s, int e, int k, int renorm, int32_t* idx,
+                             float* gate, int32_t* status, const DeviceInfo& di, cudaStream_t st);
+
+// --- layout -------------------------------------------------------------
+struct LayoutPlan {
+  int tiles = 1;            // CTAs (all co-resident: cooperative launch)
+  int subtiles_per_tile = 1;
+};
+LayoutPlan plan_layout(int s, const DeviceInfo& di);
+
+struct LayoutOut {
+  int32_t* idx;
+  int32_t* loc;
+  int32_t* row;
+  uint8_t* drop;
+  int32_t* raw_counts;
+  int32_t* counts;
+  int32_t* offsets;
+  uint8_t* token_in_rank;
+  int32_t* rank_counts;
+  unsigned long long* lookback;  // [tiles][e], zero before the launch
+  int32_t* status;
+};
+
+cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity, int R,
+                          const LayoutPlan& plan, const LayoutOut& out, int hold_tile,
+                          long long timeout_ns, cudaStream_t st);
+
+// --- dispatch (bulk-copy gather) -----------------------------------------
+cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, int s, int k, int e,
+                            int capacity, const void* x, void* X, long long row_bytes,
+                            int32_t* status, const DeviceInfo& di, cudaStream_t st);
+
+// --- combine family -----------------------------------------------------
+// dtype: 0 = f32, 1 = bf16.  gate == nullptr means unit weights.
+cudaError_t launch_combine(const int32_t* row, const float* gate, int s, int k, int m, int dtype,
+                           const void* y, void* out, const DeviceInfo& di, cudaStream_t st);
+
+cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const float* gate, int s,
+                               int k, int e, int capacity, int m, int dtype, const void* dout,
+                               const void* y, void* dY, float* dgate, const DeviceInfo& di,
+                               cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,216 @@
+/*
+ * moe_gb300.h -- C ABI of the GB300 (sm_103a) mixture-of-experts token path:
+ * top-k softmax gating, the dispatch layout, dispatch into the
+ * expert-grouped buffer, the weighted combine, and the two backward duals
+ * replayed on a cached layout handle.
+ *
+ * Sources (page title, then the part of the page that defines the call):
+ *  [P1] NVIDIA-NeMo/Automodel #3684 "perf(moe): reuse the DeepEP dispatch
+ *       layout on activation-checkpoint recompute": description and "How"
+ *       (a handle from an earlier dispatch skips the layout; replayed
+ *       counts must be identical to the forward's).
+ *  [P3] deepspeedai/DeepSpeed #8213 "Add an opt-in DeepEP transport for the
+ *       AutoEP expert all-to-all": description (a token is sent once per
+ *       destination rank; the gradient of a combine is a dispatch and the
+ *       gradient of a dispatch is a combine, both replayed on the forward's
+ *       handle) and its review thread (the routing weights must really be
+ *       applied in the combine; their gradient must reach the router; fp16
+ *       is rejected; row counts come from the host, without a device read).
+ *  [P4] deepspeedai/DeepSpeed #8195 "MoE dispatch: fix silent Tutel + TP
+ *       corruption, speed up native and Tutel paths": change 1 (per-route
+ *       index / location / gate, contiguous int32 routes, capacity resolved
+ *       once), change 2 (the capacity buffer is [e, c, m], never a flat
+ *       reinterpretation), change 3 (dispatch and combine are gathers
+ *       through capacity slots; combine accumulates in fp32).
+ *
+ * Common rules
+ *  - Every device pointer is caller-owned, device-resident on the current
+ *    device, C-contiguous, 16-byte aligned, and is never retained after the
+ *    call returns.  Tensor payload rows (m elements) must be a multiple of
+ *    16 bytes long.
+ *  - Every call only enqueues work on `stream` (a cudaStream_t passed as
+ *    void*; NULL = the legacy default stream) and returns at once.  No call
+ *    reads device memory on the host; row totals are host integers.
+ *  - Arguments are validated on the host before anything is enqueued.  On
+ *    any non-MOE_OK status nothing has been enqueued and no output changed.
+ *  - Conditions only the device can see (non-finite logits, invalid expert
+ *    ids, a bounded wait that ran out) set bits in a device status word; no
+ *    kernel traps.  Read it with moe_handle_status (a synchronising helper).
+ *  - Activations are fp32 or bf16; logits, gates and gate gradients fp32;
+ *    expert ids and rows int32.  fp16 is rejected with MOE_ERR_DTYPE [P3].
+ *  - Limits: 1 <= e <= 256, 1 <= k <= min(e, 16), 0 <= s, s*k < 2^31,
+ *    rows < 2^31, 1 <= m, 0 <= R <= 64 with R dividing e.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,     /* null / misaligned / out-of-range argument          */
+  MOE_ERR_UNSUPPORTED = 2,     /* valid request this build does not support          */
+  MOE_ERR_DTYPE = 3,           /* dtype other than fp32 / bf16 (fp16 included)       */
+  MOE_ERR_HANDLE_MISMATCH = 4, /* handle unknown, destroyed, or sizes disagree      */
+  MOE_ERR_CUDA = 5,            /* a CUDA runtime call failed                         */
+  MOE_ERR_OOM = 6,             /* device allocation failed                           */
+  MOE_ERR_TIMEOUT = 7,         /* device status: a bounded wait ran out              */
+  MOE_ERR_NONFINITE = 8,       /* device status: a logit was NaN or infinite         */
+  MOE_ERR_BAD_ROUTE = 9        /* device status: expert id out of range or repeated  */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_F16 = 2 /* always rejected */ } moe_dtype;
+
+/* Bits of a device status word (an int32 in device memory). */
+#define MOE_DEV_NONFINITE 0x1
+#define MOE_DEV_BAD_ROUTE 0x2
+#define MOE_DEV_TIMEOUT 0x4
+
+/* Kernel ids for moe_launch_count. */
+enum {
+  MOE_KERNEL_TOPK_GATE = 0,
+  MOE_KERNEL_LAYOUT = 1,
+  MOE_KERNEL_DISPATCH = 2,
+  MOE_KERNEL_COMBINE = 3,
+  MOE_KERNEL_COMBINE_BWD = 4,
+  MOE_KERNEL_DISPATCH_BWD = 5,
+  MOE_KERNEL_COUNT = 6
+};
+
+/* Opaque layout handle [P1 "How"; P3 description].  Owned by the library:
+ * built by moe_dispatch_layout, immutable afterwards, replayable any number
+ * of times by dispatch / combine and their backwards, alive until
+ * moe_handle_destroy (so a backward issued after later forwards still finds
+ * it).  Its device arrays come from a library memory pool, allocated and
+ * freed in stream order on the stream it was built on. */
+typedef struct moe_handle_s* moe_handle;
+
+/* Host view of a handle: sizes and read-only device pointers. */
+typedef struct {
+  int32_t s, e, k;
+  int32_t capacity;   /* slots per expert; 0 = dropless grouped layout          */
+  int32_t R;          /* virtual ranks of the dedup counts; 0 = none            */
+  int32_t rows;       /* rows of the dispatched buffer: e*capacity, or s*k      */
+  int32_t device;     /* CUDA device the handle lives on                        */
+  const int32_t* idx;           /* [s,k] copy of the expert ids                 */
+  const int32_t* loc;           /* [s,k] token-order slot within the expert     */
+  const int32_t* row;           /* [s,k] row in the dispatched buffer, -1 = dropped */
+  const uint8_t* drop;          /* [s,k] 1 = dropped (capacity) or invalid      */
+  const int32_t* raw_counts;    /* [e]   routes per expert before capacity      */
+  const int32_t* counts;        /* [e]   kept routes per expert                 */
+  const int32_t* offsets;       /* [e+1] first row of each expert; [e] = rows   */
+  const uint8_t* token_in_rank; /* [s,R] 1 = token sends to that virtual rank   */
+  const int32_t* rank_counts;   /* [R]   tokens sent to each virtual rank       */
+  const int32_t* status;        /* device status word of this handle            */
+} moe_layout_info;
+
+/* Top-k softmax gating [P4 change 1; P1 description: recompute must route
+ * identically].  logits f32 [s,e] -> topk_idx i32 [s,k], topk_gate f32 [s,k].
+ * Selection is on the logits: larger first, the lower expert index on ties
+ * (+0.0 and -0.0 tie).  renorm = 0: gate = softmax over all e experts, read
+ * at the selected ones; renorm = 1: softmax over the k selected logits.
+ * fp32 arithmetic with expf.  Deterministic.  device_status (nullable): an
+ * int32 in device memory that gets MOE_DEV_NONFINITE OR-ed in when a logit
+ * of a token is NaN or infinite (that token's outputs are then unspecified).
+ */
+moe_status moe_topk_gate(const float* logits, int s, int e, int k, int renorm,
+                         int32_t* topk_idx, float* topk_gate, int32_t* device_status,
+                         void* stream);
+
+/* Dispatch layout [P4 changes 1 and 3: location = cumulative count - 1 in
+ * token order; P3 description: dedup once per destination rank].
+ * topk_idx i32 [s,k] -> a new handle in *out (see moe_layout_info):
+ *   loc[t,j]  = number of earlier tokens t' < t routed to expert idx[t,j];
+ *   capacity > 0: dropped iff loc >= capacity; row = x*capacity + loc;
+ *                 counts = min(raw_counts, capacity); offsets[x] = x*capacity;
+ *   capacity = 0: nothing dropped; offsets = exclusive prefix of counts;
+ *                 row = offsets[x] + loc;
+ *   R > 0: token_in_rank[t,r] = 1 iff a kept route of t goes to one of the
+ *          e/R experts of virtual rank r; rank_counts[r] = sum over t.
+ *          Computed only; nothing is sent anywhere.
+ * One kernel: a shared-memory histogram per tile and a decoupled look-back
+ * over tiles; integer-exact and bitwise reproducible on every rebuild.
+ * Expert ids out of [0, e) or repeated within a token are reported through
+ * the handle's status word (MOE_DEV_BAD_ROUTE) and those routes get
+ * row = -1.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_OOM, MOE_ERR_CUDA. */
+moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity,
+                               int num_virtual_ranks, void* stream, moe_handle* out);
+
+/* Dispatch [P4 change 3; P4 change 2 for the [e, c, m] layout].
+ * x [s,m] -> X [rows,m]: X[row[t,j]] = x[t] for every kept route; in
+ * capacity mode the unused slots [counts[x], capacity) of every expert are
+ * written with zeros, so X is fully defined.  Bit-exact copy.
+ * s and rows must equal the handle's (else MOE_ERR_HANDLE_MISMATCH). */
+moe_status moe_dispatch(moe_handle h, int s, int rows, int m, moe_dtype dtype,
+                        const void* x, void* X, void* stream);
+
+/* Combine [P3 review thread: the weights are applied; P4 change 3: fp32
+ * accumulation].  y [rows,m], gate f32 [s,k] -> out [s,m]:
+ *   acc = +0.0f; for j = 0..k-1 with row[t,j] >= 0:
+ *       acc = fmaf(gate[t,j], (float)y[row[t,j]], acc);
+ *   out[t] = acc rounded to nearest-even in the output type.
+ * A token whose routes were all dropped gets zeros.  gate may not be NULL. */
+moe_status moe_combine(moe_handle h, int s, int rows, int m, moe_dtype dtype,
+                       const void* y, const float* gate, void* out, void* stream);
+
+/* Combine backward = a dispatch [P3 description].  dout [s,m], gate f32
+ * [s,k], y [rows,m] -> dY [rows,m], dgate f32 [s,k]:
+ *   dY[row[t,j]] = (gate[t,j] * (float)dout[t]) rounded to the type (one fp32
+ *   multiply, then nearest-even); rows no kept route owns are zero;
+ *   dgate[t,j] = sum_m dout[t,m]*y[row[t,j],m] accumulated in fp32; 0 if the
+ *   route was dropped.  This is the router's gradient path [P3 review]. */
+moe_status moe_combine_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype,
+                           const void* dout, const float* gate, const void* y,
+                           void* dY, float* dgate, void* stream);
+
+/* Dispatch backward = a combine with unit weights [P3 description].
+ * dX [rows,m] -> dx [s,m]: dx[t] = sum over kept routes, in route order,
+ * accumulated in fp32 as in moe_combine. */
+moe_status moe_dispatch_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype,
+                            const void* dX, void* dx, void* stream);
+
+/* Fill *info with the handle's sizes and device pointers (valid until the
+ * handle is destroyed). */
+moe_status moe_handle_info(moe_handle h, moe_layout_info* info);
+
+/* Synchronise `stream`, then copy the handle's device status word (bits
+ * MOE_DEV_*) to *device_status.  A test / debugging helper: it blocks. */
+moe_status moe_handle_status(moe_handle h, void* stream, int32_t* device_status);
+
+/* Release the handle: its device arrays are freed in stream order on the
+ * stream it was built on, so work already enqueued there that uses it
+ * completes first.  Work on other streams must be complete (or ordered
+ * before that stream) by the caller.  Using the handle afterwards returns
+ * MOE_ERR_HANDLE_MISMATCH. */
+moe_status moe_handle_destroy(moe_handle h);
+
+/* ceil(capacity_factor * s * k / e) computed in double on the host
+ * [P4 change 1: capacity resolved once]; 0 if an argument is out of range. */
+int moe_capacity(double capacity_factor, int s, int k, int e);
+
+/* Static text for a status code. */
+const char* moe_status_string(moe_status st);
+
+/* Text of the last validation or CUDA error seen by this host thread. */
+const char* moe_last_error(void);
+
+/* Number of launches of one kernel (MOE_KERNEL_*) since the library was
+ * loaded, process-wide.  A replay on a cached handle leaves the layout
+ * count unchanged [P1 "How"]. */
+uint64_t moe_launch_count(int kernel_id);
+
+/* Test hook for the bounded waits: the next layout build whose tile count
+ * exceeds `tile` leaves that tile's look-back words unpublished, so every
+ * later tile's wait runs out (after timeout_ms) and sets MOE_DEV_TIMEOUT in
+ * the handle's status word.  The hook disarms itself after one build;
+ * tile = -1 disarms it.  Never used on the product path. */
+moe_status moe_debug_hold_layout_tile(int tile, int timeout_ms);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

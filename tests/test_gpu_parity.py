@@ -1,0 +1,274 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Reduced sizes run every output of every op element by element, at sizes that
+still span several layout tiles (256 tokens each) and end in a ragged tail.
+The full workload shapes compare every integer output and the gates in
+full, and sampled payload rows / tokens for the floating outputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import tolerance as T
+from combine_moe_topk_gb300 import binding as B
+from combine_moe_topk_gb300 import workloads as W
+from gpu_util import bits, check_layout, full_parity, to_dev
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+REDUCED = {
+    "tiny-capacity": W.WORKLOADS["tiny-capacity"],
+    "mixtral-dropless": W.WORKLOADS["mixtral-dropless"].replace(s=1000, m=512),
+    "fine-grained-skewed": W.WORKLOADS["fine-grained-skewed"].replace(s=3000, m=256),
+    "diffusiongemma-replay": W.WORKLOADS["diffusiongemma-replay"].replace(m=256),
+    "gshard-capacity": W.WORKLOADS["gshard-capacity"].replace(s=5000, m=128, capacity=469),
+}
+
+
+@pytest.mark.parametrize("name", list(REDUCED))
+def test_reduced_full_parity(name):
+    full_parity(REDUCED[name], DEV)
+
+
+def test_tiny_capacity_full_softmax_gates():
+    full_parity(W.WORKLOADS["tiny-capacity"], DEV, renorm=0)
+
+
+@pytest.mark.parametrize("case", [
+    dict(s=1, m=8, e=1, k=1, dtype="bf16", capacity=0, R=0),
+    dict(s=1, m=4, e=4, k=4, dtype="f32", capacity=1, R=2),
+    dict(s=37, m=8, e=256, k=16, dtype="bf16", capacity=0, R=64),
+    dict(s=300, m=12288, e=16, k=3, dtype="bf16", capacity=0, R=4),   # rows split into 2 bulk pieces
+    dict(s=513, m=36, e=5, k=2, dtype="f32", capacity=7, R=5),        # heavy drops, odd widths
+    dict(s=2049, m=64, e=64, k=6, dtype="bf16", capacity=200, R=8),
+])
+def test_edge_shapes(case):
+    w = W.Workload("edge", seed=7, **case)
+    full_parity(w, DEV)
+
+
+def test_all_logits_equal_ties_and_drops():
+    """Every token ties on every expert: all pick experts 0..k-1 (lower index
+    wins), and capacity keeps only the first c tokens of each."""
+    s, e, k, m, cap = 600, 8, 2, 64, 100
+    logits = torch.zeros(s, e)
+    idx, gate = B.moe_topk_gate(logits.to(DEV), k, 1)
+    assert (bits(idx) == np.array([[0, 1]] * s)).all()
+    assert (bits(gate) == 0.5).all()
+    h = B.moe_dispatch_layout(idx, e, cap)
+    L = oracle.layout(bits(idx), e, cap)
+    check_layout(h, L, bits(idx))
+    x = torch.randn(s, m, dtype=torch.float32)
+    X = B.moe_dispatch(h, x.to(DEV))
+    OX = oracle.dispatch(L["row"], x.numpy(), L["rows"])
+    np.testing.assert_array_equal(bits(X), OX)
+    og = np.full((s, k), 0.5, np.float32)
+    out = B.moe_combine(h, to_dev(OX, DEV), to_dev(og, DEV))
+    ref = oracle.combine(L["row"], og, OX)
+    np.testing.assert_array_equal(bits(out)[cap:], 0)  # tokens past the capacity were fully dropped
+    T.assert_close(bits(out), ref, T.combine_scale(L["row"], og, OX), "combine")
+
+
+def test_empty_batch():
+    for cap in (0, 3):
+        idx = torch.empty(0, 2, dtype=torch.int32, device=DEV)
+        h = B.moe_dispatch_layout(idx, 4, cap)
+        assert h.rows == (4 * cap if cap else 0)
+        assert bits(h.counts()).tolist() == [0, 0, 0, 0]
+        assert bits(h.offsets()).tolist() == ([0, 3, 6, 9, 12] if cap else [0] * 5)
+        x = torch.empty(0, 8, dtype=torch.bfloat16, device=DEV)
+        X = B.moe_dispatch(h, x)
+        if cap:
+            assert X.shape == (12, 8) and (X == 0).all()
+        out = B.moe_combine(h, X, torch.empty(0, 2, device=DEV))
+        assert out.shape == (0, 8)
+        assert h.status() == 0
+
+
+# ------------------------------------------------------------- full sizes --
+
+def _sample_rows(n, count, gen):
+    return torch.randperm(n, generator=gen)[:count].sort().values.numpy()
+
+
+@pytest.mark.parametrize("name", ["tiny-capacity", "mixtral-dropless", "fine-grained-skewed",
+                                  "diffusiongemma-replay", "gshard-capacity"])
+def test_full_size_workloads(name):
+    """The exact workload shapes, in the launch configuration the benchmark
+    times: integer outputs and gates in full, payload outputs on samples."""
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w, device=DEV)
+    logits = inp["logits"]
+    idx, gate = B.moe_topk_gate(logits, w.k, w.renorm)
+    oi, og = oracle.topk_gate(bits(logits), w.k, w.renorm)
+    np.testing.assert_array_equal(bits(idx), oi)
+    T.assert_gates_close(bits(gate), og)
+    # from here on both sides take the oracle's routing and gates
+    h = B.moe_dispatch_layout(to_dev(oi, DEV), w.e, w.capacity, w.R)
+    L = oracle.layout(oi, w.e, w.capacity, w.R)
+    check_layout(h, L, oi)
+    gd = to_dev(og, DEV)
+
+    X = B.moe_dispatch(h, inp["x"])
+    out = B.moe_combine(h, inp["y"], gd)
+    dY, dgate = B.moe_combine_bwd(h, inp["dout"], gd, inp["y"])
+    dx = B.moe_dispatch_bwd(h, inp["y"])  # the unit-weight combine of y
+    torch.cuda.synchronize()
+    assert h.status() == 0
+
+    gen = torch.Generator().manual_seed(123)
+    row = L["row"]
+    # dispatch: sampled destination rows, including zero-tail rows in capacity mode
+    rs = _sample_rows(L["rows"], 512, gen)
+    xb = bits(inp["x"])
+    owner = np.full(L["rows"], -1, np.int64)
+    kept = row >= 0
+    owner[row[kept]] = np.nonzero(kept)[0]
+    Xs = bits(X[torch.from_numpy(rs).to(DEV)])
+    for i, r in enumerate(rs):
+        if owner[r] >= 0:
+            np.testing.assert_array_equal(Xs[i], xb[owner[r]])
+        else:
+            assert not Xs[i].any(), "unowned rows are zero"
+
+    # combine / combine_bwd / dispatch_bwd on sampled tokens through the oracle
+    ts = _sample_rows(w.s, 256, gen)
+    rsub = row[ts]
+    uniq = np.unique(rsub[rsub >= 0])
+    remap = np.full(L["rows"], -1, np.int64)
+    remap[uniq] = np.arange(len(uniq))
+    rloc = np.where(rsub >= 0, remap[np.maximum(rsub, 0)], -1).astype(np.int32)
+    ysub = bits(inp["y"][torch.from_numpy(uniq).to(DEV)])
+    dsub = bits(inp["dout"][torch.from_numpy(ts).to(DEV)])
+    gsub = np.ascontiguousarray(og[ts])
+    tsd = torch.from_numpy(ts).to(DEV)
+    T.assert_close(bits(out[tsd]), oracle.combine(rloc, gsub, ysub), T.combine_scale(rloc, gsub, ysub), "combine")
+    OdY, Odg = oracle.combine_bwd(rloc, gsub, dsub, ysub)
+    T.assert_close(bits(dgate)[ts], Odg, T.dot_scale(rloc, dsub, ysub), "dgate")
+    dYs = bits(dY[torch.from_numpy(uniq).to(DEV)])
+    T.assert_close(dYs, OdY, np.abs(T.as_f64(OdY)), "dY")
+    T.assert_close(bits(dx[tsd]), oracle.dispatch_bwd(rloc, ysub),
+                   T.combine_scale(rloc, None, ysub), "dispatch_bwd")
+    if w.capacity:
+        # zero tail of dY
+        unowned = np.nonzero(owner < 0)[0]
+        if len(unowned):
+            pick = unowned[_sample_rows(len(unowned), 64, gen)]
+            assert not bits(dY[torch.from_numpy(pick).to(DEV)]).any()
+    h.destroy()
+
+
+# ----------------------------------------------------------- determinism --
+
+def test_layout_rebuilds_are_bit_identical():
+    w = W.WORKLOADS["fine-grained-skewed"]
+    logits = W.make_logits(w, device=DEV)
+    idx, _ = B.moe_topk_gate(logits, w.k)
+    ref = None
+    for _ in range(20):
+        h = B.moe_dispatch_layout(idx, w.e, 0, w.R)
+        got = [bits(getattr(h, n)()) for n in ("loc", "row", "counts", "offsets", "rank_counts")]
+        if ref is None:
+            ref = got
+        for a, b in zip(got, ref):
+            np.testing.assert_array_equal(a, b)
+        h.destroy()
+    wc = W.WORKLOADS["gshard-capacity"]
+    idx, _ = B.moe_topk_gate(W.make_logits(wc, device=DEV), wc.k)
+    ref = None
+    for _ in range(10):
+        h = B.moe_dispatch_layout(idx, wc.e, wc.capacity)
+        got = [bits(getattr(h, n)()) for n in ("loc", "row", "drop", "counts")]
+        if ref is None:
+            ref = got
+        for a, b in zip(got, ref):
+            np.testing.assert_array_equal(a, b)
+
+
+def test_replay_skips_layout_and_is_bit_identical():
+    w = REDUCED["mixtral-dropless"]
+    inp = W.make_inputs(w, device=DEV)
+    idx, gate = B.moe_topk_gate(inp["logits"], w.k)
+    h = B.moe_dispatch_layout(idx, w.e)
+    X1 = B.moe_dispatch(h, inp["x"])
+    o1 = B.moe_combine(h, inp["y"], gate)
+    n_layout = B.moe_launch_count("layout")
+    n_disp = B.moe_launch_count("dispatch")
+    for _ in range(5):
+        X2 = B.moe_dispatch(h, inp["x"])
+        o2 = B.moe_combine(h, inp["y"], gate)
+        assert torch.equal(X1, X2) and torch.equal(o1, o2)
+    assert B.moe_launch_count("layout") == n_layout
+    assert B.moe_launch_count("dispatch") == n_disp + 5
+
+
+# --------------------------------------------------------- device errors --
+
+def test_nonfinite_logits_are_flagged():
+    logits = torch.randn(100, 16, device=DEV)
+    logits[37, 3] = float("nan")
+    logits[80, 0] = float("inf")
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    B.moe_topk_gate(logits, 2, 1, device_status=status)
+    assert int(status.item()) & B.MOE_DEV_NONFINITE
+    status.zero_()
+    B.moe_topk_gate(torch.randn(100, 16, device=DEV), 2, 1, device_status=status)
+    assert int(status.item()) == 0
+
+
+def test_bad_routes_are_flagged_not_followed():
+    idx = torch.tensor([[0, 1], [2, 2], [5, 1], [-1, 3], [3, 0]], dtype=torch.int32, device=DEV)
+    h = B.moe_dispatch_layout(idx, 4)
+    assert h.status() & B.MOE_DEV_BAD_ROUTE
+    row = bits(h.row())
+    assert row[1, 1] == -1 and row[2, 0] == -1 and row[3, 0] == -1  # repeat, out of range, negative
+    assert row[1, 0] >= 0 and row[0, 0] >= 0
+    kept = row[row >= 0]
+    assert len(np.unique(kept)) == len(kept)
+    X = B.moe_dispatch(h, torch.ones(5, 8, device=DEV))  # must not fault
+    torch.cuda.synchronize()
+
+
+def test_layout_wait_times_out_without_hanging():
+    """A tile that never publishes: later tiles' bounded waits run out, the
+    handle reports MOE_DEV_TIMEOUT, and the context stays usable."""
+    s, e, k = 256 * 6, 8, 2
+    idx = W.random_routes(s, e, k, device=DEV, seed=1)
+    B.moe_debug_hold_layout_tile(2, timeout_ms=200)
+    h = B.moe_dispatch_layout(idx, e)
+    assert h.status() & B.MOE_DEV_TIMEOUT
+    h.destroy()
+    h = B.moe_dispatch_layout(idx, e)  # the hook disarmed itself
+    assert h.status() == 0
+    check_layout(h, oracle.layout(bits(idx), e), bits(idx))
+
+
+# -------------------------------------------------------------- host API --
+
+def test_host_validation_on_device():
+    x = torch.randn(4, 8, device=DEV)
+    idx = torch.tensor([[0, 1]] * 4, dtype=torch.int32, device=DEV)
+    h = B.moe_dispatch_layout(idx, 2)
+    with pytest.raises(B.MoEError) as ei:
+        B.moe_dispatch(h, x.half())
+    assert ei.value.name == "MOE_ERR_DTYPE"
+    with pytest.raises(B.MoEError) as ei:
+        B.moe_dispatch(h, torch.randn(5, 8, device=DEV))
+    assert ei.value.name == "MOE_ERR_HANDLE_MISMATCH"
+    with pytest.raises(B.MoEError) as ei:
+        B.moe_combine(h, torch.randn(7, 8, device=DEV), torch.ones(4, 2, device=DEV))
+    assert ei.value.name == "MOE_ERR_HANDLE_MISMATCH"
+    with pytest.raises(B.MoEError) as ei:
+        B.moe_dispatch(h, torch.randn(4, 8))  # host memory
+    assert ei.value.name == "MOE_ERR_INVALID_ARG"
+    with pytest.raises(B.MoEError) as ei:
+        B.moe_dispatch(h, torch.randn(4, 6, device=DEV))  # 24-byte rows
+    assert ei.value.name == "MOE_ERR_INVALID_ARG"
+    raw = h.raw
+    h.destroy()
+    import ctypes
+
+    rc = B.lib().moe_dispatch(raw, 4, 8, 8, B.MOE_F32, ctypes.c_void_p(x.data_ptr()), None, None)
+    assert B.STATUS[rc] == "MOE_ERR_HANDLE_MISMATCH"
