@@ -1,0 +1,463 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE token path on GB300.
+
+One step = one pass of the whole path over one batch of seeded synthetic
+input: top-k gate -> dispatch layout -> dispatch -> combine -> combine
+backward (gate-scaled dispatch + gate gradient) -> dispatch backward, all on
+the layout handle the step built, then the handle is released.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle, on a bounded sample
+
+Prints ONE JSON line.  ``value`` = algorithmic HBM bytes of a step / device
+time of a step (GB/s), inputs resident in HBM; ``e2e`` = the same with the
+inputs copied from pinned host memory and the results copied back inside
+the timed region.  The step's working set is several times the 129 MB L2,
+so no L2 flush is inserted between steps.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine HBM GB/s and routed tokens/s on 1 GB300 vs HBM peak"
+DEFAULT_WORKLOAD = "mixtral-dropless"
+OPS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd"]
+KERNEL_FILE = {"topk_gate": "gate.cu", "layout": "layout.cu", "dispatch": "dispatch.cu", "combine": "combine.cu",
+               "combine_bwd": "combine.cu", "dispatch_bwd": "combine.cu"}
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------ byte model --
+
+def step_bytes(w, kept: int, u: int) -> dict:
+    """Algorithmic HBM bytes of each op.  kept = kept routes, u = tokens with
+    at least one kept route (both equal s*k and s when nothing is dropped)."""
+    b, s, m, e, k = w.elem_bytes, w.s, w.m, w.e, w.k
+    R = w.rows * m * b          # whole dispatched buffer (capacity: incl. the zero tail)
+    x = s * m * b
+    routes = s * k
+    meta_r = routes * 4         # reading row[] (or idx)
+    return {
+        "topk_gate": s * e * 4 + routes * 8,
+        "layout": routes * 4 + routes * 13 + e * 12 + (s * w.R + w.R * 4 if w.R else 0),
+        "dispatch": u * m * b + R + meta_r,
+        "combine": kept * m * b + x + meta_r + routes * 4,
+        "combine_bwd": x + kept * m * b + R + meta_r + routes * 8,
+        "dispatch_bwd": kept * m * b + x + meta_r,
+    }
+
+
+def payload_bytes(w, kept: int, u: int) -> dict:
+    b, m = w.elem_bytes, w.m
+    x = w.s * m * b
+    R = w.rows * m * b
+    return {"dispatch": u * m * b + R, "combine": kept * m * b + x}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record(op: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the kernel source as it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    r = rec.get(op)
+    if not r:
+        return None
+    src = os.path.join(ROOT, "combine_moe_topk_gb300", "csrc", KERNEL_FILE[op])
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    if r.get("source_sha") != sha:
+        return None
+    return r
+
+
+# ---------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        rows = []
+        for l in getattr(self, "lines", []):
+            p = [x.strip() for x in l.split(",")]
+            try:
+                rows.append((float(p[0]), float(p[1]), p[4:8], p[3]))
+            except Exception:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------- our arm -----
+
+def run_ours(args, rank: int, world: int, dist):
+    import torch
+
+    from combine_moe_topk_gb300 import binding as B
+    from combine_moe_topk_gb300 import workloads as W
+
+    w = W.WORKLOADS[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    B.lib()
+    inp = W.make_inputs(w, device=dev, seed=w.seed + 1000 * rank)
+    logits, x, y, dout = inp["logits"], inp["x"], inp["y"], inp["dout"]
+    dt = w.torch_dtype
+    X = torch.empty(w.rows, w.m, dtype=dt, device=dev)
+    out = torch.empty(w.s, w.m, dtype=dt, device=dev)
+    dY = torch.empty(w.rows, w.m, dtype=dt, device=dev)
+    dx = torch.empty(w.s, w.m, dtype=dt, device=dev)
+    idx = torch.empty(w.s, w.k, dtype=torch.int32, device=dev)
+    gate = torch.empty(w.s, w.k, dtype=torch.float32, device=dev)
+    dgate = torch.empty(w.s, w.k, dtype=torch.float32, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record()
+        B.moe_topk_gate(logits, w.k, w.renorm, idx, gate)
+        if ev is not None:
+            ev[1].record()
+        h = B.moe_dispatch_layout(idx, w.e, w.capacity, w.R)
+        if ev is not None:
+            ev[2].record()
+        B.moe_dispatch(h, x, X)
+        if ev is not None:
+            ev[3].record()
+        B.moe_combine(h, y, gate, out)
+        if ev is not None:
+            ev[4].record()
+        B.moe_combine_bwd(h, dout, gate, y, dY, dgate)
+        if ev is not None:
+            ev[5].record()
+        B.moe_dispatch_bwd(h, dY, dx)
+        if ev is not None:
+            ev[6].record()
+        return h
+
+    # kept routes / sending tokens for the byte model (outside any timing)
+    h = step()
+    drop = h.drop()
+    kept = int((drop == 0).sum().item())
+    u = int((drop == 0).any(dim=1).sum().item())
+    assert h.status() == 0, "device status after the first step"
+    h.destroy()
+    nbytes = step_bytes(w, kept, u)
+    step_total = sum(nbytes.values())
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step().destroy()
+    barrier()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    launches0 = [B.moe_launch_count(i) for i in range(len(B.KERNELS))]
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(K):
+            step(evs[i]).destroy()
+        t1.record()
+        barrier()
+    launches = sum(B.moe_launch_count(i) - launches0[i] for i in range(len(B.KERNELS)))
+    elapsed_ms = t0.elapsed_time(t1)
+    per_op = {op: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) for j, op in enumerate(OPS)}
+
+    # end to end: pinned host inputs in, results out, inside the timed region
+    h_in = {n: t.cpu().pin_memory() for n, t in (("logits", logits), ("x", x), ("y", y), ("dout", dout))}
+    h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in (("out", out), ("dx", dx),
+                                                                               ("dgate", dgate))}
+    d_in = {"logits": logits, "x": x, "y": y, "dout": dout}
+    d_out = {"out": out, "dx": dx, "dgate": dgate}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    Ke = max(3, min(K, 50))
+
+    def e2e_step():
+        for n, t in h_in.items():
+            d_in[n].copy_(t, non_blocking=True)
+        step().destroy()
+        for n, t in h_out.items():
+            t.copy_(d_out[n], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(Ke):
+        e2e_step()
+    e1.record()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+
+    if dist is not None:
+        t = torch.tensor([elapsed_ms, e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+
+    ms_per_step = elapsed_ms / K
+    value = world * step_total / (ms_per_step * 1e-3) / 1e9
+    peak, peak_src = peaks()
+    dom = max(per_op, key=per_op.get)
+    achieved = nbytes[dom] / (per_op[dom] * 1e-3) / 1e9
+    tr = traffic_record(dom)
+    pay = payload_bytes(w, kept, u)
+    dc_ms = per_op["dispatch"] + per_op["combine"]
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic: seeded N(0,1) router logits and activations (no trained weights or routing traces)",
+        "config": {
+            "workload": w.name, "s": w.s, "m": w.m, "e": w.e, "k": w.k,
+            "mode": f"capacity {w.capacity}" if w.capacity else "dropless", "virtual_ranks": w.R,
+            "step": "topk_gate+layout+dispatch+combine+combine_bwd+dispatch_bwd on the step's handle",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": f"no flush: step working set {round((step_total) / 1e6)} MB algorithmic vs 129 MB L2",
+        },
+        "routed_tokens_per_s": round(world * w.s * w.k / (ms_per_step * 1e-3), 1),
+        "dispatch_combine": {
+            "us": round(dc_ms * 1e3, 2),
+            "gbs": round((nbytes["dispatch"] + nbytes["combine"]) / (dc_ms * 1e-3) / 1e9, 1),
+            "payload_gbs": round((pay["dispatch"] + pay["combine"]) / (dc_ms * 1e-3) / 1e9, 1),
+            "frac_of_peak": round((nbytes["dispatch"] + nbytes["combine"]) / (dc_ms * 1e-3) / 1e9 / peak, 4),
+            "routed_tokens_per_s": round(w.s * w.k / (dc_ms * 1e-3), 1),
+        },
+        "ops": {op: {"us": round(per_op[op] * 1e3, 2), "bytes": nbytes[op],
+                     "gbs": round(nbytes[op] / (per_op[op] * 1e-3) / 1e9, 1)} for op in OPS},
+        "roofline": {
+            "kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (copy bandwidth)",
+            "traffic": (tr["dram_bytes_per_launch"] if tr else None),
+            "traffic_note": (tr.get("note") if tr else "no ncu capture of this kernel source"),
+            "algorithmic_bytes": nbytes[dom],
+        },
+        "e2e": {"value": round(world * step_total / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": Ke},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "kept_routes": kept,
+        "sending_tokens": u,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args)
+    return line
+
+
+# --------------------------------------------------------- oracle (CPU) --
+
+def oracle_sample(w, s_sample: int):
+    """Inputs of the first s_sample tokens of the workload, drawn on the CPU."""
+    from combine_moe_topk_gb300 import workloads as W
+
+    cap = 0
+    if w.capacity:
+        cap = max(1, -(-w.capacity * s_sample // w.s))  # same capacity factor on the sample
+    ws = w.replace(s=s_sample, capacity=cap)
+    return ws, W.make_inputs(ws)
+
+
+def oracle_step(ws, inp):
+    import numpy as np
+
+    import oracle
+
+    def nb(t):
+        import torch
+
+        t = t.contiguous()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16)
+        return t.numpy()
+
+    arrs = {k: nb(v) for k, v in inp.items()}
+    t0 = time.perf_counter()
+    idx, gate = oracle.topk_gate(arrs["logits"], ws.k, ws.renorm)
+    L = oracle.layout(idx, ws.e, ws.capacity, ws.R)
+    oracle.dispatch(L["row"], arrs["x"], L["rows"])
+    oracle.combine(L["row"], gate, arrs["y"])
+    dY, _ = oracle.combine_bwd(L["row"], gate, arrs["dout"], arrs["y"])
+    oracle.dispatch_bwd(L["row"], dY)
+    dt = time.perf_counter() - t0
+    kept = int((L["drop"] == 0).sum())
+    u = int((L["drop"] == 0).any(axis=1).sum())
+    return dt, step_bytes(ws, kept, u)
+
+
+def oracle_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, args):
+    """The oracle, as it stands, on the host cores: whole steps of the full
+    workload, repeated for about args.cpu_seconds of CPU work."""
+    import oracle
+
+    cores = oracle.set_threads(oracle_cores())
+    ws, inp = oracle_sample(w, w.s)
+    times, nbytes = [], None
+    t_start = time.perf_counter()
+    while not times or (time.perf_counter() - t_start < args.cpu_seconds and len(times) < 100):
+        dt, nbytes = oracle_step(ws, inp)
+        times.append(dt)
+    oracle.set_threads(1)
+    per = statistics.median(times)
+    return {"value": round(sum(nbytes.values()) / per / 1e9, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(times)} full steps of {w.name} (s={w.s}, m={w.m}), median {per:.3f} s each"}
+
+
+def run_reference(args, rank: int, world: int):
+    """The CPU oracle as the reference arm: each step is the whole path on the
+    first s' tokens of the workload, s' sized so that warmup + steps take
+    about args.ref_seconds in total."""
+    if rank != 0:
+        return None
+    from combine_moe_topk_gb300 import workloads as W
+
+    import oracle
+
+    w = W.WORKLOADS[args.workload]
+    cores = oracle.set_threads(oracle_cores())
+    probe = min(w.s, 256)
+    ws, inp = oracle_sample(w, probe)
+    oracle_step(ws, inp)
+    dt, _ = oracle_step(ws, inp)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
+    s_sample = int(max(32, min(w.s, probe * budget / max(dt, 1e-6))))
+    ws, inp = oracle_sample(w, s_sample)
+    for _ in range(args.warmup):
+        oracle_step(ws, inp)
+    times = []
+    nbytes = None
+    for _ in range(args.steps):
+        dt, nbytes = oracle_step(ws, inp)
+        times.append(dt)
+    per = sum(times) / len(times)
+    value = sum(nbytes.values()) / per / 1e9
+    sample = f"{ws.s} of {w.s} tokens of {w.name} (m={w.m}) per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic: seeded N(0,1) router logits and activations",
+        "config": {"workload": w.name, "s": w.s, "m": w.m, "e": w.e, "k": w.k,
+                   "mode": f"capacity {w.capacity}" if w.capacity else "dropless", "virtual_ranks": w.R,
+                   "step": "topk_gate+layout+dispatch+combine+combine_bwd+dispatch_bwd (CPU oracle)"},
+        "routed_tokens_per_s": round(ws.s * ws.k / per, 1),
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle work for cpu_baseline")
+    ap.add_argument("--ref-seconds", type=float, default=120.0, help="total oracle work of --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as td
+
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+            td.init_process_group("nccl")
+            dist = td
+        line = run_ours(args, rank, world, dist)
+        if dist is not None:
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

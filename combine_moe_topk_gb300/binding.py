@@ -106,7 +106,9 @@ def _ptr(t: torch.Tensor | None):
 
 
 def _stream(device: torch.device):
-    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    # a host tensor still goes to the library, which rejects it; use the current device's stream
+    dev = device if device.type == "cuda" else None
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
 
 
 def _dtype(t: torch.Tensor) -> int:
@@ -122,12 +124,12 @@ def _dtype(t: torch.Tensor) -> int:
 # ------------------------------------------------------------------ handle --
 
 class _DeviceArray:
-    """A read-only CUDA array view of handle memory (``__cuda_array_interface__``)."""
+    """A CUDA array view of handle memory (``__cuda_array_interface__``); treat it as read-only."""
 
     def __init__(self, owner, ptr: int, shape: tuple, typestr: str):
         self._owner = owner  # keeps the handle (and its memory) alive
         self.__cuda_array_interface__ = {
-            "shape": shape, "typestr": typestr, "data": (ptr or 0, True), "version": 3, "strides": None,
+            "shape": shape, "typestr": typestr, "data": (ptr or 0, False), "version": 3, "strides": None,
             "stream": None,
         }
 

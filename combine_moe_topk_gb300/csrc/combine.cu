@@ -190,6 +190,7 @@ cudaError_t combine_t(const int32_t* row, const float* gate, int s, int k, int m
                       void* out, const DeviceInfo& di, cudaStream_t st) {
   constexpr int UNR = KMAX <= 2 ? 4 : (KMAX <= 4 ? 2 : 1);
   const int nvec = m / Vec<T>::N;
+  (void)cudaGetLastError();  // clear a stale error left by an earlier, unrelated call
   if (gate) {
     auto kern = combine_kernel<T, KMAX, UNR, true>;
     static const int bps = occupancy(kern);
@@ -214,6 +215,7 @@ cudaError_t combine_bwd_t(const int32_t* row, const int32_t* counts, const float
   const int nvec = m / Vec<T>::N;
   auto kern = combine_bwd_kernel<T, KMAX, UNR>;
   static const int bps = occupancy(kern);
+  (void)cudaGetLastError();  // clear a stale error left by an earlier, unrelated call
   long long warps = s;
   if (capacity > 0 && (long long)e * capacity > warps) warps = (long long)e * capacity;
   kern<<<grid_for(warps, di, bps), kThreads, 0, st>>>(

@@ -218,14 +218,21 @@ Config choose(long long row_bytes, const DeviceInfo& di) {
 cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, int s, int k, int e,
                             int capacity, const void* x, void* X, long long row_bytes,
                             int32_t* status, const DeviceInfo& di, cudaStream_t st) {
-  static bool attr_set[64] = {};
+  // allow the kernel the device's whole opt-in shared memory (less its static
+  // part) once per device; occupancy still follows the dynamic size launched
+  static bool opted_in[64] = {};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           di.max_smem_optin);
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!opted_in[dev]) {
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, dispatch_kernel);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 di.max_smem_optin - (int)fa.sharedSizeBytes);
     if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
+    opted_in[dev] = true;
   }
   Config c = choose(row_bytes, di);
   Params p;
@@ -253,6 +260,7 @@ cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, int s, in
   long long grid = (long long)di.sms * c.ctas_per_sm;
   if (grid > work) grid = work;
   if (grid < 1) grid = 1;
+  (void)cudaGetLastError();  // clear a stale error left by an earlier, unrelated call
   dispatch_kernel<<<(int)grid, 32, c.smem, st>>>(p);
   return cudaGetLastError();
 }

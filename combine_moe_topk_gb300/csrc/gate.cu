@@ -105,6 +105,7 @@ cudaError_t launch_epl(const float* logits, int s, int e, int k, int renorm, int
   const long long cap = (long long)di.sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  (void)cudaGetLastError();  // clear a stale error left by an earlier, unrelated call
   topk_gate_kernel<EPL><<<(int)blocks, threads, 0, st>>>(logits, s, e, k, renorm, idx, gate, status);
   return cudaGetLastError();
 }
