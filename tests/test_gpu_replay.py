@@ -1,0 +1,117 @@
+"""Activation-checkpoint replay on cached handles, and the autograd wrappers.
+
+Automodel #3684 "perf(moe): reuse the DeepEP dispatch layout on
+activation-checkpoint recompute": 30 layers x 3 passes need 90 dispatches;
+activation checkpointing replays the encoder and the real-decode passes
+(60 replays), each of which must reuse the logged handle -- no layout
+rebuild -- and reproduce bit-identical counts and outputs; the top-k index
+checksum of a recompute equals the forward's.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import tolerance as T
+from combine_moe_topk_gb300 import autograd as A
+from combine_moe_topk_gb300 import binding as B
+from combine_moe_topk_gb300 import workloads as W
+from gpu_util import bits, check_layout, to_dev
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def test_stacked_replay_90_builds_60_replays():
+    w = W.WORKLOADS["diffusiongemma-replay"]
+    replayed_passes = (0, 2)  # the checkpointed passes; pass 1 runs without grad
+    recorders = {}
+    fwd = {}
+    n_builds = 0
+    for p in range(w.passes):
+        for layer in range(w.layers):
+            inp = W.make_inputs(w, device=DEV, seed=W.replay_seed(w, p, layer), with_grad=False)
+            idx, gate = B.moe_topk_gate(inp["logits"], w.k)
+            rec = A.HandleRecorder(verify=True) if p in replayed_passes else None
+            h = rec.layout(idx, w.e) if rec is not None else B.moe_dispatch_layout(idx, w.e)
+            n_builds += 1
+            X = B.moe_dispatch(h, inp["x"])
+            out = B.moe_combine(h, X, gate)  # identity expert
+            if rec is not None:
+                recorders[(p, layer)] = rec
+                fwd[(p, layer)] = (int(idx.sum()), bits(h.counts()), bits(h.offsets()), X, out)
+            if p == 1 and layer == 0:
+                # one sampled build checked against the oracle in full
+                oi, og = oracle.topk_gate(bits(inp["logits"]), w.k)
+                np.testing.assert_array_equal(bits(idx), oi)
+                check_layout(h, oracle.layout(oi, w.e), oi)
+    assert n_builds == 90
+
+    layouts = B.moe_launch_count("layout")
+    n_replays = 0
+    for p in reversed(replayed_passes):          # backward runs the later pass first
+        for layer in reversed(range(w.layers)):  # and the layers in reverse
+            inp = W.make_inputs(w, device=DEV, seed=W.replay_seed(w, p, layer), with_grad=False)
+            idx, gate = B.moe_topk_gate(inp["logits"], w.k)  # routing pinned: recomputed identically
+            rec = recorders[(p, layer)].replay()
+            h = rec.layout(idx, w.e)
+            X = B.moe_dispatch(h, inp["x"])
+            out = B.moe_combine(h, X, gate)
+            checksum, counts, offsets, X0, out0 = fwd[(p, layer)]
+            assert int(idx.sum()) == checksum
+            np.testing.assert_array_equal(bits(h.counts()), counts)
+            np.testing.assert_array_equal(bits(h.offsets()), offsets)
+            assert torch.equal(X, X0) and torch.equal(out, out0)
+            assert rec.replayed == 1 and rec.fallbacks == 0
+            n_replays += 1
+    assert n_replays == 60
+    assert B.moe_launch_count("layout") == layouts, "a replay must not launch the layout kernel"
+
+
+def test_recorder_outrun_rebuilds_on_gpu():
+    w = W.WORKLOADS["diffusiongemma-replay"].replace(m=256)
+    inp = W.make_inputs(w, device=DEV, with_grad=False)
+    idx, _ = B.moe_topk_gate(inp["logits"], w.k)
+    rec = A.HandleRecorder()
+    h0 = rec.layout(idx, w.e)
+    rec.replay()
+    n = B.moe_launch_count("layout")
+    assert rec.layout(idx, w.e) is h0 and B.moe_launch_count("layout") == n
+    h1 = rec.layout(idx, w.e)  # log exhausted: a fresh, correct build
+    assert h1 is not h0 and B.moe_launch_count("layout") == n + 1 and rec.fallbacks == 1
+    assert torch.equal(h1.row(), h0.row())
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("capacity", [0, 150])
+def test_autograd_matches_oracle(dtype, capacity):
+    """loss = <combine(2 * dispatch(x), gate), dout>: x.grad and gate.grad from
+    torch.autograd through the library's backward entry points."""
+    s, m, e, k = 700, 64, 16, 4
+    w = W.Workload("autograd", s=s, m=m, e=e, k=k, dtype=dtype, capacity=capacity, R=0, seed=31)
+    inp = W.make_inputs(w)
+    oi, og = oracle.topk_gate(inp["logits"].numpy(), k)
+    L = oracle.layout(oi, e, capacity)
+    h = B.moe_dispatch_layout(to_dev(oi, DEV), e, capacity)
+
+    x = inp["x"].to(DEV).requires_grad_(True)
+    gate = to_dev(og, DEV).requires_grad_(True)
+    X = A.dispatch(x, h)
+    y = X * 2
+    out = A.combine(y, gate, h)
+    dout = inp["dout"].to(DEV)
+    out.backward(dout)
+
+    xb, db = bits(inp["x"]), bits(inp["dout"])
+    OX = oracle.dispatch(L["row"], xb, L["rows"])
+    np.testing.assert_array_equal(bits(X), OX)
+    Oy = (T.as_f64(OX) * 2).astype(np.float32)
+    if dtype == "bf16":
+        Oy = bits(torch.from_numpy(Oy).to(torch.bfloat16))  # exact: doubling a bf16 value
+    OdY, Odg = oracle.combine_bwd(L["row"], og, db, Oy)
+    T.assert_close(bits(gate.grad), Odg, T.dot_scale(L["row"], db, Oy), "gate.grad")
+    OdX = (T.as_f64(OdY) * 2).astype(np.float32)
+    if dtype == "bf16":
+        OdX = bits(torch.from_numpy(OdX).to(torch.bfloat16))
+    Odx = oracle.dispatch_bwd(L["row"], OdX)
+    T.assert_close(bits(x.grad), Odx, T.combine_scale(L["row"], None, OdX), "x.grad")
