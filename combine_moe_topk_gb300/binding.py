@@ -33,6 +33,7 @@ EXPORTS = [
     "moe_topk_gate", "moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_combine_bwd",
     "moe_dispatch_bwd", "moe_handle_info", "moe_handle_status", "moe_handle_destroy", "moe_capacity",
     "moe_status_string", "moe_last_error", "moe_launch_count", "moe_debug_hold_layout_tile",
+    "moe_dispatch_layout_noalloc",
 ]
 
 
@@ -74,6 +75,7 @@ def lib() -> ctypes.CDLL:
             "moe_handle_status": [P, P, ctypes.POINTER(ctypes.c_int32)],
             "moe_handle_destroy": [P],
             "moe_debug_hold_layout_tile": [I, I],
+            "moe_dispatch_layout_noalloc": [P, I, I, I, I, I] + [P] * 11,
         }
         for name, args in sig.items():
             f = getattr(L, name)

@@ -482,4 +482,68 @@ moe_status moe_dispatch_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtyp
   return MOE_OK;
 }
 
+moe_status moe_dispatch_layout_noalloc(const int32_t* topk_idx, int s, int e, int k, int capacity,
+                                       int num_virtual_ranks, int32_t* idx_out, int32_t* loc,
+                                       int32_t* row, uint8_t* drop, int32_t* raw_counts,
+                                       int32_t* counts, int32_t* offsets, uint8_t* token_in_rank,
+                                       int32_t* rank_counts, int32_t* device_status, void* stream) {
+  const int R = num_virtual_ranks;
+  if (s < 0 || e < 1 || e > kMaxE || k < 1 || k > e || k > kMaxK)
+    return fail(MOE_ERR_INVALID_ARG, "need s >= 0, 1 <= e <= 256, 1 <= k <= min(e, 16)");
+  if (capacity < 0) return fail(MOE_ERR_INVALID_ARG, "capacity must be >= 0 (0 = dropless)");
+  if (R < 0 || R > kMaxR || (R > 0 && e % R != 0))
+    return fail(MOE_ERR_INVALID_ARG, "num_virtual_ranks must be in [0, 64] and divide e");
+  const long long routes = (long long)s * k;
+  const long long rows = capacity > 0 ? (long long)e * capacity : routes;
+  if (routes > 2147483647LL || rows > 2147483647LL)
+    return fail(MOE_ERR_INVALID_ARG, "s*k and the row count must be < 2^31");
+  void* per_route[5] = {const_cast<int32_t*>(topk_idx), idx_out, loc, row, drop};
+  const char* route_names[5] = {"topk_idx", "idx_out", "loc", "row", "drop"};
+  if (s > 0)
+    for (int i = 0; i < 5; ++i) MOE_TRY(check_ptr(per_route[i], route_names[i]));
+  MOE_TRY(check_ptr(raw_counts, "raw_counts"));
+  MOE_TRY(check_ptr(counts, "counts"));
+  MOE_TRY(check_ptr(offsets, "offsets"));
+  if (R > 0) {
+    MOE_TRY(check_ptr(rank_counts, "rank_counts"));
+    if (s > 0) MOE_TRY(check_ptr(token_in_rank, "token_in_rank"));
+  }
+  if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u))
+    return fail(MOE_ERR_INVALID_ARG, "device_status is not 4-byte aligned");
+
+  int dev = 0;
+  MOE_TRY(current_device(&dev));
+  const void* all[11] = {topk_idx, idx_out, loc, row, drop, raw_counts, counts, offsets,
+                         R > 0 ? token_in_rank : nullptr, R > 0 ? rank_counts : nullptr,
+                         device_status};
+  const char* all_names[11] = {"topk_idx", "idx_out", "loc", "row", "drop", "raw_counts", "counts",
+                               "offsets", "token_in_rank", "rank_counts", "device_status"};
+  for (int i = 0; i < 11; ++i)
+    if (i >= 5 || s > 0) MOE_TRY(check_device_ptr(all[i], all_names[i], dev));
+
+  moe::LayoutOut out = {};
+  out.idx = idx_out;
+  out.loc = loc;
+  out.row = row;
+  out.drop = drop;
+  out.raw_counts = raw_counts;
+  out.counts = counts;
+  out.offsets = offsets;
+  out.token_in_rank = R > 0 ? token_in_rank : nullptr;
+  out.rank_counts = R > 0 ? rank_counts : nullptr;
+  out.status = device_status;
+  int words = 0;
+  cudaError_t err = moe::launch_layout_noalloc(topk_idx, s, e, k, capacity, R, out, &words,
+                                               static_cast<cudaStream_t>(stream));
+  if (err == cudaErrorInvalidValue && words > moe::noalloc_lookback_words())
+    return fail(MOE_ERR_UNSUPPORTED,
+                "the allocation-free layout needs " + std::to_string(words) +
+                    " look-back words (tiles x experts) but holds " +
+                    std::to_string(moe::noalloc_lookback_words()) + "; use moe_dispatch_layout");
+  if (err != cudaSuccess) return cuda_fail(err, "allocation-free layout launch");
+  g_launches[MOE_KERNEL_LAYOUT]++;
+  return MOE_OK;
+}
+
 }  // extern "C"
+

@@ -44,6 +44,13 @@ cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capa
                           const LayoutPlan& plan, const LayoutOut& out, int hold_tile,
                           long long timeout_ns, cudaStream_t st);
 
+// Allocation-free layout: the look-back scratch is a file-scope device array
+// of noalloc_lookback_words() words; returns cudaErrorInvalidValue (and sets
+// *words_needed) when tiles * e exceeds it.  out.lookback is ignored.
+int noalloc_lookback_words();
+cudaError_t launch_layout_noalloc(const int32_t* topk_idx, int s, int e, int k, int capacity, int R,
+                                  const LayoutOut& out, int* words_needed, cudaStream_t st);
+
 // --- dispatch (bulk-copy gather) -----------------------------------------
 cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, int s, int k, int e,
                             int capacity, const void* x, void* X, long long row_bytes,

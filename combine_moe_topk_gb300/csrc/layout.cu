@@ -29,6 +29,8 @@
 // records MOE_DEV_TIMEOUT and carries on with what it has (no hang, no trap).
 // All tiles are co-resident (cooperative launch), which is what makes the
 // wait for the last tile safe.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -344,6 +346,83 @@ cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capa
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, layout_kernel, p);
+}
+
+}  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the layout launch.
+//
+// For callers that cannot allocate device memory at the point they build a
+// layout: code running inside a CUDA-graph-captured region where a pool
+// allocation is not wanted, allocators that must not be re-entered (an
+// allocator's own hook or a custom memory manager), or embedded runtimes
+// that hand out only fixed buffers.  The caller passes every input and
+// output; the kernel's only scratch -- the look-back words -- lives in the
+// file-scope array below, which every GPU that loads this library holds
+// until the process exits.
+//
+// The array is shared by every call on a device and keeps the last call's
+// contents, so each call clears the words it uses first; calls whose
+// kernels overlap on the GPU (different streams without ordering) race on it.
+// ---------------------------------------------------------------------------
+namespace moe {
+
+constexpr int kNoAllocLookbackWords = 65536;  // 512 KB: tiles * e must fit
+
+static __device__ __align__(256) unsigned long long g_noalloc_lookback[kNoAllocLookbackWords];
+
+namespace {
+
+struct NoAllocSetup {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  unsigned long long* scratch = nullptr;  // device address of g_noalloc_lookback
+  DeviceInfo info;
+};
+NoAllocSetup g_noalloc[64];
+
+// Once per device, with that device current: resolve the scratch array's
+// device address (its host-side name is only a stand-in) and the sizes the
+// tile plan needs.  Allocates nothing.
+void noalloc_setup(int dev) {
+  NoAllocSetup& st = g_noalloc[dev];
+  void* ptr = nullptr;
+  st.err = cudaGetSymbolAddress(&ptr, g_noalloc_lookback);
+  if (st.err != cudaSuccess) return;
+  st.scratch = static_cast<unsigned long long*>(ptr);
+  st.err = cudaDeviceGetAttribute(&st.info.sms, cudaDevAttrMultiProcessorCount, dev);
+  if (st.err != cudaSuccess) return;
+  st.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&st.info.layout_blocks_per_sm, layout_kernel,
+                                                         kThreads, 0);
+}
+
+}  // namespace
+
+int noalloc_lookback_words() { return kNoAllocLookbackWords; }
+
+cudaError_t launch_layout_noalloc(const int32_t* topk_idx, int s, int e, int k, int capacity, int R,
+                                  const LayoutOut& out_in, int* words_needed, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::call_once(g_noalloc[dev].once, noalloc_setup, dev);
+  const NoAllocSetup& setup = g_noalloc[dev];
+  if (setup.err != cudaSuccess) return setup.err;
+
+  const LayoutPlan plan = plan_layout(s, setup.info);
+  const long long words = (long long)plan.tiles * e;
+  *words_needed = (int)(words > 0x7fffffffLL ? 0x7fffffffLL : words);
+  if (words > kNoAllocLookbackWords) return cudaErrorInvalidValue;  // caller reports the limit
+
+  LayoutOut out = out_in;
+  out.lookback = setup.scratch;
+  err = cudaMemsetAsync(setup.scratch, 0, (size_t)words * sizeof(unsigned long long), st);
+  if (err == cudaSuccess && R > 0)
+    err = cudaMemsetAsync(out.rank_counts, 0, (size_t)R * sizeof(int32_t), st);
+  if (err != cudaSuccess) return err;
+  return launch_layout(topk_idx, s, e, k, capacity, R, plan, out, -1, 2000000000LL, st);
 }
 
 }  // namespace moe

@@ -140,6 +140,32 @@ moe_status moe_topk_gate(const float* logits, int s, int e, int k, int renorm,
 moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity,
                                int num_virtual_ranks, void* stream, moe_handle* out);
 
+/* Allocation-free dispatch layout.  No counterpart on the pages: an
+ * addition of this library for callers that cannot allocate device memory
+ * when they build a layout (inside a captured CUDA graph where a pool
+ * allocation is unwanted, from an allocator's own hook that must not
+ * re-enter it, or in runtimes that hand out only fixed buffers).
+ * Computes exactly what moe_dispatch_layout computes, but writes it into
+ * caller-owned arrays instead of a handle: idx_out, loc, row [s,k] int32;
+ * drop [s,k] uint8; raw_counts, counts [e] int32; offsets [e+1] int32; and,
+ * when num_virtual_ranks R > 0, token_in_rank [s,R] uint8 and rank_counts
+ * [R] int32 (ignored when R = 0).  device_status (nullable): an int32 in
+ * device memory that gets MOE_DEV_* bits OR-ed in (the caller zeroes it).
+ * It calls no allocating routine.  The kernel's scratch (its look-back
+ * words, tiles x e of them) is a fixed library array of 65536 words (512 KB)
+ * per device, held until the process exits; a size whose tiling needs more
+ * returns MOE_ERR_UNSUPPORTED (use moe_dispatch_layout).  Every call shares
+ * that array and clears the part it uses, so calls whose work overlaps on the
+ * GPU (unordered streams) race; order them.  The first call on each device
+ * resolves the array's device address (one-time set-up); make that first call
+ * before any stream capture.  The dispatch / combine calls still take a
+ * handle, so this suits callers that consume the layout arrays themselves. */
+moe_status moe_dispatch_layout_noalloc(const int32_t* topk_idx, int s, int e, int k, int capacity,
+                                       int num_virtual_ranks, int32_t* idx_out, int32_t* loc,
+                                       int32_t* row, uint8_t* drop, int32_t* raw_counts,
+                                       int32_t* counts, int32_t* offsets, uint8_t* token_in_rank,
+                                       int32_t* rank_counts, int32_t* device_status, void* stream);
+
 /* Dispatch [P4 change 3; P4 change 2 for the [e, c, m] layout].
  * x [s,m] -> X [rows,m]: X[row[t,j]] = x[t] for every kept route; in
  * capacity mode the unused slots [counts[x], capacity) of every expert are
