@@ -17,10 +17,6 @@
 #include "../../include/moe_gb300.h"
 #include "internal.h"
 
-namespace moe {
-int layout_blocks_per_sm();
-}
-
 struct moe_handle_s {
   int device;
   cudaStream_t stream;
@@ -271,14 +267,14 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int
   h->capacity = capacity;
   h->R = R;
   h->rows = (int)rows;
-  h->plan = moe::plan_layout(s, *di);
+  h->plan = moe::plan_layout(s, e, *di);
 
   // one blob: [zeroed: status, rank_counts, look-back words] then the rest
   const size_t A = 256;
   size_t off = 0;
   const size_t o_status = off; off = align_up(off + 4, A);
   const size_t o_rank = off;   off = align_up(off + 4 * (size_t)(R > 0 ? R : 1), A);
-  const size_t o_lb = off;     off = align_up(off + 8 * (size_t)h->plan.tiles * e, A);
+  const size_t o_lb = off;     off = align_up(off + moe::lookback_bytes(h->plan, e), A);
   const size_t zero_bytes = off;
   const size_t o_idx = off;    off = align_up(off + 4 * (size_t)routes, A);
   const size_t o_loc = off;    off = align_up(off + 4 * (size_t)routes, A);
@@ -298,7 +294,7 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int
   char* base = static_cast<char*>(h->blob);
   h->out.status = reinterpret_cast<int32_t*>(base + o_status);
   h->out.rank_counts = R > 0 ? reinterpret_cast<int32_t*>(base + o_rank) : nullptr;
-  h->out.lookback = reinterpret_cast<unsigned long long*>(base + o_lb);
+  h->out.lookback = reinterpret_cast<unsigned*>(base + o_lb);
   h->out.idx = reinterpret_cast<int32_t*>(base + o_idx);
   h->out.loc = reinterpret_cast<int32_t*>(base + o_loc);
   h->out.row = reinterpret_cast<int32_t*>(base + o_row);
@@ -546,4 +542,3 @@ moe_status moe_dispatch_layout_noalloc(const int32_t* topk_idx, int s, int e, in
 }
 
 }  // extern "C"
-

@@ -24,6 +24,23 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Tuning: 16-byte loads in flight per lane for the combine and for its
+// backward (UNR = loads / KMAX),
+// an optional cap on resident blocks per SM, and the width of a combine work
+// unit in 16-byte vectors (0 = a whole token row per warp).
+#ifndef MOE_CMB_LOADS
+#define MOE_CMB_LOADS 16
+#endif
+#ifndef MOE_CMB_BWD_LOADS
+#define MOE_CMB_BWD_LOADS 8
+#endif
+#ifndef MOE_CMB_MAX_BPS
+#define MOE_CMB_MAX_BPS 0
+#endif
+#ifndef MOE_CMB_CHUNK
+#define MOE_CMB_CHUNK 0
+#endif
+
 // Route rows and gates of token t, broadcast from lanes 0..k-1.
 template <int KMAX, bool WEIGHTED>
 __device__ __forceinline__ void token_routes(const int32_t* __restrict__ row,
@@ -41,34 +58,40 @@ __device__ __forceinline__ void token_routes(const int32_t* __restrict__ row,
 template <typename T, int KMAX, int UNR, bool WEIGHTED>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __restrict__ row,
                                                            const float* __restrict__ gate, int s,
-                                                           int k, int nvec,
+                                                           int k, int nvec, int chunk, int nchunks,
                                                            const uint4* __restrict__ y,
                                                            uint4* __restrict__ out) {
   constexpr int N = Vec<T>::N;
   const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < s; t += warps) {
+  const long long warps = (gridDim.x * blockDim.x) >> 5;
+  const long long units = (long long)s * nchunks;
+  grid_dependency_wait();
+  pdl_trigger_early();
+  for (long long u = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < units; u += warps) {
+    const int t = (int)(u / nchunks);
+    const int c0 = (int)(u - (long long)t * nchunks) * chunk;
+    const int c1 = min(nvec, c0 + chunk);
     int r[KMAX];
     float g[KMAX];
     token_routes<KMAX, WEIGHTED>(row, gate, t, k, lane, r, g);
     uint4* o = out + (size_t)t * nvec;
-    for (int v0 = lane; v0 < nvec; v0 += 32 * UNR) {
+    for (int v0 = c0 + lane; v0 < c1; v0 += 32 * UNR) {
       uint4 val[KMAX][UNR];
 #pragma unroll
       for (int j = 0; j < KMAX; ++j) {
         if (r[j] >= 0) {
           const uint4* src = y + (size_t)r[j] * nvec;
 #pragma unroll
-          for (int u = 0; u < UNR; ++u) {
-            const int v = v0 + 32 * u;
-            if (v < nvec) val[j][u] = ld_stream(src + v);
+          for (int u2 = 0; u2 < UNR; ++u2) {
+            const int v = v0 + 32 * u2;
+            if (v < c1) val[j][u2] = ld_stream(src + v);
           }
         }
       }
 #pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        const int v = v0 + 32 * u;
-        if (v >= nvec) break;
+      for (int u2 = 0; u2 < UNR; ++u2) {
+        const int v = v0 + 32 * u2;
+        if (v >= c1) break;
         float acc[N];
 #pragma unroll
         for (int i = 0; i < N; ++i) acc[i] = 0.0f;
@@ -76,7 +99,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __rest
         for (int j = 0; j < KMAX; ++j) {
           if (r[j] >= 0) {
             float f[N];
-            Vec<T>::to_float(val[j][u], f);
+            Vec<T>::to_float(val[j][u2], f);
 #pragma unroll
             for (int i = 0; i < N; ++i) acc[i] = __fmaf_rn(g[j], f[i], acc[i]);
           }
@@ -85,6 +108,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __rest
       }
     }
   }
+  pdl_trigger_late();
 }
 
 template <typename T, int KMAX, int UNR>
@@ -97,6 +121,8 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  grid_dependency_wait();
+  pdl_trigger_early();
   for (int t = gw; t < s; t += warps) {
     int r[KMAX];
     float g[KMAX];
@@ -155,6 +181,7 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     }
     if (lane < k) dgate[(size_t)t * k + lane] = mine;
   }
+  pdl_trigger_late();
 
   // capacity mode: slots no kept route owns get zero gradient
   if (capacity > 0) {
@@ -174,6 +201,7 @@ template <typename K>
 int occupancy(K kern) {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, 0) != cudaSuccess) return 1;
+  if (MOE_CMB_MAX_BPS > 0 && n > MOE_CMB_MAX_BPS) n = MOE_CMB_MAX_BPS;
   return n;
 }
 
@@ -188,40 +216,40 @@ int grid_for(long long warps_wanted, const DeviceInfo& di, int blocks_per_sm) {
 template <typename T, int KMAX>
 cudaError_t combine_t(const int32_t* row, const float* gate, int s, int k, int m, const void* y,
                       void* out, const DeviceInfo& di, cudaStream_t st) {
-  constexpr int UNR = KMAX <= 2 ? 4 : (KMAX <= 4 ? 2 : 1);
+  constexpr int UNR = MOE_CMB_LOADS / KMAX > 1 ? MOE_CMB_LOADS / KMAX : 1;
   const int nvec = m / Vec<T>::N;
-  (void)cudaGetLastError();  // clear a stale error left by an earlier, unrelated call
+  const int chunk = MOE_CMB_CHUNK > 0 && MOE_CMB_CHUNK < nvec ? MOE_CMB_CHUNK : nvec;
+  const int nchunks = (nvec + chunk - 1) / chunk;
+  const long long units = (long long)s * nchunks;
   if (gate) {
     auto kern = combine_kernel<T, KMAX, UNR, true>;
     static const int bps = occupancy(kern);
-    kern<<<grid_for(s, di, bps), kThreads, 0, st>>>(row, gate, s, k, nvec,
-                                                    static_cast<const uint4*>(y),
-                                                    static_cast<uint4*>(out));
+    return launch_pdl(MOE_KERNEL_COMBINE, kern, dim3(grid_for(units, di, bps)), dim3(kThreads), 0, st,
+                      row, gate, s, k,
+                      nvec, chunk, nchunks, static_cast<const uint4*>(y), static_cast<uint4*>(out));
   } else {
     auto kern = combine_kernel<T, KMAX, UNR, false>;
     static const int bps = occupancy(kern);
-    kern<<<grid_for(s, di, bps), kThreads, 0, st>>>(row, nullptr, s, k, nvec,
-                                                    static_cast<const uint4*>(y),
-                                                    static_cast<uint4*>(out));
+    return launch_pdl(MOE_KERNEL_DISPATCH_BWD, kern, dim3(grid_for(units, di, bps)), dim3(kThreads), 0,
+                      st, row, static_cast<const float*>(nullptr), s, k, nvec, chunk, nchunks,
+                      static_cast<const uint4*>(y), static_cast<uint4*>(out));
   }
-  return cudaGetLastError();
 }
 
 template <typename T, int KMAX>
 cudaError_t combine_bwd_t(const int32_t* row, const int32_t* counts, const float* gate, int s,
                           int k, int e, int capacity, int m, const void* dout, const void* y,
                           void* dY, float* dgate, const DeviceInfo& di, cudaStream_t st) {
-  constexpr int UNR = KMAX <= 2 ? 4 : (KMAX <= 4 ? 2 : 1);
+  constexpr int UNR = MOE_CMB_BWD_LOADS / KMAX > 1 ? MOE_CMB_BWD_LOADS / KMAX : 1;
   const int nvec = m / Vec<T>::N;
   auto kern = combine_bwd_kernel<T, KMAX, UNR>;
   static const int bps = occupancy(kern);
-  (void)cudaGetLastError();  // clear a stale error left by an earlier, unrelated call
   long long warps = s;
   if (capacity > 0 && (long long)e * capacity > warps) warps = (long long)e * capacity;
-  kern<<<grid_for(warps, di, bps), kThreads, 0, st>>>(
-      row, counts, gate, s, k, e, capacity, nvec, static_cast<const uint4*>(dout),
-      static_cast<const uint4*>(y), static_cast<uint4*>(dY), dgate);
-  return cudaGetLastError();
+  return launch_pdl(MOE_KERNEL_COMBINE_BWD, kern, dim3(grid_for(warps, di, bps)), dim3(kThreads), 0, st,
+                    row, counts, gate, s,
+                    k, e, capacity, nvec, static_cast<const uint4*>(dout),
+                    static_cast<const uint4*>(y), static_cast<uint4*>(dY), dgate);
 }
 
 template <typename T>

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe_gb300.h"
 
 namespace moe {
@@ -34,6 +36,34 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// ------------------------------------------- programmatic dependent launch --
+// A kernel launched with programmatic stream serialisation may start while
+// the previous kernel in the stream is still running; it must wait here
+// before touching anything that kernel (or an earlier one) wrote.  A no-op
+// when the kernel was launched without the attribute.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next kernel in the stream begin its launch (it still waits for this
+// grid to complete before reading its results).
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Where a kernel lets its dependent launch: 0 = programmatic launch off,
+// 1 = as soon as the kernel may read its inputs, 2 = once its CTA's work is
+// issued.
+#ifndef MOE_PDL
+#define MOE_PDL 2
+#endif
+__device__ __forceinline__ void pdl_trigger_early() {
+  if (MOE_PDL == 1) grid_dependents_launch();
+}
+__device__ __forceinline__ void pdl_trigger_late() {
+  if (MOE_PDL == 2) grid_dependents_launch();
 }
 
 // ------------------------------------------------------ 16-byte vectors ----
@@ -174,6 +204,32 @@ __device__ __forceinline__ void bulk_wait_read() {
 // Wait until all of this thread's bulk groups have completed.
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Launch on `st` with programmatic stream serialisation: the kernel may begin
+// while the previous kernel in the stream drains; it calls
+// grid_dependency_wait() before reading anything that kernel wrote.
+// Bit mask of the launches that use programmatic serialisation (bit i =
+// kernel id i of moe_launch_count: gate 0, dispatch 2, combine 3,
+// combine backward 4, dispatch backward 5).
+#ifndef MOE_PDL_MASK
+#define MOE_PDL_MASK 0x35
+#endif
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(int kernel_id, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (MOE_PDL != 0 && ((MOE_PDL_MASK >> kernel_id) & 1)) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 }  // namespace moe

@@ -28,6 +28,20 @@ namespace moe {
 
 namespace {
 
+// Tuning: ring depth, largest bulk piece in bytes, cap on CTAs per SM.
+#ifndef MOE_DSP_STAGES
+#define MOE_DSP_STAGES 4
+#endif
+#ifndef MOE_DSP_PIECE
+#define MOE_DSP_PIECE 16384
+#endif
+#ifndef MOE_DSP_LDG
+#define MOE_DSP_LDG 0
+#endif
+#ifndef MOE_DSP_MAX_CTAS
+#define MOE_DSP_MAX_CTAS 16
+#endif
+
 constexpr int kMaxStages = 8;
 constexpr int kBatch = 32;   // tokens of routing metadata staged at a time
 constexpr int kMaxK = 16;
@@ -68,6 +82,8 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const Params p) {
     for (int st = 0; st < p.stages; ++st) mbar_init(&bar[st], 1);
     fence_barrier_init();
   }
+  grid_dependency_wait();
+  pdl_trigger_early();
   if (p.capacity > 0)
     for (int x = lane; x < p.e; x += 32) s_counts[x] = __ldg(p.counts + x);
   __syncwarp();
@@ -156,6 +172,7 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const Params p) {
   }
 
   if (!ok) {
+    pdl_trigger_late();
     if (lane == 0) raise_status(p.status, MOE_DEV_TIMEOUT);
     // let the loads still in flight land before the CTA's shared memory goes
     const uint64_t drain = globaltimer_ns() + (uint64_t)p.timeout_ns;
@@ -168,6 +185,7 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const Params p) {
     return;
   }
 
+  pdl_trigger_late();
   // ---- zero tail of the capacity buffer -----------------------------------
   if (p.capacity > 0) {
     bulk_wait_all();
@@ -193,23 +211,66 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const Params p) {
   bulk_wait_all();
 }
 
+#if MOE_DSP_LDG
+// Register-staged alternative, compiled only for comparison runs: one warp per
+// token row, 16-byte loads into registers, stored once per kept route.
+template <int UNR>
+__global__ void __launch_bounds__(256) dispatch_ldg_kernel(const Params p) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nvec = (int)(p.row_bytes / 16);
+  const uint4* x = reinterpret_cast<const uint4*>(p.x);
+  uint4* X = reinterpret_cast<uint4*>(p.X);
+  grid_dependency_wait();
+  pdl_trigger_early();
+  for (int t = gw; t < p.s; t += warps) {
+    const int rl = lane < p.k ? __ldg(p.row + (size_t)t * p.k + lane) : -1;
+    const unsigned kept = __ballot_sync(0xffffffffu, rl >= 0);
+    if (!kept) continue;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * UNR) {
+      uint4 val[UNR];
+#pragma unroll
+      for (int u = 0; u < UNR; ++u)
+        if (v0 + 32 * u < nvec) val[u] = ld_stream(x + (size_t)t * nvec + v0 + 32 * u);
+      for (int j = 0; j < p.k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, rl, j);
+        if (r < 0) continue;
+#pragma unroll
+        for (int u = 0; u < UNR; ++u)
+          if (v0 + 32 * u < nvec) st_stream(X + (size_t)r * nvec + v0 + 32 * u, val[u]);
+      }
+    }
+  }
+  if (p.capacity > 0) {
+    const long long E = (long long)p.e * p.capacity;
+    for (long long rr = gw; rr < E; rr += warps) {
+      const int xe = (int)(rr / p.capacity);
+      const int slot = (int)(rr - (long long)xe * p.capacity);
+      if (slot < __ldg(p.counts + xe)) continue;
+      for (int v = lane; v < nvec; v += 32) st_stream(X + (size_t)rr * nvec + v, make_uint4(0, 0, 0, 0));
+    }
+  }
+}
+#endif
+
 struct Config {
   int piece, npieces, stages, stride, smem, ctas_per_sm;
 };
 
 Config choose(long long row_bytes, const DeviceInfo& di) {
   Config c;
-  const long long kPieceMax = 16384;
+  const long long kPieceMax = MOE_DSP_PIECE;
   c.npieces = (int)((row_bytes + kPieceMax - 1) / kPieceMax);
   long long piece = (row_bytes + c.npieces - 1) / c.npieces;
   piece = (piece + 15) / 16 * 16;
   c.piece = (int)piece;
   c.stride = (int)((piece + 127) / 128 * 128);
-  c.stages = 4;
+  c.stages = MOE_DSP_STAGES;
   c.smem = c.stages * c.stride;
   int n = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dispatch_kernel, 32, c.smem);
-  c.ctas_per_sm = n < 1 ? 1 : (n > 16 ? 16 : n);
+  c.ctas_per_sm = n < 1 ? 1 : (n > MOE_DSP_MAX_CTAS ? MOE_DSP_MAX_CTAS : n);
   return c;
 }
 
@@ -260,9 +321,15 @@ cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, int s, in
   long long grid = (long long)di.sms * c.ctas_per_sm;
   if (grid > work) grid = work;
   if (grid < 1) grid = 1;
-  (void)cudaGetLastError();  // clear a stale error left by an earlier, unrelated call
-  dispatch_kernel<<<(int)grid, 32, c.smem, st>>>(p);
-  return cudaGetLastError();
+#if MOE_DSP_LDG
+  {
+    int bps = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, dispatch_ldg_kernel<MOE_DSP_LDG>, 256, 0);
+    return launch_pdl(MOE_KERNEL_DISPATCH, dispatch_ldg_kernel<MOE_DSP_LDG>, dim3(di.sms * (bps > 0 ? bps : 1)), dim3(256), 0,
+                      st, p);
+  }
+#endif
+  return launch_pdl(MOE_KERNEL_DISPATCH, dispatch_kernel, dim3((unsigned)grid), dim3(32), (size_t)c.smem, st, p);
 }
 
 }  // namespace moe

@@ -8,9 +8,11 @@
 // exactly as the forward did, so selection is a pure comparison on the
 // logits (no exp rounding can change it) with a fixed tie-break.
 //
-// Each lane holds the logits of experts lane, lane+32, ... (EPL per lane).
-// k rounds of a warp arg-max on (value desc, index asc) select the experts;
-// lane r keeps round r's winner.  The softmax max is round 0's value; the
+// Each lane holds the logits of experts lane, lane+32, ... (EPL per lane) as
+// order-preserving 32-bit keys, sorted within the lane.  Each of the k rounds
+// is two warp reductions (redux.sync): the largest head key, then the lowest
+// expert id among the lanes holding it; that lane pops its head, and lane r
+// keeps round r's winner.  The softmax max is round 0's value; the
 // denominator is a butterfly sum, so every lane sees the same bits.
 #include <math.h>
 
@@ -21,8 +23,15 @@ namespace moe {
 
 namespace {
 
-__device__ __forceinline__ bool before(float av, int ai, float bv, int bi) {
-  return av > bv || (av == bv && ai < bi);
+// Order-preserving 32-bit key of a float: a larger value gets a larger key,
+// and -0.0 and +0.0 get the same key (adding +0.0 turns -0.0 into +0.0).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
 template <int EPL>
@@ -33,51 +42,67 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float* __restrict_
                                                         int32_t* status) {
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
+  grid_dependency_wait();
+  pdl_trigger_early();
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < s; t += warps) {
     const float* l = logits + (size_t)t * e;
-    float v[EPL];
+    // this lane's candidates, experts lane + 32*i; key 0 marks padding (below -inf)
+    uint32_t key[EPL];
+    int id[EPL];
     bool bad = false;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int j = lane + 32 * i;
-      v[i] = j < e ? __ldg(l + j) : -INFINITY;  // padding is never selected: k <= e
-      if (j < e && !isfinite(v[i])) bad = true;
+      const float v = j < e ? __ldg(l + j) : 0.0f;
+      if (j < e && !isfinite(v)) bad = true;
+      key[i] = j < e ? order_key(v) : 0u;
+      id[i] = j;
     }
-    if (__any_sync(0xffffffffu, bad)) {
-      if (lane == 0) raise_status(status, MOE_DEV_NONFINITE);
-    }
-
-    unsigned taken = 0;
-    float sel_v = -INFINITY;  // lane r < k: the r-th selected logit
-    int sel_i = 0;
-    float top = 0.f;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_status(status, MOE_DEV_NONFINITE);
+    // stable sort of the lane's candidates, largest key first (equal keys keep
+    // their ascending expert order)
+#pragma unroll
+    for (int a = 0; a < EPL; ++a)
+#pragma unroll
+      for (int b = EPL - 1; b > a; --b)
+        if (key[b] > key[b - 1]) {
+          const uint32_t tk = key[b];
+          key[b] = key[b - 1];
+          key[b - 1] = tk;
+          const int ti = id[b];
+          id[b] = id[b - 1];
+          id[b - 1] = ti;
+        }
+    // the lane's values, kept for the full-softmax sum before the selection
+    // consumes them; the first `nvalid` sorted entries are real experts
+    const int nvalid = min(EPL, max(0, (e - lane + 31) / 32));
+    float all_v[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) all_v[i] = key_value(key[i]);
+    uint32_t top_key = 0;
+    uint32_t sel_key = 0;
+    int sel_id = 0;
+    // k rounds: the warp's largest head key, ties to the lower expert id
     for (int r = 0; r < k; ++r) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
+      const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
+      const uint32_t cand = key[0] == m ? (uint32_t)id[0] : 0xffffffffu;
+      const uint32_t j = __reduce_min_sync(0xffffffffu, cand);
+      if (key[0] == m && (uint32_t)id[0] == j) {  // the winner pops its head
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int j = lane + 32 * i;
-        if (!((taken >> i) & 1u) && before(v[i], j, bv, bi)) {
-          bv = v[i];
-          bi = j;
+        for (int i = 0; i + 1 < EPL; ++i) {
+          key[i] = key[i + 1];
+          id[i] = id[i + 1];
         }
+        key[EPL - 1] = 0u;
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (before(ov, oi, bv, bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane && bi < 32 * EPL) taken |= 1u << (bi >> 5);
       if (lane == r) {
-        sel_v = bv;
-        sel_i = bi;
+        sel_key = m;
+        sel_id = (int)j;
       }
-      if (r == 0) top = bv;
+      if (r == 0) top_key = m;
     }
+    const float top = key_value(top_key);
+    const float sel_v = key_value(sel_key);
 
     float z = 0.f;
     if (renorm) {
@@ -85,16 +110,17 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float* __restrict_
     } else {
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
-        if (lane + 32 * i < e) z += expf(v[i] - top);
+        if (i < nvalid) z += expf(all_v[i] - top);
     }
     float den = z;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
     if (lane < k) {
-      idx[(size_t)t * k + lane] = sel_i;
+      idx[(size_t)t * k + lane] = sel_id;
       gate[(size_t)t * k + lane] = expf(sel_v - top) / den;
     }
   }
+  pdl_trigger_late();
 }
 
 template <int EPL>
@@ -105,9 +131,8 @@ cudaError_t launch_epl(const float* logits, int s, int e, int k, int renorm, int
   const long long cap = (long long)di.sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  (void)cudaGetLastError();  // clear a stale error left by an earlier, unrelated call
-  topk_gate_kernel<EPL><<<(int)blocks, threads, 0, st>>>(logits, s, e, k, renorm, idx, gate, status);
-  return cudaGetLastError();
+  return launch_pdl(MOE_KERNEL_TOPK_GATE, topk_gate_kernel<EPL>, dim3((unsigned)blocks), dim3(threads), 0, st, logits, s, e,
+                    k, renorm, idx, gate, status);
 }
 
 }  // namespace

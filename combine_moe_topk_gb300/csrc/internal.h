@@ -24,7 +24,9 @@ struct LayoutPlan {
   int tiles = 1;            // CTAs (all co-resident: cooperative launch)
   int subtiles_per_tile = 1;
 };
-LayoutPlan plan_layout(int s, const DeviceInfo& di);
+LayoutPlan plan_layout(int s, int e, const DeviceInfo& di);
+size_t lookback_bytes(const LayoutPlan& plan, int e);  // scratch the plan's look-back needs
+int layout_blocks_per_sm();                            // co-resident layout CTAs per SM
 
 struct LayoutOut {
   int32_t* idx;
@@ -36,7 +38,7 @@ struct LayoutOut {
   int32_t* offsets;
   uint8_t* token_in_rank;
   int32_t* rank_counts;
-  unsigned long long* lookback;  // [tiles][e], zero before the launch
+  unsigned* lookback;            // [tiles][e rounded up to 4], zero before the launch
   int32_t* status;
 };
 

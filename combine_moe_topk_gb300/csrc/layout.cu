@@ -17,11 +17,14 @@
 // processed as sub-tiles of 256 tokens (thread = token).
 //   A. histogram: per-expert route count of the tile in shared memory
 //      (integer atomics: the total does not depend on their order);
-//   B. decoupled look-back over tiles, one thread per expert: publish the
-//      tile aggregate, walk back to the nearest inclusive prefix, publish
-//      the tile's inclusive prefix.  Flag and value share one 64-bit word.
-//      The last tile's inclusive prefixes are the global expert totals;
-//      dropless mode waits for them to form the row offsets;
+//   B. decoupled look-back over tiles: each tile publishes its aggregate
+//      (flag and value in one 64-bit word) as soon as its histogram is done,
+//      then reads the aggregates of all its predecessors at once -- groups of
+//      threads per expert, eight independent loads in flight each -- instead
+//      of walking back one tile at a time, so the look-back costs a few L2
+//      round trips whatever the tile count.  The same pass over all tiles
+//      gives the global expert totals, which dropless rows need everywhere
+//      and the last tile writes out;
 //   C. slots: per sub-tile, each warp builds a 32-bit token mask per expert
 //      (atomicOr: order-free), so a route's rank among the warp's tokens is
 //      popc(mask & lanes-below); warps are scanned in order per expert.
@@ -44,8 +47,15 @@ constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
 constexpr int kMaxR = 64;
 
-constexpr unsigned long long kFlagAgg = 1ull << 32;
-constexpr unsigned long long kFlagPrefix = 2ull << 32;
+// Look-back word: the published flag in bit 31, the tile's route count for
+// one expert in bits 0-30 (a count never exceeds s < 2^31).  Rows of e
+// words are padded to a multiple of four so they can be read as 16-byte
+// vectors.
+constexpr unsigned kPublished = 0x80000000u;
+constexpr int kLookbackLoads = 8;        // 16-byte look-back loads in flight per thread
+constexpr int kMaxLookbackWords = 16384;  // tiles * padded e, at most: bounds the look-back reads
+
+__host__ __device__ inline int padded_e(int e) { return (e + 3) & ~3; }
 
 struct Params {
   const int32_t* topk_idx;
@@ -56,15 +66,56 @@ struct Params {
   long long timeout_ns;
 };
 
-// Load token t's k expert ids and mark which routes are valid: in range and
-// not a repeat of an earlier route of the same token.
+__device__ __forceinline__ uint4 ld_relaxed_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u32(unsigned* p, unsigned v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ bool all_published(const uint4& w) {
+  return (w.x & w.y & w.z & w.w & kPublished) != 0;
+}
+
+// Load token t's k expert ids (16- or 8-byte loads when k allows) and mark
+// which routes are valid: in range and not a repeat of an earlier route of
+// the same token.
 __device__ __forceinline__ unsigned load_routes(const Params& p, int t, int* xs) {
+  const int32_t* src = p.topk_idx + (size_t)t * p.k;
+  if ((p.k & 3) == 0) {
+#pragma unroll
+    for (int j4 = 0; j4 < kMaxK / 4; ++j4)
+      if (4 * j4 < p.k) {
+        const int4 v = __ldg(reinterpret_cast<const int4*>(src) + j4);
+        xs[4 * j4] = v.x;
+        xs[4 * j4 + 1] = v.y;
+        xs[4 * j4 + 2] = v.z;
+        xs[4 * j4 + 3] = v.w;
+      }
+  } else if ((p.k & 1) == 0) {
+#pragma unroll
+    for (int j2 = 0; j2 < kMaxK / 2; ++j2)
+      if (2 * j2 < p.k) {
+        const int2 v = __ldg(reinterpret_cast<const int2*>(src) + j2);
+        xs[2 * j2] = v.x;
+        xs[2 * j2 + 1] = v.y;
+      }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < p.k) xs[j] = __ldg(src + j);
+  }
   unsigned valid = 0;
 #pragma unroll
   for (int j = 0; j < kMaxK; ++j) {
     if (j < p.k) {
-      const int x = __ldg(p.topk_idx + (size_t)t * p.k + j);
-      xs[j] = x;
+      const int x = xs[j];
       bool ok = x >= 0 && x < p.e;
 #pragma unroll
       for (int jj = 0; jj < j; ++jj)
@@ -75,36 +126,225 @@ __device__ __forceinline__ unsigned load_routes(const Params& p, int t, int* xs)
   return valid;
 }
 
-// Spin (bounded) until the look-back word carries a flag (any flag, or the
-// inclusive-prefix flag when `want_prefix`).  Returns the word, or 0 with
-// *timed_out set once the deadline has passed; after a time-out every later
-// wait of this thread returns at once.
-__device__ __forceinline__ unsigned long long wait_word(const unsigned long long* w,
-                                                        bool want_prefix, uint64_t deadline,
-                                                        bool* timed_out) {
-  if (*timed_out) return 0;
-  unsigned long long v = ld_relaxed_u64(w);
-  for (uint32_t it = 0;; ++it) {
-    const unsigned long long flag = v & ~0xffffffffull;
-    if (want_prefix ? flag == kFlagPrefix : flag != 0) return v;
-    __nanosleep(64);
-    if ((it & 15) == 15 && globaltimer_ns() > deadline) {
-      *timed_out = true;
-      return 0;
+// Set bit `lane` of the warp's token mask of every valid route's expert.
+__device__ __forceinline__ void mark_routes(const Params& p, unsigned (*mask)[kMaxE], int warp,
+                                            int lane, const int* xs, unsigned valid) {
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j)
+    if ((valid >> j) & 1u) atomicOr(&mask[warp][xs[j]], 1u << lane);
+}
+
+// Decoupled look-back with a full-width window.  Publishes this tile's
+// aggregate row, then reads the rows of tiles [0, nread) -- each thread a
+// column of four experts over a strided set of tiles, eight 16-byte loads in
+// flight -- and adds them up: s_excl[x] gets the routes of tiles before this
+// one, s_tot[x] (which holds this tile's own aggregate on entry) the routes
+// of every tile read.  Waits are bounded; a time-out sets *timed_out and the
+// missing rows count as empty.
+__device__ void lookback(const Params& p, int tile, int nread, const int* s_agg, int* s_excl,
+                         int* s_tot, uint64_t deadline, bool* timed_out) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int e4 = padded_e(p.e);
+  unsigned* rows = reinterpret_cast<unsigned*>(p.out.lookback);
+  if (tile != p.hold_tile)
+    for (int x = tid; x < e4; x += kThreads)
+      st_relaxed_u32(rows + (size_t)tile * e4 + x, kPublished | (unsigned)(x < p.e ? s_agg[x] : 0));
+
+  const int quads = e4 / 4;
+  const int groups = kThreads / quads;  // threads (g, q) read tiles g, g + groups, ...
+  const int g = tid / quads, q = tid - (tid / quads) * quads;
+  unsigned ex[4] = {0, 0, 0, 0}, tot[4] = {0, 0, 0, 0};
+  if (g < groups) {
+    const uint4* col = reinterpret_cast<const uint4*>(rows) + q;  // row b at col[b * quads]
+    for (int b0 = g; b0 < nread; b0 += groups * kLookbackLoads) {
+      uint4 w[kLookbackLoads];
+#pragma unroll
+      for (int u = 0; u < kLookbackLoads; ++u) {
+        const int b = b0 + groups * u;
+        w[u] = (b < nread && b != tile) ? ld_relaxed_v4(col + (size_t)b * quads)
+                                         : make_uint4(kPublished, kPublished, kPublished, kPublished);
+      }
+#pragma unroll
+      for (int u = 0; u < kLookbackLoads; ++u) {
+        const int b = b0 + groups * u;
+        if (b >= nread || b == tile) continue;
+        for (uint32_t it = 0; !all_published(w[u]) && !*timed_out; ++it) {
+          __nanosleep(32);
+          if ((it & 15) == 15 && globaltimer_ns() > deadline) *timed_out = true;
+          w[u] = ld_relaxed_v4(col + (size_t)b * quads);
+        }
+        if (*timed_out && !all_published(w[u])) continue;
+        const unsigned v[4] = {w[u].x & ~kPublished, w[u].y & ~kPublished, w[u].z & ~kPublished,
+                               w[u].w & ~kPublished};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tot[c] += v[c];
+          if (b < tile) ex[c] += v[c];
+        }
+      }
     }
-    v = ld_relaxed_u64(w);
+  }
+  // sum the lanes of the warp that read the same column (xor shuffles, when
+  // the column count is a power of two), then shared atomics per column
+  bool leader = g < groups;
+  if (quads < 32 && (quads & (quads - 1)) == 0) {
+    for (int off = quads; off < 32; off <<= 1)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        ex[c] += __shfl_xor_sync(0xffffffffu, ex[c], off);
+        tot[c] += __shfl_xor_sync(0xffffffffu, tot[c], off);
+      }
+    leader = lane < quads;
+  }
+  if (leader) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int x = 4 * q + c;
+      if (x < p.e) {
+        atomicAdd(&s_excl[x], (int)ex[c]);
+        atomicAdd(&s_tot[x], (int)tot[c]);
+      }
+    }
   }
 }
 
+// Per-expert exclusive scan of the counts (e <= 256: eight per lane of warp
+// 0, then a warp scan) into s_off[0..e]; the tile that holds the totals of
+// record also writes raw_counts, counts and offsets to the handle.
+__device__ void expert_offsets(const Params& p, const int* s_tot, int* s_off, bool write_out) {
+  const int lane = threadIdx.x & 31;
+  if ((threadIdx.x >> 5) != 0) return;
+  int raw[8], v[8];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int x = lane * 8 + i;
+    raw[i] = x < p.e ? s_tot[x] : 0;
+    v[i] = p.capacity > 0 ? min(raw[i], p.capacity) : raw[i];
+    sum += v[i];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  int run = incl - sum;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int x = lane * 8 + i;
+    if (x < p.e) {
+      const int off = p.capacity > 0 ? x * p.capacity : run;
+      s_off[x] = off;
+      if (write_out) {
+        p.out.raw_counts[x] = raw[i];
+        p.out.counts[x] = v[i];
+        p.out.offsets[x] = off;
+      }
+    }
+    run += v[i];
+  }
+  if (lane == 31) {
+    const int end = p.capacity > 0 ? p.e * p.capacity : run;
+    s_off[p.e] = end;
+    if (write_out) p.out.offsets[p.e] = end;
+  }
+}
+
+// Store k int32 values of one token (16- or 8-byte stores when k allows).
+__device__ __forceinline__ void store_route_ints(int32_t* dst, const int* v, int k) {
+  if ((k & 3) == 0) {
+#pragma unroll
+    for (int j4 = 0; j4 < kMaxK / 4; ++j4)
+      if (4 * j4 < k)
+        reinterpret_cast<int4*>(dst)[j4] = make_int4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+  } else if ((k & 1) == 0) {
+#pragma unroll
+    for (int j2 = 0; j2 < kMaxK / 2; ++j2)
+      if (2 * j2 < k) reinterpret_cast<int2*>(dst)[j2] = make_int2(v[2 * j2], v[2 * j2 + 1]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < k) dst[j] = v[j];
+  }
+}
+
+// Write one token's routes: token-order slot, row, drop flag, and its
+// virtual-rank set.  base[x] is the slot of this warp's first token routed
+// to x; mask[x] the warp's token mask for x.  Returns the token's rank set.
+__device__ __forceinline__ unsigned long long write_routes(const Params& p, int t, int lane,
+                                                           const int* xs, unsigned valid,
+                                                           const int* base, const unsigned* mask,
+                                                           const int* s_off) {
+  const unsigned below = (1u << lane) - 1u;
+  const int per_rank = p.R > 0 ? p.e / p.R : 1;
+  unsigned long long ranks = 0;
+  int loc[kMaxK], row[kMaxK];
+  uint32_t dropw[kMaxK / 4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    loc[j] = -1;
+    row[j] = -1;
+    if (j < p.k && ((valid >> j) & 1u)) {
+      const int x = xs[j];
+      const int l = base[x] + __popc(mask[x] & below);
+      loc[j] = l;
+      if (p.capacity > 0) {
+        if (l < p.capacity) row[j] = x * p.capacity + l;
+      } else {
+        row[j] = s_off[x] + l;
+      }
+      if (row[j] >= 0) ranks |= 1ull << (x / per_rank);
+    }
+    if (row[j] < 0) dropw[j / 4] |= 1u << (8 * (j % 4));
+  }
+  store_route_ints(p.out.loc + (size_t)t * p.k, loc, p.k);
+  store_route_ints(p.out.row + (size_t)t * p.k, row, p.k);
+  uint8_t* dr = p.out.drop + (size_t)t * p.k;
+  if ((p.k & 3) == 0) {
+#pragma unroll
+    for (int j4 = 0; j4 < kMaxK / 4; ++j4)
+      if (4 * j4 < p.k) reinterpret_cast<uint32_t*>(dr)[j4] = dropw[j4];
+  } else {
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < p.k) dr[j] = (uint8_t)((dropw[j / 4] >> (8 * (j % 4))) & 0xffu);
+  }
+  if (p.R > 0) {
+    uint8_t* tir = p.out.token_in_rank + (size_t)t * p.R;
+    for (int r = 0; r < p.R; ++r) tir[r] = (uint8_t)((ranks >> r) & 1ull);
+  }
+  return ranks;
+}
+
+// Add the warp's rank sets into the per-rank token counts: one ballot per
+// rank that any lane of the warp sends to.
+__device__ __forceinline__ void count_ranks(unsigned long long ranks, int lane, int* s_rank) {
+  const unsigned lo = __reduce_or_sync(0xffffffffu, (unsigned)ranks);
+  const unsigned hi = __reduce_or_sync(0xffffffffu, (unsigned)(ranks >> 32));
+  unsigned long long any = ((unsigned long long)hi << 32) | lo;
+  while (any) {
+    const int r = __ffsll((long long)any) - 1;
+    any &= any - 1;
+    const int n = __popc(__ballot_sync(0xffffffffu, (ranks >> r) & 1ull));
+    if (lane == 0) atomicAdd(&s_rank[r], n);
+  }
+}
+
+// One CTA per tile; TPT > 0: the tile is exactly TPT sub-tiles and each
+// thread keeps its TPT tokens' routes in registers from the histogram to the
+// slot pass; TPT == 0: any number of sub-tiles, routes reloaded per pass.
+template <int TPT>
 __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
-  __shared__ int s_agg[kMaxE];       // tile aggregate per expert
-  __shared__ int s_run[kMaxE];       // running slot base per expert
-  __shared__ int s_off[kMaxE + 1];   // dropless row offsets
-  __shared__ unsigned s_mask[kWarps][kMaxE];
-  __shared__ int s_wbase[kWarps][kMaxE];
+  constexpr int NM = TPT > 0 ? TPT : 1;
+  __shared__ unsigned s_mask[NM][kWarps][kMaxE];
+  __shared__ int s_wbase[NM][kWarps][kMaxE];
+  __shared__ int s_agg[kMaxE];
+  __shared__ int s_excl[kMaxE];
+  __shared__ int s_tot[kMaxE];
+  __shared__ int s_off[kMaxE + 1];
   __shared__ int s_rank[kMaxR];
-  __shared__ int s_bad;
-  __shared__ int s_timeout;
+  __shared__ int s_flags;  // bit 0: a bad route; bit 1: a wait timed out
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x;
@@ -113,198 +353,156 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   const int sub1 = min(nsub, sub0 + p.subtiles_per_tile);
   const uint64_t deadline = globaltimer_ns() + (uint64_t)p.timeout_ns;
 
-  for (int x = tid; x < kMaxE; x += kThreads) s_agg[x] = 0;
+  grid_dependency_wait();
+  pdl_trigger_early();
+  for (int i = tid; i < NM * kWarps * kMaxE; i += kThreads) (&s_mask[0][0][0])[i] = 0u;
+  for (int x = tid; x < kMaxE; x += kThreads) {
+    s_agg[x] = 0;
+    s_excl[x] = 0;
+  }
   if (tid < kMaxR) s_rank[tid] = 0;
-  if (tid == 0) {
-    s_bad = 0;
-    s_timeout = 0;
-  }
+  if (tid == 0) s_flags = 0;
   __syncthreads();
 
-  // ---- A: histogram of the tile, and the handle's copy of the ids --------
-  int bad = 0;
-  for (int sb = sub0; sb < sub1; ++sb) {
-    const int t = sb * kThreads + tid;
-    if (t < p.s) {
-      int xs[kMaxK];
-      const unsigned valid = load_routes(p, t, xs);
+  // ---- A: token masks and the tile histogram -------------------------------
+  int xs[NM][kMaxK];
+  unsigned valid[NM];
+  bool bad = false;
+  if (TPT > 0) {
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j < p.k) {
-          p.out.idx[(size_t)t * p.k + j] = xs[j];
-          if ((valid >> j) & 1u)
-            atomicAdd(&s_agg[xs[j]], 1);
-          else
-            bad = 1;
-        }
+    for (int r = 0; r < NM; ++r) {
+      const int t = (sub0 + r) * kThreads + tid;
+      valid[r] = 0;
+      if (sub0 + r < sub1 && t < p.s) {
+        valid[r] = load_routes(p, t, xs[r]);
+        bad |= valid[r] != (1u << p.k) - 1u;
+        store_route_ints(p.out.idx + (size_t)t * p.k, xs[r], p.k);
+        mark_routes(p, s_mask[r], warp, lane, xs[r], valid[r]);
       }
     }
+    __syncthreads();
+    for (int x = tid; x < p.e; x += kThreads) {
+      int run = 0;
+#pragma unroll
+      for (int r = 0; r < NM; ++r)
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          s_wbase[r][w][x] = run;
+          run += __popc(s_mask[r][w][x]);
+        }
+      s_agg[x] = run;
+    }
+  } else {
+    for (int sb = sub0; sb < sub1; ++sb) {
+      const int t = sb * kThreads + tid;
+      int ys[kMaxK];
+      unsigned vy = 0;
+      if (t < p.s) {
+        vy = load_routes(p, t, ys);
+        bad |= vy != (1u << p.k) - 1u;
+        store_route_ints(p.out.idx + (size_t)t * p.k, ys, p.k);
+        mark_routes(p, s_mask[0], warp, lane, ys, vy);
+      }
+      __syncthreads();
+      for (int x = tid; x < p.e; x += kThreads) {
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) c += __popc(s_mask[0][w][x]);
+        s_agg[x] += c;
+      }
+      __syncthreads();
+      for (int i = tid; i < kWarps * kMaxE; i += kThreads) (&s_mask[0][0][0])[i] = 0u;
+      __syncthreads();
+    }
   }
-  if (bad) s_bad = 1;
+  if (bad) atomicOr(&s_flags, 1);
+  __syncthreads();
+  for (int x = tid; x < p.e; x += kThreads) s_tot[x] = s_agg[x];
   __syncthreads();
 
-  // ---- B: decoupled look-back over tiles, one thread per expert ----------
-  bool timed_out = false;
-  for (int x = tid; x < p.e; x += kThreads) {
-    const int agg = s_agg[x];
-    unsigned long long* col = p.out.lookback + x;  // word of tile b is col[b * e]
-    const bool publish = tile != p.hold_tile;
-    if (publish)
-      st_relaxed_u64(col + (size_t)tile * p.e,
-                     (tile == 0 ? kFlagPrefix : kFlagAgg) | (unsigned)agg);
-    int excl = 0;
-    for (int b = tile - 1; b >= 0; --b) {
-      const unsigned long long w = wait_word(col + (size_t)b * p.e, false, deadline, &timed_out);
-      if (timed_out) break;
-      excl += (int)(unsigned)w;
-      if ((w & ~0xffffffffull) == kFlagPrefix) break;
-    }
-    if (publish && tile > 0)
-      st_relaxed_u64(col + (size_t)tile * p.e, kFlagPrefix | (unsigned)(excl + agg));
-    s_run[x] = excl;
-
-    // global totals = inclusive prefix of the last tile (dropless rows need
-    // them in every tile; capacity mode only in the last tile, which has them)
-    int total = excl + agg;
-    if (p.capacity == 0 && tile != p.tiles - 1) {
-      const unsigned long long w =
-          wait_word(col + (size_t)(p.tiles - 1) * p.e, true, deadline, &timed_out);
-      total = (int)(unsigned)w;
-    }
-    s_off[x] = total;  // holds totals until the scan below
-  }
-  if (timed_out) s_timeout = 1;
-  __syncthreads();
-
-  // totals -> counts, offsets (every tile in dropless mode; the last tile
-  // alone also writes them to the handle)
+  // ---- B: look-back over every earlier tile (all tiles when totals are needed)
   const bool last = tile == p.tiles - 1;
+  const int nread = (p.capacity == 0 || last) ? p.tiles : tile;
+  bool timed_out = false;
+  lookback(p, tile, nread, s_agg, s_excl, s_tot, deadline, &timed_out);
+  if (timed_out) atomicOr(&s_flags, 2);
+  __syncthreads();
   if (p.capacity == 0 || last) {
-    if (warp == 0) {
-      // exclusive scan of e <= 256 counts: 8 per lane, then a warp scan
-      int v[8];
-      int sum = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int x = lane * 8 + i;
-        int c = x < p.e ? s_off[x] : 0;
-        if (p.capacity > 0) c = min(c, p.capacity);
-        v[i] = c;
-        sum += c;
-      }
-      int incl = sum;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-      }
-      int run = incl - sum;
-      int raw[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) raw[i] = (lane * 8 + i) < p.e ? s_off[lane * 8 + i] : 0;
-      __syncwarp();
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int x = lane * 8 + i;
-        if (x < p.e) {
-          const int off = p.capacity > 0 ? x * p.capacity : run;
-          s_off[x] = off;
-          if (last) {
-            p.out.raw_counts[x] = raw[i];
-            p.out.counts[x] = v[i];
-            p.out.offsets[x] = off;
-          }
-        }
-        run += v[i];
-      }
-      if (lane == 31) {
-        const int end = p.capacity > 0 ? p.e * p.capacity : run;
-        s_off[p.e] = end;
-        if (last) p.out.offsets[p.e] = end;
-      }
-    }
+    expert_offsets(p, s_tot, s_off, last);
     __syncthreads();
   }
 
   // ---- C: token-order slots, rows, drops, dedup ----------------------------
-  const int per_rank = p.R > 0 ? p.e / p.R : 1;
-  for (int sb = sub0; sb < sub1; ++sb) {
-    for (int i = tid; i < kWarps * kMaxE; i += kThreads) (&s_mask[0][0])[i] = 0u;
-    __syncthreads();
-    const int t = sb * kThreads + tid;
-    int xs[kMaxK];
-    unsigned valid = 0;
-    if (t < p.s) {
-      valid = load_routes(p, t, xs);
+  if (TPT > 0) {
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
-        if ((valid >> j) & 1u) atomicOr(&s_mask[warp][xs[j]], 1u << lane);
+    for (int r = 0; r < NM; ++r) {
+      for (int x = tid; x < p.e; x += kThreads)
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s_wbase[r][w][x] += s_excl[x];
     }
     __syncthreads();
-    for (int x = tid; x < p.e; x += kThreads) {
-      int run = s_run[x];
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        s_wbase[w][x] = run;
-        run += __popc(s_mask[w][x]);
-      }
-      s_run[x] = run;
-    }
-    __syncthreads();
-    if (t < p.s) {
-      const unsigned below = (1u << lane) - 1u;
+    for (int r = 0; r < NM; ++r) {
+      const int t = (sub0 + r) * kThreads + tid;
       unsigned long long ranks = 0;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j < p.k) {
-          const size_t q = (size_t)t * p.k + j;
-          int loc = -1, row = -1;
-          uint8_t drop = 1;
-          if ((valid >> j) & 1u) {
-            const int x = xs[j];
-            loc = s_wbase[warp][x] + __popc(s_mask[warp][x] & below);
-            if (p.capacity > 0) {
-              drop = loc >= p.capacity;
-              row = drop ? -1 : x * p.capacity + loc;
-            } else {
-              drop = 0;
-              row = s_off[x] + loc;
-            }
-            if (!drop) ranks |= 1ull << (x / per_rank);
-          }
-          p.out.loc[q] = loc;
-          p.out.row[q] = row;
-          p.out.drop[q] = drop;
-        }
-      }
-      if (p.R > 0) {
-        uint8_t* tir = p.out.token_in_rank + (size_t)t * p.R;
-        for (int r = 0; r < p.R; ++r) tir[r] = (uint8_t)((ranks >> r) & 1ull);
-        while (ranks) {
-          const int r = __ffsll((long long)ranks) - 1;
-          ranks &= ranks - 1;
-          atomicAdd(&s_rank[r], 1);
-        }
-      }
+      if (sub0 + r < sub1 && t < p.s)
+        ranks = write_routes(p, t, lane, xs[r], valid[r], s_wbase[r][warp], s_mask[r][warp], s_off);
+      if (p.R > 0) count_ranks(ranks, lane, s_rank);
     }
+  } else {
+    for (int x = tid; x < p.e; x += kThreads) s_agg[x] = s_excl[x];  // running base per expert
     __syncthreads();
+    for (int sb = sub0; sb < sub1; ++sb) {
+      const int t = sb * kThreads + tid;
+      int ys[kMaxK];
+      unsigned vy = 0;
+      if (t < p.s) {
+        vy = load_routes(p, t, ys);
+        mark_routes(p, s_mask[0], warp, lane, ys, vy);
+      }
+      __syncthreads();
+      for (int x = tid; x < p.e; x += kThreads) {
+        int run = s_agg[x];
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          s_wbase[0][w][x] = run;
+          run += __popc(s_mask[0][w][x]);
+        }
+        s_agg[x] = run;
+      }
+      __syncthreads();
+      unsigned long long ranks = 0;
+      if (t < p.s) ranks = write_routes(p, t, lane, ys, vy, s_wbase[0][warp], s_mask[0][warp], s_off);
+      if (p.R > 0) count_ranks(ranks, lane, s_rank);
+      __syncthreads();
+      for (int i = tid; i < kWarps * kMaxE; i += kThreads) (&s_mask[0][0][0])[i] = 0u;
+      __syncthreads();
+    }
   }
-
+  __syncthreads();
+  pdl_trigger_late();
   if (p.R > 0 && tid < p.R && s_rank[tid]) atomicAdd(&p.out.rank_counts[tid], s_rank[tid]);
-  if (tid == 0) {
+  if (tid == 0 && s_flags) {
     int bits = 0;
-    if (s_bad) bits |= MOE_DEV_BAD_ROUTE;
-    if (s_timeout) bits |= MOE_DEV_TIMEOUT;
-    if (bits) raise_status(p.out.status, bits);
+    if (s_flags & 1) bits |= MOE_DEV_BAD_ROUTE;
+    if (s_flags & 2) bits |= MOE_DEV_TIMEOUT;
+    raise_status(p.out.status, bits);
   }
+}
+
+int blocks_per_sm(const void* kern) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, 0) != cudaSuccess) return 0;
+  return n;
 }
 
 }  // namespace
 
-LayoutPlan plan_layout(int s, const DeviceInfo& di) {
+LayoutPlan plan_layout(int s, int e, const DeviceInfo& di) {
   LayoutPlan plan;
   const int nsub = s > 0 ? (s + kThreads - 1) / kThreads : 1;
-  const int max_tiles = di.sms * (di.layout_blocks_per_sm > 0 ? di.layout_blocks_per_sm : 1);
+  int max_tiles = di.sms * (di.layout_blocks_per_sm > 0 ? di.layout_blocks_per_sm : 1);
+  if (max_tiles > kMaxLookbackWords / padded_e(e)) max_tiles = kMaxLookbackWords / padded_e(e);
   plan.subtiles_per_tile = (nsub + max_tiles - 1) / max_tiles;
   if (plan.subtiles_per_tile < 1) plan.subtiles_per_tile = 1;
   plan.tiles = (nsub + plan.subtiles_per_tile - 1) / plan.subtiles_per_tile;
@@ -312,11 +510,17 @@ LayoutPlan plan_layout(int s, const DeviceInfo& di) {
   return plan;
 }
 
+size_t lookback_bytes(const LayoutPlan& plan, int e) {
+  return sizeof(unsigned) * (size_t)plan.tiles * (size_t)padded_e(e);
+}
+
+// The fewest co-resident blocks per SM over the kernel variants, so that a
+// plan fits whichever variant runs it.
 int layout_blocks_per_sm() {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, layout_kernel, kThreads, 0) != cudaSuccess)
-    return 0;
-  return n;
+  int a = blocks_per_sm((const void*)layout_kernel<0>);
+  int b = blocks_per_sm((const void*)layout_kernel<1>);
+  int c = blocks_per_sm((const void*)layout_kernel<2>);
+  return a < b ? (a < c ? a : c) : (b < c ? b : c);
 }
 
 cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity, int R,
@@ -345,7 +549,9 @@ cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capa
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, layout_kernel, p);
+  if (plan.subtiles_per_tile == 1) return cudaLaunchKernelEx(&cfg, layout_kernel<1>, p);
+  if (plan.subtiles_per_tile == 2) return cudaLaunchKernelEx(&cfg, layout_kernel<2>, p);
+  return cudaLaunchKernelEx(&cfg, layout_kernel<0>, p);
 }
 
 }  // namespace moe
@@ -368,16 +574,18 @@ cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capa
 // ---------------------------------------------------------------------------
 namespace moe {
 
-constexpr int kNoAllocLookbackWords = 65536;  // 512 KB: tiles * e must fit
+// 64 KB: the tile plan never needs more than kMaxLookbackWords words; the
+// launcher still refuses a plan that would not fit.
+constexpr int kNoAllocLookbackWords = kMaxLookbackWords;
 
-static __device__ __align__(256) unsigned long long g_noalloc_lookback[kNoAllocLookbackWords];
+static __device__ __align__(256) unsigned g_noalloc_lookback[kNoAllocLookbackWords];
 
 namespace {
 
 struct NoAllocSetup {
   std::once_flag once;
   cudaError_t err = cudaSuccess;
-  unsigned long long* scratch = nullptr;  // device address of g_noalloc_lookback
+  unsigned* scratch = nullptr;  // device address of g_noalloc_lookback
   DeviceInfo info;
 };
 NoAllocSetup g_noalloc[64];
@@ -390,11 +598,10 @@ void noalloc_setup(int dev) {
   void* ptr = nullptr;
   st.err = cudaGetSymbolAddress(&ptr, g_noalloc_lookback);
   if (st.err != cudaSuccess) return;
-  st.scratch = static_cast<unsigned long long*>(ptr);
+  st.scratch = static_cast<unsigned*>(ptr);
   st.err = cudaDeviceGetAttribute(&st.info.sms, cudaDevAttrMultiProcessorCount, dev);
   if (st.err != cudaSuccess) return;
-  st.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&st.info.layout_blocks_per_sm, layout_kernel,
-                                                         kThreads, 0);
+  st.info.layout_blocks_per_sm = layout_blocks_per_sm();
 }
 
 }  // namespace
@@ -411,14 +618,14 @@ cudaError_t launch_layout_noalloc(const int32_t* topk_idx, int s, int e, int k, 
   const NoAllocSetup& setup = g_noalloc[dev];
   if (setup.err != cudaSuccess) return setup.err;
 
-  const LayoutPlan plan = plan_layout(s, setup.info);
-  const long long words = (long long)plan.tiles * e;
+  const LayoutPlan plan = plan_layout(s, e, setup.info);
+  const long long words = (long long)(lookback_bytes(plan, e) / sizeof(unsigned));
   *words_needed = (int)(words > 0x7fffffffLL ? 0x7fffffffLL : words);
   if (words > kNoAllocLookbackWords) return cudaErrorInvalidValue;  // caller reports the limit
 
   LayoutOut out = out_in;
   out.lookback = setup.scratch;
-  err = cudaMemsetAsync(setup.scratch, 0, (size_t)words * sizeof(unsigned long long), st);
+  err = cudaMemsetAsync(setup.scratch, 0, (size_t)words * sizeof(unsigned), st);
   if (err == cudaSuccess && R > 0)
     err = cudaMemsetAsync(out.rank_counts, 0, (size_t)R * sizeof(int32_t), st);
   if (err != cudaSuccess) return err;

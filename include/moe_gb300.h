@@ -152,9 +152,10 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int
  * [R] int32 (ignored when R = 0).  device_status (nullable): an int32 in
  * device memory that gets MOE_DEV_* bits OR-ed in (the caller zeroes it).
  * It calls no allocating routine.  The kernel's scratch (its look-back
- * words, tiles x e of them) is a fixed library array of 65536 words (512 KB)
- * per device, held until the process exits; a size whose tiling needs more
- * returns MOE_ERR_UNSUPPORTED (use moe_dispatch_layout).  Every call shares
+ * words, tiles x e of them) is a fixed library array of 16384 words (128 KB)
+ * per device, held until the process exits.  The tile plan keeps tiles x e
+ * within 16384 for every accepted size; a plan that would need more returns
+ * MOE_ERR_UNSUPPORTED (use moe_dispatch_layout) instead of overrunning it.  Every call shares
  * that array and clears the part it uses, so calls whose work overlaps on the
  * GPU (unordered streams) race; order them.  The first call on each device
  * resolves the array's device address (one-time set-up); make that first call
