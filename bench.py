@@ -10,10 +10,14 @@ the layout handle the step built, then the handle is released.
     python bench.py --impl reference ...   # the CPU oracle, on a bounded sample
 
 Prints ONE JSON line.  ``value`` = algorithmic HBM bytes of a step / device
-time of a step (GB/s), inputs resident in HBM; ``e2e`` = the same with the
-inputs copied from pinned host memory and the results copied back inside
-the timed region.  The step's working set is several times the 129 MB L2,
-so no L2 flush is inserted between steps.
+time of a step (GB/s), inputs resident in HBM, the K steps timed back to
+back with no events between kernels (as one CUDA graph of the step when it
+can be captured, else eager calls; ``config.launch`` says which).  Per-kernel
+durations for ``ops`` and ``roofline`` come from a separate loop with events
+around every call.  ``e2e`` = the same metric with every step's inputs
+copied from pinned host memory and its results copied back inside the timed
+region.  The step's working set is several times the 129 MB L2, so no L2
+flush is inserted between steps.
 """
 from __future__ import annotations
 
@@ -155,36 +159,41 @@ def run_ours(args, rank: int, world: int, dist):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     B.lib()
-    inp = W.make_inputs(w, device=dev, seed=w.seed + 1000 * rank)
-    logits, x, y, dout = inp["logits"], inp["x"], inp["y"], inp["dout"]
     dt = w.torch_dtype
-    X = torch.empty(w.rows, w.m, dtype=dt, device=dev)
-    out = torch.empty(w.s, w.m, dtype=dt, device=dev)
-    dY = torch.empty(w.rows, w.m, dtype=dt, device=dev)
-    dx = torch.empty(w.s, w.m, dtype=dt, device=dev)
-    idx = torch.empty(w.s, w.k, dtype=torch.int32, device=dev)
-    gate = torch.empty(w.s, w.k, dtype=torch.float32, device=dev)
-    dgate = torch.empty(w.s, w.k, dtype=torch.float32, device=dev)
 
-    def step(ev=None):
+    def buffers(seed):
+        inp = W.make_inputs(w, device=dev, seed=seed)
+        return dict(
+            logits=inp["logits"], x=inp["x"], y=inp["y"], dout=inp["dout"],
+            X=torch.empty(w.rows, w.m, dtype=dt, device=dev), out=torch.empty(w.s, w.m, dtype=dt, device=dev),
+            dY=torch.empty(w.rows, w.m, dtype=dt, device=dev), dx=torch.empty(w.s, w.m, dtype=dt, device=dev),
+            idx=torch.empty(w.s, w.k, dtype=torch.int32, device=dev),
+            gate=torch.empty(w.s, w.k, dtype=torch.float32, device=dev),
+            dgate=torch.empty(w.s, w.k, dtype=torch.float32, device=dev))
+
+    S = buffers(w.seed + 1000 * rank)
+
+    def step(b=S, ev=None):
+        """One pass of the path: gate, layout, dispatch, combine, combine
+        backward, dispatch backward on the step's handle; the handle is freed."""
         if ev is not None:
             ev[0].record()
-        B.moe_topk_gate(logits, w.k, w.renorm, idx, gate)
+        B.moe_topk_gate(b["logits"], w.k, w.renorm, b["idx"], b["gate"])
         if ev is not None:
             ev[1].record()
-        h = B.moe_dispatch_layout(idx, w.e, w.capacity, w.R)
+        h = B.moe_dispatch_layout(b["idx"], w.e, w.capacity, w.R)
         if ev is not None:
             ev[2].record()
-        B.moe_dispatch(h, x, X)
+        B.moe_dispatch(h, b["x"], b["X"])
         if ev is not None:
             ev[3].record()
-        B.moe_combine(h, y, gate, out)
+        B.moe_combine(h, b["y"], b["gate"], b["out"])
         if ev is not None:
             ev[4].record()
-        B.moe_combine_bwd(h, dout, gate, y, dY, dgate)
+        B.moe_combine_bwd(h, b["dout"], b["gate"], b["y"], b["dY"], b["dgate"])
         if ev is not None:
             ev[5].record()
-        B.moe_dispatch_bwd(h, dY, dx)
+        B.moe_dispatch_bwd(h, b["dY"], b["dx"])
         if ev is not None:
             ev[6].record()
         return h
@@ -204,59 +213,73 @@ def run_ours(args, rank: int, world: int, dist):
             dist.barrier()
         torch.cuda.synchronize()
 
+    # the step as one CUDA graph (replays skip the per-call host work); eager if capture fails
+    graph, launch_mode, graph_launches = None, "eager", 0
+    if not args.eager:
+        try:
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                for _ in range(2):
+                    step().destroy()
+            torch.cuda.current_stream(dev).wait_stream(side)
+            torch.cuda.synchronize()
+            c0 = sum(B.moe_launch_count(i) for i in range(len(B.KERNELS)))
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                step().destroy()
+            graph_launches = sum(B.moe_launch_count(i) for i in range(len(B.KERNELS))) - c0
+            graph.replay()
+            torch.cuda.synchronize()
+            launch_mode = "cuda graph of the step (replayed)"
+        except Exception as exc:  # capture unsupported here: time the eager path
+            graph = None
+            launch_mode = f"eager (graph capture failed: {type(exc).__name__})"
+            torch.cuda.synchronize()
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step().destroy()
+
     for _ in range(args.warmup):
-        step().destroy()
+        run_step()
     barrier()
 
+    # ---- the timed region: exactly K steps, no events inside ----------------
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
     launches0 = [B.moe_launch_count(i) for i in range(len(B.KERNELS))]
     with ClockSampler(dev.index) as clk:
         barrier()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
-        for i in range(K):
-            step(evs[i]).destroy()
+        for _ in range(K):
+            run_step()
         t1.record()
         barrier()
     launches = sum(B.moe_launch_count(i) - launches0[i] for i in range(len(B.KERNELS)))
+    if graph is not None:
+        launches = graph_launches * K
     elapsed_ms = t0.elapsed_time(t1)
-    per_op = {op: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) for j, op in enumerate(OPS)}
 
-    # end to end: pinned host inputs in, results out, inside the timed region
-    h_in = {n: t.cpu().pin_memory() for n, t in (("logits", logits), ("x", x), ("y", y), ("dout", dout))}
-    h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in (("out", out), ("dx", dx),
-                                                                               ("dgate", dgate))}
-    d_in = {"logits": logits, "x": x, "y": y, "dout": dout}
-    d_out = {"out": out, "dx": dx, "dgate": dgate}
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
-    Ke = max(3, min(K, 50))
+    # ---- per-kernel durations: events around each call, eager, own loop -----
+    Kr = max(3, min(K, 200))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(Kr)]
+    for i in range(Kr):
+        step(ev=evs[i]).destroy()
+    torch.cuda.synchronize()
+    per_op = {op: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(Kr))
+              for j, op in enumerate(OPS)}
 
-    def e2e_step():
-        for n, t in h_in.items():
-            d_in[n].copy_(t, non_blocking=True)
-        step().destroy()
-        for n, t in h_out.items():
-            t.copy_(d_out[n], non_blocking=True)
-
-    for _ in range(2):
-        e2e_step()
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(Ke):
-        e2e_step()
-    e1.record()
-    barrier()
-    e2e_ms = e0.elapsed_time(e1) / Ke
+    # ---- end to end: pinned host inputs in, results out, every step ----------
+    e2e = run_e2e(w, S, step, buffers, dev, max(3, min(K, 50)), args.warmup)
 
     if dist is not None:
-        t = torch.tensor([elapsed_ms, e2e_ms], device=dev, dtype=torch.float64)
+        t = torch.tensor([elapsed_ms, e2e["ms"]], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+        elapsed_ms, e2e["ms"] = float(t[0]), float(t[1])
     if rank != 0:
         return None
 
@@ -285,8 +308,9 @@ def run_ours(args, rank: int, world: int, dist):
             "workload": w.name, "s": w.s, "m": w.m, "e": w.e, "k": w.k,
             "mode": f"capacity {w.capacity}" if w.capacity else "dropless", "virtual_ranks": w.R,
             "step": "topk_gate+layout+dispatch+combine+combine_bwd+dispatch_bwd on the step's handle",
+            "launch": launch_mode,
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "l2": f"no flush: step working set {round((step_total) / 1e6)} MB algorithmic vs 129 MB L2",
+            "l2": f"no flush: step working set {round(step_total / 1e6)} MB algorithmic vs 129 MB L2",
         },
         "routed_tokens_per_s": round(world * w.s * w.k / (ms_per_step * 1e-3), 1),
         "dispatch_combine": {
@@ -298,6 +322,7 @@ def run_ours(args, rank: int, world: int, dist):
         },
         "ops": {op: {"us": round(per_op[op] * 1e3, 2), "bytes": nbytes[op],
                      "gbs": round(nbytes[op] / (per_op[op] * 1e-3) / 1e9, 1)} for op in OPS},
+        "ops_note": f"per-kernel times from events around each call, eager, {Kr} separate steps",
         "roofline": {
             "kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (copy bandwidth)",
@@ -305,9 +330,9 @@ def run_ours(args, rank: int, world: int, dist):
             "traffic_note": (tr.get("note") if tr else "no ncu capture of this kernel source"),
             "algorithmic_bytes": nbytes[dom],
         },
-        "e2e": {"value": round(world * step_total / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": Ke},
+        "e2e": {"value": round(world * step_total / (e2e["ms"] * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e["ms"], 4), "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"], "how": e2e["how"]},
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "kept_routes": kept,
@@ -316,6 +341,65 @@ def run_ours(args, rank: int, world: int, dist):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args)
     return line
+
+
+def run_e2e(w, S, step, buffers, dev, K, warmup):
+    """Every step copies its inputs from pinned host memory to the device,
+    runs the path and copies its results (out, dx, dgate) back.  Steps are
+    pipelined over three streams (copy in, compute, copy out) with two
+    device buffer sets, so step i+1's inputs travel while step i computes."""
+    import torch
+
+    sets = [S, buffers(w.seed + 7)]
+    in_names = ("logits", "x", "y", "dout")
+    out_names = ("out", "dx", "dgate")
+    h_in = [{n: sets[j][n].cpu().pin_memory() for n in in_names} for j in range(2)]
+    h_out = [{n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype).pin_memory() for n in out_names}
+             for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in[0].values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def run(n):
+        for i in range(n):
+            j = i % 2
+            b = sets[j]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_cmp[j])  # the set's previous step has read its inputs
+                for name in in_names:
+                    b[name].copy_(h_in[j][name], non_blocking=True)
+                ev_in[j].record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(ev_in[j])
+                if i >= 2:
+                    s_cmp.wait_event(ev_out[j])  # its previous results have left
+                step(b).destroy()
+                ev_cmp[j].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_cmp[j])
+                for name in out_names:
+                    h_out[j][name].copy_(b[name], non_blocking=True)
+                ev_out[j].record(s_out)
+
+    run(max(2, warmup))
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    s_cmp.wait_event(t0)
+    s_out.wait_event(t0)
+    run(K)
+    s_in.wait_stream(s_out)
+    s_in.wait_stream(s_cmp)
+    t1.record(s_in)
+    torch.cuda.synchronize()
+    return {"ms": t0.elapsed_time(t1) / K, "h2d": h2d, "d2h": d2h, "steps": K,
+            "how": "pinned host -> device copies, the path, device -> host copies of out, dx, dgate; "
+                   "pipelined over copy-in / compute / copy-out streams, two buffer sets"}
 
 
 # --------------------------------------------------------- oracle (CPU) --
@@ -436,6 +520,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle work for cpu_baseline")
     ap.add_argument("--ref-seconds", type=float, default=120.0, help="total oracle work of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager calls instead of a CUDA graph of the step")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -216,7 +216,10 @@ int grid_for(long long warps_wanted, const DeviceInfo& di, int blocks_per_sm) {
 template <typename T, int KMAX>
 cudaError_t combine_t(const int32_t* row, const float* gate, int s, int k, int m, const void* y,
                       void* out, const DeviceInfo& di, cudaStream_t st) {
-  constexpr int UNR = MOE_CMB_LOADS / KMAX > 1 ? MOE_CMB_LOADS / KMAX : 1;
+  // two routes: 8 loads per lane already keep enough bytes in flight, and
+  // the lower register count doubles the resident warps
+  constexpr int LOADS = KMAX <= 2 ? MOE_CMB_LOADS / 2 : MOE_CMB_LOADS;
+  constexpr int UNR = LOADS / KMAX > 1 ? LOADS / KMAX : 1;
   const int nvec = m / Vec<T>::N;
   const int chunk = MOE_CMB_CHUNK > 0 && MOE_CMB_CHUNK < nvec ? MOE_CMB_CHUNK : nvec;
   const int nchunks = (nvec + chunk - 1) / chunk;
