@@ -44,11 +44,12 @@ def lib() -> ctypes.CDLL:
         L.ora_f32_to_bf16.restype = ctypes.c_uint16
         L.ora_topk_gate.argtypes = [P, I, I, I, I, P, P]
         L.ora_layout.argtypes = [P, I, I, I, I, I, P, P, P, P, P, P, P, P]
+        L.ora_topk_gate_bwd.argtypes = [P, P, P, P, I, I, I, I, P]
         L.ora_dispatch.argtypes = [P, I, I, I, I, P, I, P]
         L.ora_combine.argtypes = [P, P, I, I, I, I, P, P]
         L.ora_combine_bwd.argtypes = [P, P, I, I, I, I, P, P, I, P, P]
         L.ora_dispatch_bwd.argtypes = [P, I, I, I, I, P, P]
-        for f in ("ora_topk_gate", "ora_layout", "ora_dispatch", "ora_combine",
+        for f in ("ora_topk_gate", "ora_topk_gate_bwd", "ora_layout", "ora_dispatch", "ora_combine",
                   "ora_combine_bwd", "ora_dispatch_bwd"):
             getattr(L, f).restype = I
         _lib = L
@@ -94,6 +95,19 @@ def topk_gate(logits: np.ndarray, k: int, renorm: int = 1):
     gate = np.empty((s, k), np.float32)
     _check(lib().ora_topk_gate(_p(logits), s, e, k, int(renorm), _p(idx), _p(gate)), "topk_gate")
     return idx, gate
+
+
+def topk_gate_bwd(logits: np.ndarray | None, idx: np.ndarray, gate: np.ndarray, dgate: np.ndarray,
+                  e: int, renorm: int = 1) -> np.ndarray:
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    gate = np.ascontiguousarray(gate, dtype=np.float32)
+    dgate = np.ascontiguousarray(dgate, dtype=np.float32)
+    lg = None if logits is None else np.ascontiguousarray(logits, dtype=np.float32)
+    s, k = idx.shape
+    dl = np.empty((s, e), np.float32)
+    rc = lib().ora_topk_gate_bwd(_p(lg), _p(idx), _p(gate), _p(dgate), s, e, k, int(renorm), _p(dl))
+    _check(rc, "topk_gate_bwd")
+    return dl
 
 
 def layout(idx: np.ndarray, e: int, capacity: int = 0, R: int = 0) -> dict:

@@ -106,6 +106,46 @@ int ora_topk_gate(const float* logits, int s, int e, int k, int renorm,
   return ORA_OK;
 }
 
+int ora_topk_gate_bwd(const float* logits, const int32_t* idx, const float* gate,
+                      const float* dgate, int s, int e, int k, int renorm, float* dlogits) {
+  if (!idx || !gate || !dgate || !dlogits || s < 0 || e < 1 || k < 1 || k > e) return ORA_EARG;
+  if (!renorm && !logits) return ORA_EARG;
+  if (!renorm)
+    for (size_t i = 0; i < (size_t)s * (size_t)e; ++i)
+      if (!isfinite(logits[i])) return ORA_ENONFINITE;
+  for (size_t q = 0; q < (size_t)s * k; ++q)
+    if (idx[q] < 0 || idx[q] >= e) return ORA_EROUTE;
+
+#pragma omp parallel for schedule(static) num_threads(g_threads)
+  for (int t = 0; t < s; ++t) {
+    const int32_t* it = idx + (size_t)t * k;
+    const float* gt = gate + (size_t)t * k;
+    const float* dt = dgate + (size_t)t * k;
+    float* out = dlogits + (size_t)t * e;
+    double c = 0.0; /* sum_j g_j dgate_j */
+    for (int j = 0; j < k; ++j) c += (double)gt[j] * (double)dt[j];
+    if (renorm) {
+      for (int i = 0; i < e; ++i) out[i] = 0.0f;
+      for (int j = 0; j < k; ++j) out[it[j]] = (float)((double)gt[j] * ((double)dt[j] - c));
+    } else {
+      const float* l = logits + (size_t)t * e;
+      double M = (double)l[0];
+      for (int i = 1; i < e; ++i)
+        if ((double)l[i] > M) M = (double)l[i];
+      double den = 0.0;
+      for (int i = 0; i < e; ++i) den += exp((double)l[i] - M);
+      for (int i = 0; i < e; ++i) {
+        double dg = 0.0;
+        for (int j = 0; j < k; ++j)
+          if (it[j] == i) dg = (double)dt[j];
+        const double p = exp((double)l[i] - M) / den;
+        out[i] = (float)(p * (dg - c));
+      }
+    }
+  }
+  return ORA_OK;
+}
+
 /* -------------------------------------------------------------- layout -- */
 
 int ora_layout(const int32_t* idx, int s, int e, int k, int capacity, int R,

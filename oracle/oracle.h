@@ -67,6 +67,19 @@ uint16_t ora_f32_to_bf16(float f);
 int ora_topk_gate(const float* logits, int s, int e, int k, int renorm,
                   int32_t* idx, float* gate);
 
+/* Top-k gate backward [P3 review thread: the routing weights' gradient must
+ * reach the router].  With the selection idx fixed (it is piecewise
+ * constant in the logits), the gates are a softmax of the logits:
+ * renorm = 1: g_j = exp(l_{i_j}) / sum_{j'} exp(l_{i_j'}) over the selected;
+ *   dlogits[i_j] = g_j * (dgate_j - sum_{j'} g_{j'} dgate_{j'}), others 0.
+ * renorm = 0: g_j = p_{i_j}, p = softmax over all e logits;
+ *   dlogits[i] = p_i * (dgate(i) - sum_j g_j dgate_j), dgate(i) = dgate_j
+ *   when i = i_j, else 0 (every expert gets a gradient).
+ * gate holds the forward's gates; p is recomputed from the logits in double.
+ * Everything in double, rounded once to float. */
+int ora_topk_gate_bwd(const float* logits, const int32_t* idx, const float* gate,
+                      const float* dgate, int s, int e, int k, int renorm, float* dlogits);
+
 /* Dispatch layout [P4 change 1 and 3: location = cumsum - 1 in token order;
  * P3 description: one send per destination rank].
  * loc[t,j]  = #{ t' < t : expert idx[t,j] is among idx[t',:] }

@@ -465,3 +465,61 @@ def test_threads_do_not_change_results():
     oracle.set_threads(1)
     for a, b in zip(outs[0], outs[1]):
         np.testing.assert_array_equal(a, b)
+
+
+# ------------------------------------------------------------ gate backward --
+
+def gate_forward_f64(logits, idx, renorm):
+    """The gates as a function of the logits with the selection held fixed,
+    written with SciPy's softmax (float64)."""
+    l = logits.astype(np.float64)
+    if renorm:
+        return scipy.special.softmax(np.take_along_axis(l, idx.astype(np.int64), 1), axis=1)
+    return np.take_along_axis(scipy.special.softmax(l, axis=1), idx.astype(np.int64), 1)
+
+
+@pytest.mark.parametrize("renorm", [0, 1])
+def test_gate_backward_matches_central_differences(renorm):
+    rng = np.random.default_rng(40 + renorm)
+    s, e, k = 12, 16, 4
+    logits = rng.standard_normal((s, e)).astype(np.float32)
+    idx, gate = oracle.topk_gate(logits, k, renorm=renorm)
+    dgate = rng.standard_normal((s, k)).astype(np.float32)
+    dl = oracle.topk_gate_bwd(logits, idx, gate, dgate, e, renorm)
+    h = 1e-5
+    for t in range(s):
+        for i in range(e):
+            lp, ln = logits.astype(np.float64).copy(), logits.astype(np.float64).copy()
+            lp[t, i] += h
+            ln[t, i] -= h
+            fd = (np.sum(gate_forward_f64(lp, idx, renorm)[t] * dgate[t]) -
+                  np.sum(gate_forward_f64(ln, idx, renorm)[t] * dgate[t])) / (2 * h)
+            assert abs(dl[t, i] - fd) <= 1e-6 + 1e-5 * abs(fd), (t, i, dl[t, i], fd)
+    if renorm:
+        sel = np.zeros((s, e), bool)
+        np.put_along_axis(sel, idx.astype(np.int64), True, 1)
+        assert np.all(dl[~sel] == 0), "experts outside the top-k get no gradient"
+    # softmax gradients sum to zero over the logits they depend on
+    np.testing.assert_allclose(dl.astype(np.float64).sum(1), 0, atol=1e-6)
+
+
+def test_gate_backward_special_cases():
+    # k = 1 with renorm: the gate is constant 1, so no gradient at all
+    rng = np.random.default_rng(3)
+    logits = rng.standard_normal((5, 8)).astype(np.float32)
+    idx, gate = oracle.topk_gate(logits, 1, renorm=1)
+    dl = oracle.topk_gate_bwd(logits, idx, gate, rng.standard_normal((5, 1)).astype(np.float32), 8, 1)
+    assert np.all(dl == 0)
+    # uniform upstream gradient with renorm: sum of gates is 1, so again zero
+    idx, gate = oracle.topk_gate(logits, 3, renorm=1)
+    dl = oracle.topk_gate_bwd(logits, idx, gate, np.full((5, 3), 2.5, np.float32), 8, 1)
+    np.testing.assert_allclose(dl, 0, atol=1e-7)
+    # k = e without renorm is the full softmax Jacobian-vector product: p*(v - <p, v>)
+    idx, gate = oracle.topk_gate(logits, 8, renorm=0)
+    v = rng.standard_normal((5, 8)).astype(np.float32)
+    dl = oracle.topk_gate_bwd(logits, idx, gate, v, 8, 0)
+    p = scipy.special.softmax(logits.astype(np.float64), axis=1)
+    vf = np.zeros((5, 8))
+    np.put_along_axis(vf, idx.astype(np.int64), v.astype(np.float64), 1)
+    ref = p * (vf - np.sum(p * vf, axis=1, keepdims=True))
+    np.testing.assert_allclose(dl, ref, rtol=1e-6, atol=1e-8)
