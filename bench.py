@@ -3,8 +3,9 @@
 
 One step = one pass of the whole path over one batch of seeded synthetic
 input: top-k gate -> dispatch layout -> dispatch -> combine -> combine
-backward (gate-scaled dispatch + gate gradient) -> dispatch backward, all on
-the layout handle the step built, then the handle is released.
+backward (gate-scaled dispatch + gate gradient) -> gate backward (router
+logits' gradient) -> dispatch backward, all on the layout handle the step
+built, then the handle is released.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the CPU oracle, on a bounded sample
@@ -35,9 +36,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "dispatch+combine HBM GB/s and routed tokens/s on 1 GB300 vs HBM peak"
 DEFAULT_WORKLOAD = "mixtral-dropless"
-OPS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd"]
+OPS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "topk_gate_bwd", "dispatch_bwd"]
 KERNEL_FILE = {"topk_gate": "gate.cu", "layout": "layout.cu", "dispatch": "dispatch.cu", "combine": "combine.cu",
-               "combine_bwd": "combine.cu", "dispatch_bwd": "combine.cu"}
+               "combine_bwd": "combine.cu", "topk_gate_bwd": "gate.cu", "dispatch_bwd": "combine.cu"}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -57,6 +58,7 @@ def step_bytes(w, kept: int, u: int) -> dict:
         "dispatch": u * m * b + R + meta_r,
         "combine": kept * m * b + x + meta_r + routes * 4,
         "combine_bwd": x + kept * m * b + R + meta_r + routes * 8,
+        "topk_gate_bwd": routes * 12 + s * e * 4 + (0 if w.renorm else s * e * 4),
         "dispatch_bwd": kept * m * b + x + meta_r,
     }
 
@@ -169,13 +171,14 @@ def run_ours(args, rank: int, world: int, dist):
             dY=torch.empty(w.rows, w.m, dtype=dt, device=dev), dx=torch.empty(w.s, w.m, dtype=dt, device=dev),
             idx=torch.empty(w.s, w.k, dtype=torch.int32, device=dev),
             gate=torch.empty(w.s, w.k, dtype=torch.float32, device=dev),
-            dgate=torch.empty(w.s, w.k, dtype=torch.float32, device=dev))
+            dgate=torch.empty(w.s, w.k, dtype=torch.float32, device=dev),
+            dlogits=torch.empty(w.s, w.e, dtype=torch.float32, device=dev))
 
     S = buffers(w.seed + 1000 * rank)
 
     def step(b=S, ev=None):
         """One pass of the path: gate, layout, dispatch, combine, combine
-        backward, dispatch backward on the step's handle; the handle is freed."""
+        backward, gate backward, dispatch backward on the step's handle."""
         if ev is not None:
             ev[0].record()
         B.moe_topk_gate(b["logits"], w.k, w.renorm, b["idx"], b["gate"])
@@ -193,9 +196,13 @@ def run_ours(args, rank: int, world: int, dist):
         B.moe_combine_bwd(h, b["dout"], b["gate"], b["y"], b["dY"], b["dgate"])
         if ev is not None:
             ev[5].record()
-        B.moe_dispatch_bwd(h, b["dY"], b["dx"])
+        B.moe_topk_gate_bwd(None if w.renorm else b["logits"], b["idx"], b["gate"], b["dgate"], w.e, w.renorm,
+                            b["dlogits"])
         if ev is not None:
             ev[6].record()
+        B.moe_dispatch_bwd(h, b["dY"], b["dx"])
+        if ev is not None:
+            ev[7].record()
         return h
 
     # kept routes / sending tokens for the byte model (outside any timing)
@@ -266,7 +273,7 @@ def run_ours(args, rank: int, world: int, dist):
 
     # ---- per-kernel durations: events around each call, eager, own loop -----
     Kr = max(3, min(K, 200))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(Kr)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(OPS) + 1)] for _ in range(Kr)]
     for i in range(Kr):
         step(ev=evs[i]).destroy()
     torch.cuda.synchronize()
@@ -307,7 +314,7 @@ def run_ours(args, rank: int, world: int, dist):
         "config": {
             "workload": w.name, "s": w.s, "m": w.m, "e": w.e, "k": w.k,
             "mode": f"capacity {w.capacity}" if w.capacity else "dropless", "virtual_ranks": w.R,
-            "step": "topk_gate+layout+dispatch+combine+combine_bwd+dispatch_bwd on the step's handle",
+            "step": "topk_gate+layout+dispatch+combine+combine_bwd+topk_gate_bwd+dispatch_bwd on the step's handle",
             "launch": launch_mode,
             "parallelism": "replicas" if world > 1 else "single GPU",
             "l2": f"no flush: step working set {round(step_total / 1e6)} MB algorithmic vs 129 MB L2",
@@ -352,7 +359,7 @@ def run_e2e(w, S, step, buffers, dev, K, warmup):
 
     sets = [S, buffers(w.seed + 7)]
     in_names = ("logits", "x", "y", "dout")
-    out_names = ("out", "dx", "dgate")
+    out_names = ("out", "dx", "dlogits")
     h_in = [{n: sets[j][n].cpu().pin_memory() for n in in_names} for j in range(2)]
     h_out = [{n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype).pin_memory() for n in out_names}
              for _ in range(2)]
@@ -398,7 +405,7 @@ def run_e2e(w, S, step, buffers, dev, K, warmup):
     t1.record(s_in)
     torch.cuda.synchronize()
     return {"ms": t0.elapsed_time(t1) / K, "h2d": h2d, "d2h": d2h, "steps": K,
-            "how": "pinned host -> device copies, the path, device -> host copies of out, dx, dgate; "
+            "how": "pinned host -> device copies, the path, device -> host copies of out, dx, dlogits; "
                    "pipelined over copy-in / compute / copy-out streams, two buffer sets"}
 
 
@@ -434,7 +441,8 @@ def oracle_step(ws, inp):
     L = oracle.layout(idx, ws.e, ws.capacity, ws.R)
     oracle.dispatch(L["row"], arrs["x"], L["rows"])
     oracle.combine(L["row"], gate, arrs["y"])
-    dY, _ = oracle.combine_bwd(L["row"], gate, arrs["dout"], arrs["y"])
+    dY, dgate = oracle.combine_bwd(L["row"], gate, arrs["dout"], arrs["y"])
+    oracle.topk_gate_bwd(arrs["logits"], idx, gate, dgate, ws.e, ws.renorm)
     oracle.dispatch_bwd(L["row"], dY)
     dt = time.perf_counter() - t0
     kept = int((L["drop"] == 0).sum())
@@ -503,7 +511,7 @@ def run_reference(args, rank: int, world: int):
         "data": "synthetic: seeded N(0,1) router logits and activations",
         "config": {"workload": w.name, "s": w.s, "m": w.m, "e": w.e, "k": w.k,
                    "mode": f"capacity {w.capacity}" if w.capacity else "dropless", "virtual_ranks": w.R,
-                   "step": "topk_gate+layout+dispatch+combine+combine_bwd+dispatch_bwd (CPU oracle)"},
+                   "step": "topk_gate+layout+dispatch+combine+combine_bwd+topk_gate_bwd+dispatch_bwd (CPU oracle)"},
         "routed_tokens_per_s": round(ws.s * ws.k / per, 1),
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -20,4 +20,5 @@ from .binding import (  # noqa: F401
     moe_launch_count,
     moe_status_string,
     moe_topk_gate,
+    moe_topk_gate_bwd,
 )

@@ -27,6 +27,31 @@ import torch
 from . import binding as B
 
 
+class MoETopkGateFn(torch.autograd.Function):
+    """(idx, gate) = topk_gate(logits); dlogits = topk_gate_bwd(dgate).  The
+    expert ids are not differentiable; the gates' gradient reaches the router."""
+
+    @staticmethod
+    def forward(ctx, logits: torch.Tensor, k: int, renorm: int):
+        logits = logits.contiguous()
+        idx, gate = B.moe_topk_gate(logits, k, renorm)
+        ctx.renorm = int(renorm)
+        ctx.e = logits.shape[1]
+        ctx.save_for_backward(None if renorm else logits, idx, gate)
+        ctx.mark_non_differentiable(idx)
+        return idx, gate
+
+    @staticmethod
+    def backward(ctx, didx, dgate: torch.Tensor):
+        logits, idx, gate = ctx.saved_tensors
+        dl = B.moe_topk_gate_bwd(logits, idx, gate, dgate.contiguous(), ctx.e, ctx.renorm)
+        return dl, None, None
+
+
+def topk_gate(logits: torch.Tensor, k: int, renorm: int = 1):
+    return MoETopkGateFn.apply(logits, k, renorm)
+
+
 class MoEDispatchFn(torch.autograd.Function):
     """X = dispatch(x) on a layout handle; dx = dispatch_bwd(dX) on the same handle."""
 

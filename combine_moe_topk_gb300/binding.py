@@ -25,7 +25,7 @@ STATUS = {
 }
 MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
 MOE_DEV_NONFINITE, MOE_DEV_BAD_ROUTE, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4
-KERNELS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd"]
+KERNELS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd", "topk_gate_bwd"]
 KERNEL_ID = {n: i for i, n in enumerate(KERNELS)}
 
 # every entry point the header declares (checked by the CPU test-suite)
@@ -33,7 +33,7 @@ EXPORTS = [
     "moe_topk_gate", "moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_combine_bwd",
     "moe_dispatch_bwd", "moe_handle_info", "moe_handle_status", "moe_handle_destroy", "moe_capacity",
     "moe_status_string", "moe_last_error", "moe_launch_count", "moe_debug_hold_layout_tile",
-    "moe_dispatch_layout_noalloc",
+    "moe_dispatch_layout_noalloc", "moe_topk_gate_bwd",
 ]
 
 
@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
         P, I, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
         sig = {
             "moe_topk_gate": [P, I, I, I, I, P, P, P, P],
+            "moe_topk_gate_bwd": [P, P, P, P, I, I, I, I, P, P],
             "moe_dispatch_layout": [P, I, I, I, I, I, P, ctypes.POINTER(P)],
             "moe_dispatch": [P, I, I, I, I, P, P, P],
             "moe_combine": [P, I, I, I, I, P, P, P, P],
@@ -226,6 +227,24 @@ def moe_topk_gate(logits: torch.Tensor, k: int, renorm: int = 1, topk_idx: torch
                              _ptr(device_status), _stream(dev))
     _check(rc, "moe_topk_gate")
     return topk_idx, topk_gate
+
+
+def moe_topk_gate_bwd(logits: torch.Tensor | None, topk_idx: torch.Tensor, topk_gate: torch.Tensor,
+                      dgate: torch.Tensor, e: int, renorm: int = 1, dlogits: torch.Tensor | None = None):
+    """(logits f32 [s,e] or None when renorm=1, idx [s,k], gate [s,k], dgate [s,k]) -> dlogits f32 [s,e]."""
+    s, k = topk_idx.shape
+    for t, name in ((topk_gate, "topk_gate"), (dgate, "dgate")):
+        if t.dtype != torch.float32 or tuple(t.shape) != (s, k):
+            raise MoEError(1, "moe_topk_gate_bwd", f"{name} must be float32 [s, k]")
+    if logits is not None and (logits.dtype != torch.float32 or tuple(logits.shape) != (s, e)):
+        raise MoEError(1, "moe_topk_gate_bwd", "logits must be float32 [s, e]")
+    dev = topk_idx.device
+    if dlogits is None:
+        dlogits = torch.empty(s, e, dtype=torch.float32, device=dev)
+    rc = lib().moe_topk_gate_bwd(_ptr(logits), _ptr(topk_idx), _ptr(topk_gate), _ptr(dgate), s, int(e), k,
+                                 int(renorm), _ptr(dlogits), _stream(dev))
+    _check(rc, "moe_topk_gate_bwd")
+    return dlogits
 
 
 def moe_dispatch_layout(topk_idx: torch.Tensor, e: int, capacity: int = 0, num_virtual_ranks: int = 0) -> Handle:

@@ -236,6 +236,33 @@ moe_status moe_topk_gate(const float* logits, int s, int e, int k, int renorm, i
   return MOE_OK;
 }
 
+moe_status moe_topk_gate_bwd(const float* logits, const int32_t* topk_idx, const float* topk_gate,
+                             const float* dgate, int s, int e, int k, int renorm, float* dlogits,
+                             void* stream) {
+  if (s < 0 || e < 1 || e > kMaxE || k < 1 || k > e || k > kMaxK)
+    return fail(MOE_ERR_INVALID_ARG, "need s >= 0, 1 <= e <= 256, 1 <= k <= min(e, 16)");
+  if ((long long)s * e > 2147483647LL) return fail(MOE_ERR_INVALID_ARG, "s*e must be < 2^31");
+  if (renorm != 0 && renorm != 1) return fail(MOE_ERR_INVALID_ARG, "renorm must be 0 or 1");
+  if (s == 0) return MOE_OK;
+  if (!renorm) MOE_TRY(check_ptr(logits, "logits"));
+  MOE_TRY(check_ptr(topk_idx, "topk_idx"));
+  MOE_TRY(check_ptr(topk_gate, "topk_gate"));
+  MOE_TRY(check_ptr(dgate, "dgate"));
+  MOE_TRY(check_ptr(dlogits, "dlogits"));
+  int dev = 0;
+  MOE_TRY(current_device(&dev));
+  const void* ptrs[5] = {renorm ? nullptr : logits, topk_idx, topk_gate, dgate, dlogits};
+  const char* names[5] = {"logits", "topk_idx", "topk_gate", "dgate", "dlogits"};
+  for (int i = 0; i < 5; ++i) MOE_TRY(check_device_ptr(ptrs[i], names[i], dev));
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(dev, &di));
+  cudaError_t err = moe::launch_topk_gate_bwd(renorm ? nullptr : logits, topk_idx, topk_gate, dgate, s, e,
+                                              k, renorm, dlogits, *di, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "topk_gate_bwd launch");
+  g_launches[MOE_KERNEL_TOPK_GATE_BWD]++;
+  return MOE_OK;
+}
+
 moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity,
                                int num_virtual_ranks, void* stream, moe_handle* out) {
   if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");

@@ -1,4 +1,4 @@
-// gate.cu -- top-k softmax gating, one warp per token.
+// gate.cu -- top-k softmax gating and its backward, one warp per token.
 //
 // DeepSpeed #8195 "MoE dispatch: fix silent Tutel + TP corruption, speed up
 // native and Tutel paths", change 1: the gate hands out per-route expert
@@ -123,6 +123,92 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float* __restrict_
   pdl_trigger_late();
 }
 
+// Gate backward, one warp per token: lanes 0..k-1 hold (expert, gate,
+// dgate) of the selected routes; c = sum_j g_j * dgate_j by a butterfly; each
+// lane then writes the gradient of its experts lane, lane + 32, ...
+template <int EPL>
+__global__ void __launch_bounds__(256) topk_gate_bwd_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ idx,
+    const float* __restrict__ gate, const float* __restrict__ dgate, int s, int e, int k,
+    int renorm, float* __restrict__ dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  grid_dependency_wait();
+  pdl_trigger_early();
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < s; t += warps) {
+    int ij = -1;
+    float gj = 0.f, dgj = 0.f;
+    if (lane < k) {
+      ij = __ldg(idx + (size_t)t * k + lane);
+      gj = __ldg(gate + (size_t)t * k + lane);
+      dgj = __ldg(dgate + (size_t)t * k + lane);
+    }
+    float c = __fmul_rn(gj, dgj);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+    // this lane's experts: their dgate (0 if not selected) and gate factor
+    float dg[EPL], fac[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      dg[i] = 0.f;
+      fac[i] = 0.f;
+    }
+    for (int j = 0; j < k; ++j) {
+      const int x = __shfl_sync(0xffffffffu, ij, j);
+      const float g = __shfl_sync(0xffffffffu, gj, j);
+      const float d = __shfl_sync(0xffffffffu, dgj, j);
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (lane + 32 * i == x) {
+          dg[i] = d;
+          fac[i] = g;
+        }
+    }
+    if (!renorm) {
+      const float* l = logits + (size_t)t * e;
+      float v[EPL];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int x = lane + 32 * i;
+        v[i] = x < e ? __ldg(l + x) : -INFINITY;
+        mx = fmaxf(mx, v[i]);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      float z = 0.f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (lane + 32 * i < e) z += expf(v[i] - mx);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) fac[i] = expf(v[i] - mx) / z;  // p_i for every expert
+    }
+    float* out = dlogits + (size_t)t * e;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int x = lane + 32 * i;
+      // an expert outside the top-k gets exactly 0 under renormalisation
+      if (x < e) out[x] = fac[i] == 0.f ? 0.f : __fmul_rn(fac[i], __fsub_rn(dg[i], c));
+    }
+  }
+  pdl_trigger_late();
+}
+
+template <int EPL>
+cudaError_t launch_bwd_epl(const float* logits, const int32_t* idx, const float* gate,
+                           const float* dgate, int s, int e, int k, int renorm, float* dlogits,
+                           const DeviceInfo& di, cudaStream_t st) {
+  const int threads = 256;
+  long long blocks = ((long long)s * 32 + threads - 1) / threads;
+  const long long cap = (long long)di.sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(MOE_KERNEL_TOPK_GATE_BWD, topk_gate_bwd_kernel<EPL>, dim3((unsigned)blocks),
+                    dim3(threads), 0, st, logits, idx, gate, dgate, s, e, k, renorm, dlogits);
+}
+
 template <int EPL>
 cudaError_t launch_epl(const float* logits, int s, int e, int k, int renorm, int32_t* idx,
                        float* gate, int32_t* status, const DeviceInfo& di, cudaStream_t st) {
@@ -136,6 +222,18 @@ cudaError_t launch_epl(const float* logits, int s, int e, int k, int renorm, int
 }
 
 }  // namespace
+
+cudaError_t launch_topk_gate_bwd(const float* logits, const int32_t* idx, const float* gate,
+                                 const float* dgate, int s, int e, int k, int renorm,
+                                 float* dlogits, const DeviceInfo& di, cudaStream_t st) {
+  switch ((e + 31) / 32) {
+    case 1: return launch_bwd_epl<1>(logits, idx, gate, dgate, s, e, k, renorm, dlogits, di, st);
+    case 2: return launch_bwd_epl<2>(logits, idx, gate, dgate, s, e, k, renorm, dlogits, di, st);
+    case 3:
+    case 4: return launch_bwd_epl<4>(logits, idx, gate, dgate, s, e, k, renorm, dlogits, di, st);
+    default: return launch_bwd_epl<8>(logits, idx, gate, dgate, s, e, k, renorm, dlogits, di, st);
+  }
+}
 
 cudaError_t launch_topk_gate(const float* logits, int s, int e, int k, int renorm, int32_t* idx,
                              float* gate, int32_t* status, const DeviceInfo& di, cudaStream_t st) {

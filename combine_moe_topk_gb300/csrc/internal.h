@@ -19,6 +19,10 @@ const DeviceInfo& device_info(int device);
 cudaError_t launch_topk_gate(const float* logits, int s, int e, int k, int renorm, int32_t* idx,
                              float* gate, int32_t* status, const DeviceInfo& di, cudaStream_t st);
 
+cudaError_t launch_topk_gate_bwd(const float* logits, const int32_t* idx, const float* gate,
+                                 const float* dgate, int s, int e, int k, int renorm,
+                                 float* dlogits, const DeviceInfo& di, cudaStream_t st);
+
 // --- layout -------------------------------------------------------------
 struct LayoutPlan {
   int tiles = 1;            // CTAs (all co-resident: cooperative launch)

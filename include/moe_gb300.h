@@ -78,7 +78,8 @@ enum {
   MOE_KERNEL_COMBINE = 3,
   MOE_KERNEL_COMBINE_BWD = 4,
   MOE_KERNEL_DISPATCH_BWD = 5,
-  MOE_KERNEL_COUNT = 6
+  MOE_KERNEL_TOPK_GATE_BWD = 6,
+  MOE_KERNEL_COUNT = 7
 };
 
 /* Opaque layout handle [P1 "How"; P3 description].  Owned by the library:
@@ -120,6 +121,22 @@ typedef struct {
 moe_status moe_topk_gate(const float* logits, int s, int e, int k, int renorm,
                          int32_t* topk_idx, float* topk_gate, int32_t* device_status,
                          void* stream);
+
+/* Top-k gate backward [P3 review thread: the routing weights' gradient must
+ * reach the router gate, or the router silently never learns].  With the
+ * selection held fixed (top-k is piecewise constant in the logits):
+ *   renorm = 1: dlogits[i_j] = g_j * (dgate_j - sum_j' g_j' * dgate_j'),
+ *               every other expert 0;
+ *   renorm = 0: dlogits[i] = p_i * (dgate(i) - sum_j g_j * dgate_j), p the
+ *               softmax of the logits over all e experts (recomputed here in
+ *               fp32 with expf), dgate(i) = dgate_j for i = i_j, else 0.
+ * logits f32 [s,e] (may be NULL when renorm = 1), topk_idx i32 [s,k] and
+ * topk_gate f32 [s,k] as returned by moe_topk_gate, dgate f32 [s,k]
+ * (e.g. from moe_combine_bwd) -> dlogits f32 [s,e].  fp32 arithmetic, fixed
+ * summation order.  Expert ids must be in [0, e) and distinct per token. */
+moe_status moe_topk_gate_bwd(const float* logits, const int32_t* topk_idx, const float* topk_gate,
+                             const float* dgate, int s, int e, int k, int renorm, float* dlogits,
+                             void* stream);
 
 /* Dispatch layout [P4 changes 1 and 3: location = cumulative count - 1 in
  * token order; P3 description: dedup once per destination rank].

@@ -54,6 +54,29 @@ def dot_scale(row: np.ndarray, dout: np.ndarray, y: np.ndarray) -> np.ndarray:
     return out
 
 
+def gate_bwd_scale(idx: np.ndarray, gate: np.ndarray, dgate_scale: np.ndarray, e: int, renorm: int,
+                   logits: np.ndarray | None = None) -> np.ndarray:
+    """Condition scale of the gate backward per logit, float64 [s, e]:
+    fac_i * (dgate_scale(i) + sum_j |g_j| dgate_scale_j), fac = the gate of
+    a selected expert (renorm) or the full-softmax probability (no renorm).
+    dgate_scale is |dgate| for an op-level check, or the upstream gate
+    gradient's own scale when dgate was computed in floating point."""
+    s, k = idx.shape
+    ii = idx.astype(np.int64)
+    ds = np.abs(np.asarray(dgate_scale, np.float64))
+    c = np.sum(np.abs(gate.astype(np.float64)) * ds, axis=1, keepdims=True)
+    dg = np.zeros((s, e))
+    np.put_along_axis(dg, ii, ds, 1)
+    if renorm:
+        fac = np.zeros((s, e))
+        np.put_along_axis(fac, ii, np.abs(gate.astype(np.float64)), 1)
+    else:
+        l = logits.astype(np.float64)
+        p = np.exp(l - l.max(axis=1, keepdims=True))
+        fac = p / p.sum(axis=1, keepdims=True)
+    return fac * (dg + c)
+
+
 def assert_close(gpu: np.ndarray, ora: np.ndarray, scale: np.ndarray | None, what: str):
     """Apply the rule for the array's type (uint16 = bf16 bits, float32)."""
     assert gpu.shape == ora.shape, f"{what}: shape {gpu.shape} vs {ora.shape}"

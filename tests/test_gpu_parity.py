@@ -87,6 +87,27 @@ def test_empty_batch():
         assert h.status() == 0
 
 
+@pytest.mark.parametrize("renorm", [0, 1])
+@pytest.mark.parametrize("name", ["tiny-capacity", "mixtral-dropless", "fine-grained-skewed", "gshard-capacity",
+                                  "diffusiongemma-replay"])
+def test_gate_backward_parity(name, renorm):
+    """Full token counts of each workload; the oracle's ids and gates and a
+    seeded upstream gradient feed both sides."""
+    w = W.WORKLOADS[name]
+    logits = W.make_logits(w)
+    oi, og = oracle.topk_gate(logits.numpy(), w.k, renorm)
+    dgate = W.random_gates(w.s, w.k, seed=9).numpy() - 0.5
+    dl = B.moe_topk_gate_bwd(logits.to(DEV) if not renorm else None, to_dev(oi, DEV), to_dev(og, DEV),
+                             to_dev(dgate, DEV), w.e, renorm)
+    ref = oracle.topk_gate_bwd(logits.numpy(), oi, og, dgate, w.e, renorm)
+    got = bits(dl)
+    T.assert_close(got, ref, T.gate_bwd_scale(oi, og, dgate, w.e, renorm, logits.numpy()), "dlogits")
+    if renorm:
+        sel = np.zeros_like(got, bool)
+        np.put_along_axis(sel, oi.astype(np.int64), True, 1)
+        assert np.all(got[~sel] == 0)
+
+
 # ------------------------------------------------------------- full sizes --
 
 def _sample_rows(n, count, gen):

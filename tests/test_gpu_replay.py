@@ -115,3 +115,34 @@ def test_autograd_matches_oracle(dtype, capacity):
         OdX = bits(torch.from_numpy(OdX).to(torch.bfloat16))
     Odx = oracle.dispatch_bwd(L["row"], OdX)
     T.assert_close(bits(x.grad), Odx, T.combine_scale(L["row"], None, OdX), "x.grad")
+
+
+@pytest.mark.parametrize("renorm", [0, 1])
+def test_router_gradient_through_the_whole_path(renorm):
+    """logits -> top-k gate -> layout -> dispatch -> expert (2x) -> combine ->
+    loss; torch.autograd reaches the logits through moe_topk_gate_bwd.  Each op
+    is held to its own bar elsewhere; here the chain (GPU gates feed the GPU
+    ops) is compared with the oracle's chain within 1e-5 of the scale."""
+    s, m, e, k = 600, 64, 32, 4
+    w = W.Workload("chain", s=s, m=m, e=e, k=k, dtype="f32", capacity=0, R=0, seed=41)
+    inp = W.make_inputs(w)
+    logits = inp["logits"].to(DEV).requires_grad_(True)
+    idx, gate = A.topk_gate(logits, k, renorm)
+    h = B.moe_dispatch_layout(idx, e)
+    X = A.dispatch(inp["x"].to(DEV), h)
+    out = A.combine(X * 2, gate, h)
+    dout = inp["dout"].to(DEV)
+    out.backward(dout)
+
+    lg = inp["logits"].numpy()
+    oi, og = oracle.topk_gate(lg, k, renorm)
+    np.testing.assert_array_equal(bits(idx), oi)
+    L = oracle.layout(oi, e)
+    Oy = (oracle.dispatch(L["row"], inp["x"].numpy(), L["rows"]) * 2).astype(np.float32)
+    _, Odg = oracle.combine_bwd(L["row"], og, inp["dout"].numpy(), Oy)
+    Odl = oracle.topk_gate_bwd(lg, oi, og, Odg, e, renorm)
+    got = bits(logits.grad)
+    # the upstream gate gradient carries its own fp32 error, on the scale sum |dout * y|
+    scale = T.gate_bwd_scale(oi, og, T.dot_scale(L["row"], inp["dout"].numpy(), Oy), e, renorm, lg)
+    bad = np.abs(got.astype(np.float64) - Odl) > 1e-5 * scale + 1e-30
+    assert not bad.any(), (int(bad.sum()), np.abs(got - Odl).max())
