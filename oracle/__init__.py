@@ -45,11 +45,12 @@ def lib() -> ctypes.CDLL:
         L.ora_topk_gate.argtypes = [P, I, I, I, I, P, P]
         L.ora_layout.argtypes = [P, I, I, I, I, I, P, P, P, P, P, P, P, P]
         L.ora_topk_gate_bwd.argtypes = [P, P, P, P, I, I, I, I, P]
+        L.ora_layout_ex.argtypes = [P, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P]
         L.ora_dispatch.argtypes = [P, I, I, I, I, P, I, P]
         L.ora_combine.argtypes = [P, P, I, I, I, I, P, P]
         L.ora_combine_bwd.argtypes = [P, P, I, I, I, I, P, P, I, P, P]
         L.ora_dispatch_bwd.argtypes = [P, I, I, I, I, P, P]
-        for f in ("ora_topk_gate", "ora_topk_gate_bwd", "ora_layout", "ora_dispatch", "ora_combine",
+        for f in ("ora_topk_gate", "ora_topk_gate_bwd", "ora_layout", "ora_layout_ex", "ora_dispatch", "ora_combine",
                   "ora_combine_bwd", "ora_dispatch_bwd"):
             getattr(L, f).restype = I
         _lib = L
@@ -110,7 +111,10 @@ def topk_gate_bwd(logits: np.ndarray | None, idx: np.ndarray, gate: np.ndarray, 
     return dl
 
 
-def layout(idx: np.ndarray, e: int, capacity: int = 0, R: int = 0) -> dict:
+def layout(idx: np.ndarray, e: int, capacity: int = 0, R: int = 0, priority: int = 0, pad_multiple: int = 1) -> dict:
+    """Dispatch layout; priority 0 = token order, 1 = k-major; pad_multiple
+    pads each expert's dropless rows to a multiple (rows is then the upper
+    bound s*k + e*(pad_multiple - 1))."""
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     s, k = idx.shape
     out = dict(
@@ -119,11 +123,12 @@ def layout(idx: np.ndarray, e: int, capacity: int = 0, R: int = 0) -> dict:
         token_in_rank=np.empty((s, R), np.uint8) if R else None,
         rank_counts=np.empty(R, np.int32) if R else None,
     )
-    rc = lib().ora_layout(_p(idx), s, e, k, int(capacity), int(R), _p(out["loc"]), _p(out["row"]),
-                          _p(out["drop"]), _p(out["raw_counts"]), _p(out["counts"]), _p(out["offsets"]),
-                          _p(out["token_in_rank"]), _p(out["rank_counts"]))
+    rc = lib().ora_layout_ex(_p(idx), s, e, k, int(capacity), int(R), int(priority), int(pad_multiple),
+                             _p(out["loc"]), _p(out["row"]), _p(out["drop"]), _p(out["raw_counts"]),
+                             _p(out["counts"]), _p(out["offsets"]), _p(out["token_in_rank"]),
+                             _p(out["rank_counts"]))
     _check(rc, "layout")
-    out["rows"] = e * capacity if capacity > 0 else s * k
+    out["rows"] = e * capacity if capacity > 0 else s * k + e * (pad_multiple - 1)
     return out
 
 

@@ -148,13 +148,15 @@ int ora_topk_gate_bwd(const float* logits, const int32_t* idx, const float* gate
 
 /* -------------------------------------------------------------- layout -- */
 
-int ora_layout(const int32_t* idx, int s, int e, int k, int capacity, int R,
-               int32_t* loc, int32_t* row, uint8_t* drop,
-               int32_t* raw_counts, int32_t* counts, int32_t* offsets,
-               uint8_t* token_in_rank, int32_t* rank_counts) {
+int ora_layout_ex(const int32_t* idx, int s, int e, int k, int capacity, int R, int priority,
+                  int pad_multiple, int32_t* loc, int32_t* row, uint8_t* drop,
+                  int32_t* raw_counts, int32_t* counts, int32_t* offsets,
+                  uint8_t* token_in_rank, int32_t* rank_counts) {
   if (!idx || !loc || !row || !drop || !raw_counts || !counts || !offsets) return ORA_EARG;
   if (s < 0 || e < 1 || k < 1 || k > e || capacity < 0 || R < 0) return ORA_EARG;
   if (R > 0 && (e % R != 0 || !token_in_rank || !rank_counts)) return ORA_EARG;
+  if ((priority != 0 && priority != 1) || pad_multiple < 1) return ORA_EARG;
+  if (pad_multiple > 1 && capacity > 0) return ORA_EARG;
 
   /* every expert id in range and distinct within its token */
   for (int t = 0; t < s; ++t)
@@ -165,16 +167,26 @@ int ora_layout(const int32_t* idx, int s, int e, int k, int capacity, int R,
         if (idx[(size_t)t * k + jj] == x) return ORA_EROUTE;
     }
 
-  /* location = running count of earlier tokens routed to the same expert,
-   * i.e. (cumulative sum of the one-hot mask over tokens) - 1 */
+  /* location = running count of earlier routes to the same expert, in the
+   * priority order: tokens in order (each token's routes together), or
+   * route slot by route slot (all first choices, then all second ...) */
   int32_t* run = (int32_t*)calloc((size_t)e, sizeof(int32_t));
   if (!run) return ORA_EARG;
-  for (int t = 0; t < s; ++t)
-    for (int j = 0; j < k; ++j) {
-      int32_t x = idx[(size_t)t * k + j];
-      loc[(size_t)t * k + j] = run[x];
-      run[x] += 1;
-    }
+  if (priority == 0) {
+    for (int t = 0; t < s; ++t)
+      for (int j = 0; j < k; ++j) {
+        int32_t x = idx[(size_t)t * k + j];
+        loc[(size_t)t * k + j] = run[x];
+        run[x] += 1;
+      }
+  } else {
+    for (int j = 0; j < k; ++j)
+      for (int t = 0; t < s; ++t) {
+        int32_t x = idx[(size_t)t * k + j];
+        loc[(size_t)t * k + j] = run[x];
+        run[x] += 1;
+      }
+  }
   for (int x = 0; x < e; ++x) raw_counts[x] = run[x];
   free(run);
 
@@ -189,7 +201,10 @@ int ora_layout(const int32_t* idx, int s, int e, int k, int capacity, int R,
   } else {
     for (int x = 0; x < e; ++x) counts[x] = raw_counts[x];
     offsets[0] = 0;
-    for (int x = 0; x < e; ++x) offsets[x + 1] = offsets[x] + counts[x];
+    for (int x = 0; x < e; ++x) {
+      int padded = (counts[x] + pad_multiple - 1) / pad_multiple * pad_multiple;
+      offsets[x + 1] = offsets[x] + padded;
+    }
     for (size_t r = 0; r < (size_t)s * k; ++r) {
       drop[r] = 0;
       row[r] = offsets[idx[r]] + loc[r];
@@ -209,6 +224,14 @@ int ora_layout(const int32_t* idx, int s, int e, int k, int capacity, int R,
     }
   }
   return ORA_OK;
+}
+
+int ora_layout(const int32_t* idx, int s, int e, int k, int capacity, int R,
+               int32_t* loc, int32_t* row, uint8_t* drop,
+               int32_t* raw_counts, int32_t* counts, int32_t* offsets,
+               uint8_t* token_in_rank, int32_t* rank_counts) {
+  return ora_layout_ex(idx, s, e, k, capacity, R, 0, 1, loc, row, drop, raw_counts, counts,
+                       offsets, token_in_rank, rank_counts);
 }
 
 /* ------------------------------------------------------------ dispatch -- */

@@ -99,6 +99,21 @@ int ora_layout(const int32_t* idx, int s, int e, int k, int capacity, int R,
                int32_t* raw_counts, int32_t* counts, int32_t* offsets,
                uint8_t* token_in_rank, int32_t* rank_counts);
 
+/* Layout variants [P4 change 1: routes ranked for capacity; Automodel #3684
+ * description: HybridEP pads each expert's rows to pad_multiple].
+ * priority = 0: token order (ora_layout).  priority = 1: k-major (all first
+ *   choices before any second choice): loc[t,j] = #{ (t',j') routed to the
+ *   same expert with j' < j, or j' == j and t' < t }.
+ * pad_multiple = P >= 1 (dropless only): each expert's rows are padded to a
+ *   multiple of P: offsets[x+1] = offsets[x] + ceil(counts[x] / P) * P, and
+ *   `rows` = s*k + e*(P-1) is the buffer size the caller allocates (an upper
+ *   bound of offsets[e]).  P = 1 is the plain grouped layout.
+ * Dedup and drops as in ora_layout (drops apply to the k-major locations). */
+int ora_layout_ex(const int32_t* idx, int s, int e, int k, int capacity, int R, int priority,
+                  int pad_multiple, int32_t* loc, int32_t* row, uint8_t* drop,
+                  int32_t* raw_counts, int32_t* counts, int32_t* offsets,
+                  uint8_t* token_in_rank, int32_t* rank_counts);
+
 /* Dispatch [P4 change 3]: X has `rows` rows of m elements; every row is first
  * zero, then X[row[t,j]] = x[t] for each kept route (row >= 0). */
 int ora_dispatch(const int32_t* row, int s, int k, int m, int dtype,

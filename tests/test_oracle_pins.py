@@ -523,3 +523,67 @@ def test_gate_backward_special_cases():
     np.put_along_axis(vf, idx.astype(np.int64), v.astype(np.float64), 1)
     ref = p * (vf - np.sum(p * vf, axis=1, keepdims=True))
     np.testing.assert_allclose(dl, ref, rtol=1e-6, atol=1e-8)
+
+
+# ---------------------------------------------------------- layout variants --
+
+def brute_kmajor_loc(idx):
+    s, k = idx.shape
+    loc = np.zeros_like(idx)
+    for t in range(s):
+        for j in range(k):
+            x = idx[t, j]
+            loc[t, j] = sum(1 for t2 in range(s) for j2 in range(k)
+                            if idx[t2, j2] == x and (j2 < j or (j2 == j and t2 < t)))
+    return loc
+
+
+@pytest.mark.parametrize("cap", [0, 4])
+def test_kmajor_priority_brute_force(cap):
+    idx = W.random_routes(30, 6, 3, seed=12).numpy()
+    L = oracle.layout(idx, 6, cap, priority=1)
+    np.testing.assert_array_equal(L["loc"], brute_kmajor_loc(idx))
+    # closed form: the token-order formula applied to the slot-major route list
+    flat = np.ascontiguousarray(idx.T).reshape(-1, 1)
+    np.testing.assert_array_equal(L["loc"].T.reshape(-1, 1), cumsum_locations(flat, 6))
+    check_invariants_kmajor(idx, 6, cap, L)
+
+
+def check_invariants_kmajor(idx, e, cap, L):
+    s, k = idx.shape
+    drop = L["drop"].astype(bool)
+    assert L["raw_counts"].sum() == s * k
+    assert L["counts"].sum() == s * k - drop.sum()
+    kept = L["row"][~drop]
+    assert len(np.unique(kept)) == len(kept)
+    if cap:
+        # first choices are never dropped while a later choice to the same expert is kept
+        for x in range(e):
+            first_dropped = drop[:, 0] & (idx[:, 0] == x)
+            later_kept = (~drop[:, 1:]) & (idx[:, 1:] == x)
+            assert not (first_dropped.any() and later_kept.any())
+
+
+def test_kmajor_differs_from_token_order_and_matches_hand_example():
+    # the hand-worked example, k-major: expert 0 gets t1 (1st choice), t2 (1st),
+    # then t3 (2nd); expert 1 gets t0 (1st), t3 (1st), then t1 (2nd)
+    g = json.load(open(os.path.join(GOLDEN, "hand_worked_s4_e3_k2.json")))
+    idx = np.array(g["idx"], np.int32)
+    L = oracle.layout(idx, 3, 0, priority=1)
+    assert L["loc"].tolist() == [[0, 0], [0, 2], [1, 1], [1, 2]]
+    assert L["loc"].tolist() != g["loc"]
+
+
+@pytest.mark.parametrize("P", [1, 4, 128])
+def test_pad_multiple_offsets(P):
+    idx = W.random_routes(200, 8, 2, seed=3).numpy()
+    L = oracle.layout(idx, 8, 0, pad_multiple=P)
+    counts = L["counts"]
+    seg = np.diff(L["offsets"])
+    assert np.all(seg % P == 0) and np.all(seg >= counts) and np.all(seg - counts < P)
+    assert L["offsets"][0] == 0 and L["offsets"][-1] <= L["rows"] == 200 * 2 + 8 * (P - 1)
+    base = oracle.layout(idx, 8, 0)
+    np.testing.assert_array_equal(L["loc"], base["loc"])
+    np.testing.assert_array_equal(L["row"], L["offsets"][idx] + L["loc"])
+    with pytest.raises(oracle.OracleError):
+        oracle.layout(idx, 8, capacity=10, pad_multiple=4)
