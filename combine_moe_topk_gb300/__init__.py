@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     moe_dispatch,
     moe_dispatch_bwd,
     moe_dispatch_layout,
+    moe_dispatch_layout_ex,
     moe_launch_count,
     moe_status_string,
     moe_topk_gate,

@@ -33,7 +33,7 @@ EXPORTS = [
     "moe_topk_gate", "moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_combine_bwd",
     "moe_dispatch_bwd", "moe_handle_info", "moe_handle_status", "moe_handle_destroy", "moe_capacity",
     "moe_status_string", "moe_last_error", "moe_launch_count", "moe_debug_hold_layout_tile",
-    "moe_dispatch_layout_noalloc", "moe_topk_gate_bwd",
+    "moe_dispatch_layout_noalloc", "moe_topk_gate_bwd", "moe_dispatch_layout_ex",
 ]
 
 
@@ -44,10 +44,18 @@ class MoEError(RuntimeError):
         super().__init__(f"{where}: {self.name}" + (f" ({detail})" if detail else ""))
 
 
+class LayoutOptions(ctypes.Structure):
+    _fields_ = [("capacity", ctypes.c_int32), ("num_virtual_ranks", ctypes.c_int32), ("priority", ctypes.c_int32),
+                ("pad_multiple", ctypes.c_int32)]
+
+
+PRIORITY = {"token": 0, "kmajor": 1}
+
+
 class LayoutInfo(ctypes.Structure):
     _fields_ = [("s", ctypes.c_int32), ("e", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("capacity", ctypes.c_int32), ("R", ctypes.c_int32), ("rows", ctypes.c_int32),
-                ("device", ctypes.c_int32)] + [
+                ("device", ctypes.c_int32), ("priority", ctypes.c_int32), ("pad_multiple", ctypes.c_int32)] + [
         (n, ctypes.c_void_p) for n in ("idx", "loc", "row", "drop", "raw_counts", "counts", "offsets",
                                        "token_in_rank", "rank_counts", "status")]
 
@@ -68,6 +76,7 @@ def lib() -> ctypes.CDLL:
             "moe_topk_gate": [P, I, I, I, I, P, P, P, P],
             "moe_topk_gate_bwd": [P, P, P, P, I, I, I, I, P, P],
             "moe_dispatch_layout": [P, I, I, I, I, I, P, ctypes.POINTER(P)],
+            "moe_dispatch_layout_ex": [P, I, I, I, ctypes.POINTER(LayoutOptions), P, ctypes.POINTER(P)],
             "moe_dispatch": [P, I, I, I, I, P, P, P],
             "moe_combine": [P, I, I, I, I, P, P, P, P],
             "moe_combine_bwd": [P, I, I, I, I, P, P, P, P, P, P],
@@ -148,6 +157,7 @@ class Handle:
         self.info = info
         self.s, self.e, self.k = info.s, info.e, info.k
         self.capacity, self.R, self.rows = info.capacity, info.R, info.rows
+        self.priority, self.pad_multiple = info.priority, info.pad_multiple
 
     @property
     def raw(self):
@@ -257,6 +267,22 @@ def moe_dispatch_layout(topk_idx: torch.Tensor, e: int, capacity: int = 0, num_v
     rc = lib().moe_dispatch_layout(_ptr(topk_idx), s, int(e), k, int(capacity), int(num_virtual_ranks),
                                    _stream(dev), ctypes.byref(raw))
     _check(rc, "moe_dispatch_layout")
+    return Handle(raw, dev)
+
+
+def moe_dispatch_layout_ex(topk_idx: torch.Tensor, e: int, capacity: int = 0, num_virtual_ranks: int = 0,
+                           priority: str = "token", pad_multiple: int = 1) -> Handle:
+    """Layout with a capacity priority ("token" or "kmajor") and per-expert
+    padding of the dropless rows (handle.rows is then an upper bound)."""
+    if topk_idx.dim() != 2 or topk_idx.dtype != torch.int32:
+        raise ValueError("topk_idx must be int32 [s, k]")
+    s, k = topk_idx.shape
+    opt = LayoutOptions(int(capacity), int(num_virtual_ranks), PRIORITY[priority], int(pad_multiple))
+    raw = ctypes.c_void_p()
+    dev = topk_idx.device
+    rc = lib().moe_dispatch_layout_ex(_ptr(topk_idx), s, int(e), k, ctypes.byref(opt), _stream(dev),
+                                      ctypes.byref(raw))
+    _check(rc, "moe_dispatch_layout_ex")
     return Handle(raw, dev)
 
 

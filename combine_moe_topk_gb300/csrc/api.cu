@@ -21,6 +21,8 @@ struct moe_handle_s {
   int device;
   cudaStream_t stream;
   int s, e, k, capacity, R, rows;
+  int priority, pad;
+  int zero_fill;  // the dispatched buffer has rows no route owns
   void* blob;
   size_t blob_bytes;
   moe::LayoutOut out;
@@ -263,18 +265,26 @@ moe_status moe_topk_gate_bwd(const float* logits, const int32_t* topk_idx, const
   return MOE_OK;
 }
 
-moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity,
-                               int num_virtual_ranks, void* stream, moe_handle* out) {
+moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
+                                  const moe_layout_options* options, void* stream, moe_handle* out) {
   if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
-  const int R = num_virtual_ranks;
+  if (!options) return fail(MOE_ERR_INVALID_ARG, "options is NULL");
+  const int capacity = options->capacity;
+  const int R = options->num_virtual_ranks;
+  const int priority = options->priority;
+  const int pad = options->pad_multiple < 1 ? 1 : options->pad_multiple;
+  if (priority != MOE_PRIORITY_TOKEN && priority != MOE_PRIORITY_KMAJOR)
+    return fail(MOE_ERR_INVALID_ARG, "unknown priority");
+  if (pad > 1 && capacity > 0) return fail(MOE_ERR_INVALID_ARG, "pad_multiple applies to the dropless layout only");
+  if (pad > 65536) return fail(MOE_ERR_INVALID_ARG, "pad_multiple must be <= 65536");
   if (s < 0 || e < 1 || e > kMaxE || k < 1 || k > e || k > kMaxK)
     return fail(MOE_ERR_INVALID_ARG, "need s >= 0, 1 <= e <= 256, 1 <= k <= min(e, 16)");
   if (capacity < 0) return fail(MOE_ERR_INVALID_ARG, "capacity must be >= 0 (0 = dropless)");
   if (R < 0 || R > kMaxR || (R > 0 && e % R != 0))
     return fail(MOE_ERR_INVALID_ARG, "num_virtual_ranks must be in [0, 64] and divide e");
   const long long routes = (long long)s * k;
-  const long long rows = capacity > 0 ? (long long)e * capacity : routes;
+  const long long rows = capacity > 0 ? (long long)e * capacity : routes + (long long)e * (pad - 1);
   if (routes > 2147483647LL || rows > 2147483647LL)
     return fail(MOE_ERR_INVALID_ARG, "s*k and the row count must be < 2^31");
   if (s > 0) MOE_TRY(check_ptr(topk_idx, "topk_idx"));
@@ -294,7 +304,11 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int
   h->capacity = capacity;
   h->R = R;
   h->rows = (int)rows;
-  h->plan = moe::plan_layout(s, e, *di);
+  h->priority = priority;
+  h->pad = pad;
+  h->zero_fill = capacity > 0 || pad > 1;
+  // the scan runs over s*k one-route units in k-major order
+  h->plan = moe::plan_layout(priority == MOE_PRIORITY_KMAJOR ? s * k : s, e, *di);
 
   // one blob: [zeroed: status, rank_counts, look-back words] then the rest
   const size_t A = 256;
@@ -343,8 +357,8 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int
     }
   }
   if (err == cudaSuccess)
-    err = moe::launch_layout(topk_idx, s, e, k, capacity, R, h->plan, h->out, hold, timeout_ns,
-                             h->stream);
+    err = moe::launch_layout(topk_idx, s, e, k, capacity, R, priority, pad, h->plan, h->out, hold,
+                             timeout_ns, h->stream);
   if (err != cudaSuccess) {
     cudaFreeAsync(h->blob, h->stream);
     delete h;
@@ -359,6 +373,16 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int
   return MOE_OK;
 }
 
+moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity,
+                               int num_virtual_ranks, void* stream, moe_handle* out) {
+  moe_layout_options opt;
+  opt.capacity = capacity;
+  opt.num_virtual_ranks = num_virtual_ranks;
+  opt.priority = MOE_PRIORITY_TOKEN;
+  opt.pad_multiple = 1;
+  return moe_dispatch_layout_ex(topk_idx, s, e, k, &opt, stream, out);
+}
+
 moe_status moe_handle_info(moe_handle h, moe_layout_info* info) {
   MOE_TRY(live_handle(h));
   if (!info) return fail(MOE_ERR_INVALID_ARG, "info is NULL");
@@ -369,6 +393,8 @@ moe_status moe_handle_info(moe_handle h, moe_layout_info* info) {
   info->R = h->R;
   info->rows = h->rows;
   info->device = h->device;
+  info->priority = h->priority;
+  info->pad_multiple = h->pad;
   info->idx = h->out.idx;
   info->loc = h->out.loc;
   info->row = h->out.row;
@@ -424,8 +450,9 @@ moe_status moe_dispatch(moe_handle h, int s, int rows, int m, moe_dtype dtype, c
   if (rows == 0) return MOE_OK;
   const moe::DeviceInfo* di = nullptr;
   MOE_TRY(device_state(h->device, &di));
-  cudaError_t err = moe::launch_dispatch(h->out.row, h->out.counts, s, h->k, h->e, h->capacity, x, X,
-                                         rb, h->out.status, *di, static_cast<cudaStream_t>(stream));
+  cudaError_t err = moe::launch_dispatch(h->out.row, h->out.counts, h->out.offsets, s, h->k, h->e,
+                                         h->capacity, h->rows, h->zero_fill, x, X, rb, h->out.status, *di,
+                                         static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "dispatch launch");
   g_launches[MOE_KERNEL_DISPATCH]++;
   return MOE_OK;
@@ -476,9 +503,9 @@ moe_status moe_combine_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype
   for (int i = 0; i < 5; ++i) MOE_TRY(check_device_ptr(ptrs[i], names[i], h->device));
   const moe::DeviceInfo* di = nullptr;
   MOE_TRY(device_state(h->device, &di));
-  cudaError_t err = moe::launch_combine_bwd(h->out.row, h->out.counts, gate, s, h->k, h->e, h->capacity,
-                                            m, dtype == MOE_F32 ? 0 : 1, dout, y, dY, dgate, *di,
-                                            static_cast<cudaStream_t>(stream));
+  cudaError_t err = moe::launch_combine_bwd(h->out.row, h->out.counts, h->out.offsets, h->rows,
+                                            h->zero_fill, gate, s, h->k, h->e, m, dtype == MOE_F32 ? 0 : 1,
+                                            dout, y, dY, dgate, *di, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "combine_bwd launch");
   g_launches[MOE_KERNEL_COMBINE_BWD]++;
   return MOE_OK;

@@ -114,7 +114,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __rest
 template <typename T, int KMAX, int UNR>
 __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     const int32_t* __restrict__ row, const int32_t* __restrict__ counts,
-    const float* __restrict__ gate, int s, int k, int e, int capacity, int nvec,
+    const int32_t* __restrict__ offsets, long long rows, int zero_fill,
+    const float* __restrict__ gate, int s, int k, int e, int nvec,
     const uint4* __restrict__ dout, const uint4* __restrict__ y, uint4* __restrict__ dY,
     float* __restrict__ dgate) {
   constexpr int N = Vec<T>::N;
@@ -183,14 +184,11 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
   }
   pdl_trigger_late();
 
-  // capacity mode: slots no kept route owns get zero gradient
-  if (capacity > 0) {
-    const long long E = (long long)e * capacity;
+  // rows no kept route owns (capacity slots, padding) get zero gradient
+  if (zero_fill) {
     const uint4 z = make_uint4(0, 0, 0, 0);
-    for (long long rr = gw; rr < E; rr += warps) {
-      const int x = (int)(rr / capacity);
-      const int slot = (int)(rr - (long long)x * capacity);
-      if (slot < __ldg(counts + x)) continue;
+    for (long long rr = gw; rr < rows; rr += warps) {
+      if (row_is_owned(rr, offsets, counts, e)) continue;
       uint4* dst = dY + (size_t)rr * nvec;
       for (int v = lane; v < nvec; v += 32) st_stream(dst + v, z);
     }
@@ -240,18 +238,19 @@ cudaError_t combine_t(const int32_t* row, const float* gate, int s, int k, int m
 }
 
 template <typename T, int KMAX>
-cudaError_t combine_bwd_t(const int32_t* row, const int32_t* counts, const float* gate, int s,
-                          int k, int e, int capacity, int m, const void* dout, const void* y,
-                          void* dY, float* dgate, const DeviceInfo& di, cudaStream_t st) {
+cudaError_t combine_bwd_t(const int32_t* row, const int32_t* counts, const int32_t* offsets,
+                          long long rows, int zero_fill, const float* gate, int s, int k, int e,
+                          int m, const void* dout, const void* y, void* dY, float* dgate,
+                          const DeviceInfo& di, cudaStream_t st) {
   constexpr int UNR = MOE_CMB_BWD_LOADS / KMAX > 1 ? MOE_CMB_BWD_LOADS / KMAX : 1;
   const int nvec = m / Vec<T>::N;
   auto kern = combine_bwd_kernel<T, KMAX, UNR>;
   static const int bps = occupancy(kern);
   long long warps = s;
-  if (capacity > 0 && (long long)e * capacity > warps) warps = (long long)e * capacity;
+  if (zero_fill && rows > warps) warps = rows;
   return launch_pdl(MOE_KERNEL_COMBINE_BWD, kern, dim3(grid_for(warps, di, bps)), dim3(kThreads), 0, st,
-                    row, counts, gate, s,
-                    k, e, capacity, nvec, static_cast<const uint4*>(dout),
+                    row, counts, offsets, rows, zero_fill, gate, s, k, e, nvec,
+                    static_cast<const uint4*>(dout),
                     static_cast<const uint4*>(y), static_cast<uint4*>(dY), dgate);
 }
 
@@ -265,16 +264,18 @@ cudaError_t combine_k(const int32_t* row, const float* gate, int s, int k, int m
 }
 
 template <typename T>
-cudaError_t combine_bwd_k(const int32_t* row, const int32_t* counts, const float* gate, int s,
-                          int k, int e, int capacity, int m, const void* dout, const void* y,
-                          void* dY, float* dgate, const DeviceInfo& di, cudaStream_t st) {
-  if (k <= 2)
-    return combine_bwd_t<T, 2>(row, counts, gate, s, k, e, capacity, m, dout, y, dY, dgate, di, st);
-  if (k <= 4)
-    return combine_bwd_t<T, 4>(row, counts, gate, s, k, e, capacity, m, dout, y, dY, dgate, di, st);
-  if (k <= 8)
-    return combine_bwd_t<T, 8>(row, counts, gate, s, k, e, capacity, m, dout, y, dY, dgate, di, st);
-  return combine_bwd_t<T, 16>(row, counts, gate, s, k, e, capacity, m, dout, y, dY, dgate, di, st);
+cudaError_t combine_bwd_k(const int32_t* row, const int32_t* counts, const int32_t* offsets,
+                          long long rows, int zero_fill, const float* gate, int s, int k, int e,
+                          int m, const void* dout, const void* y, void* dY, float* dgate,
+                          const DeviceInfo& di, cudaStream_t st) {
+#define MOE_CBWD(KM)                                                                              \
+  combine_bwd_t<T, KM>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout, y, dY, dgate, \
+                       di, st)
+  if (k <= 2) return MOE_CBWD(2);
+  if (k <= 4) return MOE_CBWD(4);
+  if (k <= 8) return MOE_CBWD(8);
+  return MOE_CBWD(16);
+#undef MOE_CBWD
 }
 
 }  // namespace
@@ -285,14 +286,15 @@ cudaError_t launch_combine(const int32_t* row, const float* gate, int s, int k, 
   return combine_k<__nv_bfloat16>(row, gate, s, k, m, y, out, di, st);
 }
 
-cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const float* gate, int s,
-                               int k, int e, int capacity, int m, int dtype, const void* dout,
-                               const void* y, void* dY, float* dgate, const DeviceInfo& di,
-                               cudaStream_t st) {
+cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const int32_t* offsets,
+                               long long rows, int zero_fill, const float* gate, int s, int k,
+                               int e, int m, int dtype, const void* dout, const void* y, void* dY,
+                               float* dgate, const DeviceInfo& di, cudaStream_t st) {
   if (dtype == 0)
-    return combine_bwd_k<float>(row, counts, gate, s, k, e, capacity, m, dout, y, dY, dgate, di, st);
-  return combine_bwd_k<__nv_bfloat16>(row, counts, gate, s, k, e, capacity, m, dout, y, dY, dgate,
-                                      di, st);
+    return combine_bwd_k<float>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout, y, dY,
+                                dgate, di, st);
+  return combine_bwd_k<__nv_bfloat16>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout,
+                                      y, dY, dgate, di, st);
 }
 
 }  // namespace moe

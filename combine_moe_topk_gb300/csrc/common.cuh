@@ -66,6 +66,22 @@ __device__ __forceinline__ void pdl_trigger_late() {
   if (MOE_PDL == 2) grid_dependents_launch();
 }
 
+// ------------------------------------------------------- row ownership -----
+// Row r of a dispatched buffer whose expert segments are [offsets[x],
+// offsets[x+1]) holds a route iff it lies in the first counts[x] rows of its
+// segment (capacity slots past the count, per-expert padding and rows past
+// offsets[e] hold none).  Binary search over the e + 1 offsets.
+template <typename P>
+__device__ __forceinline__ bool row_is_owned(long long r, const P* offsets, const P* counts, int e) {
+  if (r >= (long long)offsets[e]) return false;
+  int lo = 0, hi = e;  // offsets[lo] <= r < offsets[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((long long)offsets[mid] <= r) lo = mid; else hi = mid;
+  }
+  return r - (long long)offsets[lo] < (long long)counts[lo];
+}
+
 // ------------------------------------------------------ 16-byte vectors ----
 
 template <typename T>

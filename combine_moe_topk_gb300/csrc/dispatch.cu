@@ -52,7 +52,10 @@ struct Params {
   char* X;
   const int32_t* row;
   const int32_t* counts;
+  const int32_t* offsets;
   int s, k, e, capacity;
+  long long rows;   // rows of X
+  int zero_fill;    // X has rows no route owns (capacity slots, padding): zero them
   long long row_bytes;
   int piece;       // bytes per unit (multiple of 16)
   int npieces;     // units per token row
@@ -71,6 +74,7 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const Params p) {
   __shared__ int b_rows[kBatch * kMaxK];
   __shared__ unsigned b_mask[kBatch];
   __shared__ int s_counts[kMaxE];
+  __shared__ int s_offsets[kMaxE + 1];
 
   const int lane = threadIdx.x;
   const long long G = gridDim.x, b = blockIdx.x;
@@ -84,8 +88,10 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const Params p) {
   }
   grid_dependency_wait();
   pdl_trigger_early();
-  if (p.capacity > 0)
+  if (p.zero_fill) {
     for (int x = lane; x < p.e; x += 32) s_counts[x] = __ldg(p.counts + x);
+    for (int x = lane; x <= p.e; x += 32) s_offsets[x] = __ldg(p.offsets + x);
+  }
   __syncwarp();
 
   // ---- unit iterator (uniform across the warp) ----------------------------
@@ -186,20 +192,17 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const Params p) {
   }
 
   pdl_trigger_late();
-  // ---- zero tail of the capacity buffer -----------------------------------
-  if (p.capacity > 0) {
+  // ---- rows no route owns: capacity slots past counts, padding ------------
+  if (p.zero_fill) {
     bulk_wait_all();
     __syncwarp();
     uint4* z = reinterpret_cast<uint4*>(buf);
     for (int i = lane; i < p.stage_stride / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     __syncwarp();
-    const long long E = (long long)p.e * p.capacity;
-    const long long r0 = E * b / G, r1 = E * (b + 1) / G;
+    const long long r0 = p.rows * b / G, r1 = p.rows * (b + 1) / G;
     for (long long r = r0 + lane; r < r1; r += 32) {
-      const int x = (int)(r / p.capacity);
-      const int slot = (int)(r - (long long)x * p.capacity);
-      if (slot < s_counts[x]) continue;
+      if (row_is_owned(r, s_offsets, s_counts, p.e)) continue;
       for (int pc = 0; pc < p.npieces; ++pc) {
         const long long off = (long long)pc * p.piece;
         const uint32_t bytes = (uint32_t)min((long long)p.piece, p.row_bytes - off);
@@ -242,12 +245,9 @@ __global__ void __launch_bounds__(256) dispatch_ldg_kernel(const Params p) {
       }
     }
   }
-  if (p.capacity > 0) {
-    const long long E = (long long)p.e * p.capacity;
-    for (long long rr = gw; rr < E; rr += warps) {
-      const int xe = (int)(rr / p.capacity);
-      const int slot = (int)(rr - (long long)xe * p.capacity);
-      if (slot < __ldg(p.counts + xe)) continue;
+  if (p.zero_fill) {
+    for (long long rr = gw; rr < p.rows; rr += warps) {
+      if (row_is_owned(rr, p.offsets, p.counts, p.e)) continue;
       for (int v = lane; v < nvec; v += 32) st_stream(X + (size_t)rr * nvec + v, make_uint4(0, 0, 0, 0));
     }
   }
@@ -276,9 +276,10 @@ Config choose(long long row_bytes, const DeviceInfo& di) {
 
 }  // namespace
 
-cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, int s, int k, int e,
-                            int capacity, const void* x, void* X, long long row_bytes,
-                            int32_t* status, const DeviceInfo& di, cudaStream_t st) {
+cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, const int32_t* offsets, int s,
+                            int k, int e, int capacity, long long rows, int zero_fill, const void* x,
+                            void* X, long long row_bytes, int32_t* status, const DeviceInfo& di,
+                            cudaStream_t st) {
   // allow the kernel the device's whole opt-in shared memory (less its static
   // part) once per device; occupancy still follows the dynamic size launched
   static bool opted_in[64] = {};
@@ -301,6 +302,9 @@ cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, int s, in
   p.X = static_cast<char*>(X);
   p.row = row;
   p.counts = counts;
+  p.offsets = offsets;
+  p.rows = rows;
+  p.zero_fill = zero_fill;
   p.s = s;
   p.k = k;
   p.e = e;
@@ -314,8 +318,8 @@ cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, int s, in
   p.timeout_ns = 2000000000LL;
 
   long long work = s;
-  if (capacity > 0) {
-    const long long zero_groups = ((long long)e * capacity + 31) / 32;
+  if (zero_fill) {
+    const long long zero_groups = (rows + 31) / 32;
     if (zero_groups > work) work = zero_groups;
   }
   long long grid = (long long)di.sms * c.ctas_per_sm;

@@ -46,9 +46,12 @@ struct LayoutOut {
   int32_t* status;
 };
 
+// priority 0 = token order, 1 = k-major; pad_multiple >= 1 pads dropless
+// expert segments.  The plan must be made for s units (s * k when k-major).
 cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity, int R,
-                          const LayoutPlan& plan, const LayoutOut& out, int hold_tile,
-                          long long timeout_ns, cudaStream_t st);
+                          int priority, int pad_multiple, const LayoutPlan& plan,
+                          const LayoutOut& out, int hold_tile, long long timeout_ns,
+                          cudaStream_t st);
 
 // Allocation-free layout: the look-back scratch is a file-scope device array
 // of noalloc_lookback_words() words; returns cudaErrorInvalidValue (and sets
@@ -58,18 +61,21 @@ cudaError_t launch_layout_noalloc(const int32_t* topk_idx, int s, int e, int k, 
                                   const LayoutOut& out, int* words_needed, cudaStream_t st);
 
 // --- dispatch (bulk-copy gather) -----------------------------------------
-cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, int s, int k, int e,
-                            int capacity, const void* x, void* X, long long row_bytes,
-                            int32_t* status, const DeviceInfo& di, cudaStream_t st);
+// zero_fill: X has rows no route owns (capacity slots past the count,
+// per-expert padding); they are written with zeros.
+cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, const int32_t* offsets, int s,
+                            int k, int e, int capacity, long long rows, int zero_fill, const void* x,
+                            void* X, long long row_bytes, int32_t* status, const DeviceInfo& di,
+                            cudaStream_t st);
 
 // --- combine family -----------------------------------------------------
 // dtype: 0 = f32, 1 = bf16.  gate == nullptr means unit weights.
 cudaError_t launch_combine(const int32_t* row, const float* gate, int s, int k, int m, int dtype,
                            const void* y, void* out, const DeviceInfo& di, cudaStream_t st);
 
-cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const float* gate, int s,
-                               int k, int e, int capacity, int m, int dtype, const void* dout,
-                               const void* y, void* dY, float* dgate, const DeviceInfo& di,
-                               cudaStream_t st);
+cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const int32_t* offsets,
+                               long long rows, int zero_fill, const float* gate, int s, int k,
+                               int e, int m, int dtype, const void* dout, const void* y, void* dY,
+                               float* dgate, const DeviceInfo& di, cudaStream_t st);
 
 }  // namespace moe

@@ -57,14 +57,30 @@ constexpr int kMaxLookbackWords = 16384;  // tiles * padded e, at most: bounds t
 
 __host__ __device__ inline int padded_e(int e) { return (e + 3) & ~3; }
 
+// The scan runs over "units" in priority order.  Token-major priority: a
+// unit is a token with its k routes.  k-major priority (every first choice
+// before any second choice): a unit is one route, units ordered slot by slot,
+// so the same token-order scan over s*k one-route units gives k-major slots.
 struct Params {
   const int32_t* topk_idx;
-  int s, e, k, capacity, R;
+  int s, e, k;           // units, experts, routes per unit
+  int s_tok, k_tok;      // tokens and routes per token of the caller's arrays
+  int kmajor;            // units are single routes in slot-major order
+  int capacity, R;       // R: dedup ranks counted in this kernel (0 in k-major mode)
+  int R_tok;             // the caller's dedup rank count
+  int pad;               // dropless rows per expert padded to a multiple of pad
   int tiles, subtiles_per_tile;
   LayoutOut out;
   int hold_tile;
   long long timeout_ns;
 };
+
+// Index of unit v's first route in the caller's [s_tok, k_tok] arrays.
+__device__ __forceinline__ size_t unit_base(const Params& p, int v) {
+  if (!p.kmajor) return (size_t)v * p.k;
+  const int j = v / p.s_tok;
+  return (size_t)(v - j * p.s_tok) * p.k_tok + j;
+}
 
 __device__ __forceinline__ uint4 ld_relaxed_v4(const uint4* p) {
   uint4 v;
@@ -87,7 +103,7 @@ __device__ __forceinline__ bool all_published(const uint4& w) {
 // which routes are valid: in range and not a repeat of an earlier route of
 // the same token.
 __device__ __forceinline__ unsigned load_routes(const Params& p, int t, int* xs) {
-  const int32_t* src = p.topk_idx + (size_t)t * p.k;
+  const int32_t* src = p.topk_idx + unit_base(p, t);
   if ((p.k & 3) == 0) {
 #pragma unroll
     for (int j4 = 0; j4 < kMaxK / 4; ++j4)
@@ -221,7 +237,7 @@ __device__ void expert_offsets(const Params& p, const int* s_tot, int* s_off, bo
     const int x = lane * 8 + i;
     raw[i] = x < p.e ? s_tot[x] : 0;
     v[i] = p.capacity > 0 ? min(raw[i], p.capacity) : raw[i];
-    sum += v[i];
+    sum += (v[i] + p.pad - 1) / p.pad * p.pad;  // rows of the expert's segment
   }
   int incl = sum;
 #pragma unroll
@@ -242,7 +258,7 @@ __device__ void expert_offsets(const Params& p, const int* s_tot, int* s_off, bo
         p.out.offsets[x] = off;
       }
     }
-    run += v[i];
+    run += (v[i] + p.pad - 1) / p.pad * p.pad;
   }
   if (lane == 31) {
     const int end = p.capacity > 0 ? p.e * p.capacity : run;
@@ -298,9 +314,10 @@ __device__ __forceinline__ unsigned long long write_routes(const Params& p, int 
     }
     if (row[j] < 0) dropw[j / 4] |= 1u << (8 * (j % 4));
   }
-  store_route_ints(p.out.loc + (size_t)t * p.k, loc, p.k);
-  store_route_ints(p.out.row + (size_t)t * p.k, row, p.k);
-  uint8_t* dr = p.out.drop + (size_t)t * p.k;
+  const size_t q0 = unit_base(p, t);
+  store_route_ints(p.out.loc + q0, loc, p.k);
+  store_route_ints(p.out.row + q0, row, p.k);
+  uint8_t* dr = p.out.drop + q0;
   if ((p.k & 3) == 0) {
 #pragma unroll
     for (int j4 = 0; j4 < kMaxK / 4; ++j4)
@@ -376,7 +393,7 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
       if (sub0 + r < sub1 && t < p.s) {
         valid[r] = load_routes(p, t, xs[r]);
         bad |= valid[r] != (1u << p.k) - 1u;
-        store_route_ints(p.out.idx + (size_t)t * p.k, xs[r], p.k);
+        store_route_ints(p.out.idx + unit_base(p, t), xs[r], p.k);
         mark_routes(p, s_mask[r], warp, lane, xs[r], valid[r]);
       }
     }
@@ -400,7 +417,7 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
       if (t < p.s) {
         vy = load_routes(p, t, ys);
         bad |= vy != (1u << p.k) - 1u;
-        store_route_ints(p.out.idx + (size_t)t * p.k, ys, p.k);
+        store_route_ints(p.out.idx + unit_base(p, t), ys, p.k);
         mark_routes(p, s_mask[0], warp, lane, ys, vy);
       }
       __syncthreads();
@@ -490,6 +507,46 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   }
 }
 
+// k-major mode: the per-token work the unit scan cannot do -- expert ids
+// repeated within a token, and the dedup rank sets -- from the rows the scan
+// wrote.  One thread per token.
+__global__ void __launch_bounds__(kThreads) token_ranks_kernel(const Params p) {
+  __shared__ int s_rank[kMaxR];
+  __shared__ int s_bad;
+  const int tid = threadIdx.x, lane = tid & 31;
+  grid_dependency_wait();
+  if (tid < kMaxR) s_rank[tid] = 0;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  const int per_rank = p.R_tok > 0 ? p.e / p.R_tok : 1;
+  bool bad = false;
+  for (int t0 = blockIdx.x * kThreads; t0 < p.s_tok; t0 += gridDim.x * kThreads) {
+    const int t = t0 + tid;
+    unsigned long long ranks = 0;
+    if (t < p.s_tok) {
+      int xs[kMaxK];
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < p.k_tok) {
+          xs[j] = __ldg(p.topk_idx + (size_t)t * p.k_tok + j);
+          if (__ldg(p.out.row + (size_t)t * p.k_tok + j) >= 0) ranks |= 1ull << (xs[j] / per_rank);
+#pragma unroll
+          for (int jj = 0; jj < j; ++jj)
+            if (xs[jj] == xs[j]) bad = true;
+        }
+      if (p.R_tok > 0) {
+        uint8_t* tir = p.out.token_in_rank + (size_t)t * p.R_tok;
+        for (int r = 0; r < p.R_tok; ++r) tir[r] = (uint8_t)((ranks >> r) & 1ull);
+      }
+    }
+    if (p.R_tok > 0) count_ranks(ranks, lane, s_rank);
+  }
+  if (bad) atomicOr(&s_bad, 1);
+  __syncthreads();
+  if (p.R_tok > 0 && tid < p.R_tok && s_rank[tid]) atomicAdd(&p.out.rank_counts[tid], s_rank[tid]);
+  if (tid == 0 && s_bad) raise_status(p.out.status, MOE_DEV_BAD_ROUTE);
+}
+
 int blocks_per_sm(const void* kern) {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, 0) != cudaSuccess) return 0;
@@ -524,15 +581,21 @@ int layout_blocks_per_sm() {
 }
 
 cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity, int R,
-                          const LayoutPlan& plan, const LayoutOut& out, int hold_tile,
-                          long long timeout_ns, cudaStream_t st) {
+                          int priority, int pad_multiple, const LayoutPlan& plan,
+                          const LayoutOut& out, int hold_tile, long long timeout_ns,
+                          cudaStream_t st) {
   Params p;
   p.topk_idx = topk_idx;
-  p.s = s;
+  p.kmajor = priority == 1;
+  p.s = p.kmajor ? s * k : s;
   p.e = e;
-  p.k = k;
+  p.k = p.kmajor ? 1 : k;
+  p.s_tok = s;
+  p.k_tok = k;
   p.capacity = capacity;
-  p.R = R;
+  p.R = p.kmajor ? 0 : R;
+  p.R_tok = R;
+  p.pad = pad_multiple > 1 ? pad_multiple : 1;
   p.tiles = plan.tiles;
   p.subtiles_per_tile = plan.subtiles_per_tile;
   p.out = out;
@@ -549,9 +612,19 @@ cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capa
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (plan.subtiles_per_tile == 1) return cudaLaunchKernelEx(&cfg, layout_kernel<1>, p);
-  if (plan.subtiles_per_tile == 2) return cudaLaunchKernelEx(&cfg, layout_kernel<2>, p);
-  return cudaLaunchKernelEx(&cfg, layout_kernel<0>, p);
+  cudaError_t err;
+  if (plan.subtiles_per_tile == 1)
+    err = cudaLaunchKernelEx(&cfg, layout_kernel<1>, p);
+  else if (plan.subtiles_per_tile == 2)
+    err = cudaLaunchKernelEx(&cfg, layout_kernel<2>, p);
+  else
+    err = cudaLaunchKernelEx(&cfg, layout_kernel<0>, p);
+  if (err != cudaSuccess || !p.kmajor || s == 0) return err;
+  constexpr int kMaxPostBlocks = 1024;  // grid-stride beyond this
+  int blocks = (s + kThreads - 1) / kThreads;
+  if (blocks > kMaxPostBlocks) blocks = kMaxPostBlocks;
+  token_ranks_kernel<<<blocks, kThreads, 0, st>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace moe
@@ -629,7 +702,7 @@ cudaError_t launch_layout_noalloc(const int32_t* topk_idx, int s, int e, int k, 
   if (err == cudaSuccess && R > 0)
     err = cudaMemsetAsync(out.rank_counts, 0, (size_t)R * sizeof(int32_t), st);
   if (err != cudaSuccess) return err;
-  return launch_layout(topk_idx, s, e, k, capacity, R, plan, out, -1, 2000000000LL, st);
+  return launch_layout(topk_idx, s, e, k, capacity, R, 0, 1, plan, out, -1, 2000000000LL, st);
 }
 
 }  // namespace moe

@@ -96,8 +96,10 @@ def make_logits(w: Workload, device="cpu", seed: int | None = None) -> torch.Ten
     return logits
 
 
-def make_inputs(w: Workload, device="cpu", seed: int | None = None, with_grad: bool = True) -> dict:
-    """Draw logits [s,e] f32, x [s,m], y [rows,m] and dout [s,m] from one seed."""
+def make_inputs(w: Workload, device="cpu", seed: int | None = None, with_grad: bool = True,
+                rows: int | None = None) -> dict:
+    """Draw logits [s,e] f32, x [s,m], y [rows,m] and dout [s,m] from one seed
+    (rows defaults to the workload's; a padded layout needs more)."""
     seed = w.seed if seed is None else seed
     g = _gen(device, seed)
     logits = torch.randn(w.s, w.e, generator=g, device=device, dtype=torch.float32)
@@ -108,7 +110,8 @@ def make_inputs(w: Workload, device="cpu", seed: int | None = None, with_grad: b
     x = torch.randn(w.s, w.m, generator=g, device=device, dtype=torch.float32).to(dt)
     out = dict(logits=logits, x=x)
     if with_grad:
-        out["y"] = torch.randn(w.rows, w.m, generator=g, device=device, dtype=torch.float32).to(dt)
+        out["y"] = torch.randn(w.rows if rows is None else rows, w.m, generator=g, device=device,
+                               dtype=torch.float32).to(dt)
         out["dout"] = torch.randn(w.s, w.m, generator=g, device=device, dtype=torch.float32).to(dt)
     return out
 

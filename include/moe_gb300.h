@@ -90,6 +90,21 @@ enum {
  * freed in stream order on the stream it was built on. */
 typedef struct moe_handle_s* moe_handle;
 
+/* Capacity priority of moe_dispatch_layout_ex. */
+enum {
+  MOE_PRIORITY_TOKEN = 0,  /* slots fill in token order, each token's routes together */
+  MOE_PRIORITY_KMAJOR = 1  /* every first choice before any second choice, ... */
+};
+
+/* Options of moe_dispatch_layout_ex. */
+typedef struct {
+  int32_t capacity;          /* slots per expert; 0 = dropless grouped layout        */
+  int32_t num_virtual_ranks; /* dedup ranks R; 0 = none                              */
+  int32_t priority;          /* MOE_PRIORITY_*                                       */
+  int32_t pad_multiple;      /* dropless only: each expert's rows padded to a
+                                multiple of this; 1 (or 0) = no padding            */
+} moe_layout_options;
+
 /* Host view of a handle: sizes and read-only device pointers. */
 typedef struct {
   int32_t s, e, k;
@@ -97,6 +112,8 @@ typedef struct {
   int32_t R;          /* virtual ranks of the dedup counts; 0 = none            */
   int32_t rows;       /* rows of the dispatched buffer: e*capacity, or s*k      */
   int32_t device;     /* CUDA device the handle lives on                        */
+  int32_t priority;   /* MOE_PRIORITY_TOKEN or MOE_PRIORITY_KMAJOR               */
+  int32_t pad_multiple; /* dropless segments padded to a multiple of this (>= 1) */
   const int32_t* idx;           /* [s,k] copy of the expert ids                 */
   const int32_t* loc;           /* [s,k] token-order slot within the expert     */
   const int32_t* row;           /* [s,k] row in the dispatched buffer, -1 = dropped */
@@ -183,6 +200,21 @@ moe_status moe_dispatch_layout_noalloc(const int32_t* topk_idx, int s, int e, in
                                        int32_t* row, uint8_t* drop, int32_t* raw_counts,
                                        int32_t* counts, int32_t* offsets, uint8_t* token_in_rank,
                                        int32_t* rank_counts, int32_t* device_status, void* stream);
+
+/* Dispatch layout with options [P4 change 1: the routes' capacity ranking;
+ * Automodel #3684 description: per-expert padding of the grouped rows].
+ * As moe_dispatch_layout, plus:
+ *   priority = MOE_PRIORITY_KMAJOR: loc[t,j] counts the routes to the same
+ *     expert with j' < j, or j' == j and t' < t (GShard's order: a first
+ *     choice is never dropped for a later choice of another token);
+ *   pad_multiple = P > 1 (dropless only): offsets[x+1] = offsets[x] +
+ *     ceil(counts[x] / P) * P; the handle's rows is the upper bound
+ *     s*k + e*(P-1), so it stays a host integer; dispatch and the combine
+ *     backward write zeros into padding rows and rows past offsets[e].
+ * Errors as moe_dispatch_layout; pad_multiple > 1 with capacity > 0, or an
+ * unknown priority, is MOE_ERR_INVALID_ARG. */
+moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
+                                  const moe_layout_options* options, void* stream, moe_handle* out);
 
 /* Dispatch [P4 change 3; P4 change 2 for the [e, c, m] layout].
  * x [s,m] -> X [rows,m]: X[row[t,j]] = x[t] for every kept route; in

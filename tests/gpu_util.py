@@ -38,11 +38,16 @@ def check_layout(h: B.Handle, L: dict, idx: np.ndarray):
         np.testing.assert_array_equal(bits(h.rank_counts()), L["rank_counts"], err_msg="rank_counts")
 
 
-def full_parity(w, dev, renorm=None, seed=None):
+def full_parity(w, dev, renorm=None, seed=None, priority="token", pad_multiple=1):
     """Run gate -> layout -> dispatch -> combine -> combine_bwd -> dispatch_bwd
-    on the GPU and in the oracle on the same seeded inputs; compare all."""
+    on the GPU and in the oracle on the same seeded inputs; compare all.
+    priority / pad_multiple select a layout variant (moe_dispatch_layout_ex)."""
     renorm = w.renorm if renorm is None else renorm
-    inp = W.make_inputs(w, seed=seed)
+    if pad_multiple > 1:
+        w = w.replace(capacity=0)
+    # a padded layout's buffer has e * (pad_multiple - 1) more rows than the workload's
+    rows = w.rows + (w.e * (pad_multiple - 1) if pad_multiple > 1 else 0)
+    inp = W.make_inputs(w, seed=seed, rows=rows)
     g = {k: v.to(dev) for k, v in inp.items()}
 
     # gate
@@ -52,8 +57,13 @@ def full_parity(w, dev, renorm=None, seed=None):
     T.assert_gates_close(bits(gate), og)
 
     # layout on the oracle's ids (equal to the GPU's, asserted above)
-    h = B.moe_dispatch_layout(to_dev(oi, dev), w.e, w.capacity, w.R)
-    L = oracle.layout(oi, w.e, w.capacity, w.R)
+    if priority == "token" and pad_multiple == 1:
+        h = B.moe_dispatch_layout(to_dev(oi, dev), w.e, w.capacity, w.R)
+    else:
+        h = B.moe_dispatch_layout_ex(to_dev(oi, dev), w.e, w.capacity, w.R, priority, pad_multiple)
+    L = oracle.layout(oi, w.e, w.capacity, w.R, priority=1 if priority == "kmajor" else 0,
+                      pad_multiple=pad_multiple)
+    assert h.rows == L["rows"]
     check_layout(h, L, oi)
     row = L["row"]
 

@@ -32,6 +32,23 @@ def test_reduced_full_parity(name):
     full_parity(REDUCED[name], DEV)
 
 
+@pytest.mark.parametrize("name", ["tiny-capacity", "gshard-capacity", "fine-grained-skewed", "mixtral-dropless"])
+def test_kmajor_priority_parity(name):
+    """GShard's order: every first choice before any second choice."""
+    full_parity(REDUCED[name], DEV, priority="kmajor")
+
+
+@pytest.mark.parametrize("pad", [4, 128])
+@pytest.mark.parametrize("name", ["mixtral-dropless", "fine-grained-skewed", "diffusiongemma-replay"])
+def test_padded_grouped_layout_parity(name, pad):
+    """Dropless rows padded per expert to a multiple: padding rows are zero."""
+    full_parity(REDUCED[name], DEV, pad_multiple=pad)
+
+
+def test_kmajor_with_padding_and_dedup():
+    full_parity(REDUCED["fine-grained-skewed"].replace(s=1500), DEV, priority="kmajor", pad_multiple=8)
+
+
 def test_tiny_capacity_full_softmax_gates():
     full_parity(W.WORKLOADS["tiny-capacity"], DEV, renorm=0)
 
