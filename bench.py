@@ -100,6 +100,23 @@ def traffic_record(op: str):
     return r
 
 
+def max_over_ranks(values, dist, device=None):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the
+    job's time); identity without a process group."""
+    if dist is None:
+        return list(values)
+    import torch
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_gbs(world: int, bytes_per_step: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank moves bytes_per_step per step."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- clocks --
 
 class ClockSampler:
@@ -283,15 +300,12 @@ def run_ours(args, rank: int, world: int, dist):
     # ---- end to end: pinned host inputs in, results out, every step ----------
     e2e = run_e2e(w, S, step, buffers, dev, max(3, min(K, 50)), args.warmup)
 
-    if dist is not None:
-        t = torch.tensor([elapsed_ms, e2e["ms"]], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, e2e["ms"] = float(t[0]), float(t[1])
+    elapsed_ms, e2e["ms"] = max_over_ranks([elapsed_ms, e2e["ms"]], dist, dev)
     if rank != 0:
         return None
 
     ms_per_step = elapsed_ms / K
-    value = world * step_total / (ms_per_step * 1e-3) / 1e9
+    value = job_gbs(world, step_total, ms_per_step)
     peak, peak_src = peaks()
     dom = max(per_op, key=per_op.get)
     achieved = nbytes[dom] / (per_op[dom] * 1e-3) / 1e9
@@ -337,7 +351,7 @@ def run_ours(args, rank: int, world: int, dist):
             "traffic_note": (tr.get("note") if tr else "no ncu capture of this kernel source"),
             "algorithmic_bytes": nbytes[dom],
         },
-        "e2e": {"value": round(world * step_total / (e2e["ms"] * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(job_gbs(world, step_total, e2e["ms"]), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e["ms"], 4), "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"], "how": e2e["how"]},
         "gpu_launches": launches,

@@ -1,0 +1,80 @@
+"""Host-side pieces of bench.py that need no GPU: the byte model, the
+max-over-ranks aggregation on a two-process gloo group, and the reference
+arm's rank behaviour under a multi-process launch."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from combine_moe_topk_gb300 import workloads as W  # noqa: E402
+
+
+def test_byte_model_of_the_mixtral_like_step():
+    w = W.WORKLOADS["mixtral-dropless"]
+    b = bench.step_bytes(w, kept=w.s * w.k, u=w.s)
+    x = w.s * w.m * 2  # 67,108,864
+    assert x == 67108864
+    # dispatch: x once + 2x written (+ the row indices); combine: 2x read + x written (+ rows, gates)
+    assert b["dispatch"] == 3 * x + w.s * w.k * 4
+    assert b["combine"] == 3 * x + w.s * w.k * 8
+    assert b["combine_bwd"] == 5 * x + w.s * w.k * 12
+    assert b["dispatch_bwd"] == 3 * x + w.s * w.k * 4
+    assert bench.payload_bytes(w, w.s * w.k, w.s) == {"dispatch": 3 * x, "combine": 3 * x}
+
+
+def test_byte_model_counts_the_capacity_zero_tail():
+    w = W.WORKLOADS["gshard-capacity"]
+    kept, u = 150000, 30000
+    b = bench.step_bytes(w, kept, u)
+    rows_bytes = w.e * w.capacity * w.m * 2
+    assert b["dispatch"] == u * w.m * 2 + rows_bytes + w.s * w.k * 4
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    local = [10.0 + rank, 3.0 - rank]
+    got = bench.max_over_ranks(local, dist)
+    q.put((rank, got))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_processes():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert out[0] == out[1] == [11.0, 3.0]
+    assert bench.job_gbs(2, 1_000_000_000, 1.0) == pytest.approx(2000.0)
+    assert bench.max_over_ranks([1.5], None) == [1.5]
+
+
+def test_reference_arm_prints_only_on_rank_zero():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "1", "--workload", "tiny-capacity", "--ref-seconds", "1"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+                        "--warmup", "1", "--workload", "tiny-capacity", "--ref-seconds", "2"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
