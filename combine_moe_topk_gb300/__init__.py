@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     moe_dispatch_bwd,
     moe_dispatch_layout,
     moe_dispatch_layout_ex,
+    moe_grouped_gemm,
     moe_launch_count,
     moe_status_string,
     moe_topk_gate,

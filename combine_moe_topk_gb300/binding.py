@@ -25,7 +25,8 @@ STATUS = {
 }
 MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
 MOE_DEV_NONFINITE, MOE_DEV_BAD_ROUTE, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4
-KERNELS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd", "topk_gate_bwd"]
+KERNELS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd", "topk_gate_bwd",
+           "grouped_gemm"]
 KERNEL_ID = {n: i for i, n in enumerate(KERNELS)}
 
 # every entry point the header declares (checked by the CPU test-suite)
@@ -33,7 +34,7 @@ EXPORTS = [
     "moe_topk_gate", "moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_combine_bwd",
     "moe_dispatch_bwd", "moe_handle_info", "moe_handle_status", "moe_handle_destroy", "moe_capacity",
     "moe_status_string", "moe_last_error", "moe_launch_count", "moe_debug_hold_layout_tile",
-    "moe_dispatch_layout_noalloc", "moe_topk_gate_bwd", "moe_dispatch_layout_ex",
+    "moe_dispatch_layout_noalloc", "moe_topk_gate_bwd", "moe_dispatch_layout_ex", "moe_grouped_gemm",
 ]
 
 
@@ -81,6 +82,7 @@ def lib() -> ctypes.CDLL:
             "moe_combine": [P, I, I, I, I, P, P, P, P],
             "moe_combine_bwd": [P, I, I, I, I, P, P, P, P, P, P],
             "moe_dispatch_bwd": [P, I, I, I, I, P, P, P],
+            "moe_grouped_gemm": [P, I, I, I, P, P, P, P],
             "moe_handle_info": [P, ctypes.POINTER(LayoutInfo)],
             "moe_handle_status": [P, P, ctypes.POINTER(ctypes.c_int32)],
             "moe_handle_destroy": [P],
@@ -351,3 +353,18 @@ def moe_dispatch_bwd(h: Handle, dX: torch.Tensor, dx: torch.Tensor | None = None
     _check(lib().moe_dispatch_bwd(h.raw, s, rows, m, _dtype(dX), _ptr(dX), _ptr(dx), _stream(dX.device)),
            "moe_dispatch_bwd")
     return dx
+
+
+def moe_grouped_gemm(h: Handle, X: torch.Tensor, W: torch.Tensor, Y: torch.Tensor | None = None) -> torch.Tensor:
+    """X bf16 [rows,K], W bf16 [e,N,K] -> Y bf16 [rows,N] per expert segment (tensor cores)."""
+    rows, K = _rows2(X, "X")
+    if W.dim() != 3 or W.shape[0] != h.e or W.shape[2] != K:
+        raise MoEError(1, "moe_grouped_gemm", "W must be [e, N, K]")
+    if X.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise MoEError(3, "moe_grouped_gemm", "X and W must be bf16")
+    N = W.shape[1]
+    if Y is None:
+        Y = torch.empty(rows, N, dtype=torch.bfloat16, device=X.device)
+    _check(lib().moe_grouped_gemm(h.raw, rows, K, N, _ptr(X), _ptr(W), _ptr(Y), _stream(X.device)),
+           "moe_grouped_gemm")
+    return Y

@@ -383,6 +383,36 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int
   return moe_dispatch_layout_ex(topk_idx, s, e, k, &opt, stream, out);
 }
 
+moe_status moe_grouped_gemm(moe_handle h, int rows, int K, int N, const void* X, const void* W,
+                            void* Y, void* stream) {
+  MOE_TRY(live_handle(h));
+  if (rows != h->rows) return fail(MOE_ERR_HANDLE_MISMATCH, "row count differs from the handle's");
+  if (K < 64 || K % 64 != 0) return fail(MOE_ERR_INVALID_ARG, "K must be a positive multiple of 64");
+  if (N < 256 || N % 256 != 0) return fail(MOE_ERR_INVALID_ARG, "N must be a positive multiple of 256");
+  if ((long long)rows * K > 2147483647LL * 16 || (long long)h->e * N > 2147483647LL)
+    return fail(MOE_ERR_INVALID_ARG, "operands too large");
+  const bool aligned = h->capacity > 0 ? (h->capacity % 128 == 0) : (h->pad % 128 == 0);
+  if (!aligned)
+    return fail(MOE_ERR_UNSUPPORTED,
+                "segments must start on multiples of 128 rows: use pad_multiple (or capacity) a multiple of 128");
+  if (rows == 0) return MOE_OK;
+  MOE_TRY(check_ptr(X, "X"));
+  MOE_TRY(check_ptr(W, "W"));
+  MOE_TRY(check_ptr(Y, "Y"));
+  MOE_TRY(handle_device(h));
+  MOE_TRY(check_device_ptr(X, "X", h->device));
+  MOE_TRY(check_device_ptr(W, "W", h->device));
+  MOE_TRY(check_device_ptr(Y, "Y", h->device));
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(h->device, &di));
+  cudaError_t err = moe::launch_grouped_gemm(h->out.offsets, h->out.counts, h->e, rows, K, N, X, W, Y,
+                                             h->out.status, *di, static_cast<cudaStream_t>(stream));
+  if (err == cudaErrorInvalidValue) return fail(MOE_ERR_CUDA, "tensor-map encoding failed (driver entry point)");
+  if (err != cudaSuccess) return cuda_fail(err, "grouped_gemm launch");
+  g_launches[MOE_KERNEL_GROUPED_GEMM]++;
+  return MOE_OK;
+}
+
 moe_status moe_handle_info(moe_handle h, moe_layout_info* info) {
   MOE_TRY(live_handle(h));
   if (!info) return fail(MOE_ERR_INVALID_ARG, "info is NULL");

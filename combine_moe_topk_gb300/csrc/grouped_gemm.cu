@@ -1,0 +1,362 @@
+// grouped_gemm.cu -- the expert-grouped GEMM that consumes the dispatched
+// buffer, on the 5th-generation tensor cores (tcgen05, TMEM accumulators,
+// TMA tile loads).
+//
+// DeepSpeed #8213 "Add an opt-in DeepEP transport for the AutoEP expert
+// all-to-all", description: the dispatch groups arrivals by expert for the
+// grouped GEMM, whose groups are bounded by offsets = cumsum(counts).
+// Automodel #3684 "perf(moe): reuse the DeepEP dispatch layout on
+// activation-checkpoint recompute": each expert's rows padded to a multiple
+// (pad_multiple), which is what lets a 128-row tile never straddle experts.
+//
+// Y[r] = X[r] . W[x]^T for every 128-row block of expert x's segment that a
+// route owns (blocks entirely past counts[x] are skipped).  X [rows, K],
+// W [e, N, K] and Y [rows, N] are bf16, row-major; the accumulation is fp32
+// in TMEM.  One CTA per SM, persistent over (block, 256-column) tiles:
+//   warp 0 lane 0  -- TMA producer: A (128 x 64) and B (256 x 64) K-blocks
+//                     into a 4-stage SWIZZLE_128B ring, mbarrier complete_tx;
+//   warp 1 lane 0  -- MMA issuer: four tcgen05.mma (M128 N256 K16) per
+//                     K-block into one of two 256-column TMEM accumulators,
+//                     tcgen05.commit frees the ring stage / hands over the tile;
+//   warp 2         -- allocates (and at the end frees) 512 TMEM columns;
+//   warps 4..7     -- epilogue: tcgen05.ld 32 lanes x 32 columns at a time,
+//                     fp32 -> bf16 (nearest-even), 16-byte stores.
+// Every mbarrier wait is bounded on the global timer; a time-out records
+// MOE_DEV_TIMEOUT and the roles wind down to the TMEM release.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;  // 16 KB
+constexpr int kBBytes = BN * BK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kTmemCols = 2 * BN;     // two fp32 accumulators of 128 lanes x 256 columns
+constexpr int kThreads = 256;
+constexpr int kMaxE = 256;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+
+struct GemmParams {
+  const int32_t* offsets;
+  const int32_t* counts;
+  int e, rows, K, N;
+  __nv_bfloat16* Y;
+  int32_t* status;
+  long long timeout_ns;
+};
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A
+// and B, both K-major, M = 128, N = 256.
+__device__ __forceinline__ uint32_t mma_idesc() {
+  uint32_t d = 0;
+  d |= 1u << 4;                        // accumulator format: f32
+  d |= 1u << 7;                        // A format: bf16
+  d |= 1u << 10;                       // B format: bf16
+  d |= (uint32_t)(BN >> 3) << 17;      // N / 8
+  d |= (uint32_t)(BM >> 4) << 24;      // M / 16
+  return d;
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle (as TMA writes
+// it), 8-row groups 1024 bytes apart.  The tile base is 1024-byte aligned.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3ffffu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                    // leading byte offset (unused when swizzled)
+  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
+  d |= (uint64_t)1 << 46;                    // descriptor version
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* sdst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(sdst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, int accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns of TMEM into registers.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Expert of the 128-row block starting at r0, or -1 when no route owns a row
+// of it (past offsets[e], or entirely past the expert's count).
+__device__ __forceinline__ int block_expert(int r0, const int* s_off, const int* s_cnt, int e) {
+  if (r0 >= s_off[e]) return -1;
+  int lo = 0, hi = e;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_off[mid] <= r0) lo = mid; else hi = mid;
+  }
+  return r0 - s_off[lo] < s_cnt[lo] ? lo : -1;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_off[kMaxE + 1], s_cnt[kMaxE];
+  __shared__ int s_err;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+  const uint64_t deadline = globaltimer_ns() + (uint64_t)p.timeout_ns;
+
+  for (int x = threadIdx.x; x <= p.e; x += kThreads) s_off[x] = __ldg(p.offsets + x);
+  for (int x = threadIdx.x; x < p.e; x += kThreads) s_cnt[x] = __ldg(p.counts + x);
+  if (threadIdx.x == 0) {
+    s_err = 0;
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
+
+  const int ntn = p.N / BN;
+  const int nunits = ((p.rows + BM - 1) / BM) * ntn;
+  const int kblocks = p.K / BK;
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer ----------------------------------------------------
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      const int r0 = (u / ntn) * BM, n0 = (u % ntn) * BN;
+      const int x = block_expert(r0, s_off, s_cnt, p.e);
+      if (x < 0) continue;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, deadline)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem + stage * kStageBytes;
+        mbar_arrive_expect_tx(&full[stage], kStageBytes);
+        tma_load_2d(sa, &tmA, kb * BK, r0, &full[stage]);
+        tma_load_2d(sa + kABytes, &tmB, kb * BK, x * p.N + n0, &full[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) atomicOr(&s_err, 1);
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer ------------------------------------------------------
+    const uint32_t idesc = mma_idesc();
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, tphase[2] = {0u, 0u};
+    bool ok = true;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      const int r0 = (u / ntn) * BM;
+      if (block_expert(r0, s_off, s_cnt, p.e) < 0) continue;
+      if (!mbar_wait_bounded(&tempty[acc], tphase[acc] ^ 1u, deadline)) {
+        ok = false;
+        break;
+      }
+      tphase[acc] ^= 1u;
+      tc_fence_after();
+      const uint32_t dt = tbase + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_bounded(&full[stage], phase, deadline)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_addr(smem + stage * kStageBytes);
+        const uint64_t ad = smem_desc(sa), bd = smem_desc(sa + kABytes);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 per MMA: advance 32 bytes in the swizzled row
+          mma_bf16(dt, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (kb | kk) != 0);
+        mma_commit(&empty[stage]);  // the ring stage is free once these MMAs have read it
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      mma_commit(&tfull[acc]);  // the accumulator is complete
+      acc ^= 1;
+    }
+    if (!ok) atomicOr(&s_err, 1);
+  } else if (warp >= 4) {
+    // ---- epilogue: TMEM -> registers -> bf16 -> Y ------------------------
+    const int ew = warp - 4;  // TMEM lanes 32*ew .. 32*ew+31
+    int acc = 0;
+    uint32_t tphase[2] = {0u, 0u};
+    bool ok = true;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      const int r0 = (u / ntn) * BM, n0 = (u % ntn) * BN;
+      if (block_expert(r0, s_off, s_cnt, p.e) < 0) continue;
+      if (!mbar_wait_bounded(&tfull[acc], tphase[acc], deadline)) {
+        ok = false;
+        break;
+      }
+      tphase[acc] ^= 1u;
+      tc_fence_after();
+      const int r = r0 + 32 * ew + lane;
+      const bool in_range = r < p.rows;  // a block never crosses offsets[e] <= rows; guard anyway
+      __nv_bfloat16* yrow = p.Y + (size_t)(in_range ? r : 0) * p.N + n0;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + ((uint32_t)(32 * ew) << 16) + (uint32_t)(acc * BN + 32 * c), v);
+        uint4 out[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float f[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v[8 * q + i]);
+          out[q] = Vec<__nv_bfloat16>::from_float(f);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(yrow + 32 * c);
+        if (in_range)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = out[q];
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+    }
+    if (!ok) atomicOr(&s_err, 1);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),
+                 "r"(kTmemCols)
+                 : "memory");
+  if (threadIdx.x == 0 && s_err) raise_status(p.status, MOE_DEV_TIMEOUT);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 row-major [outer, inner] tensor, box (BK inner) x box_rows, 128-B swizzle.
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {BK, box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(const int32_t* offsets, const int32_t* counts, int e, int rows, int K,
+                                int N, const void* X, const void* W, void* Y, int32_t* status,
+                                const DeviceInfo& di, cudaStream_t st) {
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, X, (uint64_t)K, (uint64_t)rows, BM) ||
+      !make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN))
+    return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err != cudaSuccess) return err;
+    attr = true;
+  }
+  GemmParams p;
+  p.offsets = offsets;
+  p.counts = counts;
+  p.e = e;
+  p.rows = rows;
+  p.K = K;
+  p.N = N;
+  p.Y = static_cast<__nv_bfloat16*>(Y);
+  p.status = status;
+  p.timeout_ns = 2000000000LL;
+  const int nunits = ((rows + BM - 1) / BM) * (N / BN);
+  int grid = di.sms < nunits ? di.sms : nunits;
+  if (grid < 1) grid = 1;
+  grouped_gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

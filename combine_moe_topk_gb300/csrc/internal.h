@@ -78,4 +78,11 @@ cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const 
                                int e, int m, int dtype, const void* dout, const void* y, void* dY,
                                float* dgate, const DeviceInfo& di, cudaStream_t st);
 
+// --- expert-grouped GEMM on the tensor cores -----------------------------
+// Y[r] = X[r] . W[x]^T over the 128-row blocks of each expert segment that a
+// route owns.  K % 64 == 0, N % 256 == 0, segments 128-row aligned.
+cudaError_t launch_grouped_gemm(const int32_t* offsets, const int32_t* counts, int e, int rows, int K,
+                                int N, const void* X, const void* W, void* Y, int32_t* status,
+                                const DeviceInfo& di, cudaStream_t st);
+
 }  // namespace moe

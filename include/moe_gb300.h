@@ -79,7 +79,8 @@ enum {
   MOE_KERNEL_COMBINE_BWD = 4,
   MOE_KERNEL_DISPATCH_BWD = 5,
   MOE_KERNEL_TOPK_GATE_BWD = 6,
-  MOE_KERNEL_COUNT = 7
+  MOE_KERNEL_GROUPED_GEMM = 7,
+  MOE_KERNEL_COUNT = 8
 };
 
 /* Opaque layout handle [P1 "How"; P3 description].  Owned by the library:
@@ -248,6 +249,25 @@ moe_status moe_combine_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype
  * accumulated in fp32 as in moe_combine. */
 moe_status moe_dispatch_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype,
                             const void* dX, void* dx, void* stream);
+
+/* Expert-grouped GEMM over the dispatched buffer, on the tensor cores
+ * [P3 description: the dispatch groups arrivals by expert for the grouped
+ * GEMM, groups bounded by offsets; Automodel #3684 description: per-expert
+ * padding of the rows (pad_multiple)].  For every 128-row block of expert
+ * x's segment [offsets[x], offsets[x+1]) that holds at least one kept route:
+ *   Y[r, :] = X[r, :] . W[x]^T   (bf16 in, fp32 accumulation, bf16 out,
+ *                                 round to nearest-even)
+ * X bf16 [rows, K] (the output of moe_dispatch), W bf16 [e, N, K] (each
+ * expert's weight N x K with K contiguous), Y bf16 [rows, N].  Rows of
+ * blocks that hold no route are not written.  Requires every segment to
+ * start on a multiple of 128 rows: a padded layout (moe_dispatch_layout_ex,
+ * pad_multiple a multiple of 128) or capacity a multiple of 128; K a
+ * multiple of 64; N a multiple of 256; rows equal to the handle's.
+ * tcgen05 MMA with TMEM accumulators, TMA-fed; the expert of each block is
+ * read from the handle on the device.  Errors: MOE_ERR_INVALID_ARG,
+ * MOE_ERR_UNSUPPORTED (unaligned segments), MOE_ERR_HANDLE_MISMATCH. */
+moe_status moe_grouped_gemm(moe_handle h, int rows, int K, int N, const void* X, const void* W,
+                            void* Y, void* stream);
 
 /* Fill *info with the handle's sizes and device pointers (valid until the
  * handle is destroyed). */

@@ -178,3 +178,19 @@ def dispatch_bwd(row: np.ndarray, dX: np.ndarray) -> np.ndarray:
     dx = np.empty((s, m), dX.dtype)
     _check(lib().ora_dispatch_bwd(_p(row), s, k, m, _dtype_code(dX), _p(dX), _p(dx)), "dispatch_bwd")
     return dx
+
+
+def grouped_gemm(X: np.ndarray, W: np.ndarray, offsets: np.ndarray, counts: np.ndarray) -> np.ndarray:
+    """Y[r] = X[r] . W[x]^T in float64 for the rows a route owns (the first
+    counts[x] rows of expert x's segment); other rows NaN.  X [rows,K] and W
+    [e,N,K] as float32 or bf16-as-uint16.  One library matmul per expert."""
+    def f64(a):
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64) if a.dtype == np.uint16 \
+            else a.astype(np.float64)
+    Xf, Wf = f64(X), f64(W)
+    Y = np.full((X.shape[0], W.shape[1]), np.nan)
+    for x in range(W.shape[0]):
+        r0, n = int(offsets[x]), int(counts[x])
+        if n:
+            Y[r0:r0 + n] = Xf[r0:r0 + n] @ Wf[x].T
+    return Y
