@@ -175,7 +175,7 @@ moe_status moe_topk_gate_bwd(const float* logits, const int32_t* topk_idx, const
 moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity,
                                int num_virtual_ranks, void* stream, moe_handle* out);
 
-/* Allocation-free dispatch layout.  No counterpart on the pages: an
+/* Allocation-free dispatch layout.  The paper has no counterpart: an
  * addition of this library for callers that cannot allocate device memory
  * when they build a layout (inside a captured CUDA graph where a pool
  * allocation is unwanted, from an allocator's own hook that must not
@@ -187,7 +187,7 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int
  * [R] int32 (ignored when R = 0).  device_status (nullable): an int32 in
  * device memory that gets MOE_DEV_* bits OR-ed in (the caller zeroes it).
  * It calls no allocating routine.  The kernel's scratch (its look-back
- * words, tiles x e of them) is a fixed library array of 16384 words (128 KB)
+ * words, tiles x e of them) is a fixed library array of 16384 32-bit words (64 KB)
  * per device, held until the process exits.  The tile plan keeps tiles x e
  * within 16384 for every accepted size; a plan that would need more returns
  * MOE_ERR_UNSUPPORTED (use moe_dispatch_layout) instead of overrunning it.  Every call shares
