@@ -26,7 +26,7 @@ STATUS = {
 MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
 MOE_DEV_NONFINITE, MOE_DEV_BAD_ROUTE, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4
 KERNELS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd", "topk_gate_bwd",
-           "grouped_gemm"]
+           "grouped_gemm", "dispatch_gemm"]
 KERNEL_ID = {n: i for i, n in enumerate(KERNELS)}
 
 # every entry point the header declares (checked by the CPU test-suite)
@@ -35,6 +35,7 @@ EXPORTS = [
     "moe_dispatch_bwd", "moe_handle_info", "moe_handle_status", "moe_handle_destroy", "moe_capacity",
     "moe_status_string", "moe_last_error", "moe_launch_count", "moe_debug_hold_layout_tile",
     "moe_dispatch_layout_noalloc", "moe_topk_gate_bwd", "moe_dispatch_layout_ex", "moe_grouped_gemm",
+    "moe_dispatch_grouped_gemm",
 ]
 
 
@@ -58,7 +59,7 @@ class LayoutInfo(ctypes.Structure):
                 ("capacity", ctypes.c_int32), ("R", ctypes.c_int32), ("rows", ctypes.c_int32),
                 ("device", ctypes.c_int32), ("priority", ctypes.c_int32), ("pad_multiple", ctypes.c_int32)] + [
         (n, ctypes.c_void_p) for n in ("idx", "loc", "row", "drop", "raw_counts", "counts", "offsets",
-                                       "token_in_rank", "rank_counts", "status")]
+                                       "token_in_rank", "rank_counts", "status", "inv_row")]
 
 
 _lib = None
@@ -83,6 +84,7 @@ def lib() -> ctypes.CDLL:
             "moe_combine_bwd": [P, I, I, I, I, P, P, P, P, P, P],
             "moe_dispatch_bwd": [P, I, I, I, I, P, P, P],
             "moe_grouped_gemm": [P, I, I, I, P, P, P, P],
+            "moe_dispatch_grouped_gemm": [P, I, I, I, I, P, P, P, P],
             "moe_handle_info": [P, ctypes.POINTER(LayoutInfo)],
             "moe_handle_status": [P, P, ctypes.POINTER(ctypes.c_int32)],
             "moe_handle_destroy": [P],
@@ -184,6 +186,7 @@ class Handle:
     def offsets(self): return self._view("offsets", (self.e + 1,), "<i4")
     def token_in_rank(self): return self._view("token_in_rank", (self.s, self.R), "|u1")
     def rank_counts(self): return self._view("rank_counts", (self.R,), "<i4")
+    def inv_row(self): return self._view("inv_row", (self.rows,), "<i4")
 
     def status(self) -> int:
         """Synchronise and read the device status word (MOE_DEV_* bits)."""
@@ -367,4 +370,21 @@ def moe_grouped_gemm(h: Handle, X: torch.Tensor, W: torch.Tensor, Y: torch.Tenso
         Y = torch.empty(rows, N, dtype=torch.bfloat16, device=X.device)
     _check(lib().moe_grouped_gemm(h.raw, rows, K, N, _ptr(X), _ptr(W), _ptr(Y), _stream(X.device)),
            "moe_grouped_gemm")
+    return Y
+
+
+def moe_dispatch_grouped_gemm(h: Handle, x: torch.Tensor, W: torch.Tensor,
+                              Y: torch.Tensor | None = None) -> torch.Tensor:
+    """x bf16 [s,K], W bf16 [e,N,K] -> Y bf16 [rows,N]: the grouped GEMM on the
+    token rows gathered through the handle, without a dispatched buffer."""
+    s, K = _rows2(x, "x")
+    if W.dim() != 3 or W.shape[0] != h.e or W.shape[2] != K:
+        raise MoEError(1, "moe_dispatch_grouped_gemm", "W must be [e, N, K]")
+    if x.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise MoEError(3, "moe_dispatch_grouped_gemm", "x and W must be bf16")
+    N = W.shape[1]
+    if Y is None:
+        Y = torch.empty(h.rows, N, dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_dispatch_grouped_gemm(h.raw, s, h.rows, K, N, _ptr(x), _ptr(W), _ptr(Y),
+                                           _stream(x.device)), "moe_dispatch_grouped_gemm")
     return Y

@@ -325,6 +325,7 @@ moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
   const size_t o_cnt = off;    off = align_up(off + 4 * (size_t)e, A);
   const size_t o_off = off;    off = align_up(off + 4 * (size_t)(e + 1), A);
   const size_t o_tir = off;    off = align_up(off + (size_t)s * (R > 0 ? R : 0) + 1, A);
+  const size_t o_inv = off;    off = align_up(off + 4 * (size_t)rows + 4, A);
   h->blob_bytes = off;
 
   cudaError_t err = cudaMallocFromPoolAsync(&h->blob, h->blob_bytes, g_pool[dev], h->stream);
@@ -344,6 +345,7 @@ moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
   h->out.counts = reinterpret_cast<int32_t*>(base + o_cnt);
   h->out.offsets = reinterpret_cast<int32_t*>(base + o_off);
   h->out.token_in_rank = R > 0 ? reinterpret_cast<uint8_t*>(base + o_tir) : nullptr;
+  h->out.inv_row = reinterpret_cast<int32_t*>(base + o_inv);
 
   err = cudaMemsetAsync(base, 0, zero_bytes, h->stream);
   int hold = -1;
@@ -383,34 +385,58 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int
   return moe_dispatch_layout_ex(topk_idx, s, e, k, &opt, stream, out);
 }
 
-moe_status moe_grouped_gemm(moe_handle h, int rows, int K, int N, const void* X, const void* W,
-                            void* Y, void* stream) {
-  MOE_TRY(live_handle(h));
+namespace {
+
+moe_status check_gemm(moe_handle h, int rows, int K, int N, const void* A, const char* a_name,
+                      const void* W, const void* Y) {
   if (rows != h->rows) return fail(MOE_ERR_HANDLE_MISMATCH, "row count differs from the handle's");
   if (K < 64 || K % 64 != 0) return fail(MOE_ERR_INVALID_ARG, "K must be a positive multiple of 64");
   if (N < 256 || N % 256 != 0) return fail(MOE_ERR_INVALID_ARG, "N must be a positive multiple of 256");
-  if ((long long)rows * K > 2147483647LL * 16 || (long long)h->e * N > 2147483647LL)
-    return fail(MOE_ERR_INVALID_ARG, "operands too large");
-  const bool aligned = h->capacity > 0 ? (h->capacity % 128 == 0) : (h->pad % 128 == 0);
-  if (!aligned)
-    return fail(MOE_ERR_UNSUPPORTED,
-                "segments must start on multiples of 128 rows: use pad_multiple (or capacity) a multiple of 128");
+  if ((long long)h->e * N > 2147483647LL) return fail(MOE_ERR_INVALID_ARG, "e * N must be < 2^31");
   if (rows == 0) return MOE_OK;
-  MOE_TRY(check_ptr(X, "X"));
+  MOE_TRY(check_ptr(A, a_name));
   MOE_TRY(check_ptr(W, "W"));
   MOE_TRY(check_ptr(Y, "Y"));
   MOE_TRY(handle_device(h));
-  MOE_TRY(check_device_ptr(X, "X", h->device));
+  MOE_TRY(check_device_ptr(A, a_name, h->device));
   MOE_TRY(check_device_ptr(W, "W", h->device));
   MOE_TRY(check_device_ptr(Y, "Y", h->device));
+  return MOE_OK;
+}
+
+moe_status gemm_result(cudaError_t err, const char* where, int kernel) {
+  if (err == cudaErrorInvalidValue) return fail(MOE_ERR_CUDA, "tensor-map encoding failed (driver entry point)");
+  if (err != cudaSuccess) return cuda_fail(err, where);
+  g_launches[kernel]++;
+  return MOE_OK;
+}
+
+}  // namespace
+
+moe_status moe_grouped_gemm(moe_handle h, int rows, int K, int N, const void* X, const void* W,
+                            void* Y, void* stream) {
+  MOE_TRY(live_handle(h));
+  MOE_TRY(check_gemm(h, rows, K, N, X, "X", W, Y));
+  if (rows == 0) return MOE_OK;
   const moe::DeviceInfo* di = nullptr;
   MOE_TRY(device_state(h->device, &di));
-  cudaError_t err = moe::launch_grouped_gemm(h->out.offsets, h->out.counts, h->e, rows, K, N, X, W, Y,
-                                             h->out.status, *di, static_cast<cudaStream_t>(stream));
-  if (err == cudaErrorInvalidValue) return fail(MOE_ERR_CUDA, "tensor-map encoding failed (driver entry point)");
-  if (err != cudaSuccess) return cuda_fail(err, "grouped_gemm launch");
-  g_launches[MOE_KERNEL_GROUPED_GEMM]++;
-  return MOE_OK;
+  return gemm_result(moe::launch_grouped_gemm(h->out.offsets, h->out.counts, h->e, rows, K, N, X, W, Y,
+                                              h->out.status, *di, static_cast<cudaStream_t>(stream)),
+                     "grouped_gemm launch", MOE_KERNEL_GROUPED_GEMM);
+}
+
+moe_status moe_dispatch_grouped_gemm(moe_handle h, int s, int rows, int K, int N, const void* x,
+                                     const void* W, void* Y, void* stream) {
+  MOE_TRY(live_handle(h));
+  MOE_TRY(check_shape(h, s, rows));
+  MOE_TRY(check_gemm(h, rows, K, N, x, "x", W, Y));
+  if (rows == 0 || s == 0) return MOE_OK;
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(h->device, &di));
+  return gemm_result(moe::launch_dispatch_gemm(h->out.offsets, h->out.counts, h->out.inv_row, h->e, rows, s,
+                                               K, N, x, W, Y, h->out.status, *di,
+                                               static_cast<cudaStream_t>(stream)),
+                     "dispatch_grouped_gemm launch", MOE_KERNEL_DISPATCH_GEMM);
 }
 
 moe_status moe_handle_info(moe_handle h, moe_layout_info* info) {
@@ -435,6 +461,7 @@ moe_status moe_handle_info(moe_handle h, moe_layout_info* info) {
   info->token_in_rank = h->out.token_in_rank;
   info->rank_counts = h->out.rank_counts;
   info->status = h->out.status;
+  info->inv_row = h->out.inv_row;
   return MOE_OK;
 }
 

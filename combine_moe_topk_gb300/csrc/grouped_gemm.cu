@@ -1,26 +1,35 @@
 // grouped_gemm.cu -- the expert-grouped GEMM that consumes the dispatched
-// buffer, on the 5th-generation tensor cores (tcgen05, TMEM accumulators,
-// TMA tile loads).
+// rows, on the 5th-generation tensor cores (tcgen05, TMEM accumulators,
+// TMA tile loads), and its fused form that gathers the token rows itself.
 //
 // DeepSpeed #8213 "Add an opt-in DeepEP transport for the AutoEP expert
 // all-to-all", description: the dispatch groups arrivals by expert for the
 // grouped GEMM, whose groups are bounded by offsets = cumsum(counts).
 // Automodel #3684 "perf(moe): reuse the DeepEP dispatch layout on
-// activation-checkpoint recompute": each expert's rows padded to a multiple
-// (pad_multiple), which is what lets a 128-row tile never straddle experts.
+// activation-checkpoint recompute": each expert's rows may be padded to a
+// multiple (pad_multiple); nothing here needs it.
 //
-// Y[r] = X[r] . W[x]^T for every 128-row block of expert x's segment that a
-// route owns (blocks entirely past counts[x] are skipped).  X [rows, K],
-// W [e, N, K] and Y [rows, N] are bf16, row-major; the accumulation is fp32
-// in TMEM.  One CTA per SM, persistent over (block, 256-column) tiles:
-//   warp 0 lane 0  -- TMA producer: A (128 x 64) and B (256 x 64) K-blocks
-//                     into a 4-stage SWIZZLE_128B ring, mbarrier complete_tx;
+// Y[r] = A[r] . W[x]^T for every row r that a kept route to expert x owns,
+// r in [offsets[x], offsets[x] + counts[x]).  A[r] is the dispatched row
+// X[r] (moe_grouped_gemm) or the token row x[inv_row[r]] (fused dispatch:
+// the dispatched buffer is never written).  bf16 operands, row-major, K
+// contiguous; the accumulation is fp32 in TMEM.  Work units are 128-row
+// blocks of one expert's segment (ceil(counts[x] / 128) of them, the first
+// at offsets[x], so a segment may start on any row) times 256-column tiles
+// of N.  One CTA per SM, persistent over the units:
+//   warp 0         -- TMA producer: B (256 x 64) K-blocks, and A (128 x 64)
+//                     either as one tile load (lane 0) or as 32 four-row
+//                     gathers (tile::gather4, one per lane), into a 4-stage
+//                     SWIZZLE_128B ring, mbarrier complete_tx;
 //   warp 1 lane 0  -- MMA issuer: four tcgen05.mma (M128 N256 K16) per
 //                     K-block into one of two 256-column TMEM accumulators,
 //                     tcgen05.commit frees the ring stage / hands over the tile;
 //   warp 2         -- allocates (and at the end frees) 512 TMEM columns;
+//   warp 3         -- the per-expert block prefix, once;
 //   warps 4..7     -- epilogue: tcgen05.ld 32 lanes x 32 columns at a time,
-//                     fp32 -> bf16 (nearest-even), 16-byte stores.
+//                     fp32 -> bf16 (nearest-even), 16-byte stores of the
+//                     block's owned rows only (a block's tail may belong to
+//                     the next segment or to no route).
 // Every mbarrier wait is bounded on the global timer; a time-out records
 // MOE_DEV_TIMEOUT and the roles wind down to the TMEM release.
 #include <cuda.h>
@@ -46,7 +55,9 @@ constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
 struct GemmParams {
   const int32_t* offsets;
   const int32_t* counts;
+  const int32_t* inv_row;  // gather mode: token of each owned row
   int e, rows, K, N;
+  int s;                   // gather mode: token rows of x
   __nv_bfloat16* Y;
   int32_t* status;
   long long timeout_ns;
@@ -82,6 +93,18 @@ __device__ __forceinline__ void tma_load_2d(void* sdst, const CUtensorMap* map, 
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(sdst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Four rows (r0..r3) of a 2-D map whose box is 64 columns x 1 row, written
+// as four consecutive 128-byte rows at sdst with the map's swizzle.
+__device__ __forceinline__ void tma_gather4(void* sdst, const CUtensorMap* map, int x, int r0, int r1,
+                                            int r2, int r3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(sdst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_addr(bar))
       : "memory");
 }
 
@@ -128,25 +151,38 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Expert of the 128-row block starting at r0, or -1 when no route owns a row
-// of it (past offsets[e], or entirely past the expert's count).
-__device__ __forceinline__ int block_expert(int r0, const int* s_off, const int* s_cnt, int e) {
-  if (r0 >= s_off[e]) return -1;
-  int lo = 0, hi = e;
+// Unit u -> expert x, first row r0 and owned rows of its 128-row block, and
+// the column tile n0.  s_blk[x] = blocks of the experts before x.
+struct Unit {
+  int x, r0, nvalid, n0;
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, int ntn, const int* s_blk, const int* s_off,
+                                            const int* s_cnt, int e) {
+  const int b = u / ntn;
+  int lo = 0, hi = e;  // s_blk[lo] <= b < s_blk[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (s_off[mid] <= r0) lo = mid; else hi = mid;
+    if (s_blk[mid] <= b) lo = mid; else hi = mid;
   }
-  return r0 - s_off[lo] < s_cnt[lo] ? lo : -1;
+  Unit t;
+  const int i = b - s_blk[lo];
+  t.x = lo;
+  t.r0 = s_off[lo] + BM * i;
+  const int left = s_cnt[lo] - BM * i;
+  t.nvalid = left < BM ? left : BM;
+  t.n0 = (u - b * ntn) * BN;
+  return t;
 }
 
+template <bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
   __shared__ uint32_t tmem_base;
-  __shared__ int s_off[kMaxE + 1], s_cnt[kMaxE];
+  __shared__ int s_off[kMaxE + 1], s_cnt[kMaxE], s_blk[kMaxE + 1];
   __shared__ int s_err;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -167,12 +203,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_barrier_init();
   }
+  __syncthreads();
   if (warp == 2) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&tmem_base)),
                  "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  } else if (warp == 3) {
+    // exclusive prefix over experts of their 128-row block counts
+    int carry = 0;
+    for (int x0 = 0; x0 < p.e; x0 += 32) {
+      const int x = x0 + lane;
+      const int c = x < p.e ? s_cnt[x] : 0;
+      int v = c > 0 ? (c + BM - 1) / BM : 0;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int w = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += w;
+      }
+      const int blocks = x < p.e ? (c > 0 ? (c + BM - 1) / BM : 0) : 0;
+      if (x < p.e) s_blk[x] = carry + v - blocks;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) s_blk[p.e] = carry;
   }
   tc_fence_before();
   __syncthreads();
@@ -180,34 +234,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = tmem_base;
 
   const int ntn = p.N / BN;
-  const int nunits = ((p.rows + BM - 1) / BM) * ntn;
+  const int nunits = s_blk[p.e] * ntn;
   const int kblocks = p.K / BK;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ---- TMA producer ----------------------------------------------------
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-      const int r0 = (u / ntn) * BM, n0 = (u % ntn) * BN;
-      const int x = block_expert(r0, s_off, s_cnt, p.e);
-      if (x < 0) continue;
+      const Unit t = decode_unit(u, ntn, s_blk, s_off, s_cnt, p.e);
+      int tok[4] = {0, 0, 0, 0};
+      if (kGather) {
+        // this lane gathers rows 4*lane .. 4*lane+3 of the block; rows no
+        // route owns read token 0 (their results are not stored)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = 4 * lane + i;
+          if (rr < t.nvalid) {
+            const int v = __ldg(p.inv_row + t.r0 + rr);
+            tok[i] = (unsigned)v < (unsigned)p.s ? v : 0;
+          }
+        }
+      }
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, deadline)) {
+        bool waited = true;
+        if (lane == 0) waited = mbar_wait_bounded(&empty[stage], phase ^ 1u, deadline);
+        if (!__shfl_sync(0xffffffffu, waited ? 1 : 0, 0)) {
           ok = false;
           break;
         }
         uint8_t* sa = smem + stage * kStageBytes;
-        mbar_arrive_expect_tx(&full[stage], kStageBytes);
-        tma_load_2d(sa, &tmA, kb * BK, r0, &full[stage]);
-        tma_load_2d(sa + kABytes, &tmB, kb * BK, x * p.N + n0, &full[stage]);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          tma_load_2d(sa + kABytes, &tmB, kb * BK, t.x * p.N + t.n0, &full[stage]);
+          if (!kGather) tma_load_2d(sa, &tmA, kb * BK, t.r0, &full[stage]);
+        }
+        if (kGather) {
+          __syncwarp();
+          tma_gather4(sa + 4 * 128 * lane, &tmA, kb * BK, tok[0], tok[1], tok[2], tok[3], &full[stage]);
+        }
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    if (!ok) atomicOr(&s_err, 1);
+    if (!ok && lane == 0) atomicOr(&s_err, 1);
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ------------------------------------------------------
     const uint32_t idesc = mma_idesc();
@@ -215,8 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0, tphase[2] = {0u, 0u};
     bool ok = true;
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-      const int r0 = (u / ntn) * BM;
-      if (block_expert(r0, s_off, s_cnt, p.e) < 0) continue;
       if (!mbar_wait_bounded(&tempty[acc], tphase[acc] ^ 1u, deadline)) {
         ok = false;
         break;
@@ -253,17 +324,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tphase[2] = {0u, 0u};
     bool ok = true;
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-      const int r0 = (u / ntn) * BM, n0 = (u % ntn) * BN;
-      if (block_expert(r0, s_off, s_cnt, p.e) < 0) continue;
+      const Unit t = decode_unit(u, ntn, s_blk, s_off, s_cnt, p.e);
       if (!mbar_wait_bounded(&tfull[acc], tphase[acc], deadline)) {
         ok = false;
         break;
       }
       tphase[acc] ^= 1u;
       tc_fence_after();
-      const int r = r0 + 32 * ew + lane;
-      const bool in_range = r < p.rows;  // a block never crosses offsets[e] <= rows; guard anyway
-      __nv_bfloat16* yrow = p.Y + (size_t)(in_range ? r : 0) * p.N + n0;
+      const int rr = 32 * ew + lane;
+      const bool owned = rr < t.nvalid && t.r0 + rr < p.rows;
+      __nv_bfloat16* yrow = p.Y + (size_t)(owned ? t.r0 + rr : 0) * p.N + t.n0;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t v[32];
@@ -277,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           out[q] = Vec<__nv_bfloat16>::from_float(f);
         }
         uint4* dst = reinterpret_cast<uint4*>(yrow + 32 * c);
-        if (in_range)
+        if (owned)
 #pragma unroll
           for (int q = 0; q < 4; ++q) dst[q] = out[q];
       }
@@ -326,6 +396,51 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <bool kGather>
+cudaError_t enable_smem(int dev) {
+  static bool done[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (done[dev]) return cudaSuccess;
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<kGather>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (err == cudaSuccess) done[dev] = true;
+  return err;
+}
+
+template <bool kGather>
+cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
+                   const DeviceInfo& di, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = enable_smem<kGather>(dev);
+  if (err != cudaSuccess) return err;
+  // units: at most ceil(rows / 128) + e row blocks (one partial block per
+  // segment), times the column tiles; the kernel reads the exact count
+  const long long blocks = ((long long)p.rows + BM - 1) / BM + p.e;
+  const long long nunits = blocks * (p.N / BN);
+  int grid = (long long)di.sms < nunits ? di.sms : (int)nunits;
+  if (grid < 1) grid = 1;
+  grouped_gemm_kernel<kGather><<<grid, kThreads, kSmemBytes, st>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+GemmParams params(const int32_t* offsets, const int32_t* counts, int e, int rows, int K, int N,
+                  void* Y, int32_t* status) {
+  GemmParams p;
+  p.offsets = offsets;
+  p.counts = counts;
+  p.inv_row = nullptr;
+  p.e = e;
+  p.rows = rows;
+  p.K = K;
+  p.N = N;
+  p.s = 0;
+  p.Y = static_cast<__nv_bfloat16*>(Y);
+  p.status = status;
+  p.timeout_ns = 2000000000LL;
+  return p;
+}
+
 }  // namespace
 
 cudaError_t launch_grouped_gemm(const int32_t* offsets, const int32_t* counts, int e, int rows, int K,
@@ -335,28 +450,20 @@ cudaError_t launch_grouped_gemm(const int32_t* offsets, const int32_t* counts, i
   if (!make_map(&ma, X, (uint64_t)K, (uint64_t)rows, BM) ||
       !make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN))
     return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (err != cudaSuccess) return err;
-    attr = true;
-  }
-  GemmParams p;
-  p.offsets = offsets;
-  p.counts = counts;
-  p.e = e;
-  p.rows = rows;
-  p.K = K;
-  p.N = N;
-  p.Y = static_cast<__nv_bfloat16*>(Y);
-  p.status = status;
-  p.timeout_ns = 2000000000LL;
-  const int nunits = ((rows + BM - 1) / BM) * (N / BN);
-  int grid = di.sms < nunits ? di.sms : nunits;
-  if (grid < 1) grid = 1;
-  grouped_gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(ma, mb, p);
-  return cudaGetLastError();
+  return launch<false>(ma, mb, params(offsets, counts, e, rows, K, N, Y, status), di, st);
+}
+
+cudaError_t launch_dispatch_gemm(const int32_t* offsets, const int32_t* counts, const int32_t* inv_row,
+                                 int e, int rows, int s, int K, int N, const void* x, const void* W,
+                                 void* Y, int32_t* status, const DeviceInfo& di, cudaStream_t st) {
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, x, (uint64_t)K, (uint64_t)s, 1) ||
+      !make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN))
+    return cudaErrorInvalidValue;
+  GemmParams p = params(offsets, counts, e, rows, K, N, Y, status);
+  p.inv_row = inv_row;
+  p.s = s;
+  return launch<true>(ma, mb, p, di, st);
 }
 
 }  // namespace moe

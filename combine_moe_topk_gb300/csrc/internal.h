@@ -44,6 +44,7 @@ struct LayoutOut {
   int32_t* rank_counts;
   unsigned* lookback;            // [tiles][e rounded up to 4], zero before the launch
   int32_t* status;
+  int32_t* inv_row = nullptr;    // [rows]: token of each kept route's row (optional)
 };
 
 // priority 0 = token order, 1 = k-major; pad_multiple >= 1 pads dropless
@@ -80,9 +81,15 @@ cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const 
 
 // --- expert-grouped GEMM on the tensor cores -----------------------------
 // Y[r] = X[r] . W[x]^T over the 128-row blocks of each expert segment that a
-// route owns.  K % 64 == 0, N % 256 == 0, segments 128-row aligned.
+// route owns.  K % 64 == 0, N % 256 == 0; a segment may start on any row.
 cudaError_t launch_grouped_gemm(const int32_t* offsets, const int32_t* counts, int e, int rows, int K,
                                 int N, const void* X, const void* W, void* Y, int32_t* status,
                                 const DeviceInfo& di, cudaStream_t st);
+
+// Fused dispatch + grouped GEMM: A rows gathered from the token rows x [s,K]
+// through inv_row; same output as launch_grouped_gemm on the dispatched rows.
+cudaError_t launch_dispatch_gemm(const int32_t* offsets, const int32_t* counts, const int32_t* inv_row,
+                                 int e, int rows, int s, int K, int N, const void* x, const void* W,
+                                 void* Y, int32_t* status, const DeviceInfo& di, cudaStream_t st);
 
 }  // namespace moe

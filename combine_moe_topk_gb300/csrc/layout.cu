@@ -286,7 +286,8 @@ __device__ __forceinline__ void store_route_ints(int32_t* dst, const int* v, int
 }
 
 // Write one token's routes: token-order slot, row, drop flag, and its
-// virtual-rank set.  base[x] is the slot of this warp's first token routed
+// virtual-rank set; with inv_row, the token number at each kept row.
+// base[x] is the slot of this warp's first token routed
 // to x; mask[x] the warp's token mask for x.  Returns the token's rank set.
 __device__ __forceinline__ unsigned long long write_routes(const Params& p, int t, int lane,
                                                            const int* xs, unsigned valid,
@@ -315,6 +316,12 @@ __device__ __forceinline__ unsigned long long write_routes(const Params& p, int 
     if (row[j] < 0) dropw[j / 4] |= 1u << (8 * (j % 4));
   }
   const size_t q0 = unit_base(p, t);
+  if (p.out.inv_row) {
+    const int token = p.kmajor ? t - (t / p.s_tok) * p.s_tok : t;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < p.k && row[j] >= 0) p.out.inv_row[row[j]] = token;
+  }
   store_route_ints(p.out.loc + q0, loc, p.k);
   store_route_ints(p.out.row + q0, row, p.k);
   uint8_t* dr = p.out.drop + q0;

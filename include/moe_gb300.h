@@ -80,7 +80,8 @@ enum {
   MOE_KERNEL_DISPATCH_BWD = 5,
   MOE_KERNEL_TOPK_GATE_BWD = 6,
   MOE_KERNEL_GROUPED_GEMM = 7,
-  MOE_KERNEL_COUNT = 8
+  MOE_KERNEL_DISPATCH_GEMM = 8,
+  MOE_KERNEL_COUNT = 9
 };
 
 /* Opaque layout handle [P1 "How"; P3 description].  Owned by the library:
@@ -125,6 +126,8 @@ typedef struct {
   const uint8_t* token_in_rank; /* [s,R] 1 = token sends to that virtual rank   */
   const int32_t* rank_counts;   /* [R]   tokens sent to each virtual rank       */
   const int32_t* status;        /* device status word of this handle            */
+  const int32_t* inv_row;       /* [rows] token whose kept route owns the row;
+                                   unspecified at rows no route owns           */
 } moe_layout_info;
 
 /* Top-k softmax gating [P4 change 1; P1 description: recompute must route
@@ -252,22 +255,33 @@ moe_status moe_dispatch_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtyp
 
 /* Expert-grouped GEMM over the dispatched buffer, on the tensor cores
  * [P3 description: the dispatch groups arrivals by expert for the grouped
- * GEMM, groups bounded by offsets; Automodel #3684 description: per-expert
- * padding of the rows (pad_multiple)].  For every 128-row block of expert
- * x's segment [offsets[x], offsets[x+1]) that holds at least one kept route:
+ * GEMM, groups bounded by offsets = cumsum(counts)].  For every row r that a
+ * kept route to expert x owns, r in [offsets[x], offsets[x] + counts[x]):
  *   Y[r, :] = X[r, :] . W[x]^T   (bf16 in, fp32 accumulation, bf16 out,
  *                                 round to nearest-even)
  * X bf16 [rows, K] (the output of moe_dispatch), W bf16 [e, N, K] (each
- * expert's weight N x K with K contiguous), Y bf16 [rows, N].  Rows of
- * blocks that hold no route are not written.  Requires every segment to
- * start on a multiple of 128 rows: a padded layout (moe_dispatch_layout_ex,
- * pad_multiple a multiple of 128) or capacity a multiple of 128; K a
- * multiple of 64; N a multiple of 256; rows equal to the handle's.
- * tcgen05 MMA with TMEM accumulators, TMA-fed; the expert of each block is
- * read from the handle on the device.  Errors: MOE_ERR_INVALID_ARG,
- * MOE_ERR_UNSUPPORTED (unaligned segments), MOE_ERR_HANDLE_MISMATCH. */
+ * expert's weight N x K with K contiguous), Y bf16 [rows, N].  Rows no route
+ * owns (capacity tails, padding) are not written.  Any layout of the handle:
+ * token or k-major, capacity or dropless, padded or not.  K a multiple of
+ * 64; N a multiple of 256; rows equal to the handle's; e <= 256.
+ * tcgen05 MMA with TMEM accumulators, TMA-fed; the segments are read from
+ * the handle on the device (no host sync).  Errors: MOE_ERR_INVALID_ARG,
+ * MOE_ERR_HANDLE_MISMATCH, MOE_ERR_CUDA. */
 moe_status moe_grouped_gemm(moe_handle h, int rows, int K, int N, const void* X, const void* W,
                             void* Y, void* stream);
+
+/* Dispatch fused into the grouped GEMM [P3 description: the grouped GEMM
+ * consumes the arrivals grouped by expert; P4 change 3: gather rows by index
+ * instead of materialising a one-hot product].  The same Y as
+ * moe_dispatch followed by moe_grouped_gemm, without the dispatched buffer:
+ * the A operand's rows are gathered from the token rows by the tensor
+ * memory accelerator (four rows per request) through the handle's inv_row.
+ *   Y[r, :] = x[inv_row[r], :] . W[x]^T   for every owned row r,
+ * x bf16 [s, K] (the tokens' activations, K = m), W bf16 [e, N, K], Y bf16
+ * [rows, N]; rows no route owns are not written.  Same limits and errors as
+ * moe_grouped_gemm; s must equal the handle's. */
+moe_status moe_dispatch_grouped_gemm(moe_handle h, int s, int rows, int K, int N, const void* x,
+                                     const void* W, void* Y, void* stream);
 
 /* Fill *info with the handle's sizes and device pointers (valid until the
  * handle is destroyed). */

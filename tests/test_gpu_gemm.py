@@ -1,10 +1,14 @@
-"""The expert-grouped GEMM on the tensor cores against the oracle.
+"""The expert-grouped GEMM on the tensor cores, plain and fused with the
+dispatch, against the oracle.
 
 DeepSpeed #8213 "Add an opt-in DeepEP transport for the AutoEP expert
 all-to-all": the dispatched buffer is grouped by expert for the grouped
 GEMM, groups bounded by offsets.  Identity weights must give the dispatched
-rows back bit for bit (a swizzle or descriptor slip would permute them);
-random weights are compared with a float64 matmul per expert segment.
+rows back bit for bit (a swizzle, descriptor or gather slip would permute
+them); random weights are compared with a float64 matmul per expert segment.
+The fused form gathers the token rows itself and must equal the plain GEMM
+on the dispatched rows bit for bit (same operands, same MMA order).  Rows no
+route owns are left as they were.
 """
 import numpy as np
 import pytest
@@ -18,21 +22,23 @@ from gpu_util import bits, to_dev
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
+SENTINEL = 0x7FC1  # a bf16 NaN pattern no GEMM result equals
 
 
-def _setup(s, e, k, m, seed, capacity=0, pad=128):
+def _setup(s, e, k, m, seed, capacity=0, pad=1, priority="token"):
     idx = W.random_routes(s, e, k, seed=seed)
-    if capacity:
-        h = B.moe_dispatch_layout(idx.to(DEV), e, capacity)
+    if pad > 1 or priority != "token":
+        h = B.moe_dispatch_layout_ex(idx.to(DEV), e, capacity, 0, priority, pad)
     else:
-        h = B.moe_dispatch_layout_ex(idx.to(DEV), e, 0, 0, "token", pad)
+        h = B.moe_dispatch_layout(idx.to(DEV), e, capacity)
     g = torch.Generator().manual_seed(seed)
     x = torch.randn(s, m, generator=g).to(torch.bfloat16)
     X = B.moe_dispatch(h, x.to(DEV))
-    L = oracle.layout(idx.numpy(), e, capacity, pad_multiple=1 if capacity else pad)
+    L = oracle.layout(idx.numpy(), e, capacity, priority=1 if priority == "kmajor" else 0,
+                      pad_multiple=pad)
     OX = oracle.dispatch(L["row"], bits(x), L["rows"])
     np.testing.assert_array_equal(bits(X), OX)
-    return h, X, OX, L
+    return h, x, X, OX, L
 
 
 def _owned_rows(L):
@@ -42,31 +48,18 @@ def _owned_rows(L):
     return np.array(rows, np.int64)
 
 
-def test_identity_weights_return_the_dispatched_rows():
-    s, e, k, K = 300, 4, 2, 256
-    h, X, OX, L = _setup(s, e, k, K, seed=1)
-    Wt = torch.eye(K, dtype=torch.bfloat16).expand(e, K, K).contiguous()
-    Y = B.moe_grouped_gemm(h, X, Wt.to(DEV))
-    torch.cuda.synchronize()
-    assert h.status() == 0
-    r = _owned_rows(L)
-    np.testing.assert_array_equal(bits(Y)[r], OX[r])
+def _sentinel_out(rows, N):
+    return torch.full((rows, N), SENTINEL, dtype=torch.int16, device=DEV).view(torch.bfloat16)
 
 
-@pytest.mark.parametrize("case", [
-    dict(s=150, e=2, k=1, K=64, N=256, cap=0),
-    dict(s=2000, e=8, k=2, K=1024, N=512, cap=0),
-    dict(s=1500, e=6, k=3, K=512, N=768, cap=768),     # capacity mode, 128-aligned slots
-    dict(s=4096, e=16, k=4, K=2048, N=256, cap=0),
-])
-def test_grouped_gemm_matches_float64_matmul(case):
-    s, e, k, K, N, cap = case["s"], case["e"], case["k"], case["K"], case["N"], case["cap"]
-    h, X, OX, L = _setup(s, e, k, K, seed=3, capacity=cap)
-    g = torch.Generator().manual_seed(7)
-    Wt = (torch.randn(e, N, K, generator=g) / np.sqrt(K)).to(torch.bfloat16)
-    Y = B.moe_grouped_gemm(h, X, Wt.to(DEV))
-    torch.cuda.synchronize()
-    assert h.status() == 0
+def _check_unowned_untouched(Y, L):
+    own = np.zeros(int(L["rows"]), bool)
+    own[_owned_rows(L)] = True
+    rest = bits(Y)[~own]
+    assert (rest == SENTINEL).all(), "a row no route owns was written"
+
+
+def _check_float64(Y, OX, Wt, L):
     Wb = bits(Wt)
     ref = oracle.grouped_gemm(OX, Wb, L["offsets"], L["counts"])
     r = _owned_rows(L)
@@ -74,7 +67,7 @@ def test_grouped_gemm_matches_float64_matmul(case):
     # bf16 output: one ulp of the exact value plus the fp32 accumulation over K
     scale = np.zeros_like(ref[r])
     Xa, Wa = np.abs(T.as_f64(OX)), np.abs(T.as_f64(Wb))
-    for x in range(e):
+    for x in range(len(L["counts"])):
         o, n = int(L["offsets"][x]), int(L["counts"][x])
         sel = (r >= o) & (r < o + n)
         scale[sel] = Xa[r[sel]] @ Wa[x].T
@@ -82,11 +75,79 @@ def test_grouped_gemm_matches_float64_matmul(case):
     assert not bad.any(), (int(bad.sum()), np.argwhere(bad)[:3])
 
 
-def test_unaligned_segments_are_refused():
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("layout", [dict(pad=128), dict(pad=1), dict(capacity=100)])
+def test_identity_weights_return_the_dispatched_rows(fused, layout):
+    s, e, k, K = 300, 4, 2, 256
+    h, x, X, OX, L = _setup(s, e, k, K, seed=1, **layout)
+    Wt = torch.eye(K, dtype=torch.bfloat16).expand(e, K, K).contiguous().to(DEV)
+    Y = _sentinel_out(h.rows, K)
+    if fused:
+        B.moe_dispatch_grouped_gemm(h, x.to(DEV), Wt, Y)
+    else:
+        B.moe_grouped_gemm(h, X, Wt, Y)
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    r = _owned_rows(L)
+    np.testing.assert_array_equal(bits(Y)[r], OX[r])
+    _check_unowned_untouched(Y, L)
+
+
+CASES = [
+    dict(s=150, e=2, k=1, K=64, N=256),
+    dict(s=2000, e=8, k=2, K=1024, N=512),                       # plain dropless: segments start anywhere
+    dict(s=1500, e=6, k=3, K=512, N=768, capacity=768),          # capacity, 128-aligned slots
+    dict(s=1500, e=6, k=3, K=512, N=256, capacity=333),          # capacity, unaligned slots, drops
+    dict(s=4096, e=16, k=4, K=2048, N=256, pad=128),             # padded
+    dict(s=3000, e=64, k=6, K=256, N=512, capacity=200, priority="kmajor"),
+    dict(s=700, e=128, k=8, K=128, N=256),                       # many small and empty segments
+    dict(s=40, e=4, k=1, K=64, N=256),                           # fewer rows than one block
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_grouped_gemm_matches_float64_matmul_and_fused_is_identical(case):
+    c = dict(case)
+    s, e, k, K, N = (c.pop(n) for n in ("s", "e", "k", "K", "N"))
+    h, x, X, OX, L = _setup(s, e, k, K, seed=3, **c)
+    g = torch.Generator().manual_seed(7)
+    Wt = (torch.randn(e, N, K, generator=g) / np.sqrt(K)).to(torch.bfloat16)
+    Wd = Wt.to(DEV)
+    Y = B.moe_grouped_gemm(h, X, Wd, _sentinel_out(h.rows, N))
+    Yf = B.moe_dispatch_grouped_gemm(h, x.to(DEV), Wd, _sentinel_out(h.rows, N))
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    _check_float64(Y, OX, Wt, L)
+    np.testing.assert_array_equal(bits(Yf), bits(Y))  # owned rows equal, the rest untouched in both
+    _check_unowned_untouched(Y, L)
+
+
+def test_inv_row_names_the_token_of_every_owned_row():
+    s, e, k = 5000, 32, 4
+    for kw in (dict(capacity=500), dict(capacity=0), dict(capacity=600, priority="kmajor")):
+        idx = W.random_routes(s, e, k, seed=9)
+        pri = kw.get("priority", "token")
+        h = B.moe_dispatch_layout_ex(idx.to(DEV), e, kw["capacity"], 0, pri, 1)
+        L = oracle.layout(idx.numpy(), e, kw["capacity"], priority=1 if pri == "kmajor" else 0)
+        want = np.full(int(L["rows"]), -1, np.int64)
+        t, j = np.nonzero(L["row"] >= 0)
+        want[L["row"][t, j]] = t
+        r = _owned_rows(L)
+        np.testing.assert_array_equal(bits(h.inv_row())[r], want[r])
+
+
+def test_gemm_argument_checks():
     idx = W.random_routes(100, 4, 2, seed=2).to(DEV)
-    h = B.moe_dispatch_layout_ex(idx, 4, 0, 0, "token", 4)
-    X = torch.zeros(h.rows, 64, dtype=torch.bfloat16, device=DEV)
-    Wt = torch.zeros(4, 256, 64, dtype=torch.bfloat16, device=DEV)
+    h = B.moe_dispatch_layout(idx, 4)
+    X = torch.zeros(h.rows, 96, dtype=torch.bfloat16, device=DEV)
+    Wt = torch.zeros(4, 256, 96, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(B.MoEError) as ei:
-        B.moe_grouped_gemm(h, X, Wt)
-    assert ei.value.name == "MOE_ERR_UNSUPPORTED"
+        B.moe_grouped_gemm(h, X, Wt)  # K = 96: not a multiple of 64
+    assert ei.value.name == "MOE_ERR_INVALID_ARG"
+    x = torch.zeros(101, 64, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(B.MoEError) as ei:
+        B.moe_dispatch_grouped_gemm(h, x, torch.zeros(4, 256, 64, dtype=torch.bfloat16, device=DEV))
+    assert ei.value.name == "MOE_ERR_HANDLE_MISMATCH"  # 101 token rows, the handle has 100
+    with pytest.raises(B.MoEError) as ei:
+        B.moe_grouped_gemm(h, X[:, :64].contiguous(), torch.zeros(4, 200, 64, dtype=torch.bfloat16, device=DEV))
+    assert ei.value.name == "MOE_ERR_INVALID_ARG"  # N = 200
