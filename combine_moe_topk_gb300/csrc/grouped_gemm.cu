@@ -12,15 +12,20 @@
 // Y[r] = A[r] . W[x]^T for every row r that a kept route to expert x owns,
 // r in [offsets[x], offsets[x] + counts[x]).  A[r] is the dispatched row
 // X[r] (moe_grouped_gemm) or the token row x[inv_row[r]] (fused dispatch:
-// the dispatched buffer is never written).  bf16 operands, row-major, K
+// the dispatched buffer is never written or read).  bf16 operands, row-major, K
 // contiguous; the accumulation is fp32 in TMEM.  Work units are 128-row
 // blocks of one expert's segment (ceil(counts[x] / 128) of them, the first
 // at offsets[x], so a segment may start on any row) times 256-column tiles
 // of N.  One CTA per SM, persistent over the units:
-//   warp 0         -- TMA producer: B (256 x 64) K-blocks, and A (128 x 64)
-//                     either as one tile load (lane 0) or as 32 four-row
-//                     gathers (tile::gather4, one per lane), into a 4-stage
+//   warp 0 lane 0  -- TMA producer: B (256 x 64) K-blocks, and in the plain
+//                     form A (128 x 64) as one tile load, into a 4-stage
 //                     SWIZZLE_128B ring, mbarrier complete_tx;
+//   warps 8..11    -- fused form only: gather the A rows with 16-byte
+//                     cp.async in the same swizzle, each thread arriving on
+//                     a stage once its copies have landed (a TMA tile::gather4
+//                     of four rows per request was tried first: correct, but
+//                     at 33 copy requests per K-block it held the GEMM to a
+//                     third of the tensor rate);
 //   warp 1 lane 0  -- MMA issuer: four tcgen05.mma (M128 N256 K16) per
 //                     K-block into one of two 256-column TMEM accumulators,
 //                     tcgen05.commit frees the ring stage / hands over the tile;
@@ -48,11 +53,18 @@ constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kBBytes = BN * BK * 2;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTmemCols = 2 * BN;     // two fp32 accumulators of 128 lanes x 256 columns
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;        // tile-fed form
+constexpr int kGatherThreads = 384;  // fused form: + 4 warps gathering the A rows
+#ifndef MOE_GEMM_LAG
+#define MOE_GEMM_LAG 2
+#endif
+constexpr int kGatherLag = MOE_GEMM_LAG;  // stages a gather thread's arrivals trail its copies
+static_assert(kGatherLag >= 1 && kGatherLag < 4, "the ring must keep a stage the gather has not yet claimed");
 constexpr int kMaxE = 256;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
 
 struct GemmParams {
+  const __nv_bfloat16* x;  // gather mode: token rows [s, K]
   const int32_t* offsets;
   const int32_t* counts;
   const int32_t* inv_row;  // gather mode: token of each owned row
@@ -96,16 +108,19 @@ __device__ __forceinline__ void tma_load_2d(void* sdst, const CUtensorMap* map, 
       : "memory");
 }
 
-// Four rows (r0..r3) of a 2-D map whose box is 64 columns x 1 row, written
-// as four consecutive 128-byte rows at sdst with the map's swizzle.
-__device__ __forceinline__ void tma_gather4(void* sdst, const CUtensorMap* map, int x, int r0, int r1,
-                                            int r2, int r3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(sdst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(smem_addr(bar))
-      : "memory");
+// 16-byte asynchronous copy global -> shared (L2 only), grouped per stage.
+__device__ __forceinline__ void cp_async16(uint32_t sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sdst), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Order this thread's completed shared-memory writes before later reads of
+// the tensor cores (the async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -176,7 +191,7 @@ __device__ __forceinline__ Unit decode_unit(int u, int ntn, const int* s_blk, co
 }
 
 template <bool kGather>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -189,12 +204,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   const uint64_t deadline = globaltimer_ns() + (uint64_t)p.timeout_ns;
 
-  for (int x = threadIdx.x; x <= p.e; x += kThreads) s_off[x] = __ldg(p.offsets + x);
-  for (int x = threadIdx.x; x < p.e; x += kThreads) s_cnt[x] = __ldg(p.counts + x);
+  for (int x = threadIdx.x; x <= p.e; x += blockDim.x) s_off[x] = __ldg(p.offsets + x);
+  for (int x = threadIdx.x; x < p.e; x += blockDim.x) s_cnt[x] = __ldg(p.counts + x);
   if (threadIdx.x == 0) {
     s_err = 0;
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&full[i], 1);
+      // the B tile's expect_tx arrival, plus one per gathering thread
+      mbar_init(&full[i], kGather ? 1 + (kGatherThreads - kThreads) : 1);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -237,25 +253,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nunits = s_blk[p.e] * ntn;
   const int kblocks = p.K / BK;
 
-  if (warp == 0) {
-    // ---- TMA producer ----------------------------------------------------
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer: B always, A in the tile-fed form ------------------
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
       const Unit t = decode_unit(u, ntn, s_blk, s_off, s_cnt, p.e);
-      int tok[4] = {0, 0, 0, 0};
-      if (kGather) {
-        // this lane gathers rows 4*lane .. 4*lane+3 of the block; rows no
-        // route owns read token 0 (their results are not stored)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int rr = 4 * lane + i;
-          if (rr < t.nvalid) {
-            const int v = __ldg(p.inv_row + t.r0 + rr);
-            tok[i] = (unsigned)v < (unsigned)p.s ? v : 0;
-          }
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, deadline)) {
+          ok = false;
+          break;
         }
+        uint8_t* sa = smem + stage * kStageBytes;
+        mbar_arrive_expect_tx(&full[stage], kGather ? kBBytes : kStageBytes);
+        tma_load_2d(sa + kABytes, &tmB, kb * BK, t.x * p.N + t.n0, &full[stage]);
+        if (!kGather) tma_load_2d(sa, &tmA, kb * BK, t.r0, &full[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) atomicOr(&s_err, 1);
+  } else if (kGather && warp >= kThreads / 32) {
+    // ---- A gather (fused form): 128 threads, 16-byte cp.async ------------
+    // Warp gw copies rows 32*gw .. 32*gw+31 of the block; per instruction 8
+    // lanes cover one row's 128 bytes (4 rows at a time), written in the
+    // 128-byte swizzle the MMA descriptor reads (16-byte chunk c of row r at
+    // chunk c ^ (r & 7)).  A thread arrives on a stage's full barrier once
+    // its copies to it have landed, kGatherLag stages behind its issue.
+    const int gw = warp - kThreads / 32, chunk = lane & 7;
+    int stage = 0, astage = 0, pending = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      const Unit t = decode_unit(u, ntn, s_blk, s_off, s_cnt, p.e);
+      const __nv_bfloat16* src[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 32 * gw + 4 * i + (lane >> 3);
+        int tok = 0;  // rows no route owns read token 0; their results are not stored
+        if (rr < t.nvalid) {
+          const int v = __ldg(p.inv_row + t.r0 + rr);
+          tok = (unsigned)v < (unsigned)p.s ? v : 0;
+        }
+        src[i] = p.x + (size_t)tok * p.K + chunk * 8;
       }
       for (int kb = 0; kb < kblocks; ++kb) {
         bool waited = true;
@@ -264,15 +307,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        uint8_t* sa = smem + stage * kStageBytes;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          tma_load_2d(sa + kABytes, &tmB, kb * BK, t.x * p.N + t.n0, &full[stage]);
-          if (!kGather) tma_load_2d(sa, &tmA, kb * BK, t.r0, &full[stage]);
+        const uint32_t sa = smem_addr(smem + stage * kStageBytes);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 32 * gw + 4 * i + (lane >> 3);
+          cp_async16(sa + rr * 128 + ((chunk ^ (rr & 7)) << 4), src[i] + kb * BK);
         }
-        if (kGather) {
-          __syncwarp();
-          tma_gather4(sa + 4 * 128 * lane, &tmA, kb * BK, tok[0], tok[1], tok[2], tok[3], &full[stage]);
+        cp_async_commit();
+        if (++pending > kGatherLag) {
+          cp_async_wait<kGatherLag>();
+          fence_proxy_async_smem();
+          mbar_arrive(&full[astage]);
+          --pending;
+          if (++astage == kStages) astage = 0;
         }
         if (++stage == kStages) {
           stage = 0;
@@ -280,7 +327,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (!ok && lane == 0) atomicOr(&s_err, 1);
+    cp_async_wait<0>();  // nothing of this thread's stays in flight
+    if (ok) {
+      fence_proxy_async_smem();
+      for (; pending > 0; --pending) {
+        mbar_arrive(&full[astage]);
+        if (++astage == kStages) astage = 0;
+      }
+    } else if (lane == 0) {
+      atomicOr(&s_err, 1);
+    }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ------------------------------------------------------
     const uint32_t idesc = mma_idesc();
@@ -317,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
     }
     if (!ok) atomicOr(&s_err, 1);
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ---- epilogue: TMEM -> registers -> bf16 -> Y ------------------------
     const int ew = warp - 4;  // TMEM lanes 32*ew .. 32*ew+31
     int acc = 0;
@@ -420,13 +476,14 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParam
   const long long nunits = blocks * (p.N / BN);
   int grid = (long long)di.sms < nunits ? di.sms : (int)nunits;
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<kGather><<<grid, kThreads, kSmemBytes, st>>>(ma, mb, p);
+  grouped_gemm_kernel<kGather><<<grid, kGather ? kGatherThreads : kThreads, kSmemBytes, st>>>(ma, mb, p);
   return cudaGetLastError();
 }
 
 GemmParams params(const int32_t* offsets, const int32_t* counts, int e, int rows, int K, int N,
                   void* Y, int32_t* status) {
   GemmParams p;
+  p.x = nullptr;
   p.offsets = offsets;
   p.counts = counts;
   p.inv_row = nullptr;
@@ -456,14 +513,13 @@ cudaError_t launch_grouped_gemm(const int32_t* offsets, const int32_t* counts, i
 cudaError_t launch_dispatch_gemm(const int32_t* offsets, const int32_t* counts, const int32_t* inv_row,
                                  int e, int rows, int s, int K, int N, const void* x, const void* W,
                                  void* Y, int32_t* status, const DeviceInfo& di, cudaStream_t st) {
-  CUtensorMap ma, mb;
-  if (!make_map(&ma, x, (uint64_t)K, (uint64_t)s, 1) ||
-      !make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN))
-    return cudaErrorInvalidValue;
+  CUtensorMap mb;
+  if (!make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN)) return cudaErrorInvalidValue;
   GemmParams p = params(offsets, counts, e, rows, K, N, Y, status);
+  p.x = static_cast<const __nv_bfloat16*>(x);
   p.inv_row = inv_row;
   p.s = s;
-  return launch<true>(ma, mb, p, di, st);
+  return launch<true>(mb, mb, p, di, st);  // A is gathered by threads: no A map
 }
 
 }  // namespace moe

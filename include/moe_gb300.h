@@ -274,8 +274,9 @@ moe_status moe_grouped_gemm(moe_handle h, int rows, int K, int N, const void* X,
  * consumes the arrivals grouped by expert; P4 change 3: gather rows by index
  * instead of materialising a one-hot product].  The same Y as
  * moe_dispatch followed by moe_grouped_gemm, without the dispatched buffer:
- * the A operand's rows are gathered from the token rows by the tensor
- * memory accelerator (four rows per request) through the handle's inv_row.
+ * the A operand's rows are gathered from the token rows through the
+ * handle's inv_row (row -> token), straight into the GEMM's shared-memory
+ * tiles.
  *   Y[r, :] = x[inv_row[r], :] . W[x]^T   for every owned row r,
  * x bf16 [s, K] (the tokens' activations, K = m), W bf16 [e, N, K], Y bf16
  * [rows, N]; rows no route owns are not written.  Same limits and errors as
