@@ -40,6 +40,7 @@ OPS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "topk_gate_b
 KERNEL_FILE = {"topk_gate": "gate.cu", "layout": "layout.cu", "dispatch": "dispatch.cu", "combine": "combine.cu",
                "combine_bwd": "combine.cu", "topk_gate_bwd": "gate.cu", "dispatch_bwd": "combine.cu"}
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 # ------------------------------------------------------------ byte model --
@@ -78,6 +79,15 @@ def peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def bf16_peak():
+    """Dense bf16 tensor throughput (TFLOP/s) for a kernel timed on its own."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def traffic_record(op: str):
@@ -300,6 +310,9 @@ def run_ours(args, rank: int, world: int, dist):
     # ---- end to end: pinned host inputs in, results out, every step ----------
     e2e = run_e2e(w, S, step, buffers, dev, max(3, min(K, 50)), args.warmup)
 
+    # ---- the tensor-core consumer of the dispatched rows (outside value) ------
+    gemm = None if args.no_gemm else run_expert_gemm(w, S, dev)
+
     elapsed_ms, e2e["ms"] = max_over_ranks([elapsed_ms, e2e["ms"]], dist, dev)
     if rank != 0:
         return None
@@ -359,9 +372,66 @@ def run_ours(args, rank: int, world: int, dist):
         "kept_routes": kept,
         "sending_tokens": u,
     }
+    if gemm is not None:
+        line["expert_gemm"] = gemm
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args)
     return line
+
+
+def run_expert_gemm(w, S, dev, reps: int = 10):
+    """The grouped-GEMM consumer of the dispatched rows (not part of the step
+    or of ``value``): synthetic expert weights W [e, N, m], N = m, bf16.
+    Times dispatch, the grouped GEMM on the dispatched rows, and the fused
+    dispatch + GEMM that gathers the token rows itself (CUDA events, one
+    call each, median of ``reps``)."""
+    import torch
+
+    from combine_moe_topk_gb300 import binding as B
+
+    if w.dtype != "bf16" or w.m % 256:
+        return {"skipped": "the tensor-core GEMM takes bf16 rows with m a multiple of 256"}
+    N = w.m
+    g = torch.Generator(device=dev).manual_seed(w.seed + 77)
+    Wt = (torch.randn(w.e, N, w.m, device=dev, generator=g) * w.m ** -0.5).to(torch.bfloat16)
+    h = B.moe_dispatch_layout(S["idx"], w.e, w.capacity, w.R)
+    X = torch.empty(h.rows, w.m, dtype=torch.bfloat16, device=dev)
+    Y = torch.empty(h.rows, N, dtype=torch.bfloat16, device=dev)
+    kept = int(h.counts().sum().item())
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    t_d = timed(lambda: B.moe_dispatch(h, S["x"], X))
+    t_g = timed(lambda: B.moe_grouped_gemm(h, X, Wt, Y))
+    t_f = timed(lambda: B.moe_dispatch_grouped_gemm(h, S["x"], Wt, Y))
+    assert h.status() == 0
+    h.destroy()
+    flops = 2.0 * kept * w.m * N
+    peak, src = bf16_peak()
+    tf = lambda ms: flops / (ms * 1e-3) / 1e12
+    return {
+        "N": N, "K": w.m, "rows": int(Y.shape[0]), "kept_rows": kept, "flops": flops,
+        "us_dispatch": round(t_d * 1e3, 1), "us_gemm": round(t_g * 1e3, 1),
+        "us_fused_dispatch_gemm": round(t_f * 1e3, 1),
+        "tflops_gemm": round(tf(t_g), 1), "tflops_fused": round(tf(t_f), 1),
+        "tflops_dispatch_then_gemm": round(tf(t_d + t_g), 1),
+        "roofline": {"bound": "tensor", "peak": peak, "unit": "TFLOP/s",
+                     "peak_source": f"{src} bf16 dense (burst, kernel timed alone)",
+                     "frac_gemm": round(tf(t_g) / peak, 4), "frac_fused": round(tf(t_f) / peak, 4)},
+        "note": "synthetic N(0,1)/sqrt(m) expert weights; events around single calls, median of "
+                f"{reps}; not included in value",
+    }
 
 
 def run_e2e(w, S, step, buffers, dev, K, warmup):
@@ -542,6 +612,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle work for cpu_baseline")
     ap.add_argument("--ref-seconds", type=float, default=120.0, help="total oracle work of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-gemm", action="store_true", help="skip the expert_gemm figures")
     ap.add_argument("--eager", action="store_true", help="time eager calls instead of a CUDA graph of the step")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -587,3 +587,61 @@ def test_pad_multiple_offsets(P):
     np.testing.assert_array_equal(L["row"], L["offsets"][idx] + L["loc"])
     with pytest.raises(oracle.OracleError):
         oracle.layout(idx, 8, capacity=10, pad_multiple=4)
+
+
+# ------------------------------------------------ grouped GEMM consumer --
+# DeepSpeed #8213 description: the arrivals are grouped by expert for a
+# grouped GEMM bounded by offsets.  The oracle multiplies each owned row by
+# its own expert's weight, transposed (W [e, N, K]).
+
+def _gemm_layout():
+    idx = W.random_routes(60, 3, 2, seed=11).numpy()
+    return oracle.layout(idx, 3, capacity=35)  # capacity: tails no route owns
+
+
+def test_grouped_gemm_identity_weights_return_owned_rows():
+    L = _gemm_layout()
+    rng = np.random.default_rng(0)
+    X = rng.standard_normal((L["rows"], 6)).astype(np.float32)
+    Y = oracle.grouped_gemm(X, np.stack([np.eye(6, dtype=np.float32)] * 3), L["offsets"], L["counts"])
+    for x in range(3):
+        o, n = int(L["offsets"][x]), int(L["counts"][x])
+        np.testing.assert_array_equal(Y[o:o + n], X[o:o + n].astype(np.float64))
+        assert np.isnan(Y[o + n:o + 35]).all()  # rows past counts[x] are nobody's
+
+
+def test_grouped_gemm_uses_each_segments_own_weight_untransposed():
+    # W[x] = (x + 1) * P with P a non-symmetric permutation: Y[r, i] must be
+    # (x + 1) * X[r, p(i)].  Another expert's weight scales wrongly; P^T
+    # (a transposed operand) permutes the other way.
+    L = _gemm_layout()
+    K = 5
+    p = np.array([1, 2, 3, 4, 0])
+    P = np.zeros((K, K), np.float32)
+    P[np.arange(K), p] = 1.0
+    assert not np.array_equal(P, P.T)
+    rng = np.random.default_rng(1)
+    X = rng.standard_normal((L["rows"], K)).astype(np.float32)
+    Y = oracle.grouped_gemm(X, np.stack([(x + 1) * P for x in range(3)]), L["offsets"], L["counts"])
+    for x in range(3):
+        o, n = int(L["offsets"][x]), int(L["counts"][x])
+        np.testing.assert_array_equal(Y[o:o + n], (x + 1) * X[o:o + n][:, p].astype(np.float64))
+
+
+def test_grouped_gemm_brute_force_and_bf16_decoding():
+    idx = np.array([[0, 2], [1, 2], [2, 0], [2, 1]], np.int32)
+    L = oracle.layout(idx, 3, 0)
+    Xb = torch.randn(L["rows"], 4, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    Wb = torch.randn(3, 2, 4, generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    Xbits = Xb.view(torch.int16).numpy().view(np.uint16)
+    Wbits = Wb.view(torch.int16).numpy().view(np.uint16)
+    Y = oracle.grouped_gemm(Xbits, Wbits, L["offsets"], L["counts"])
+    Xv, Wv = Xb.double().tolist(), Wb.double().tolist()
+    for x in range(3):
+        for r in range(int(L["offsets"][x]), int(L["offsets"][x + 1])):
+            for n in range(2):
+                want = math.fsum(Xv[r][kk] * Wv[x][n][kk] for kk in range(4))
+                assert abs(Y[r, n] - want) <= 1e-12 * (1 + abs(want))
+    # the same values as float32 give the same result
+    np.testing.assert_array_equal(Y, oracle.grouped_gemm(Xb.float().numpy(), Wb.float().numpy(),
+                                                         L["offsets"], L["counts"]))
