@@ -41,6 +41,7 @@ KERNEL_FILE = {"topk_gate": "gate.cu", "layout": "layout.cu", "dispatch": "dispa
                "combine_bwd": "combine.cu", "topk_gate_bwd": "gate.cu", "dispatch_bwd": "combine.cu"}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+SLEEP_CYCLES = 100_000  # ~50 us at 2 GHz: longer than the host's enqueue of one call
 
 
 # ------------------------------------------------------------ byte model --
@@ -90,13 +91,14 @@ def bf16_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def traffic_record(op: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the kernel source as it is now (else None)."""
+def traffic_record(op: str, workload: str):
+    """Per-launch DRAM bytes of this op on this workload from the committed
+    ncu summary, if it was taken on the kernel source as it is now (else
+    None)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f)
+            rec = json.load(f).get(workload, {})
     except Exception:
         return None
     r = rec.get(op)
@@ -203,33 +205,43 @@ def run_ours(args, rank: int, world: int, dist):
 
     S = buffers(w.seed + 1000 * rank)
 
+    pad = getattr(torch.cuda, "_sleep", None)
+
     def step(b=S, ev=None):
         """One pass of the path: gate, layout, dispatch, combine, combine
-        backward, gate backward, dispatch backward on the step's handle."""
-        if ev is not None:
-            ev[0].record()
+        backward, gate backward, dispatch backward on the step's handle.
+        With ev (pairs of events per op), each op is bracketed by its own
+        events, preceded by a short GPU sleep so that the host has enqueued
+        the op before the start event is reached: the pair then times the
+        kernel, not the host's launch overhead."""
+        def mark(i, j):
+            if ev is not None:
+                if j == 0 and pad is not None:
+                    pad(SLEEP_CYCLES)
+                ev[i][j].record()
+
+        mark(0, 0)
         B.moe_topk_gate(b["logits"], w.k, w.renorm, b["idx"], b["gate"])
-        if ev is not None:
-            ev[1].record()
+        mark(0, 1)
+        mark(1, 0)
         h = B.moe_dispatch_layout(b["idx"], w.e, w.capacity, w.R)
-        if ev is not None:
-            ev[2].record()
+        mark(1, 1)
+        mark(2, 0)
         B.moe_dispatch(h, b["x"], b["X"])
-        if ev is not None:
-            ev[3].record()
+        mark(2, 1)
+        mark(3, 0)
         B.moe_combine(h, b["y"], b["gate"], b["out"])
-        if ev is not None:
-            ev[4].record()
+        mark(3, 1)
+        mark(4, 0)
         B.moe_combine_bwd(h, b["dout"], b["gate"], b["y"], b["dY"], b["dgate"])
-        if ev is not None:
-            ev[5].record()
+        mark(4, 1)
+        mark(5, 0)
         B.moe_topk_gate_bwd(None if w.renorm else b["logits"], b["idx"], b["gate"], b["dgate"], w.e, w.renorm,
                             b["dlogits"])
-        if ev is not None:
-            ev[6].record()
+        mark(5, 1)
+        mark(6, 0)
         B.moe_dispatch_bwd(h, b["dY"], b["dx"])
-        if ev is not None:
-            ev[7].record()
+        mark(6, 1)
         return h
 
     # kept routes / sending tokens for the byte model (outside any timing)
@@ -300,12 +312,16 @@ def run_ours(args, rank: int, world: int, dist):
 
     # ---- per-kernel durations: events around each call, eager, own loop -----
     Kr = max(3, min(K, 200))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(OPS) + 1)] for _ in range(Kr)]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in OPS] for _ in range(Kr)]
     for i in range(Kr):
         step(ev=evs[i]).destroy()
     torch.cuda.synchronize()
-    per_op = {op: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(Kr))
+    per_op = {op: statistics.mean(evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(Kr))
               for j, op in enumerate(OPS)}
+
+    # ---- dispatch + combine in steady state: a graph of the pair on one
+    # handle (the cached-replay case), replayed back to back -----------------
+    dc = run_dispatch_combine(w, S, dev, K)
 
     # ---- end to end: pinned host inputs in, results out, every step ----------
     e2e = run_e2e(w, S, step, buffers, dev, max(3, min(K, 50)), args.warmup)
@@ -313,7 +329,7 @@ def run_ours(args, rank: int, world: int, dist):
     # ---- the tensor-core consumer of the dispatched rows (outside value) ------
     gemm = None if args.no_gemm else run_expert_gemm(w, S, dev)
 
-    elapsed_ms, e2e["ms"] = max_over_ranks([elapsed_ms, e2e["ms"]], dist, dev)
+    elapsed_ms, e2e["ms"], dc["ms"] = max_over_ranks([elapsed_ms, e2e["ms"], dc["ms"]], dist, dev)
     if rank != 0:
         return None
 
@@ -322,9 +338,9 @@ def run_ours(args, rank: int, world: int, dist):
     peak, peak_src = peaks()
     dom = max(per_op, key=per_op.get)
     achieved = nbytes[dom] / (per_op[dom] * 1e-3) / 1e9
-    tr = traffic_record(dom)
+    tr = traffic_record(dom, w.name)
     pay = payload_bytes(w, kept, u)
-    dc_ms = per_op["dispatch"] + per_op["combine"]
+    dc_ms = dc["ms"]
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -348,7 +364,8 @@ def run_ours(args, rank: int, world: int, dist):
         },
         "routed_tokens_per_s": round(world * w.s * w.k / (ms_per_step * 1e-3), 1),
         "dispatch_combine": {
-            "us": round(dc_ms * 1e3, 2),
+            "us": round(dc_ms * 1e3, 2), "how": dc["how"],
+            "sum_of_op_events_us": round((per_op["dispatch"] + per_op["combine"]) * 1e3, 2),
             "gbs": round((nbytes["dispatch"] + nbytes["combine"]) / (dc_ms * 1e-3) / 1e9, 1),
             "payload_gbs": round((pay["dispatch"] + pay["combine"]) / (dc_ms * 1e-3) / 1e9, 1),
             "frac_of_peak": round((nbytes["dispatch"] + nbytes["combine"]) / (dc_ms * 1e-3) / 1e9 / peak, 4),
@@ -356,12 +373,14 @@ def run_ours(args, rank: int, world: int, dist):
         },
         "ops": {op: {"us": round(per_op[op] * 1e3, 2), "bytes": nbytes[op],
                      "gbs": round(nbytes[op] / (per_op[op] * 1e-3) / 1e9, 1)} for op in OPS},
-        "ops_note": f"per-kernel times from events around each call, eager, {Kr} separate steps",
+        "ops_note": f"per-kernel times from events around each call, eager, {Kr} separate steps, each call "
+                    f"after a {SLEEP_CYCLES}-cycle GPU sleep so the events bracket the kernel"
+                    + ("" if pad is not None else " (sleep unavailable: host gaps included)"),
         "roofline": {
             "kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (copy bandwidth)",
             "traffic": (tr["dram_bytes_per_launch"] if tr else None),
-            "traffic_note": (tr.get("note") if tr else "no ncu capture of this kernel source"),
+            "traffic_note": (tr.get("note") if tr else "no ncu capture of this kernel source on this workload"),
             "algorithmic_bytes": nbytes[dom],
         },
         "e2e": {"value": round(job_gbs(world, step_total, e2e["ms"]), 1), "unit": "GB/s",
@@ -377,6 +396,52 @@ def run_ours(args, rank: int, world: int, dist):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args)
     return line
+
+
+def run_dispatch_combine(w, S, dev, K: int):
+    """Dispatch + combine on one handle, as a CUDA graph of the pair replayed
+    K times back to back (events around the whole loop): the steady-state
+    time of the pair with no host work between kernels.  Inputs and outputs
+    of one pair (x, X, y, out) exceed the 129 MB L2 for every workload but
+    the smallest, so no flush is inserted."""
+    import torch
+
+    from combine_moe_topk_gb300 import binding as B
+
+    h = B.moe_dispatch_layout(S["idx"], w.e, w.capacity, w.R)
+    torch.cuda.synchronize()
+
+    def pair():
+        B.moe_dispatch(h, S["x"], S["X"])
+        B.moe_combine(h, S["y"], S["gate"], S["out"])
+
+    how = "graph of dispatch + combine on one handle, replayed back to back"
+    try:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            pair()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            pair()
+        run = g.replay
+    except Exception as exc:
+        run, how = pair, f"eager calls back to back (graph capture failed: {type(exc).__name__})"
+    for _ in range(5):
+        run()
+    torch.cuda.synchronize()
+    n = max(5, min(K, 500))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        run()
+    b.record()
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    h.destroy()
+    return {"ms": a.elapsed_time(b) / n, "how": f"{how}, {n} pairs"}
 
 
 def run_expert_gemm(w, S, dev, reps: int = 10):

@@ -78,3 +78,11 @@ def test_reference_arm_prints_only_on_rank_zero():
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_traffic_record_is_per_workload_and_tied_to_the_source():
+    rec = bench.traffic_record("combine_bwd", "mixtral-dropless")
+    assert rec is not None and rec["dram_bytes_per_launch"] > 0
+    fine = bench.traffic_record("combine_bwd", "fine-grained-skewed")
+    assert fine is not None and fine["dram_bytes_per_launch"] != rec["dram_bytes_per_launch"]
+    assert bench.traffic_record("combine_bwd", "no-such-workload") is None
