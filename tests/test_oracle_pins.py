@@ -594,9 +594,15 @@ def test_pad_multiple_offsets(P):
 # grouped GEMM bounded by offsets.  The oracle multiplies each owned row by
 # its own expert's weight, transposed (W [e, N, K]).
 
+GEMM_CAP = 40
+
+
 def _gemm_layout():
     idx = W.random_routes(60, 3, 2, seed=11).numpy()
-    return oracle.layout(idx, 3, capacity=35)  # capacity: tails no route owns
+    L = oracle.layout(idx, 3, capacity=GEMM_CAP)
+    # both cases present: an expert that drops, and one with a tail no route owns
+    assert (L["raw_counts"] > GEMM_CAP).any() and (L["counts"] < GEMM_CAP).any()
+    return L
 
 
 def test_grouped_gemm_identity_weights_return_owned_rows():
@@ -607,7 +613,7 @@ def test_grouped_gemm_identity_weights_return_owned_rows():
     for x in range(3):
         o, n = int(L["offsets"][x]), int(L["counts"][x])
         np.testing.assert_array_equal(Y[o:o + n], X[o:o + n].astype(np.float64))
-        assert np.isnan(Y[o + n:o + 35]).all()  # rows past counts[x] are nobody's
+        assert np.isnan(Y[o + n:o + GEMM_CAP]).all()  # rows past counts[x] are nobody's
 
 
 def test_grouped_gemm_uses_each_segments_own_weight_untransposed():
