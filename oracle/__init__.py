@@ -50,8 +50,9 @@ def lib() -> ctypes.CDLL:
         L.ora_combine.argtypes = [P, P, I, I, I, I, P, P]
         L.ora_combine_bwd.argtypes = [P, P, I, I, I, I, P, P, I, P, P]
         L.ora_dispatch_bwd.argtypes = [P, I, I, I, I, P, P]
+        L.ora_rank_slots.argtypes = [P, I, I, P]
         for f in ("ora_topk_gate", "ora_topk_gate_bwd", "ora_layout", "ora_layout_ex", "ora_dispatch", "ora_combine",
-                  "ora_combine_bwd", "ora_dispatch_bwd"):
+                  "ora_combine_bwd", "ora_dispatch_bwd", "ora_rank_slots"):
             getattr(L, f).restype = I
         _lib = L
     return _lib
@@ -129,6 +130,17 @@ def layout(idx: np.ndarray, e: int, capacity: int = 0, R: int = 0, priority: int
                              _p(out["rank_counts"]))
     _check(rc, "layout")
     out["rows"] = e * capacity if capacity > 0 else s * k + e * (pad_multiple - 1)
+    out["rank_slot"] = rank_slots(out["token_in_rank"]) if R else None
+    return out
+
+
+def rank_slots(token_in_rank: np.ndarray) -> np.ndarray:
+    """Token-order send slot of each token in each virtual rank it sends to
+    (-1 where it sends nothing); token_in_rank [s, R] from layout()."""
+    tir = np.ascontiguousarray(token_in_rank, dtype=np.uint8)
+    s, R = tir.shape
+    out = np.empty((s, R), np.int32)
+    _check(lib().ora_rank_slots(_p(tir), s, R, _p(out)), "rank_slots")
     return out
 
 

@@ -234,6 +234,24 @@ int ora_layout(const int32_t* idx, int s, int e, int k, int capacity, int R,
                        offsets, token_in_rank, rank_counts);
 }
 
+/* ---------------------------------------------------------- send slots -- */
+
+int ora_rank_slots(const uint8_t* token_in_rank, int s, int R, int32_t* rank_slot) {
+  if (!token_in_rank || !rank_slot || s < 0 || R < 1) return ORA_EARG;
+  for (int r = 0; r < R; ++r) {
+    int32_t next = 0; /* tokens seen so far that send to r */
+    for (int t = 0; t < s; ++t) {
+      if (token_in_rank[(size_t)t * R + r]) {
+        rank_slot[(size_t)t * R + r] = next;
+        next += 1;
+      } else {
+        rank_slot[(size_t)t * R + r] = -1;
+      }
+    }
+  }
+  return ORA_OK;
+}
+
 /* ------------------------------------------------------------ dispatch -- */
 
 int ora_dispatch(const int32_t* row, int s, int k, int m, int dtype,

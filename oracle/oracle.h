@@ -114,6 +114,15 @@ int ora_layout_ex(const int32_t* idx, int s, int e, int k, int capacity, int R, 
                   int32_t* raw_counts, int32_t* counts, int32_t* offsets,
                   uint8_t* token_in_rank, int32_t* rank_counts);
 
+/* Per-virtual-rank send slots [DeepSpeed #8213 description: a token goes to
+ * each destination rank once, whatever number of that rank's experts it
+ * selected].  For every rank r, the tokens that send to r (token_in_rank
+ * [s,R] from ora_layout) are numbered in token order:
+ *   rank_slot[t,r] = #{ t' < t : token_in_rank[t',r] = 1 }  if token_in_rank[t,r]
+ *                  = -1                                     otherwise,
+ * so slot values of rank r run 0 .. rank_counts[r]-1. */
+int ora_rank_slots(const uint8_t* token_in_rank, int s, int R, int32_t* rank_slot);
+
 /* Dispatch [P4 change 3]: X has `rows` rows of m elements; every row is first
  * zero, then X[row[t,j]] = x[t] for each kept route (row >= 0). */
 int ora_dispatch(const int32_t* row, int s, int k, int m, int dtype,

@@ -68,6 +68,7 @@ def test_hand_worked_example():
     assert L["row"].tolist() == cap["row"]
     assert L["token_in_rank"].tolist() == cap["token_in_rank_R3"]
     assert L["rank_counts"].tolist() == cap["rank_counts_R3"]
+    assert L["rank_slot"].tolist() == cap["rank_slot_R3"]
 
     dl = g["dropless"]
     L = oracle.layout(idx, e=3, capacity=0, R=3)
@@ -78,6 +79,7 @@ def test_hand_worked_example():
     assert L["row"].tolist() == dl["row"]
     assert L["token_in_rank"].tolist() == dl["token_in_rank_R3"]
     assert L["rank_counts"].tolist() == dl["rank_counts_R3"]
+    assert L["rank_slot"].tolist() == dl["rank_slot_R3"]
 
 
 # -------------------------------------------------------------------- bf16 --
@@ -651,3 +653,34 @@ def test_grouped_gemm_brute_force_and_bf16_decoding():
     # the same values as float32 give the same result
     np.testing.assert_array_equal(Y, oracle.grouped_gemm(Xb.float().numpy(), Wb.float().numpy(),
                                                          L["offsets"], L["counts"]))
+
+
+# ------------------------------------------------ per-rank send slots --
+# DeepSpeed #8213 description: a token is sent to a destination rank once;
+# its place in that rank's send buffer is its token-order rank among the
+# tokens that go there.
+
+@pytest.mark.parametrize("cap", [0, 30])
+def test_rank_slots_brute_force_and_invariants(cap):
+    idx = W.random_routes(300, 16, 4, seed=21).numpy()
+    R = 4
+    L = oracle.layout(idx, 16, cap, R)
+    tir, slot = L["token_in_rank"], L["rank_slot"]
+    s = idx.shape[0]
+    for r in range(R):
+        for t in range(0, s, 7):
+            want = sum(int(tir[t2, r]) for t2 in range(t)) if tir[t, r] else -1
+            assert slot[t, r] == want
+        used = np.sort(slot[:, r][slot[:, r] >= 0])
+        np.testing.assert_array_equal(used, np.arange(L["rank_counts"][r]))  # a permutation of 0..n-1
+    assert ((slot >= 0) == tir.astype(bool)).all()
+    if cap:
+        assert L["drop"].any()  # drops change which tokens send where
+
+
+def test_rank_slots_closed_form():
+    # slot = inclusive cumulative sum of the column - 1, where the token sends
+    tir = (np.random.default_rng(5).random((500, 8)) < 0.3).astype(np.uint8)
+    slot = oracle.rank_slots(tir)
+    want = np.where(tir == 1, np.cumsum(tir.astype(np.int64), axis=0) - 1, -1)
+    np.testing.assert_array_equal(slot, want)
