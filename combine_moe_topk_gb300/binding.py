@@ -26,7 +26,7 @@ STATUS = {
 MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
 MOE_DEV_NONFINITE, MOE_DEV_BAD_ROUTE, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4
 KERNELS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd", "topk_gate_bwd",
-           "grouped_gemm", "dispatch_gemm"]
+           "grouped_gemm", "dispatch_gemm", "rank_slots"]
 KERNEL_ID = {n: i for i, n in enumerate(KERNELS)}
 
 # every entry point the header declares (checked by the CPU test-suite)
@@ -48,7 +48,7 @@ class MoEError(RuntimeError):
 
 class LayoutOptions(ctypes.Structure):
     _fields_ = [("capacity", ctypes.c_int32), ("num_virtual_ranks", ctypes.c_int32), ("priority", ctypes.c_int32),
-                ("pad_multiple", ctypes.c_int32)]
+                ("pad_multiple", ctypes.c_int32), ("send_slots", ctypes.c_int32)]
 
 
 PRIORITY = {"token": 0, "kmajor": 1}
@@ -59,7 +59,7 @@ class LayoutInfo(ctypes.Structure):
                 ("capacity", ctypes.c_int32), ("R", ctypes.c_int32), ("rows", ctypes.c_int32),
                 ("device", ctypes.c_int32), ("priority", ctypes.c_int32), ("pad_multiple", ctypes.c_int32)] + [
         (n, ctypes.c_void_p) for n in ("idx", "loc", "row", "drop", "raw_counts", "counts", "offsets",
-                                       "token_in_rank", "rank_counts", "status", "inv_row")]
+                                       "token_in_rank", "rank_counts", "status", "inv_row", "rank_slot")]
 
 
 _lib = None
@@ -187,6 +187,10 @@ class Handle:
     def token_in_rank(self): return self._view("token_in_rank", (self.s, self.R), "|u1")
     def rank_counts(self): return self._view("rank_counts", (self.R,), "<i4")
     def inv_row(self): return self._view("inv_row", (self.rows,), "<i4")
+    def rank_slot(self):
+        if not self.info.rank_slot:
+            raise MoEError(1, "rank_slot", "the handle was built without send_slots")
+        return self._view("rank_slot", (self.s, self.R), "<i4")
 
     def status(self) -> int:
         """Synchronise and read the device status word (MOE_DEV_* bits)."""
@@ -276,13 +280,16 @@ def moe_dispatch_layout(topk_idx: torch.Tensor, e: int, capacity: int = 0, num_v
 
 
 def moe_dispatch_layout_ex(topk_idx: torch.Tensor, e: int, capacity: int = 0, num_virtual_ranks: int = 0,
-                           priority: str = "token", pad_multiple: int = 1) -> Handle:
-    """Layout with a capacity priority ("token" or "kmajor") and per-expert
-    padding of the dropless rows (handle.rows is then an upper bound)."""
+                           priority: str = "token", pad_multiple: int = 1, send_slots: bool = False) -> Handle:
+    """Layout with a capacity priority ("token" or "kmajor"), per-expert
+    padding of the dropless rows (handle.rows is then an upper bound) and,
+    with send_slots, each token's token-order slot per virtual rank
+    (handle.rank_slot())."""
     if topk_idx.dim() != 2 or topk_idx.dtype != torch.int32:
         raise ValueError("topk_idx must be int32 [s, k]")
     s, k = topk_idx.shape
-    opt = LayoutOptions(int(capacity), int(num_virtual_ranks), PRIORITY[priority], int(pad_multiple))
+    opt = LayoutOptions(int(capacity), int(num_virtual_ranks), PRIORITY[priority], int(pad_multiple),
+                        int(bool(send_slots)))
     raw = ctypes.c_void_p()
     dev = topk_idx.device
     rc = lib().moe_dispatch_layout_ex(_ptr(topk_idx), s, int(e), k, ctypes.byref(opt), _stream(dev),

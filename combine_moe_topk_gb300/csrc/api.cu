@@ -26,6 +26,7 @@ struct moe_handle_s {
   void* blob;
   size_t blob_bytes;
   moe::LayoutOut out;
+  int32_t* rank_slot;  // [s,R] send slots, or NULL
   moe::LayoutPlan plan;
 };
 
@@ -278,6 +279,10 @@ moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
     return fail(MOE_ERR_INVALID_ARG, "unknown priority");
   if (pad > 1 && capacity > 0) return fail(MOE_ERR_INVALID_ARG, "pad_multiple applies to the dropless layout only");
   if (pad > 65536) return fail(MOE_ERR_INVALID_ARG, "pad_multiple must be <= 65536");
+  const int send_slots = options->send_slots;
+  if (send_slots != 0 && send_slots != 1) return fail(MOE_ERR_INVALID_ARG, "send_slots must be 0 or 1");
+  if (send_slots && options->num_virtual_ranks <= 0)
+    return fail(MOE_ERR_INVALID_ARG, "send_slots needs num_virtual_ranks > 0");
   if (s < 0 || e < 1 || e > kMaxE || k < 1 || k > e || k > kMaxK)
     return fail(MOE_ERR_INVALID_ARG, "need s >= 0, 1 <= e <= 256, 1 <= k <= min(e, 16)");
   if (capacity < 0) return fail(MOE_ERR_INVALID_ARG, "capacity must be >= 0 (0 = dropless)");
@@ -326,6 +331,7 @@ moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
   const size_t o_off = off;    off = align_up(off + 4 * (size_t)(e + 1), A);
   const size_t o_tir = off;    off = align_up(off + (size_t)s * (R > 0 ? R : 0) + 1, A);
   const size_t o_inv = off;    off = align_up(off + 4 * (size_t)rows + 4, A);
+  const size_t o_slot = off;   off = align_up(off + (send_slots ? 4 * (size_t)s * R : 0), A);
   h->blob_bytes = off;
 
   cudaError_t err = cudaMallocFromPoolAsync(&h->blob, h->blob_bytes, g_pool[dev], h->stream);
@@ -346,6 +352,7 @@ moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
   h->out.offsets = reinterpret_cast<int32_t*>(base + o_off);
   h->out.token_in_rank = R > 0 ? reinterpret_cast<uint8_t*>(base + o_tir) : nullptr;
   h->out.inv_row = reinterpret_cast<int32_t*>(base + o_inv);
+  h->rank_slot = send_slots ? reinterpret_cast<int32_t*>(base + o_slot) : nullptr;
 
   err = cudaMemsetAsync(base, 0, zero_bytes, h->stream);
   int hold = -1;
@@ -367,6 +374,15 @@ moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
     return cuda_fail(err, "layout launch");
   }
   g_launches[MOE_KERNEL_LAYOUT]++;
+  if (h->rank_slot && s > 0) {
+    err = moe::launch_rank_slots(h->out.token_in_rank, s, R, h->rank_slot, h->stream);
+    if (err != cudaSuccess) {
+      cudaFreeAsync(h->blob, h->stream);
+      delete h;
+      return cuda_fail(err, "rank_slots launch");
+    }
+    g_launches[MOE_KERNEL_RANK_SLOTS]++;
+  }
   {
     std::lock_guard<std::mutex> lk(g_mu);
     g_live.insert(h);
@@ -382,18 +398,20 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int
   opt.num_virtual_ranks = num_virtual_ranks;
   opt.priority = MOE_PRIORITY_TOKEN;
   opt.pad_multiple = 1;
+  opt.send_slots = 0;
   return moe_dispatch_layout_ex(topk_idx, s, e, k, &opt, stream, out);
 }
 
 namespace {
 
-moe_status check_gemm(moe_handle h, int rows, int K, int N, const void* A, const char* a_name,
+// Sizes first; pointers only when there is work (a_rows rows of A, rows of Y).
+moe_status check_gemm(moe_handle h, int rows, int K, int N, const void* A, const char* a_name, int a_rows,
                       const void* W, const void* Y) {
   if (rows != h->rows) return fail(MOE_ERR_HANDLE_MISMATCH, "row count differs from the handle's");
   if (K < 64 || K % 64 != 0) return fail(MOE_ERR_INVALID_ARG, "K must be a positive multiple of 64");
   if (N < 256 || N % 256 != 0) return fail(MOE_ERR_INVALID_ARG, "N must be a positive multiple of 256");
   if ((long long)h->e * N > 2147483647LL) return fail(MOE_ERR_INVALID_ARG, "e * N must be < 2^31");
-  if (rows == 0) return MOE_OK;
+  if (rows == 0 || a_rows == 0) return MOE_OK;
   MOE_TRY(check_ptr(A, a_name));
   MOE_TRY(check_ptr(W, "W"));
   MOE_TRY(check_ptr(Y, "Y"));
@@ -416,7 +434,7 @@ moe_status gemm_result(cudaError_t err, const char* where, int kernel) {
 moe_status moe_grouped_gemm(moe_handle h, int rows, int K, int N, const void* X, const void* W,
                             void* Y, void* stream) {
   MOE_TRY(live_handle(h));
-  MOE_TRY(check_gemm(h, rows, K, N, X, "X", W, Y));
+  MOE_TRY(check_gemm(h, rows, K, N, X, "X", rows, W, Y));
   if (rows == 0) return MOE_OK;
   const moe::DeviceInfo* di = nullptr;
   MOE_TRY(device_state(h->device, &di));
@@ -429,7 +447,7 @@ moe_status moe_dispatch_grouped_gemm(moe_handle h, int s, int rows, int K, int N
                                      const void* W, void* Y, void* stream) {
   MOE_TRY(live_handle(h));
   MOE_TRY(check_shape(h, s, rows));
-  MOE_TRY(check_gemm(h, rows, K, N, x, "x", W, Y));
+  MOE_TRY(check_gemm(h, rows, K, N, x, "x", s, W, Y));
   if (rows == 0 || s == 0) return MOE_OK;
   const moe::DeviceInfo* di = nullptr;
   MOE_TRY(device_state(h->device, &di));
@@ -462,6 +480,7 @@ moe_status moe_handle_info(moe_handle h, moe_layout_info* info) {
   info->rank_counts = h->out.rank_counts;
   info->status = h->out.status;
   info->inv_row = h->out.inv_row;
+  info->rank_slot = h->rank_slot;
   return MOE_OK;
 }
 

@@ -79,6 +79,12 @@ cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const 
                                int e, int m, int dtype, const void* dout, const void* y, void* dY,
                                float* dgate, const DeviceInfo& di, cudaStream_t st);
 
+// --- per-virtual-rank send slots ------------------------------------------
+// rank_slot[t,r] = token-order position of t among the tokens sending to r,
+// -1 where token_in_rank[t,r] = 0.  [s,R] int32, one CTA per rank.
+cudaError_t launch_rank_slots(const uint8_t* token_in_rank, int s, int R, int32_t* rank_slot,
+                              cudaStream_t st);
+
 // --- expert-grouped GEMM on the tensor cores -----------------------------
 // Y[r] = X[r] . W[x]^T over the 128-row blocks of each expert segment that a
 // route owns.  K % 64 == 0, N % 256 == 0; a segment may start on any row.

@@ -81,7 +81,8 @@ enum {
   MOE_KERNEL_TOPK_GATE_BWD = 6,
   MOE_KERNEL_GROUPED_GEMM = 7,
   MOE_KERNEL_DISPATCH_GEMM = 8,
-  MOE_KERNEL_COUNT = 9
+  MOE_KERNEL_RANK_SLOTS = 9,
+  MOE_KERNEL_COUNT = 10
 };
 
 /* Opaque layout handle [P1 "How"; P3 description].  Owned by the library:
@@ -105,6 +106,7 @@ typedef struct {
   int32_t priority;          /* MOE_PRIORITY_*                                       */
   int32_t pad_multiple;      /* dropless only: each expert's rows padded to a
                                 multiple of this; 1 (or 0) = no padding            */
+  int32_t send_slots;        /* 1: also build rank_slot (needs num_virtual_ranks > 0) */
 } moe_layout_options;
 
 /* Host view of a handle: sizes and read-only device pointers. */
@@ -128,6 +130,8 @@ typedef struct {
   const int32_t* status;        /* device status word of this handle            */
   const int32_t* inv_row;       /* [rows] token whose kept route owns the row;
                                    unspecified at rows no route owns           */
+  const int32_t* rank_slot;     /* [s,R] token-order send slot per virtual rank,
+                                   -1 = not sent; NULL unless send_slots = 1   */
 } moe_layout_info;
 
 /* Top-k softmax gating [P4 change 1; P1 description: recompute must route
@@ -214,9 +218,17 @@ moe_status moe_dispatch_layout_noalloc(const int32_t* topk_idx, int s, int e, in
  *   pad_multiple = P > 1 (dropless only): offsets[x+1] = offsets[x] +
  *     ceil(counts[x] / P) * P; the handle's rows is the upper bound
  *     s*k + e*(P-1), so it stays a host integer; dispatch and the combine
- *     backward write zeros into padding rows and rows past offsets[e].
- * Errors as moe_dispatch_layout; pad_multiple > 1 with capacity > 0, or an
- * unknown priority, is MOE_ERR_INVALID_ARG. */
+ *     backward write zeros into padding rows and rows past offsets[e];
+ *   send_slots = 1 (needs num_virtual_ranks R > 0) [DeepSpeed #8213
+ *     description: a token goes to a destination rank once]: rank_slot
+ *     [s,R] int32, rank_slot[t,r] = #{t' < t : token_in_rank[t',r]} where
+ *     token_in_rank[t,r] = 1, else -1: each token's slot in the send buffer
+ *     of every virtual rank it goes to, in token order (whatever the
+ *     capacity priority); rank r's slots are 0 .. rank_counts[r]-1.  One more
+ *     kernel (MOE_KERNEL_RANK_SLOTS), one CTA per rank.
+ * Errors as moe_dispatch_layout; pad_multiple > 1 with capacity > 0, an
+ * unknown priority, or send_slots without virtual ranks is
+ * MOE_ERR_INVALID_ARG. */
 moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
                                   const moe_layout_options* options, void* stream, moe_handle* out);
 

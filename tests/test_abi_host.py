@@ -86,6 +86,15 @@ def test_layout_rejects_bad_sizes_without_a_gpu(lib):
     assert rc_name(lib.moe_dispatch_layout(fake, 4, 8, 2, 2**29, 0, None, ctypes.byref(out))) == "MOE_ERR_INVALID_ARG"
     assert rc_name(lib.moe_dispatch_layout(fake, 4, 8, 2, 0, 0, None, None)) == "MOE_ERR_INVALID_ARG"
     assert out.value is None
+    # send slots need virtual ranks; the flag is 0 or 1
+    opt = B.LayoutOptions(0, 0, 0, 1, 1)
+    assert rc_name(lib.moe_dispatch_layout_ex(fake, 4, 8, 2, ctypes.byref(opt), None, ctypes.byref(out))) \
+        == "MOE_ERR_INVALID_ARG"
+    assert "num_virtual_ranks" in lib.moe_last_error().decode()
+    opt = B.LayoutOptions(0, 2, 0, 1, 2)
+    assert rc_name(lib.moe_dispatch_layout_ex(fake, 4, 8, 2, ctypes.byref(opt), None, ctypes.byref(out))) \
+        == "MOE_ERR_INVALID_ARG"
+    assert out.value is None
 
 
 def test_unknown_handles_are_rejected_without_a_gpu(lib):

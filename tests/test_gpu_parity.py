@@ -49,6 +49,29 @@ def test_kmajor_with_padding_and_dedup():
     full_parity(REDUCED["fine-grained-skewed"].replace(s=1500), DEV, priority="kmajor", pad_multiple=8)
 
 
+@pytest.mark.parametrize("case", [
+    dict(s=16384, e=128, k=8, capacity=0, R=8, priority="token"),      # fine-grained shape, full size
+    dict(s=32768, e=64, k=6, capacity=3072, R=16, priority="token"),   # GShard shape with drops, full size
+    dict(s=5000, e=64, k=6, capacity=400, R=4, priority="kmajor"),
+    dict(s=20001, e=128, k=4, capacity=0, R=64, priority="token"),     # two scan chunks, ragged, 64 ranks
+    dict(s=3, e=4, k=2, capacity=1, R=2, priority="token"),
+], ids=lambda c: f"s{c['s']}-e{c['e']}-R{c['R']}-c{c['capacity']}-{c['priority']}")
+def test_send_slots_parity(case):
+    """Per-virtual-rank token-order send slots: bit-exact against the oracle,
+    and the rest of the layout unchanged by asking for them."""
+    idx = W.random_routes(case["s"], case["e"], case["k"], seed=17).numpy()
+    h = B.moe_dispatch_layout_ex(to_dev(idx, DEV), case["e"], case["capacity"], case["R"], case["priority"],
+                                 send_slots=True)
+    L = oracle.layout(idx, case["e"], case["capacity"], case["R"],
+                      priority=1 if case["priority"] == "kmajor" else 0)
+    check_layout(h, L, idx)
+    np.testing.assert_array_equal(bits(h.rank_slot()), L["rank_slot"])
+    assert h.status() == 0
+    plain = B.moe_dispatch_layout_ex(to_dev(idx, DEV), case["e"], case["capacity"], case["R"], case["priority"])
+    with pytest.raises(B.MoEError):
+        plain.rank_slot()
+
+
 def test_tiny_capacity_full_softmax_gates():
     full_parity(W.WORKLOADS["tiny-capacity"], DEV, renorm=0)
 
@@ -102,6 +125,12 @@ def test_empty_batch():
         out = B.moe_combine(h, X, torch.empty(0, 2, device=DEV))
         assert out.shape == (0, 8)
         assert h.status() == 0
+        hs = B.moe_dispatch_layout_ex(idx, 4, cap, 2, send_slots=True)
+        assert hs.rank_slot().shape == (0, 2) and bits(hs.rank_counts()).tolist() == [0, 0]
+        xg = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
+        Wg = torch.zeros(4, 256, 64, dtype=torch.bfloat16, device=DEV)
+        Y = B.moe_dispatch_grouped_gemm(hs, xg, Wg)  # nothing to gather: no launch, no error
+        assert Y.shape == (hs.rows, 256) and hs.status() == 0
 
 
 @pytest.mark.parametrize("renorm", [0, 1])
