@@ -16,25 +16,36 @@
 // contiguous; the accumulation is fp32 in TMEM.  Work units are 128-row
 // blocks of one expert's segment (ceil(counts[x] / 128) of them, the first
 // at offsets[x], so a segment may start on any row) times 256-column tiles
-// of N.  One CTA per SM, persistent over the units:
+// of N.
+//
+// The plain GEMM runs on pairs of SMs (grouped_gemm_pair_kernel, below): a
+// cluster of two CTAs computes a 256-row block x 256 columns with
+// tcgen05.mma.cta_group::2, each SM staging only its half of A and of B.
+// The fused form runs one CTA per SM (grouped_gemm_kernel<true>), since
+// its A rows are written by threads: in a pair, the second CTA's rows need
+// a cluster-scope release per K-block to reach the MMA issuer, and that
+// held a two-SM version to 0.56 PFLOP/s.  One CTA per SM, persistent over
+// the units:
 //   warp 0 lane 0  -- TMA producer: B (256 x 64) K-blocks, and in the plain
 //                     form A (128 x 64) as one tile load, into a 4-stage
 //                     SWIZZLE_128B ring, mbarrier complete_tx;
 //   warps 8..11    -- fused form only: gather the A rows with 16-byte
-//                     cp.async in the same swizzle, each thread arriving on
-//                     a stage once its copies have landed (a TMA tile::gather4
-//                     of four rows per request was tried first: correct, but
-//                     at 33 copy requests per K-block it held the GEMM to a
-//                     third of the tensor rate);
+//                     cp.async in the same swizzle, each warp arriving on
+//                     a stage once its lanes' copies have landed (a TMA
+//                     tile::gather4 of four rows per request was tried
+//                     first: correct, but at 33 copy requests per K-block
+//                     it held the GEMM to a third of the tensor rate);
 //   warp 1 lane 0  -- MMA issuer: four tcgen05.mma (M128 N256 K16) per
 //                     K-block into one of two 256-column TMEM accumulators,
 //                     tcgen05.commit frees the ring stage / hands over the tile;
 //   warp 2         -- allocates (and at the end frees) 512 TMEM columns;
 //   warp 3         -- the per-expert block prefix, once;
 //   warps 4..7     -- epilogue: tcgen05.ld 32 lanes x 32 columns at a time,
-//                     fp32 -> bf16 (nearest-even), 16-byte stores of the
-//                     block's owned rows only (a block's tail may belong to
-//                     the next segment or to no route).
+//                     fp32 -> bf16 (nearest-even), staged through shared
+//                     memory so each store instruction writes 4 rows x 128
+//                     bytes; only the block's owned rows are stored (a
+//                     block's tail may belong to the next segment or to no
+//                     route).
 // Every mbarrier wait is bounded on the global timer; a time-out records
 // MOE_DEV_TIMEOUT and the roles wind down to the TMEM release.
 #include <cuda.h>
@@ -55,13 +66,22 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTmemCols = 2 * BN;     // two fp32 accumulators of 128 lanes x 256 columns
 constexpr int kThreads = 256;        // tile-fed form
 constexpr int kGatherThreads = 384;  // fused form: + 4 warps gathering the A rows
+// Plain GEMM: 1 = the two-SM (cta_group::2) kernel, 0 = the one-SM kernel.
+#ifndef MOE_GEMM_PAIR
+#define MOE_GEMM_PAIR 1
+#endif
 #ifndef MOE_GEMM_LAG
 #define MOE_GEMM_LAG 2
 #endif
 constexpr int kGatherLag = MOE_GEMM_LAG;  // stages a gather thread's arrivals trail its copies
 static_assert(kGatherLag >= 1 && kGatherLag < 4, "the ring must keep a stage the gather has not yet claimed");
 constexpr int kMaxE = 256;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+// epilogue staging: per epilogue warp 32 rows x 64 bf16 columns, rows padded
+// to 144 bytes (conflict-free 16-byte writes by row and reads by column)
+constexpr int kStageRowBytes = 64 * 2 + 16;
+constexpr int kEpiWarpBytes = 32 * kStageRowBytes;
+constexpr int kEpiBytes = 4 * kEpiWarpBytes;
+constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + 1024;  // + alignment slack
 
 struct GemmParams {
   const __nv_bfloat16* x;  // gather mode: token rows [s, K]
@@ -117,12 +137,6 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-// Order this thread's completed shared-memory writes before later reads of
-// the tensor cores (the async proxy).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -164,6 +178,45 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Drain one 128 x 256 fp32 accumulator to bf16 rows of Y.  Epilogue warp ew
+// owns TMEM lanes 32ew .. 32ew+31 (rows r0 + 32ew ..); 64 columns at a time,
+// each lane converts its row (nearest-even) into the warp's padded staging
+// tile, then the warp stores it back out as 4 rows x 128 bytes per
+// instruction.  Only rows below nvalid (owned by a route) are stored.
+__device__ __forceinline__ void store_accumulator(uint32_t tcol, int ew, int lane, uint8_t* stage,
+                                                  __nv_bfloat16* Y, int N, int r0, int n0, int nvalid) {
+#pragma unroll 1
+  for (int c2 = 0; c2 < BN / 64; ++c2) {
+    uint4 out[8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v[32];
+      tmem_ld32(tcol + (uint32_t)(64 * c2 + 32 * h), v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v[8 * q + i]);
+        out[4 * h + q] = Vec<__nv_bfloat16>::from_float(f);
+      }
+    }
+    uint4* srow = reinterpret_cast<uint4*>(stage + lane * kStageRowBytes);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) srow[q] = out[q];
+    __syncwarp();
+    const int ch = lane & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int row = 4 * i + (lane >> 3);
+      if (32 * ew + row < nvalid) {
+        const uint4 val = *reinterpret_cast<const uint4*>(stage + row * kStageRowBytes + ch * 16);
+        *reinterpret_cast<uint4*>(Y + (size_t)(r0 + 32 * ew + row) * N + n0 + 64 * c2 + 8 * ch) = val;
+      }
+    }
+    __syncwarp();  // the staging tile is rewritten by the next 64 columns
+  }
 }
 
 // Unit u -> expert x, first row r0 and owned rows of its 128-row block, and
@@ -209,8 +262,8 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
   if (threadIdx.x == 0) {
     s_err = 0;
     for (int i = 0; i < kStages; ++i) {
-      // the B tile's expect_tx arrival, plus one per gathering thread
-      mbar_init(&full[i], kGather ? 1 + (kGatherThreads - kThreads) : 1);
+      // the B tile's expect_tx arrival, plus one per gathering warp
+      mbar_init(&full[i], kGather ? 1 + (kGatherThreads - kThreads) / 32 : 1);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -281,8 +334,9 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
     // Warp gw copies rows 32*gw .. 32*gw+31 of the block; per instruction 8
     // lanes cover one row's 128 bytes (4 rows at a time), written in the
     // 128-byte swizzle the MMA descriptor reads (16-byte chunk c of row r at
-    // chunk c ^ (r & 7)).  A thread arrives on a stage's full barrier once
-    // its copies to it have landed, kGatherLag stages behind its issue.
+    // chunk c ^ (r & 7)).  Each lane waits for its copies to a stage (kGatherLag
+    // stages behind its issue) and fences them for the tensor cores; then one
+    // lane arrives on the stage's full barrier for the warp.
     const int gw = warp - kThreads / 32, chunk = lane & 7;
     int stage = 0, astage = 0, pending = 0;
     uint32_t phase = 0;
@@ -317,7 +371,8 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
         if (++pending > kGatherLag) {
           cp_async_wait<kGatherLag>();
           fence_proxy_async_smem();
-          mbar_arrive(&full[astage]);
+          __syncwarp();  // every lane's copies to the stage have landed
+          if (lane == 0) mbar_arrive(&full[astage]);
           --pending;
           if (++astage == kStages) astage = 0;
         }
@@ -330,8 +385,9 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
     cp_async_wait<0>();  // nothing of this thread's stays in flight
     if (ok) {
       fence_proxy_async_smem();
+      __syncwarp();
       for (; pending > 0; --pending) {
-        mbar_arrive(&full[astage]);
+        if (lane == 0) mbar_arrive(&full[astage]);
         if (++astage == kStages) astage = 0;
       }
     } else if (lane == 0) {
@@ -387,26 +443,8 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
       }
       tphase[acc] ^= 1u;
       tc_fence_after();
-      const int rr = 32 * ew + lane;
-      const bool owned = rr < t.nvalid && t.r0 + rr < p.rows;
-      __nv_bfloat16* yrow = p.Y + (size_t)(owned ? t.r0 + rr : 0) * p.N + t.n0;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tbase + ((uint32_t)(32 * ew) << 16) + (uint32_t)(acc * BN + 32 * c), v);
-        uint4 out[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float f[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v[8 * q + i]);
-          out[q] = Vec<__nv_bfloat16>::from_float(f);
-        }
-        uint4* dst = reinterpret_cast<uint4*>(yrow + 32 * c);
-        if (owned)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) dst[q] = out[q];
-      }
+      store_accumulator(tbase + ((uint32_t)(32 * ew) << 16) + (uint32_t)(acc * BN), ew, lane,
+                        smem + kStages * kStageBytes + ew * kEpiWarpBytes, p.Y, p.N, t.r0, t.n0, t.nvalid);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
@@ -419,6 +457,286 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
   tc_fence_after();
   if (warp == 2)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),
+                 "r"(kTmemCols)
+                 : "memory");
+  if (threadIdx.x == 0 && s_err) raise_status(p.status, MOE_DEV_TIMEOUT);
+}
+
+// ---- two-SM form (cta_group::2) ------------------------------------------
+// A cluster of two CTAs on two SMs computes one 256 x 256 tile: CTA rank c
+// holds rows 128c .. 128c+127 of the 256-row block (its A half) and columns
+// 128c .. 128c+127 of the 256-column tile (its B half); one thread of rank
+// 0 issues tcgen05.mma.cta_group::2 (M256 N256 K16), which reads both
+// CTAs' shared memory at the same offsets and leaves each CTA's 128 rows
+// of the fp32 result in its own TMEM.  Per SM and K-block only 32 KB move
+// (48 KB in the one-SM form), so the ring holds six stages.
+//   both ranks, warp 0 lane 0: TMA of its A and B halves; the completion
+//     bytes of both ranks are counted on rank 0's full barrier (the
+//     .cta_group::2 form of the copy lets rank 1 signal it);
+//   rank 0, warp 1 lane 0: MMA; its commits arrive on the empty / tfull
+//     barriers of both ranks (multicast);
+//   both ranks, warp 2: one collective TMEM allocation for the pair;
+//   both ranks, warps 4..7: epilogue of its own rows, then an arrival on
+//     rank 0's tempty barrier (remote for rank 1).
+constexpr int kPairStages = 6;
+constexpr int kPairABytes = BM * BK * 2;        // 16 KB: this CTA's 128 rows of A
+constexpr int kPairBBytes = (BN / 2) * BK * 2;  // 16 KB: this CTA's 128 rows of B
+constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
+constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kEpiBytes + 1024;
+constexpr int BM2 = 2 * BM;                     // rows of a pair block
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// 2-D tile into this CTA's shared memory; completion bytes counted on the
+// mbarrier at cluster address `mbar` (rank 0's barrier for both ranks).
+__device__ __forceinline__ void tma_load_2d_pair(void* sdst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(sdst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, int accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the barrier at this offset in both CTAs of the pair once the
+// issuing thread's earlier MMAs have completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_addr(bar)),
+      "h"((uint16_t)0x3)
+      : "memory");
+}
+
+// Bounded wait with cluster-scope acquire, for barriers that receive
+// arrivals from the other CTA of the pair.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t deadline_ns) {
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 63) == 63 && globaltimer_ns() > deadline_ns) return false;
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t mbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mbar) : "memory");
+}
+
+__device__ __forceinline__ uint32_t mma_idesc_pair() {
+  uint32_t d = 0;
+  d |= 1u << 4;                        // accumulator format: f32
+  d |= 1u << 7;                        // A format: bf16
+  d |= 1u << 10;                       // B format: bf16
+  d |= (uint32_t)(BN >> 3) << 17;      // N / 8 (the pair's 256 columns)
+  d |= (uint32_t)(BM2 >> 4) << 24;     // M / 16 (the pair's 256 rows)
+  return d;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[kPairStages], empty[kPairStages], tfull[2], tempty[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_off[kMaxE + 1], s_cnt[kMaxE], s_blk[kMaxE + 1];
+  __shared__ int s_err;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0 or 1 within the pair
+  // identical static layout in both CTAs: the dynamic buffer starts at the
+  // same offset, so the MMA's descriptors address the same tiles in both
+  uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+  const uint64_t deadline = globaltimer_ns() + (uint64_t)p.timeout_ns;
+
+  for (int x = threadIdx.x; x <= p.e; x += blockDim.x) s_off[x] = __ldg(p.offsets + x);
+  for (int x = threadIdx.x; x < p.e; x += blockDim.x) s_cnt[x] = __ldg(p.counts + x);
+  if (threadIdx.x == 0) {
+    s_err = 0;
+    for (int i = 0; i < kPairStages; ++i) {
+      mbar_init(&full[i], 1);   // rank 0: its expect_tx arrival; both ranks' bytes
+      mbar_init(&empty[i], 1);  // the MMA commit, multicast to both ranks
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 2 * 128);  // rank 0: the epilogue threads of both ranks
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else if (warp == 3) {
+    // exclusive prefix over experts of their 256-row block counts
+    int carry = 0;
+    for (int x0 = 0; x0 < p.e; x0 += 32) {
+      const int x = x0 + lane;
+      const int c = x < p.e ? s_cnt[x] : 0;
+      const int blocks = c > 0 ? (c + BM2 - 1) / BM2 : 0;
+      int v = blocks;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int w = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += w;
+      }
+      if (x < p.e) s_blk[x] = carry + v - blocks;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) s_blk[p.e] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both ranks' barriers are initialised before any remote signal
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
+
+  const int ntn = p.N / BN;
+  const int nunits = s_blk[p.e] * ntn;
+  const int kblocks = p.K / BK;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer (both ranks) ---------------------------------------
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = pair; u < nunits && ok; u += npairs) {
+      const Unit t = decode_unit(u, ntn, s_blk, s_off, s_cnt, p.e);  // rows in units of BM2 below
+      const int b = u / ntn;
+      const int r0 = s_off[t.x] + BM2 * (b - s_blk[t.x]) + BM * (int)rank;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, deadline)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem + stage * kPairStageBytes;
+        const uint32_t fb = mapa_shared(smem_addr(&full[stage]), 0);
+        if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kPairStageBytes);
+        tma_load_2d_pair(sa, &tmA, kb * BK, r0, fb);
+        tma_load_2d_pair(sa + kPairABytes, &tmB, kb * BK, t.x * p.N + t.n0 + (BN / 2) * (int)rank, fb);
+        if (++stage == kPairStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // drain: every stage's last fill consumed, so no commit of rank 0 is
+    // still on its way to this CTA's barriers when it leaves
+    for (int i = 0; i < kPairStages && ok; ++i) {
+      if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, deadline)) ok = false;
+      if (++stage == kPairStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) atomicOr(&s_err, 1);
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---- MMA issuer (rank 0) ----------------------------------------------
+    const uint32_t idesc = mma_idesc_pair();
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, tphase[2] = {0u, 0u};
+    bool ok = true;
+    for (int u = pair; u < nunits && ok; u += npairs) {
+      if (!mbar_wait_cluster(&tempty[acc], tphase[acc] ^ 1u, deadline)) {
+        ok = false;
+        break;
+      }
+      tphase[acc] ^= 1u;
+      tc_fence_after();
+      const uint32_t dt = tbase + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_cluster(&full[stage], phase, deadline)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_addr(smem + stage * kPairStageBytes);
+        const uint64_t ad = smem_desc(sa), bd = smem_desc(sa + kPairABytes);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16_pair(dt, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (kb | kk) != 0);
+        mma_commit_pair(&empty[stage]);
+        if (++stage == kPairStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      mma_commit_pair(&tfull[acc]);
+      acc ^= 1;
+    }
+    if (!ok) atomicOr(&s_err, 1);
+  } else if (warp >= 4 && warp < 8) {
+    // ---- epilogue (both ranks): own 128 rows ------------------------------
+    const int ew = warp - 4;
+    const uint32_t te0 = mapa_shared(smem_addr(&tempty[0]), 0), te1 = mapa_shared(smem_addr(&tempty[1]), 0);
+    int acc = 0;
+    uint32_t tphase[2] = {0u, 0u};
+    bool ok = true;
+    for (int u = pair; u < nunits && ok; u += npairs) {
+      const Unit t = decode_unit(u, ntn, s_blk, s_off, s_cnt, p.e);
+      const int b = u / ntn;
+      const int i = b - s_blk[t.x];
+      const int r0 = s_off[t.x] + BM2 * i + BM * (int)rank;
+      const int left = s_cnt[t.x] - BM2 * i - BM * (int)rank;
+      const int nvalid = left < 0 ? 0 : (left < BM ? left : BM);
+      if (!mbar_wait_bounded(&tfull[acc], tphase[acc], deadline)) {
+        ok = false;
+        break;
+      }
+      tphase[acc] ^= 1u;
+      tc_fence_after();
+      store_accumulator(tbase + ((uint32_t)(32 * ew) << 16) + (uint32_t)(acc * BN), ew, lane,
+                        smem + kPairStages * kPairStageBytes + ew * kEpiWarpBytes, p.Y, p.N, r0, t.n0, nvalid);
+      tc_fence_before();
+      mbar_arrive_cluster(acc ? te1 : te0);
+      acc ^= 1;
+    }
+    if (!ok) atomicOr(&s_err, 1);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both ranks done with TMEM and with each other's barriers
+  tc_fence_after();
+  if (warp == 2)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tbase),
                  "r"(kTmemCols)
                  : "memory");
   if (threadIdx.x == 0 && s_err) raise_status(p.status, MOE_DEV_TIMEOUT);
@@ -480,6 +798,39 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParam
   return cudaGetLastError();
 }
 
+cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
+                        const DeviceInfo& di, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  static bool done[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!done[dev]) {
+    err = cudaFuncSetAttribute(grouped_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kPairSmemBytes);
+    if (err != cudaSuccess) return err;
+    done[dev] = true;
+  }
+  // pair units: at most ceil(rows / 256) + e blocks of 256 rows, times the column tiles
+  const long long units = (((long long)p.rows + BM2 - 1) / BM2 + p.e) * (p.N / BN);
+  long long pairs = di.sms / 2;
+  if (units < pairs) pairs = units;
+  if (pairs < 1) pairs = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, ma, mb, p);
+}
+
 GemmParams params(const int32_t* offsets, const int32_t* counts, int e, int rows, int K, int N,
                   void* Y, int32_t* status) {
   GemmParams p;
@@ -504,6 +855,12 @@ cudaError_t launch_grouped_gemm(const int32_t* offsets, const int32_t* counts, i
                                 int N, const void* X, const void* W, void* Y, int32_t* status,
                                 const DeviceInfo& di, cudaStream_t st) {
   CUtensorMap ma, mb;
+  if (MOE_GEMM_PAIR) {
+    if (!make_map(&ma, X, (uint64_t)K, (uint64_t)rows, BM) ||
+        !make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN / 2))
+      return cudaErrorInvalidValue;
+    return launch_pair(ma, mb, params(offsets, counts, e, rows, K, N, Y, status), di, st);
+  }
   if (!make_map(&ma, X, (uint64_t)K, (uint64_t)rows, BM) ||
       !make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN))
     return cudaErrorInvalidValue;
