@@ -13,19 +13,20 @@
 // r in [offsets[x], offsets[x] + counts[x]).  A[r] is the dispatched row
 // X[r] (moe_grouped_gemm) or the token row x[inv_row[r]] (fused dispatch:
 // the dispatched buffer is never written or read).  bf16 operands, row-major, K
-// contiguous; the accumulation is fp32 in TMEM.  Work units are 128-row
-// blocks of one expert's segment (ceil(counts[x] / 128) of them, the first
-// at offsets[x], so a segment may start on any row) times 256-column tiles
-// of N.
+// contiguous; the accumulation is fp32 in TMEM.  Work units are row blocks
+// of one expert's segment (256 rows on SM pairs, 128 on single SMs; the
+// first at offsets[x], so a segment may start on any row) times
+// 256-column tiles of N.
 //
-// The plain GEMM runs on pairs of SMs (grouped_gemm_pair_kernel, below): a
+// Both forms run on pairs of SMs (grouped_gemm_pair_kernel, below): a
 // cluster of two CTAs computes a 256-row block x 256 columns with
 // tcgen05.mma.cta_group::2, each SM staging only its half of A and of B.
-// The fused form runs one CTA per SM (grouped_gemm_kernel<true>), since
-// its A rows are written by threads: in a pair, the second CTA's rows need
-// a cluster-scope release per K-block to reach the MMA issuer, and that
-// held a two-SM version to 0.56 PFLOP/s.  One CTA per SM, persistent over
-// the units:
+// In the fused form the second CTA's gathered rows reach the MMA issuer
+// through a 16-byte shared-to-shared bulk copy that counts on the first
+// CTA's barrier: a per-K-block arrival with cluster-scope release instead
+// held the paired fused GEMM to 0.56 PFLOP/s.  The one-SM kernel below
+// (grouped_gemm_kernel, built when MOE_GEMM_PAIR / MOE_GEMM_FUSED_PAIR are
+// 0) has the same roles on one CTA per SM, persistent over the units:
 //   warp 0 lane 0  -- TMA producer: B (256 x 64) K-blocks, and in the plain
 //                     form A (128 x 64) as one tile load, into a 4-stage
 //                     SWIZZLE_128B ring, mbarrier complete_tx;
@@ -69,6 +70,10 @@ constexpr int kGatherThreads = 384;  // fused form: + 4 warps gathering the A ro
 // Plain GEMM: 1 = the two-SM (cta_group::2) kernel, 0 = the one-SM kernel.
 #ifndef MOE_GEMM_PAIR
 #define MOE_GEMM_PAIR 1
+#endif
+// Fused GEMM: 1 = the two-SM kernel, 0 = the one-SM kernel.
+#ifndef MOE_GEMM_FUSED_PAIR
+#define MOE_GEMM_FUSED_PAIR 1
 #endif
 #ifndef MOE_GEMM_LAG
 #define MOE_GEMM_LAG 2
@@ -437,7 +442,8 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
     bool ok = true;
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
       const Unit t = decode_unit(u, ntn, s_blk, s_off, s_cnt, p.e);
-      if (!mbar_wait_bounded(&tfull[acc], tphase[acc], deadline)) {
+      // every lane waits (and acquires) itself; the warp leaves together
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull[acc], tphase[acc], deadline))) {
         ok = false;
         break;
       }
@@ -551,6 +557,16 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   }
 }
 
+// 16 bytes from this CTA's shared memory to `dst` in another CTA of the
+// cluster, the bytes counted on the mbarrier `mbar` there: a signal that
+// travels through the async proxy (no cluster-scope release fence).
+__device__ __forceinline__ void bulk_signal_s2s(uint32_t dst, const void* src, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], 16, [%2];" ::"r"(dst),
+      "r"(smem_addr(src)), "r"(mbar)
+      : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t mbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mbar) : "memory");
 }
@@ -565,17 +581,21 @@ __device__ __forceinline__ uint32_t mma_idesc_pair() {
   return d;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kGather>
+__global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[kPairStages], empty[kPairStages], tfull[2], tempty[2];
+  __shared__ __align__(8) uint64_t gathered[kPairStages];  // fused form, rank 1: its gathered rows landed
+  __shared__ __align__(16) uint8_t s_signal[16];             // fused form: source / target of rank 1's signal
   __shared__ uint32_t tmem_base;
   __shared__ int s_off[kMaxE + 1], s_cnt[kMaxE], s_blk[kMaxE + 1];
   __shared__ int s_err;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0 or 1 within the pair
+  constexpr int kGatherWarps = (kGatherThreads - kThreads) / 32;
   // identical static layout in both CTAs: the dynamic buffer starts at the
   // same offset, so the MMA's descriptors address the same tiles in both
   uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
@@ -586,12 +606,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     s_err = 0;
     for (int i = 0; i < kPairStages; ++i) {
-      mbar_init(&full[i], 1);   // rank 0: its expect_tx arrival; both ranks' bytes
+      // rank 0: its expect_tx arrival (both ranks' TMA bytes, and in the fused
+      // form rank 1's 16-byte signal), plus one arrival per gathering warp
+      mbar_init(&full[i], kGather ? 1 + kGatherWarps : 1);
       mbar_init(&empty[i], 1);  // the MMA commit, multicast to both ranks
+      mbar_init(&gathered[i], kGatherWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 2 * 128);  // rank 0: the epilogue threads of both ranks
+      mbar_init(&tempty[i], 2 * 4);  // rank 0: the epilogue warps of both ranks
     }
     fence_barrier_init();
   }
@@ -647,8 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* sa = smem + stage * kPairStageBytes;
         const uint32_t fb = mapa_shared(smem_addr(&full[stage]), 0);
-        if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kPairStageBytes);
-        tma_load_2d_pair(sa, &tmA, kb * BK, r0, fb);
+        if (rank == 0) mbar_arrive_expect_tx(&full[stage], kGather ? 2 * kPairBBytes + 16 : 2 * kPairStageBytes);
+        if (!kGather) tma_load_2d_pair(sa, &tmA, kb * BK, r0, fb);
         tma_load_2d_pair(sa + kPairABytes, &tmB, kb * BK, t.x * p.N + t.n0 + (BN / 2) * (int)rank, fb);
         if (++stage == kPairStages) {
           stage = 0;
@@ -663,6 +686,93 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++stage == kPairStages) {
         stage = 0;
         phase ^= 1u;
+      }
+    }
+    if (!ok) atomicOr(&s_err, 1);
+  } else if (kGather && warp >= kThreads / 32) {
+    // ---- A gather (fused form, both ranks): this CTA's 128 rows ------------
+    // As in the one-SM form.  Rank 0's warps arrive on its full barrier;
+    // rank 1's on its own `gathered` barrier, forwarded below.
+    const int gw = warp - kThreads / 32, chunk = lane & 7;
+    int stage = 0, astage = 0, pending = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = pair; u < nunits && ok; u += npairs) {
+      const Unit t = decode_unit(u, ntn, s_blk, s_off, s_cnt, p.e);
+      const int i = u / ntn - s_blk[t.x];
+      const int r0 = s_off[t.x] + BM2 * i + BM * (int)rank;
+      const int left = s_cnt[t.x] - BM2 * i - BM * (int)rank;
+      const __nv_bfloat16* src[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int rr = 32 * gw + 4 * j + (lane >> 3);
+        int tok = 0;  // rows no route owns read token 0; their results are not stored
+        if (rr < left) {
+          const int v = __ldg(p.inv_row + r0 + rr);
+          tok = (unsigned)v < (unsigned)p.s ? v : 0;
+        }
+        src[j] = p.x + (size_t)tok * p.K + chunk * 8;
+      }
+      for (int kb = 0; kb < kblocks; ++kb) {
+        bool waited = true;
+        if (lane == 0) waited = mbar_wait_bounded(&empty[stage], phase ^ 1u, deadline);
+        if (!__shfl_sync(0xffffffffu, waited ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = smem_addr(smem + stage * kPairStageBytes);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int rr = 32 * gw + 4 * j + (lane >> 3);
+          cp_async16(sa + rr * 128 + ((chunk ^ (rr & 7)) << 4), src[j] + kb * BK);
+        }
+        cp_async_commit();
+        if (++pending > kGatherLag) {
+          cp_async_wait<kGatherLag>();
+          fence_proxy_async_smem();
+          __syncwarp();  // every lane's copies to the stage have landed
+          if (lane == 0) mbar_arrive(rank == 0 ? &full[astage] : &gathered[astage]);
+          --pending;
+          if (++astage == kPairStages) astage = 0;
+        }
+        if (++stage == kPairStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    cp_async_wait<0>();  // nothing of this thread's stays in flight
+    if (ok) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      for (; pending > 0; --pending) {
+        if (lane == 0) mbar_arrive(rank == 0 ? &full[astage] : &gathered[astage]);
+        if (++astage == kPairStages) astage = 0;
+      }
+    } else if (lane == 0) {
+      atomicOr(&s_err, 1);
+    }
+  } else if (kGather && warp == 1 && lane == 0 && rank == 1) {
+    // ---- forwarder (fused form, rank 1) ------------------------------------
+    // Once all of this CTA's gathering warps have landed a stage, a 16-byte
+    // shared-to-shared bulk copy into rank 0 counts on rank 0's full barrier:
+    // an async-proxy signal, ordered after the gathered rows (fenced by
+    // their writers, acquired here through the `gathered` barrier).
+    const uint32_t sig_dst = mapa_shared(smem_addr(s_signal), 0);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = pair; u < nunits && ok; u += npairs) {
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_bounded(&gathered[stage], phase, deadline)) {
+          ok = false;
+          break;
+        }
+        bulk_signal_s2s(sig_dst, s_signal, mapa_shared(smem_addr(&full[stage]), 0));
+        if (++stage == kPairStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
     if (!ok) atomicOr(&s_err, 1);
@@ -716,7 +826,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r0 = s_off[t.x] + BM2 * i + BM * (int)rank;
       const int left = s_cnt[t.x] - BM2 * i - BM * (int)rank;
       const int nvalid = left < 0 ? 0 : (left < BM ? left : BM);
-      if (!mbar_wait_bounded(&tfull[acc], tphase[acc], deadline)) {
+      // every lane waits (and acquires) itself; the warp leaves together
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull[acc], tphase[acc], deadline))) {
         ok = false;
         break;
       }
@@ -725,7 +836,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       store_accumulator(tbase + ((uint32_t)(32 * ew) << 16) + (uint32_t)(acc * BN), ew, lane,
                         smem + kPairStages * kPairStageBytes + ew * kEpiWarpBytes, p.Y, p.N, r0, t.n0, nvalid);
       tc_fence_before();
-      mbar_arrive_cluster(acc ? te1 : te0);
+      __syncwarp();  // every lane's TMEM reads are done
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(&tempty[acc]);
+        else mbar_arrive_cluster(acc ? te1 : te0);
+      }
       acc ^= 1;
     }
     if (!ok) atomicOr(&s_err, 1);
@@ -798,6 +913,7 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParam
   return cudaGetLastError();
 }
 
+template <bool kGather>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
                         const DeviceInfo& di, cudaStream_t st) {
   int dev = 0;
@@ -806,7 +922,7 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
   static bool done[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!done[dev]) {
-    err = cudaFuncSetAttribute(grouped_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kGather>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kPairSmemBytes);
     if (err != cudaSuccess) return err;
     done[dev] = true;
@@ -818,7 +934,7 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
   if (pairs < 1) pairs = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * pairs));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kGather ? kGatherThreads : kThreads);
   cfg.dynamicSmemBytes = kPairSmemBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -828,7 +944,7 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, ma, mb, p);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kGather>, ma, mb, p);
 }
 
 GemmParams params(const int32_t* offsets, const int32_t* counts, int e, int rows, int K, int N,
@@ -859,7 +975,7 @@ cudaError_t launch_grouped_gemm(const int32_t* offsets, const int32_t* counts, i
     if (!make_map(&ma, X, (uint64_t)K, (uint64_t)rows, BM) ||
         !make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN / 2))
       return cudaErrorInvalidValue;
-    return launch_pair(ma, mb, params(offsets, counts, e, rows, K, N, Y, status), di, st);
+    return launch_pair<false>(ma, mb, params(offsets, counts, e, rows, K, N, Y, status), di, st);
   }
   if (!make_map(&ma, X, (uint64_t)K, (uint64_t)rows, BM) ||
       !make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN))
@@ -871,12 +987,16 @@ cudaError_t launch_dispatch_gemm(const int32_t* offsets, const int32_t* counts, 
                                  int e, int rows, int s, int K, int N, const void* x, const void* W,
                                  void* Y, int32_t* status, const DeviceInfo& di, cudaStream_t st) {
   CUtensorMap mb;
-  if (!make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN)) return cudaErrorInvalidValue;
   GemmParams p = params(offsets, counts, e, rows, K, N, Y, status);
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.inv_row = inv_row;
   p.s = s;
-  return launch<true>(mb, mb, p, di, st);  // A is gathered by threads: no A map
+  if (MOE_GEMM_FUSED_PAIR) {
+    if (!make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN / 2)) return cudaErrorInvalidValue;
+    return launch_pair<true>(mb, mb, p, di, st);  // A is gathered by threads: no A map
+  }
+  if (!make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN)) return cudaErrorInvalidValue;
+  return launch<true>(mb, mb, p, di, st);
 }
 
 }  // namespace moe
