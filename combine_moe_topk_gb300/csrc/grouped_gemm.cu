@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int rr = 32 * gw + 4 * i + (lane >> 3);
-        int tok = 0;  // rows no route owns read token 0; their results are not stored
+        int tok = 0;  // rows no route owns are skipped below
         if (rr < t.nvalid) {
           const int v = __ldg(p.inv_row + t.r0 + rr);
           tok = (unsigned)v < (unsigned)p.s ? v : 0;
@@ -369,8 +369,10 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
         const uint32_t sa = smem_addr(smem + stage * kStageBytes);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
+          // rows no route owns are not copied: an output row depends only on
+          // its own A row, and theirs are never stored
           const int rr = 32 * gw + 4 * i + (lane >> 3);
-          cp_async16(sa + rr * 128 + ((chunk ^ (rr & 7)) << 4), src[i] + kb * BK);
+          if (rr < t.nvalid) cp_async16(sa + rr * 128 + ((chunk ^ (rr & 7)) << 4), src[i] + kb * BK);
         }
         cp_async_commit();
         if (++pending > kGatherLag) {
@@ -706,7 +708,7 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int rr = 32 * gw + 4 * j + (lane >> 3);
-        int tok = 0;  // rows no route owns read token 0; their results are not stored
+        int tok = 0;  // rows no route owns are skipped below
         if (rr < left) {
           const int v = __ldg(p.inv_row + r0 + rr);
           tok = (unsigned)v < (unsigned)p.s ? v : 0;
@@ -723,8 +725,9 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
         const uint32_t sa = smem_addr(smem + stage * kPairStageBytes);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
+          // rows no route owns are not copied (their results are never stored)
           const int rr = 32 * gw + 4 * j + (lane >> 3);
-          cp_async16(sa + rr * 128 + ((chunk ^ (rr & 7)) << 4), src[j] + kb * BK);
+          if (rr < left) cp_async16(sa + rr * 128 + ((chunk ^ (rr & 7)) << 4), src[j] + kb * BK);
         }
         cp_async_commit();
         if (++pending > kGatherLag) {
