@@ -35,9 +35,6 @@ namespace {
 #ifndef MOE_DSP_PIECE
 #define MOE_DSP_PIECE 16384
 #endif
-#ifndef MOE_DSP_LDG
-#define MOE_DSP_LDG 0
-#endif
 #ifndef MOE_DSP_MAX_CTAS
 #define MOE_DSP_MAX_CTAS 16
 #endif
@@ -214,45 +211,6 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const Params p) {
   bulk_wait_all();
 }
 
-#if MOE_DSP_LDG
-// Register-staged alternative, compiled only for comparison runs: one warp per
-// token row, 16-byte loads into registers, stored once per kept route.
-template <int UNR>
-__global__ void __launch_bounds__(256) dispatch_ldg_kernel(const Params p) {
-  const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nvec = (int)(p.row_bytes / 16);
-  const uint4* x = reinterpret_cast<const uint4*>(p.x);
-  uint4* X = reinterpret_cast<uint4*>(p.X);
-  grid_dependency_wait();
-  pdl_trigger_early();
-  for (int t = gw; t < p.s; t += warps) {
-    const int rl = lane < p.k ? __ldg(p.row + (size_t)t * p.k + lane) : -1;
-    const unsigned kept = __ballot_sync(0xffffffffu, rl >= 0);
-    if (!kept) continue;
-    for (int v0 = lane; v0 < nvec; v0 += 32 * UNR) {
-      uint4 val[UNR];
-#pragma unroll
-      for (int u = 0; u < UNR; ++u)
-        if (v0 + 32 * u < nvec) val[u] = ld_stream(x + (size_t)t * nvec + v0 + 32 * u);
-      for (int j = 0; j < p.k; ++j) {
-        const int r = __shfl_sync(0xffffffffu, rl, j);
-        if (r < 0) continue;
-#pragma unroll
-        for (int u = 0; u < UNR; ++u)
-          if (v0 + 32 * u < nvec) st_stream(X + (size_t)r * nvec + v0 + 32 * u, val[u]);
-      }
-    }
-  }
-  if (p.zero_fill) {
-    for (long long rr = gw; rr < p.rows; rr += warps) {
-      if (row_is_owned(rr, p.offsets, p.counts, p.e)) continue;
-      for (int v = lane; v < nvec; v += 32) st_stream(X + (size_t)rr * nvec + v, make_uint4(0, 0, 0, 0));
-    }
-  }
-}
-#endif
 
 struct Config {
   int piece, npieces, stages, stride, smem, ctas_per_sm;
@@ -282,20 +240,16 @@ cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, const int
                             cudaStream_t st) {
   // allow the kernel the device's whole opt-in shared memory (less its static
   // part) once per device; occupancy still follows the dynamic size launched
-  static bool opted_in[64] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!opted_in[dev]) {
+  static OncePerDevice opt_in;
+  cudaError_t err = opt_in.run([&] {
     cudaFuncAttributes fa;
-    err = cudaFuncGetAttributes(&fa, dispatch_kernel);
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 di.max_smem_optin - (int)fa.sharedSizeBytes);
-    if (err != cudaSuccess) return err;
-    opted_in[dev] = true;
-  }
+    cudaError_t e = cudaFuncGetAttributes(&fa, dispatch_kernel);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               di.max_smem_optin - (int)fa.sharedSizeBytes);
+    return e;
+  });
+  if (err != cudaSuccess) return err;
   Config c = choose(row_bytes, di);
   Params p;
   p.x = static_cast<const char*>(x);
@@ -325,14 +279,6 @@ cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, const int
   long long grid = (long long)di.sms * c.ctas_per_sm;
   if (grid > work) grid = work;
   if (grid < 1) grid = 1;
-#if MOE_DSP_LDG
-  {
-    int bps = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, dispatch_ldg_kernel<MOE_DSP_LDG>, 256, 0);
-    return launch_pdl(MOE_KERNEL_DISPATCH, dispatch_ldg_kernel<MOE_DSP_LDG>, dim3(di.sms * (bps > 0 ? bps : 1)), dim3(256), 0,
-                      st, p);
-  }
-#endif
   return launch_pdl(MOE_KERNEL_DISPATCH, dispatch_kernel, dim3((unsigned)grid), dim3(32), (size_t)c.smem, st, p);
 }
 

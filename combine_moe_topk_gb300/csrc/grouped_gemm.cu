@@ -861,17 +861,16 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  // a function-local static initialises once, thread-safe
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -889,22 +888,18 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
 }
 
 template <bool kGather>
-cudaError_t enable_smem(int dev) {
-  static bool done[64] = {};
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (done[dev]) return cudaSuccess;
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<kGather>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (err == cudaSuccess) done[dev] = true;
-  return err;
+cudaError_t enable_smem() {
+  static OncePerDevice once;
+  return once.run([] {
+    return cudaFuncSetAttribute(grouped_gemm_kernel<kGather>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemBytes);
+  });
 }
 
 template <bool kGather>
 cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
                    const DeviceInfo& di, cudaStream_t st) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err == cudaSuccess) err = enable_smem<kGather>(dev);
+  cudaError_t err = enable_smem<kGather>();
   if (err != cudaSuccess) return err;
   // units: at most ceil(rows / 128) + e row blocks (one partial block per
   // segment), times the column tiles; the kernel reads the exact count
@@ -919,17 +914,12 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParam
 template <bool kGather>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
                         const DeviceInfo& di, cudaStream_t st) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  static OncePerDevice once;
+  cudaError_t err = once.run([] {
+    return cudaFuncSetAttribute(grouped_gemm_pair_kernel<kGather>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kPairSmemBytes);
+  });
   if (err != cudaSuccess) return err;
-  static bool done[64] = {};
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!done[dev]) {
-    err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kGather>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kPairSmemBytes);
-    if (err != cudaSuccess) return err;
-    done[dev] = true;
-  }
   // pair units: at most ceil(rows / 256) + e blocks of 256 rows, times the column tiles
   const long long units = (((long long)p.rows + BM2 - 1) / BM2 + p.e) * (p.N / BN);
   long long pairs = di.sms / 2;

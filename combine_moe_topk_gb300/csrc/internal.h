@@ -5,7 +5,27 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace moe {
+
+// Runs `set_up` (returning a cudaError_t) once per device, thread-safe, and
+// hands every later caller the same result.  For per-device one-time steps
+// such as a kernel's shared-memory opt-in.
+constexpr int kOnceDevices = 64;
+struct OncePerDevice {
+  std::once_flag flag[kOnceDevices];
+  cudaError_t result[kOnceDevices] = {};
+  template <class F>
+  cudaError_t run(F&& set_up) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kOnceDevices) return cudaErrorInvalidDevice;
+    std::call_once(flag[dev], [&] { result[dev] = set_up(); });
+    return result[dev];
+  }
+};
 
 struct DeviceInfo {
   int sms = 0;                 // streaming multiprocessors
