@@ -620,8 +620,15 @@ def cpu_baseline(w, args):
         times.append(dt)
     oracle.set_threads(1)
     per = statistics.median(times)
+    # the same oracle on one core, a few steps (the parity authority's own speed)
+    one, t_start = [], time.perf_counter()
+    while not one or (time.perf_counter() - t_start < args.cpu_seconds / 2 and len(one) < 20):
+        one.append(oracle_step(ws, inp)[0])
+    per1 = statistics.median(one)
     return {"value": round(sum(nbytes.values()) / per / 1e9, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{len(times)} full steps of {w.name} (s={w.s}, m={w.m}), median {per:.3f} s each"}
+            "sample": f"{len(times)} full steps of {w.name} (s={w.s}, m={w.m}), median {per:.3f} s each",
+            "single_core": {"value": round(sum(nbytes.values()) / per1 / 1e9, 3), "unit": "GB/s", "cores": 1,
+                            "sample": f"{len(one)} full steps, median {per1:.3f} s each"}}
 
 
 def run_reference(args, rank: int, world: int):
