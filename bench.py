@@ -249,6 +249,7 @@ def run_ours(args, rank: int, world: int, dist):
     drop = h.drop()
     kept = int((drop == 0).sum().item())
     u = int((drop == 0).any(dim=1).sum().item())
+    rank_sum = int(h.rank_counts().sum().item()) if w.R else 0
     assert h.status() == 0, "device status after the first step"
     h.destroy()
     nbytes = step_bytes(w, kept, u)
@@ -323,13 +324,17 @@ def run_ours(args, rank: int, world: int, dist):
     # handle (the cached-replay case), replayed back to back -----------------
     dc = run_dispatch_combine(w, S, dev, K)
 
+    # ---- the recompute: the whole step on a saved handle, no layout --------
+    rp = run_replay_step(w, S, dev, K)
+
     # ---- end to end: pinned host inputs in, results out, every step ----------
     e2e = run_e2e(w, S, step, buffers, dev, max(3, min(K, 50)), args.warmup)
 
     # ---- the tensor-core consumer of the dispatched rows (outside value) ------
     gemm = None if args.no_gemm else run_expert_gemm(w, S, dev)
 
-    elapsed_ms, e2e["ms"], dc["ms"] = max_over_ranks([elapsed_ms, e2e["ms"], dc["ms"]], dist, dev)
+    elapsed_ms, e2e["ms"], dc["ms"], rp["ms"] = max_over_ranks([elapsed_ms, e2e["ms"], dc["ms"], rp["ms"]], dist,
+                                                               dev)
     if rank != 0:
         return None
 
@@ -390,6 +395,16 @@ def run_ours(args, rank: int, world: int, dist):
         "clocks": clk.summary(),
         "kept_routes": kept,
         "sending_tokens": u,
+        "routing": {
+            "drop_fraction": round(1.0 - kept / (w.s * w.k), 6),
+            **({"dedup": {"rank_counts_sum": rank_sum, "routes_per_sent_token": round(kept / rank_sum, 4),
+                          "virtual_ranks": w.R}} if w.R and rank_sum else {}),
+        },
+        "replay": {
+            "ms_per_step": round(rp["ms"], 5), "full_step_ms": round(ms_per_step, 5),
+            "saved_fraction": round(1.0 - rp["ms"] / ms_per_step, 4),
+            "layout_launches_during": rp["layout_launches"], "how": rp["how"],
+        },
     }
     if gemm is not None:
         line["expert_gemm"] = gemm
@@ -442,6 +457,58 @@ def run_dispatch_combine(w, S, dev, K: int):
     assert h.status() == 0
     h.destroy()
     return {"ms": a.elapsed_time(b) / n, "how": f"{how}, {n} pairs"}
+
+
+def run_replay_step(w, S, dev, K: int):
+    """The activation-checkpoint recompute of one step: the same kernels as
+    the step (the gate is recomputed, routing pinned) on a handle built
+    before the timed region, so no layout kernel runs.  A CUDA graph of it,
+    replayed back to back; the layout launch counter must not move."""
+    import torch
+
+    from combine_moe_topk_gb300 import binding as B
+
+    h = B.moe_dispatch_layout(S["idx"], w.e, w.capacity, w.R)
+    torch.cuda.synchronize()
+
+    def again():
+        B.moe_topk_gate(S["logits"], w.k, w.renorm, S["idx"], S["gate"])
+        B.moe_dispatch(h, S["x"], S["X"])
+        B.moe_combine(h, S["y"], S["gate"], S["out"])
+        B.moe_combine_bwd(h, S["dout"], S["gate"], S["y"], S["dY"], S["dgate"])
+        B.moe_topk_gate_bwd(None if w.renorm else S["logits"], S["idx"], S["gate"], S["dgate"], w.e, w.renorm,
+                            S["dlogits"])
+        B.moe_dispatch_bwd(h, S["dY"], S["dx"])
+
+    how = "graph of the step on a saved handle (gate recomputed, no layout), replayed back to back"
+    try:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            again()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            again()
+        run = g.replay
+    except Exception as exc:
+        run, how = again, f"eager calls (graph capture failed: {type(exc).__name__})"
+    for _ in range(5):
+        run()
+    torch.cuda.synchronize()
+    layouts = B.moe_launch_count("layout")
+    n = max(5, min(K, 500))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        run()
+    b.record()
+    torch.cuda.synchronize()
+    moved = B.moe_launch_count("layout") - layouts
+    assert h.status() == 0
+    h.destroy()
+    return {"ms": a.elapsed_time(b) / n, "layout_launches": moved, "how": f"{how}, {n} steps"}
 
 
 def run_expert_gemm(w, S, dev, reps: int = 10):
