@@ -408,8 +408,8 @@ namespace {
 moe_status check_gemm(moe_handle h, int rows, int K, int N, const void* A, const char* a_name, int a_rows,
                       const void* W, const void* Y) {
   if (rows != h->rows) return fail(MOE_ERR_HANDLE_MISMATCH, "row count differs from the handle's");
-  if (K < 64 || K % 64 != 0) return fail(MOE_ERR_INVALID_ARG, "K must be a positive multiple of 64");
-  if (N < 256 || N % 256 != 0) return fail(MOE_ERR_INVALID_ARG, "N must be a positive multiple of 256");
+  if (K < 64 || K % 8 != 0) return fail(MOE_ERR_INVALID_ARG, "K must be a multiple of 8, at least 64");
+  if (N < 8 || N % 8 != 0) return fail(MOE_ERR_INVALID_ARG, "N must be a positive multiple of 8");
   if ((long long)h->e * N > 2147483647LL) return fail(MOE_ERR_INVALID_ARG, "e * N must be < 2^31");
   if (rows == 0 || a_rows == 0) return MOE_OK;
   MOE_TRY(check_ptr(A, a_name));

@@ -133,9 +133,12 @@ __device__ __forceinline__ void tma_load_2d(void* sdst, const CUtensorMap* map, 
       : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared (L2 only), grouped per stage.
-__device__ __forceinline__ void cp_async16(uint32_t sdst, const void* gsrc) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sdst), "l"(gsrc) : "memory");
+// 16-byte asynchronous copy global -> shared (L2 only): copies src_bytes
+// (0 or 16) from gsrc and fills the rest of the 16 bytes with zeros; with 0
+// nothing is read.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t sdst, const void* gsrc, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sdst), "l"(gsrc), "r"(src_bytes)
+               : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -215,9 +218,10 @@ __device__ __forceinline__ void store_accumulator(uint32_t tcol, int ew, int lan
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int row = 4 * i + (lane >> 3);
-      if (32 * ew + row < nvalid) {
+      const int col = n0 + 64 * c2 + 8 * ch;  // N % 8 == 0: a 16-byte chunk is wholly in or out
+      if (32 * ew + row < nvalid && col < N) {
         const uint4 val = *reinterpret_cast<const uint4*>(stage + row * kStageRowBytes + ch * 16);
-        *reinterpret_cast<uint4*>(Y + (size_t)(r0 + 32 * ew + row) * N + n0 + 64 * c2 + 8 * ch) = val;
+        *reinterpret_cast<uint4*>(Y + (size_t)(r0 + 32 * ew + row) * N + col) = val;
       }
     }
     __syncwarp();  // the staging tile is rewritten by the next 64 columns
@@ -307,9 +311,9 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = tmem_base;
 
-  const int ntn = p.N / BN;
+  const int ntn = (p.N + BN - 1) / BN;  // the last column tile may be partial
   const int nunits = s_blk[p.e] * ntn;
-  const int kblocks = p.K / BK;
+  const int kblocks = (p.K + BK - 1) / BK;  // columns past K read as zeros
 
   if (warp == 0 && lane == 0) {
     // ---- TMA producer: B always, A in the tile-fed form ------------------
@@ -372,7 +376,12 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
           // rows no route owns are not copied: an output row depends only on
           // its own A row, and theirs are never stored
           const int rr = 32 * gw + 4 * i + (lane >> 3);
-          if (rr < t.nvalid) cp_async16(sa + rr * 128 + ((chunk ^ (rr & 7)) << 4), src[i] + kb * BK);
+          if (rr < t.nvalid) {
+            // columns past K: zeros, nothing read (the row's end may be the buffer's)
+            const bool in_k = kb * BK + chunk * 8 < p.K;
+            cp_async16_zfill(sa + rr * 128 + ((chunk ^ (rr & 7)) << 4), in_k ? src[i] + kb * BK : src[i],
+                             in_k ? 16u : 0u);
+          }
         }
         cp_async_commit();
         if (++pending > kGatherLag) {
@@ -651,9 +660,9 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = tmem_base;
 
-  const int ntn = p.N / BN;
+  const int ntn = (p.N + BN - 1) / BN;  // the last column tile may be partial
   const int nunits = s_blk[p.e] * ntn;
-  const int kblocks = p.K / BK;
+  const int kblocks = (p.K + BK - 1) / BK;  // columns past K read as zeros
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (warp == 0 && lane == 0) {
@@ -727,7 +736,12 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
         for (int j = 0; j < 8; ++j) {
           // rows no route owns are not copied (their results are never stored)
           const int rr = 32 * gw + 4 * j + (lane >> 3);
-          if (rr < left) cp_async16(sa + rr * 128 + ((chunk ^ (rr & 7)) << 4), src[j] + kb * BK);
+          if (rr < left) {
+            // columns past K: zeros, nothing read (the row's end may be the buffer's)
+            const bool in_k = kb * BK + chunk * 8 < p.K;
+            cp_async16_zfill(sa + rr * 128 + ((chunk ^ (rr & 7)) << 4), in_k ? src[j] + kb * BK : src[j],
+                             in_k ? 16u : 0u);
+          }
         }
         cp_async_commit();
         if (++pending > kGatherLag) {
@@ -904,7 +918,7 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParam
   // units: at most ceil(rows / 128) + e row blocks (one partial block per
   // segment), times the column tiles; the kernel reads the exact count
   const long long blocks = ((long long)p.rows + BM - 1) / BM + p.e;
-  const long long nunits = blocks * (p.N / BN);
+  const long long nunits = blocks * ((p.N + BN - 1) / BN);
   int grid = (long long)di.sms < nunits ? di.sms : (int)nunits;
   if (grid < 1) grid = 1;
   grouped_gemm_kernel<kGather><<<grid, kGather ? kGatherThreads : kThreads, kSmemBytes, st>>>(ma, mb, p);
@@ -921,7 +935,7 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
   });
   if (err != cudaSuccess) return err;
   // pair units: at most ceil(rows / 256) + e blocks of 256 rows, times the column tiles
-  const long long units = (((long long)p.rows + BM2 - 1) / BM2 + p.e) * (p.N / BN);
+  const long long units = (((long long)p.rows + BM2 - 1) / BM2 + p.e) * ((p.N + BN - 1) / BN);
   long long pairs = di.sms / 2;
   if (units < pairs) pairs = units;
   if (pairs < 1) pairs = 1;

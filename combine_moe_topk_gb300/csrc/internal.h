@@ -107,7 +107,7 @@ cudaError_t launch_rank_slots(const uint8_t* token_in_rank, int s, int R, int32_
 
 // --- expert-grouped GEMM on the tensor cores -----------------------------
 // Y[r] = X[r] . W[x]^T over the 128-row blocks of each expert segment that a
-// route owns.  K % 64 == 0, N % 256 == 0; a segment may start on any row.
+// route owns.  K % 8 == 0 (>= 64), N % 8 == 0; a segment may start on any row.
 cudaError_t launch_grouped_gemm(const int32_t* offsets, const int32_t* counts, int e, int rows, int K,
                                 int N, const void* X, const void* W, void* Y, int32_t* status,
                                 const DeviceInfo& di, cudaStream_t st);

@@ -275,7 +275,8 @@ moe_status moe_dispatch_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtyp
  * expert's weight N x K with K contiguous), Y bf16 [rows, N].  Rows no route
  * owns (capacity tails, padding) are not written.  Any layout of the handle:
  * token or k-major, capacity or dropless, padded or not.  K a multiple of
- * 64; N a multiple of 256; rows equal to the handle's; e <= 256.
+ * 8 and at least 64; N a multiple of 8 (16-byte rows); rows equal to the
+ * handle's; e <= 256.
  * tcgen05 MMA with TMEM accumulators, TMA-fed; the segments are read from
  * the handle on the device (no host sync).  Errors: MOE_ERR_INVALID_ARG,
  * MOE_ERR_HANDLE_MISMATCH, MOE_ERR_CUDA. */

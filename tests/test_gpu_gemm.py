@@ -75,10 +75,11 @@ def _check_float64(Y, OX, Wt, L):
     assert not bad.any(), (int(bad.sum()), np.argwhere(bad)[:3])
 
 
+@pytest.mark.parametrize("K", [256, 72])  # 72: a K tail and a partial column tile
 @pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("layout", [dict(pad=128), dict(pad=1), dict(capacity=100)])
-def test_identity_weights_return_the_dispatched_rows(fused, layout):
-    s, e, k, K = 300, 4, 2, 256
+def test_identity_weights_return_the_dispatched_rows(fused, layout, K):
+    s, e, k = 300, 4, 2
     h, x, X, OX, L = _setup(s, e, k, K, seed=1, **layout)
     Wt = torch.eye(K, dtype=torch.bfloat16).expand(e, K, K).contiguous().to(DEV)
     Y = _sentinel_out(h.rows, K)
@@ -102,6 +103,10 @@ CASES = [
     dict(s=3000, e=64, k=6, K=256, N=512, capacity=200, priority="kmajor"),
     dict(s=700, e=128, k=8, K=128, N=256),                       # many small and empty segments
     dict(s=40, e=4, k=1, K=64, N=256),                           # fewer rows than one block
+    dict(s=900, e=256, k=4, K=64, N=256),                        # the largest expert count
+    dict(s=1200, e=8, k=2, K=72, N=264),                         # K and N tails: K % 64, N % 256 != 0
+    dict(s=700, e=6, k=2, K=1000, N=1416, capacity=250),         # tails in capacity mode
+    dict(s=500, e=4, k=2, K=64, N=8),                            # one 8-column chunk
 ]
 
 
@@ -139,15 +144,17 @@ def test_inv_row_names_the_token_of_every_owned_row():
 def test_gemm_argument_checks():
     idx = W.random_routes(100, 4, 2, seed=2).to(DEV)
     h = B.moe_dispatch_layout(idx, 4)
-    X = torch.zeros(h.rows, 96, dtype=torch.bfloat16, device=DEV)
-    Wt = torch.zeros(4, 256, 96, dtype=torch.bfloat16, device=DEV)
+    bf = dict(dtype=torch.bfloat16, device=DEV)
     with pytest.raises(B.MoEError) as ei:
-        B.moe_grouped_gemm(h, X, Wt)  # K = 96: not a multiple of 64
-    assert ei.value.name == "MOE_ERR_INVALID_ARG"
-    x = torch.zeros(101, 64, dtype=torch.bfloat16, device=DEV)
+        B.moe_grouped_gemm(h, torch.zeros(h.rows, 100, **bf), torch.zeros(4, 256, 100, **bf))
+    assert ei.value.name == "MOE_ERR_INVALID_ARG"  # K = 100: not a multiple of 8
     with pytest.raises(B.MoEError) as ei:
-        B.moe_dispatch_grouped_gemm(h, x, torch.zeros(4, 256, 64, dtype=torch.bfloat16, device=DEV))
+        B.moe_grouped_gemm(h, torch.zeros(h.rows, 56, **bf), torch.zeros(4, 256, 56, **bf))
+    assert ei.value.name == "MOE_ERR_INVALID_ARG"  # K = 56 < 64
+    x = torch.zeros(101, 64, **bf)
+    with pytest.raises(B.MoEError) as ei:
+        B.moe_dispatch_grouped_gemm(h, x, torch.zeros(4, 256, 64, **bf))
     assert ei.value.name == "MOE_ERR_HANDLE_MISMATCH"  # 101 token rows, the handle has 100
     with pytest.raises(B.MoEError) as ei:
-        B.moe_grouped_gemm(h, X[:, :64].contiguous(), torch.zeros(4, 200, 64, dtype=torch.bfloat16, device=DEV))
-    assert ei.value.name == "MOE_ERR_INVALID_ARG"  # N = 200
+        B.moe_grouped_gemm(h, torch.zeros(h.rows, 64, **bf), torch.zeros(4, 200 + 4, 64, **bf))
+    assert ei.value.name == "MOE_ERR_INVALID_ARG"  # N = 204: not a multiple of 8
