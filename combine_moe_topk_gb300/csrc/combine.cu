@@ -1,6 +1,7 @@
 // combine.cu -- the weighted combine, its unit-weight twin (the backward of
 // dispatch) and the combine backward (a gate-scaled dispatch plus the gate
-// gradient).  One warp per token, 16-byte vector loads, fp32 accumulation.
+// gradient).  A warp per token (or per piece of a token row when the batch
+// is too short to fill the GPU), 16-byte vector loads, fp32 accumulation.
 //
 // DeepSpeed #8195 "MoE dispatch: fix silent Tutel + TP corruption, speed up
 // native and Tutel paths", change 3: combine is a gather through the slots
@@ -12,9 +13,10 @@
 // router gate.
 //
 // Accumulation order is fixed: acc starts at +0.0f and takes one fmaf per
-// kept route in route order, so the result does not depend on the launch
-// shape.  The gate gradient sums dout*y per lane in element order, then a
-// butterfly across the warp: also launch-shape independent.
+// kept route in route order, so the combine's result does not depend on the
+// launch shape.  The gate gradient sums dout*y per lane in element order,
+// then a butterfly across the warp, then (rows split over G warps) the G
+// partial sums in warp order: fixed for a given batch shape.
 #include "common.cuh"
 #include "internal.h"
 
@@ -111,63 +113,75 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __rest
   pdl_trigger_late();
 }
 
-template <typename T, int KMAX, int UNR>
+// G warps per token (G = 1, 2, 4 or 8): warp w of a token's group takes the
+// row's vectors [w*chunk, (w+1)*chunk); the per-route dots are reduced across
+// the warp's lanes (butterfly), then across the group's warps in warp order
+// through shared memory.  G > 1 gives short batches more warps in flight.
+template <typename T, int KMAX, int UNR, int G>
 __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     const int32_t* __restrict__ row, const int32_t* __restrict__ counts,
     const int32_t* __restrict__ offsets, long long rows, int zero_fill,
-    const float* __restrict__ gate, int s, int k, int e, int nvec,
+    const float* __restrict__ gate, int s, int k, int e, int nvec, int chunk,
     const uint4* __restrict__ dout, const uint4* __restrict__ y, uint4* __restrict__ dY,
     float* __restrict__ dgate) {
   constexpr int N = Vec<T>::N;
-  const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  constexpr int WPB = kThreads / 32;  // warps per block
+  constexpr int TPB = WPB / G;        // tokens per block and round
+  __shared__ float s_dot[G > 1 ? WPB : 1][KMAX];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gi = warp / G, w = warp - gi * G;  // token slot in the block, warp in the group
+  const int c0 = w * chunk, c1 = min(nvec, c0 + chunk);
   grid_dependency_wait();
   pdl_trigger_early();
-  for (int t = gw; t < s; t += warps) {
+  // every warp of a block runs the same number of rounds (block-uniform loop)
+  for (long long t0 = (long long)blockIdx.x * TPB; t0 < s; t0 += (long long)gridDim.x * TPB) {
+    const int t = (int)(t0 + gi);
+    const bool live = t < s;
     int r[KMAX];
     float g[KMAX];
-    token_routes<KMAX, true>(row, gate, t, k, lane, r, g);
     float dot[KMAX];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) dot[j] = 0.0f;
-    const uint4* d = dout + (size_t)t * nvec;
-    for (int v0 = lane; v0 < nvec; v0 += 32 * UNR) {
-      uint4 dv[UNR];
-      uint4 yv[KMAX][UNR];
+    if (live) {
+      token_routes<KMAX, true>(row, gate, t, k, lane, r, g);
+      const uint4* d = dout + (size_t)t * nvec;
+      for (int v0 = c0 + lane; v0 < c1; v0 += 32 * UNR) {
+        uint4 dv[UNR];
+        uint4 yv[KMAX][UNR];
 #pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        const int v = v0 + 32 * u;
-        if (v < nvec) dv[u] = ld_stream(d + v);
-      }
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (r[j] >= 0) {
-          const uint4* src = y + (size_t)r[j] * nvec;
-#pragma unroll
-          for (int u = 0; u < UNR; ++u) {
-            const int v = v0 + 32 * u;
-            if (v < nvec) yv[j][u] = ld_stream(src + v);
-          }
+        for (int u = 0; u < UNR; ++u) {
+          const int v = v0 + 32 * u;
+          if (v < c1) dv[u] = ld_stream(d + v);
         }
-      }
-#pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        const int v = v0 + 32 * u;
-        if (v >= nvec) break;
-        float df[N];
-        Vec<T>::to_float(dv[u], df);
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
           if (r[j] >= 0) {
-            float yf[N], p[N];
-            Vec<T>::to_float(yv[j][u], yf);
+            const uint4* src = y + (size_t)r[j] * nvec;
 #pragma unroll
-            for (int i = 0; i < N; ++i) {
-              dot[j] = __fmaf_rn(df[i], yf[i], dot[j]);
-              p[i] = __fmul_rn(g[j], df[i]);
+            for (int u = 0; u < UNR; ++u) {
+              const int v = v0 + 32 * u;
+              if (v < c1) yv[j][u] = ld_stream(src + v);
             }
-            st_stream(dY + (size_t)r[j] * nvec + v, Vec<T>::from_float(p));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+          const int v = v0 + 32 * u;
+          if (v >= c1) break;
+          float df[N];
+          Vec<T>::to_float(dv[u], df);
+#pragma unroll
+          for (int j = 0; j < KMAX; ++j) {
+            if (r[j] >= 0) {
+              float yf[N], p[N];
+              Vec<T>::to_float(yv[j][u], yf);
+#pragma unroll
+              for (int i = 0; i < N; ++i) {
+                dot[j] = __fmaf_rn(df[i], yf[i], dot[j]);
+                p[i] = __fmul_rn(g[j], df[i]);
+              }
+              st_stream(dY + (size_t)r[j] * nvec + v, Vec<T>::from_float(p));
+            }
           }
         }
       }
@@ -180,12 +194,26 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
       for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
       if (lane == j) mine = v;
     }
-    if (lane < k) dgate[(size_t)t * k + lane] = mine;
+    if (G == 1) {
+      if (live && lane < k) dgate[(size_t)t * k + lane] = mine;
+    } else {
+      if (lane < KMAX) s_dot[warp][lane] = mine;
+      __syncthreads();
+      if (live && w == 0 && lane < k) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int q = 0; q < G; ++q) sum += s_dot[gi * G + q][lane];
+        dgate[(size_t)t * k + lane] = sum;
+      }
+      __syncthreads();  // s_dot is rewritten next round
+    }
   }
   pdl_trigger_late();
 
   // rows no kept route owns (capacity slots, padding) get zero gradient
   if (zero_fill) {
+    const long long warps = (gridDim.x * blockDim.x) >> 5;
+    const long long gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (long long rr = gw; rr < rows; rr += warps) {
       if (row_is_owned(rr, offsets, counts, e)) continue;
@@ -211,6 +239,18 @@ int grid_for(long long warps_wanted, const DeviceInfo& di, int blocks_per_sm) {
   return (int)blocks;
 }
 
+// Pieces per token row (a power of two, 1 = whole rows) so that a short
+// batch still gives `fill` times the resident warps' worth of work units;
+// each piece keeps at least 32 vectors.  Measured best: fill 8 for the
+// combine, 4 for its backward (whose pieces also add a shared-memory
+// reduction).
+int pieces_for(long long s, int nvec, const DeviceInfo& di, int blocks_per_sm, int fill, int max_pieces) {
+  const long long resident = (long long)di.sms * (blocks_per_sm > 0 ? blocks_per_sm : 1) * (kThreads / 32);
+  int pieces = 1;
+  while (pieces < max_pieces && s * pieces < fill * resident && nvec / (2 * pieces) >= 32) pieces *= 2;
+  return pieces;
+}
+
 template <typename T, int KMAX>
 cudaError_t combine_t(const int32_t* row, const float* gate, int s, int k, int m, const void* y,
                       void* out, const DeviceInfo& di, cudaStream_t st) {
@@ -219,22 +259,46 @@ cudaError_t combine_t(const int32_t* row, const float* gate, int s, int k, int m
   constexpr int LOADS = KMAX <= 2 ? MOE_CMB_LOADS / 2 : MOE_CMB_LOADS;
   constexpr int UNR = LOADS / KMAX > 1 ? LOADS / KMAX : 1;
   const int nvec = m / Vec<T>::N;
-  const int chunk = MOE_CMB_CHUNK > 0 && MOE_CMB_CHUNK < nvec ? MOE_CMB_CHUNK : nvec;
+  auto kern_w = combine_kernel<T, KMAX, UNR, true>;
+  auto kern_u = combine_kernel<T, KMAX, UNR, false>;
+  static const int bps_w = occupancy(kern_w);
+  static const int bps_u = occupancy(kern_u);
+  const int bps = gate ? bps_w : bps_u;
+  // a unit is a piece of a token row; pieces are whole multiples of 32
+  // vectors so every lane has work (the sum per element is route-ordered,
+  // so the split does not change any result)
+  int chunk = nvec;
+  if (MOE_CMB_CHUNK > 0 && MOE_CMB_CHUNK < nvec) {
+    chunk = MOE_CMB_CHUNK;
+  } else {
+    const int pieces = pieces_for(s, nvec, di, bps, 8, 8);
+    if (pieces > 1) chunk = ((nvec + pieces - 1) / pieces + 31) / 32 * 32;
+  }
   const int nchunks = (nvec + chunk - 1) / chunk;
   const long long units = (long long)s * nchunks;
-  if (gate) {
-    auto kern = combine_kernel<T, KMAX, UNR, true>;
-    static const int bps = occupancy(kern);
-    return launch_pdl(MOE_KERNEL_COMBINE, kern, dim3(grid_for(units, di, bps)), dim3(kThreads), 0, st,
-                      row, gate, s, k,
-                      nvec, chunk, nchunks, static_cast<const uint4*>(y), static_cast<uint4*>(out));
-  } else {
-    auto kern = combine_kernel<T, KMAX, UNR, false>;
-    static const int bps = occupancy(kern);
-    return launch_pdl(MOE_KERNEL_DISPATCH_BWD, kern, dim3(grid_for(units, di, bps)), dim3(kThreads), 0,
-                      st, row, static_cast<const float*>(nullptr), s, k, nvec, chunk, nchunks,
-                      static_cast<const uint4*>(y), static_cast<uint4*>(out));
-  }
+  if (gate)
+    return launch_pdl(MOE_KERNEL_COMBINE, kern_w, dim3(grid_for(units, di, bps)), dim3(kThreads), 0, st,
+                      row, gate, s, k, nvec, chunk, nchunks, static_cast<const uint4*>(y),
+                      static_cast<uint4*>(out));
+  return launch_pdl(MOE_KERNEL_DISPATCH_BWD, kern_u, dim3(grid_for(units, di, bps)), dim3(kThreads), 0, st,
+                    row, static_cast<const float*>(nullptr), s, k, nvec, chunk, nchunks,
+                    static_cast<const uint4*>(y), static_cast<uint4*>(out));
+}
+
+template <typename T, int KMAX, int G>
+cudaError_t combine_bwd_g(const int32_t* row, const int32_t* counts, const int32_t* offsets,
+                          long long rows, int zero_fill, const float* gate, int s, int k, int e,
+                          int nvec, const void* dout, const void* y, void* dY, float* dgate,
+                          const DeviceInfo& di, int bps, cudaStream_t st) {
+  constexpr int UNR = MOE_CMB_BWD_LOADS / KMAX > 1 ? MOE_CMB_BWD_LOADS / KMAX : 1;
+  auto kern = combine_bwd_kernel<T, KMAX, UNR, G>;
+  const int chunk = G == 1 ? nvec : ((nvec + G - 1) / G + 31) / 32 * 32;
+  long long warps = (long long)s * G;
+  if (zero_fill && rows > warps) warps = rows;
+  return launch_pdl(MOE_KERNEL_COMBINE_BWD, kern, dim3(grid_for(warps, di, bps)), dim3(kThreads), 0, st,
+                    row, counts, offsets, rows, zero_fill, gate, s, k, e, nvec, chunk,
+                    static_cast<const uint4*>(dout), static_cast<const uint4*>(y), static_cast<uint4*>(dY),
+                    dgate);
 }
 
 template <typename T, int KMAX>
@@ -244,14 +308,18 @@ cudaError_t combine_bwd_t(const int32_t* row, const int32_t* counts, const int32
                           const DeviceInfo& di, cudaStream_t st) {
   constexpr int UNR = MOE_CMB_BWD_LOADS / KMAX > 1 ? MOE_CMB_BWD_LOADS / KMAX : 1;
   const int nvec = m / Vec<T>::N;
-  auto kern = combine_bwd_kernel<T, KMAX, UNR>;
-  static const int bps = occupancy(kern);
-  long long warps = s;
-  if (zero_fill && rows > warps) warps = rows;
-  return launch_pdl(MOE_KERNEL_COMBINE_BWD, kern, dim3(grid_for(warps, di, bps)), dim3(kThreads), 0, st,
-                    row, counts, offsets, rows, zero_fill, gate, s, k, e, nvec,
-                    static_cast<const uint4*>(dout),
-                    static_cast<const uint4*>(y), static_cast<uint4*>(dY), dgate);
+  static const int bps = occupancy(combine_bwd_kernel<T, KMAX, UNR, 1>);
+  // warps per token for short batches (the dot of the gate gradient is
+  // reduced across them in a fixed order, so each G gives fixed results)
+  const int G = pieces_for(s, nvec, di, bps, 4, 8);
+#define MOE_CBWD_G(GG)                                                                            \
+  combine_bwd_g<T, KMAX, GG>(row, counts, offsets, rows, zero_fill, gate, s, k, e, nvec, dout, y, dY, \
+                             dgate, di, bps, st)
+  if (G >= 8) return MOE_CBWD_G(8);
+  if (G == 4) return MOE_CBWD_G(4);
+  if (G == 2) return MOE_CBWD_G(2);
+  return MOE_CBWD_G(1);
+#undef MOE_CBWD_G
 }
 
 template <typename T>
