@@ -158,3 +158,25 @@ def test_gemm_argument_checks():
     with pytest.raises(B.MoEError) as ei:
         B.moe_grouped_gemm(h, torch.zeros(h.rows, 64, **bf), torch.zeros(4, 200 + 4, 64, **bf))
     assert ei.value.name == "MOE_ERR_INVALID_ARG"  # N = 204: not a multiple of 8
+
+
+def test_fused_pair_is_stable_over_repeated_calls():
+    """The fused form's second CTA signals its gathered rows through a
+    shared-to-shared bulk copy; any ordering slip would show as rows that
+    differ from call to call.  40 calls, each compared bit for bit with the
+    plain GEMM on the dispatched rows."""
+    s, e, k, K, N = 3000, 16, 4, 512, 512
+    h, x, X, OX, L = _setup(s, e, k, K, seed=11)
+    g = torch.Generator().manual_seed(13)
+    Wd = (torch.randn(e, N, K, generator=g) / np.sqrt(K)).to(torch.bfloat16).to(DEV)
+    ref = B.moe_grouped_gemm(h, X, Wd)
+    xd = x.to(DEV)
+    own = torch.from_numpy(_owned_rows(L)).to(DEV)
+    Y = torch.empty_like(ref)
+    bad = 0
+    for _ in range(40):
+        Y.fill_(0)
+        B.moe_dispatch_grouped_gemm(h, xd, Wd, Y)
+        bad += int((Y.view(torch.int16)[own] != ref.view(torch.int16)[own]).any(dim=1).sum().item())
+    assert h.status() == 0
+    assert bad == 0, f"{bad} rows differed over 40 calls"
