@@ -317,8 +317,9 @@ def run_ours(args, rank: int, world: int, dist):
     for i in range(Kr):
         step(ev=evs[i]).destroy()
     torch.cuda.synchronize()
-    per_op = {op: statistics.mean(evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(Kr))
-              for j, op in enumerate(OPS)}
+    samples = {op: sorted(evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(Kr)) for j, op in enumerate(OPS)}
+    per_op = {op: statistics.mean(v) for op, v in samples.items()}
+    spread = {op: (v[len(v) // 10], v[len(v) // 2], v[(9 * len(v)) // 10]) for op, v in samples.items()}
 
     # ---- dispatch + combine in steady state: a graph of the pair on one
     # handle (the cached-replay case), replayed back to back -----------------
@@ -377,7 +378,8 @@ def run_ours(args, rank: int, world: int, dist):
             "routed_tokens_per_s": round(w.s * w.k / (dc_ms * 1e-3), 1),
         },
         "ops": {op: {"us": round(per_op[op] * 1e3, 2), "bytes": nbytes[op],
-                     "gbs": round(nbytes[op] / (per_op[op] * 1e-3) / 1e9, 1)} for op in OPS},
+                     "gbs": round(nbytes[op] / (per_op[op] * 1e-3) / 1e9, 1),
+                     "us_p10_p50_p90": [round(x * 1e3, 2) for x in spread[op]]} for op in OPS},
         "ops_note": f"per-kernel times from events around each call, eager, {Kr} separate steps, each call "
                     f"after a {SLEEP_CYCLES}-cycle GPU sleep so the events bracket the kernel"
                     + ("" if pad is not None else " (sleep unavailable: host gaps included)"),

@@ -44,8 +44,25 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float* __restrict_
   const int warps = (gridDim.x * blockDim.x) >> 5;
   grid_dependency_wait();
   pdl_trigger_early();
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < s; t += warps) {
-    const float* l = logits + (size_t)t * e;
+  // this lane's logits of the warp's next token are loaded one token ahead,
+  // so their latency overlaps the current token's selection
+  int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  float nxt[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int j = lane + 32 * i;
+    nxt[i] = (t < s && j < e) ? __ldg(logits + (size_t)t * e + j) : 0.0f;
+  }
+  for (; t < s; t += warps) {
+    float cur[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) cur[i] = nxt[i];
+    const int tn = t + warps;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int j = lane + 32 * i;
+      nxt[i] = (tn < s && j < e) ? __ldg(logits + (size_t)tn * e + j) : 0.0f;
+    }
     // this lane's candidates, experts lane + 32*i; key 0 marks padding (below -inf)
     uint32_t key[EPL];
     int id[EPL];
@@ -53,7 +70,7 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float* __restrict_
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int j = lane + 32 * i;
-      const float v = j < e ? __ldg(l + j) : 0.0f;
+      const float v = cur[i];
       if (j < e && !isfinite(v)) bad = true;
       key[i] = j < e ? order_key(v) : 0u;
       id[i] = j;
@@ -135,13 +152,23 @@ __global__ void __launch_bounds__(256) topk_gate_bwd_kernel(
   const int warps = (gridDim.x * blockDim.x) >> 5;
   grid_dependency_wait();
   pdl_trigger_early();
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < s; t += warps) {
-    int ij = -1;
-    float gj = 0.f, dgj = 0.f;
-    if (lane < k) {
-      ij = __ldg(idx + (size_t)t * k + lane);
-      gj = __ldg(gate + (size_t)t * k + lane);
-      dgj = __ldg(dgate + (size_t)t * k + lane);
+  // the route data of the warp's next token is loaded one token ahead
+  int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  int n_ij = -1;
+  float n_gj = 0.f, n_dgj = 0.f;
+  if (t < s && lane < k) {
+    n_ij = __ldg(idx + (size_t)t * k + lane);
+    n_gj = __ldg(gate + (size_t)t * k + lane);
+    n_dgj = __ldg(dgate + (size_t)t * k + lane);
+  }
+  for (; t < s; t += warps) {
+    const int ij = n_ij;
+    const float gj = n_gj, dgj = n_dgj;
+    const int tn = t + warps;
+    if (tn < s && lane < k) {
+      n_ij = __ldg(idx + (size_t)tn * k + lane);
+      n_gj = __ldg(gate + (size_t)tn * k + lane);
+      n_dgj = __ldg(dgate + (size_t)tn * k + lane);
     }
     float c = __fmul_rn(gj, dgj);
 #pragma unroll
