@@ -2,7 +2,11 @@
  * moe_gb300.h -- C ABI of the GB300 (sm_103a) mixture-of-experts token path:
  * top-k softmax gating, the dispatch layout, dispatch into the
  * expert-grouped buffer, the weighted combine, and the two backward duals
- * replayed on a cached layout handle.
+ * replayed on a cached layout handle; with them the router's gradient
+ * (gate backward), layout variants (k-major capacity priority, per-expert
+ * padding, per-virtual-rank send slots), the expert-grouped GEMM that
+ * consumes the grouped rows (and its form fused with the dispatch), and an
+ * allocation-free layout entry point.
  *
  * Sources (page title, then the part of the page that defines the call):
  *  [P1] NVIDIA-NeMo/Automodel #3684 "perf(moe): reuse the DeepEP dispatch
@@ -277,9 +281,10 @@ moe_status moe_dispatch_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtyp
  * token or k-major, capacity or dropless, padded or not.  K a multiple of
  * 8 and at least 64; N a multiple of 8 (16-byte rows); rows equal to the
  * handle's; e <= 256.
- * tcgen05 MMA with TMEM accumulators, TMA-fed; the segments are read from
- * the handle on the device (no host sync).  Errors: MOE_ERR_INVALID_ARG,
- * MOE_ERR_HANDLE_MISMATCH, MOE_ERR_CUDA. */
+ * tcgen05 MMA on pairs of SMs (cta_group::2) with TMEM accumulators,
+ * TMA-fed; the segments are read from the handle on the device (no host
+ * sync).  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_HANDLE_MISMATCH,
+ * MOE_ERR_CUDA. */
 moe_status moe_grouped_gemm(moe_handle h, int rows, int K, int N, const void* X, const void* W,
                             void* Y, void* stream);
 
@@ -292,8 +297,9 @@ moe_status moe_grouped_gemm(moe_handle h, int rows, int K, int N, const void* X,
  * tiles.
  *   Y[r, :] = x[inv_row[r], :] . W[x]^T   for every owned row r,
  * x bf16 [s, K] (the tokens' activations, K = m), W bf16 [e, N, K], Y bf16
- * [rows, N]; rows no route owns are not written.  Same limits and errors as
- * moe_grouped_gemm; s must equal the handle's. */
+ * [rows, N]; rows no route owns are not written.  Each owned row equals
+ * moe_grouped_gemm's bit for bit (same operands, same MMA sequence).  Same
+ * limits and errors as moe_grouped_gemm; s must equal the handle's. */
 moe_status moe_dispatch_grouped_gemm(moe_handle h, int s, int rows, int K, int N, const void* x,
                                      const void* W, void* Y, void* stream);
 
