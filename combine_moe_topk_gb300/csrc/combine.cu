@@ -34,7 +34,7 @@ constexpr int kThreads = 256;
 #define MOE_CMB_LOADS 16
 #endif
 #ifndef MOE_CMB_BWD_LOADS
-#define MOE_CMB_BWD_LOADS 8
+#define MOE_CMB_BWD_LOADS 16
 #endif
 #ifndef MOE_CMB_MAX_BPS
 #define MOE_CMB_MAX_BPS 0
