@@ -103,7 +103,7 @@ class HandleRecorder:
     """
 
     def __init__(self, build=None, verify: bool = False):
-        self._build = build or B.moe_dispatch_layout
+        self._build = build or _build_layout
         self._log: deque = deque()
         self._replaying = False
         self.verify = verify
@@ -124,10 +124,16 @@ class HandleRecorder:
     def __len__(self):
         return len(self._log)
 
-    def layout(self, topk_idx: torch.Tensor, e: int, capacity: int = 0, num_virtual_ranks: int = 0):
-        key = (tuple(topk_idx.shape), int(e), int(capacity), int(num_virtual_ranks))
+    def layout(self, topk_idx: torch.Tensor, e: int, capacity: int = 0, num_virtual_ranks: int = 0,
+               priority: str = "token", pad_multiple: int = 1, send_slots: bool = False):
+        """The layout of ``topk_idx`` (options as ``moe_dispatch_layout_ex``):
+        built and logged while recording, the logged handle while replaying."""
+        opts = {}
+        if priority != "token" or pad_multiple != 1 or send_slots:
+            opts = dict(priority=priority, pad_multiple=int(pad_multiple), send_slots=bool(send_slots))
+        key = (tuple(topk_idx.shape), int(e), int(capacity), int(num_virtual_ranks), tuple(sorted(opts.items())))
         if not self._replaying:
-            h = self._build(topk_idx, e, capacity, num_virtual_ranks)
+            h = self._build(topk_idx, e, capacity, num_virtual_ranks, **opts)
             # routing metadata: the expert ids; the dispatched activation is not kept
             self._log.append((key, h, topk_idx.detach() if self.verify else None))
             self.recorded += 1
@@ -139,4 +145,11 @@ class HandleRecorder:
                 return h
         # outran the log, or the call does not match what was logged: build afresh
         self.fallbacks += 1
-        return self._build(topk_idx, e, capacity, num_virtual_ranks)
+        return self._build(topk_idx, e, capacity, num_virtual_ranks, **opts)
+
+
+def _build_layout(topk_idx, e, capacity, num_virtual_ranks, priority="token", pad_multiple=1, send_slots=False):
+    """Plain layouts through moe_dispatch_layout, variants through _ex."""
+    if priority == "token" and pad_multiple == 1 and not send_slots:
+        return B.moe_dispatch_layout(topk_idx, e, capacity, num_virtual_ranks)
+    return B.moe_dispatch_layout_ex(topk_idx, e, capacity, num_virtual_ranks, priority, pad_multiple, send_slots)

@@ -188,3 +188,23 @@ def test_per_call_recorders_keep_passes_apart():
         recs[p].replay()
         assert [recs[p].layout(FakeIdx((8, 2), "?"), 4) for _ in range(4)] == [f"p{p}l{l}" for l in range(4)]
     assert len(built) == n
+
+
+def test_recorder_keys_on_layout_options():
+    """A replay must match the logged call's layout options too: k-major,
+    padding and send slots are part of what was built."""
+    built = []
+
+    def build(idx, e, cap, R, **opts):
+        built.append((idx.tag, opts))
+        return idx.tag
+
+    rec = A.HandleRecorder(build=build)
+    rec.layout(FakeIdx((8, 2), "a"), 4, capacity=3, priority="kmajor")
+    rec.layout(FakeIdx((8, 2), "b"), 4, pad_multiple=8, send_slots=False)
+    assert built[0][1] == {"priority": "kmajor", "pad_multiple": 1, "send_slots": False}
+    rec.replay()
+    assert rec.layout(FakeIdx((8, 2), "?"), 4, capacity=3, priority="kmajor") == "a"
+    # same call position, but token priority this time: rebuilt, not replayed
+    assert rec.layout(FakeIdx((8, 2), "c"), 4, pad_multiple=1) == "c"
+    assert rec.replayed == 1 and rec.fallbacks == 1

@@ -146,3 +146,21 @@ def test_router_gradient_through_the_whole_path(renorm):
     scale = T.gate_bwd_scale(oi, og, T.dot_scale(L["row"], inp["dout"].numpy(), Oy), e, renorm, lg)
     bad = np.abs(got.astype(np.float64) - Odl) > 1e-5 * scale + 1e-30
     assert not bad.any(), (int(bad.sum()), np.abs(got - Odl).max())
+
+
+def test_recorder_replays_layout_variants():
+    """k-major capacity priority and padded dropless layouts (with send
+    slots) replay through the recorder like plain ones: no layout launch,
+    identical rows and slots."""
+    idx = W.random_routes(3000, 32, 4, device=DEV, seed=23)
+    rec = A.HandleRecorder(verify=True)
+    h1 = rec.layout(idx, 32, 300, 4, priority="kmajor")
+    h2 = rec.layout(idx, 32, 0, 4, pad_multiple=128, send_slots=True)
+    rows1, rows2, slots2 = h1.row().clone(), h2.row().clone(), h2.rank_slot().clone()
+    rec.replay()
+    n = B.moe_launch_count("layout")
+    r1 = rec.layout(idx, 32, 300, 4, priority="kmajor")
+    r2 = rec.layout(idx, 32, 0, 4, pad_multiple=128, send_slots=True)
+    assert r1 is h1 and r2 is h2 and B.moe_launch_count("layout") == n
+    assert torch.equal(r1.row(), rows1) and torch.equal(r2.row(), rows2) and torch.equal(r2.rank_slot(), slots2)
+    assert r1.priority == 1 and r2.pad_multiple == 128
