@@ -12,15 +12,17 @@
 // Y[r] = A[r] . W[x]^T for every row r that a kept route to expert x owns,
 // r in [offsets[x], offsets[x] + counts[x]).  A[r] is the dispatched row
 // X[r] (moe_grouped_gemm) or the token row x[inv_row[r]] (fused dispatch:
-// the dispatched buffer is never written or read).  bf16 operands, row-major, K
-// contiguous; the accumulation is fp32 in TMEM.  Work units are row blocks
+// the dispatched buffer is never written or read).  bf16 operands,
+// row-major, K contiguous; the accumulation is fp32 in TMEM.  Work units are row blocks
 // of one expert's segment (256 rows on SM pairs, 128 on single SMs; the
 // first at offsets[x], so a segment may start on any row) times
 // 256-column tiles of N.
 //
 // Both forms run on pairs of SMs (grouped_gemm_pair_kernel, below): a
 // cluster of two CTAs computes a 256-row block x 256 columns with
-// tcgen05.mma.cta_group::2, each SM staging only its half of A and of B.
+// tcgen05.mma.cta_group::2, each SM staging only its half of A and of B
+// (the plain form two 64-wide K blocks per stage of a 3-stage ring, the
+// fused form one per stage of a 6-stage ring; see PairCfg).
 // In the fused form the second CTA's gathered rows reach the MMA issuer
 // through a 16-byte shared-to-shared bulk copy that counts on the first
 // CTA's barrier: a per-K-block arrival with cluster-scope release instead
