@@ -13,12 +13,26 @@ built, then the handle is released.
 Prints ONE JSON line.  ``value`` = algorithmic HBM bytes of a step / device
 time of a step (GB/s), inputs resident in HBM, the K steps timed back to
 back with no events between kernels (as one CUDA graph of the step when it
-can be captured, else eager calls; ``config.launch`` says which).  Per-kernel
-durations for ``ops`` and ``roofline`` come from a separate loop with events
-around every call.  ``e2e`` = the same metric with every step's inputs
-copied from pinned host memory and its results copied back inside the timed
-region.  The step's working set is several times the 129 MB L2, so no L2
-flush is inserted between steps.
+can be captured, else eager calls; ``config.launch`` says which).  The
+step's working set is several times the 129 MB L2, so no L2 flush is
+inserted between steps.  Further keys:
+
+- ``ops`` / ``roofline``: per-kernel durations from a separate loop with
+  events around every call (each after a short GPU sleep, so the host's
+  enqueue is not timed); the roofline is the dominant kernel's algorithmic
+  bytes over its mean duration against the measured copy bandwidth, with
+  its ncu DRAM traffic from ``profiles/ncu_traffic.json``;
+- ``dispatch_combine``: the pair as a CUDA graph on one handle, replayed
+  back to back (the cached-replay case);
+- ``replay``: the step on a saved handle (gate recomputed, no layout), and
+  the layout launches seen meanwhile (must be 0);
+- ``routing``: drop fraction, and the dedup ratio over virtual ranks;
+- ``e2e``: the same metric with every step's inputs copied from pinned
+  host memory and its results copied back inside the timed region;
+- ``expert_gemm``: the grouped GEMM consuming the dispatched rows, plain
+  and fused with the dispatch, in TFLOP/s against the measured bf16 peak
+  (outside ``value``);
+- ``cpu_baseline``: the oracle on the host's cores (and on one core).
 """
 from __future__ import annotations
 
