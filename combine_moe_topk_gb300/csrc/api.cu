@@ -550,7 +550,7 @@ moe_status moe_combine(moe_handle h, int s, int rows, int m, moe_dtype dtype, co
   MOE_TRY(check_device_ptr(out, "out", h->device));
   const moe::DeviceInfo* di = nullptr;
   MOE_TRY(device_state(h->device, &di));
-  cudaError_t err = moe::launch_combine(h->out.row, gate, s, h->k, m, dtype == MOE_F32 ? 0 : 1, y, out,
+  cudaError_t err = moe::launch_combine(h->out.row, gate, s, h->k, m, dtype == MOE_F32 ? 0 : 1, y, out, h->capacity > 0,
                                         *di, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "combine launch");
   g_launches[MOE_KERNEL_COMBINE]++;
@@ -601,7 +601,7 @@ moe_status moe_dispatch_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtyp
   MOE_TRY(check_device_ptr(dx, "dx", h->device));
   const moe::DeviceInfo* di = nullptr;
   MOE_TRY(device_state(h->device, &di));
-  cudaError_t err = moe::launch_combine(h->out.row, nullptr, s, h->k, m, dtype == MOE_F32 ? 0 : 1, dX, dx,
+  cudaError_t err = moe::launch_combine(h->out.row, nullptr, s, h->k, m, dtype == MOE_F32 ? 0 : 1, dX, dx, h->capacity > 0,
                                         *di, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "dispatch_bwd launch");
   g_launches[MOE_KERNEL_DISPATCH_BWD]++;

@@ -113,6 +113,100 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __rest
   pdl_trigger_late();
 }
 
+// Capacity layouts, where most routes may be dropped: the token's kept
+// routes are first compacted onto lanes 0..nkept-1 (in route order), then
+// taken KC at a time, each round loading UNR vectors of each of its routes
+// and adding them into a running fp32 accumulator in route order -- the
+// same fmaf sequence per element as combine_kernel, so the same bits.  The
+// register tile is sized for KC routes rather than for k, so more warps fit
+// and the few kept routes get more loads in flight.
+template <typename T, int KC, int UNR, bool WEIGHTED>
+__global__ void __launch_bounds__(kThreads) combine_compact_kernel(const int32_t* __restrict__ row,
+                                                                   const float* __restrict__ gate, int s,
+                                                                   int k, int nvec, int chunk, int nchunks,
+                                                                   const uint4* __restrict__ y,
+                                                                   uint4* __restrict__ out) {
+  constexpr int N = Vec<T>::N;
+  const int lane = threadIdx.x & 31;
+  const long long warps = (gridDim.x * blockDim.x) >> 5;
+  const long long units = (long long)s * nchunks;
+  grid_dependency_wait();
+  pdl_trigger_early();
+  for (long long u = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < units; u += warps) {
+    const int t = (int)(u / nchunks);
+    const int c0 = (int)(u - (long long)t * nchunks) * chunk;
+    const int c1 = min(nvec, c0 + chunk);
+    const int rl = lane < k ? __ldg(row + (size_t)t * k + lane) : -1;
+    const float gl = (WEIGHTED && lane < k) ? __ldg(gate + (size_t)t * k + lane) : 1.0f;
+    unsigned kept = __ballot_sync(0xffffffffu, rl >= 0);
+    const int nkept = __popc(kept);
+    // lane c takes the c-th kept route
+    int cr = -1;
+    float cg = 0.f;
+    for (int c = 0; kept; ++c) {  // warp-uniform: at most k rounds
+      const int src = __ffs(kept) - 1;
+      kept &= kept - 1u;
+      const int rr = __shfl_sync(0xffffffffu, rl, src);
+      const float gg = __shfl_sync(0xffffffffu, gl, src);
+      if (lane == c) {
+        cr = rr;
+        cg = gg;
+      }
+    }
+    uint4* o = out + (size_t)t * nvec;
+    // the loop runs the same trips on every lane (the shuffles below need the
+    // whole warp); a lane past the piece's end loads and stores nothing
+    for (int vb = c0; vb < c1; vb += 32 * UNR) {
+      const int v0 = vb + lane;
+      float acc[UNR][N];
+#pragma unroll
+      for (int u2 = 0; u2 < UNR; ++u2)
+#pragma unroll
+        for (int i = 0; i < N; ++i) acc[u2][i] = 0.0f;
+      for (int j0 = 0; j0 < nkept; j0 += KC) {
+        int r[KC];
+        float g[KC];
+#pragma unroll
+        for (int j = 0; j < KC; ++j) {
+          r[j] = __shfl_sync(0xffffffffu, cr, (j0 + j) & 31);
+          g[j] = __shfl_sync(0xffffffffu, cg, (j0 + j) & 31);
+          if (j0 + j >= nkept) r[j] = -1;
+        }
+        uint4 val[KC][UNR];
+#pragma unroll
+        for (int j = 0; j < KC; ++j) {
+          if (r[j] >= 0) {
+            const uint4* src = y + (size_t)r[j] * nvec;
+#pragma unroll
+            for (int u2 = 0; u2 < UNR; ++u2) {
+              const int v = v0 + 32 * u2;
+              if (v < c1) val[j][u2] = ld_stream(src + v);
+            }
+          }
+        }
+#pragma unroll
+        for (int u2 = 0; u2 < UNR; ++u2) {
+#pragma unroll
+          for (int j = 0; j < KC; ++j) {
+            if (r[j] >= 0) {
+              float f[N];
+              Vec<T>::to_float(val[j][u2], f);
+#pragma unroll
+              for (int i = 0; i < N; ++i) acc[u2][i] = __fmaf_rn(g[j], f[i], acc[u2][i]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u2 = 0; u2 < UNR; ++u2) {
+        const int v = v0 + 32 * u2;
+        if (v < c1) st_stream(o + v, Vec<T>::from_float(acc[u2]));
+      }
+    }
+  }
+  pdl_trigger_late();
+}
+
 // G warps per token (G = 1, 2, 4 or 8): warp w of a token's group takes the
 // row's vectors [w*chunk, (w+1)*chunk); the per-route dots are reduced across
 // the warp's lanes (butterfly), then across the group's warps in warp order
@@ -322,6 +416,34 @@ cudaError_t combine_bwd_t(const int32_t* row, const int32_t* counts, const int32
 #undef MOE_CBWD_G
 }
 
+#ifndef MOE_CMB_COMPACT
+#define MOE_CMB_COMPACT 1
+#endif
+
+template <typename T>
+cudaError_t combine_compact_t(const int32_t* row, const float* gate, int s, int k, int m, const void* y,
+                              void* out, const DeviceInfo& di, cudaStream_t st) {
+  constexpr int KC = 4, UNR = 2;
+  const int nvec = m / Vec<T>::N;
+  auto kern_w = combine_compact_kernel<T, KC, UNR, true>;
+  auto kern_u = combine_compact_kernel<T, KC, UNR, false>;
+  static const int bps_w = occupancy(kern_w);
+  static const int bps_u = occupancy(kern_u);
+  const int bps = gate ? bps_w : bps_u;
+  int chunk = nvec;
+  const int pieces = pieces_for(s, nvec, di, bps, 8, 8);
+  if (pieces > 1) chunk = ((nvec + pieces - 1) / pieces + 31) / 32 * 32;
+  const int nchunks = (nvec + chunk - 1) / chunk;
+  const long long units = (long long)s * nchunks;
+  if (gate)
+    return launch_pdl(MOE_KERNEL_COMBINE, kern_w, dim3(grid_for(units, di, bps)), dim3(kThreads), 0, st,
+                      row, gate, s, k, nvec, chunk, nchunks, static_cast<const uint4*>(y),
+                      static_cast<uint4*>(out));
+  return launch_pdl(MOE_KERNEL_DISPATCH_BWD, kern_u, dim3(grid_for(units, di, bps)), dim3(kThreads), 0, st,
+                    row, static_cast<const float*>(nullptr), s, k, nvec, chunk, nchunks,
+                    static_cast<const uint4*>(y), static_cast<uint4*>(out));
+}
+
 template <typename T>
 cudaError_t combine_k(const int32_t* row, const float* gate, int s, int k, int m, const void* y,
                       void* out, const DeviceInfo& di, cudaStream_t st) {
@@ -349,7 +471,12 @@ cudaError_t combine_bwd_k(const int32_t* row, const int32_t* counts, const int32
 }  // namespace
 
 cudaError_t launch_combine(const int32_t* row, const float* gate, int s, int k, int m, int dtype,
-                           const void* y, void* out, const DeviceInfo& di, cudaStream_t st) {
+                           const void* y, void* out, int sparse, const DeviceInfo& di, cudaStream_t st) {
+  // capacity layouts (routes may be dropped) with more routes than a round holds
+  if (MOE_CMB_COMPACT && sparse && k > 4) {
+    if (dtype == 0) return combine_compact_t<float>(row, gate, s, k, m, y, out, di, st);
+    return combine_compact_t<__nv_bfloat16>(row, gate, s, k, m, y, out, di, st);
+  }
   if (dtype == 0) return combine_k<float>(row, gate, s, k, m, y, out, di, st);
   return combine_k<__nv_bfloat16>(row, gate, s, k, m, y, out, di, st);
 }

@@ -91,8 +91,9 @@ cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, const int
 
 // --- combine family -----------------------------------------------------
 // dtype: 0 = f32, 1 = bf16.  gate == nullptr means unit weights.
+// sparse: the layout may have dropped routes (capacity mode)
 cudaError_t launch_combine(const int32_t* row, const float* gate, int s, int k, int m, int dtype,
-                           const void* y, void* out, const DeviceInfo& di, cudaStream_t st);
+                           const void* y, void* out, int sparse, const DeviceInfo& di, cudaStream_t st);
 
 cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const int32_t* offsets,
                                long long rows, int zero_fill, const float* gate, int s, int k,
