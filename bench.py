@@ -105,23 +105,25 @@ def bf16_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def traffic_record(op: str, workload: str):
+def source_sha(op: str) -> str:
+    """Hash of the kernel source file of an op (ties a traffic record to it)."""
+    src = os.path.join(ROOT, "combine_moe_topk_gb300", "csrc", KERNEL_FILE[op])
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_record(op: str, workload: str, path: str | None = None):
     """Per-launch DRAM bytes of this op on this workload from the committed
     ncu summary, if it was taken on the kernel source as it is now (else
     None)."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    path = path or os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(workload, {})
     except Exception:
         return None
     r = rec.get(op)
-    if not r:
-        return None
-    src = os.path.join(ROOT, "combine_moe_topk_gb300", "csrc", KERNEL_FILE[op])
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    if r.get("source_sha") != sha:
+    if not r or r.get("source_sha") != source_sha(op):
         return None
     return r
 

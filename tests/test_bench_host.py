@@ -80,9 +80,17 @@ def test_reference_arm_prints_only_on_rank_zero():
     assert line["e2e"]["h2d_bytes_per_step"] == 0
 
 
-def test_traffic_record_is_per_workload_and_tied_to_the_source():
-    rec = bench.traffic_record("combine_bwd", "mixtral-dropless")
-    assert rec is not None and rec["dram_bytes_per_launch"] > 0
-    fine = bench.traffic_record("combine_bwd", "fine-grained-skewed")
-    assert fine is not None and fine["dram_bytes_per_launch"] != rec["dram_bytes_per_launch"]
-    assert bench.traffic_record("combine_bwd", "no-such-workload") is None
+def test_traffic_record_is_per_workload_and_tied_to_the_source(tmp_path):
+    sha = bench.source_sha("combine_bwd")
+    rec = {"wl-a": {"combine_bwd": {"dram_bytes_per_launch": 100, "source_sha": sha}},
+           "wl-b": {"combine_bwd": {"dram_bytes_per_launch": 200, "source_sha": sha},
+                    "combine": {"dram_bytes_per_launch": 300, "source_sha": "0" * 16}}}
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps(rec))
+    assert bench.traffic_record("combine_bwd", "wl-a", str(path))["dram_bytes_per_launch"] == 100
+    assert bench.traffic_record("combine_bwd", "wl-b", str(path))["dram_bytes_per_launch"] == 200
+    assert bench.traffic_record("combine_bwd", "no-such-workload", str(path)) is None
+    assert bench.traffic_record("combine", "wl-b", str(path)) is None  # taken on another source
+    # the committed record file parses and keys by workload
+    committed = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+    assert "mixtral-dropless" in committed and "combine_bwd" in committed["mixtral-dropless"]
