@@ -581,7 +581,8 @@ moe_status moe_combine_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype
   MOE_TRY(device_state(h->device, &di));
   cudaError_t err = moe::launch_combine_bwd(h->out.row, h->out.counts, h->out.offsets, h->rows,
                                             h->zero_fill, gate, s, h->k, h->e, m, dtype == MOE_F32 ? 0 : 1,
-                                            dout, y, dY, dgate, *di, static_cast<cudaStream_t>(stream));
+                                            dout, y, dY, dgate, h->capacity > 0, *di,
+                                            static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "combine_bwd launch");
   g_launches[MOE_KERNEL_COMBINE_BWD]++;
   return MOE_OK;

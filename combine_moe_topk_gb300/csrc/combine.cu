@@ -42,6 +42,10 @@ constexpr int kThreads = 256;
 #ifndef MOE_CMB_CHUNK
 #define MOE_CMB_CHUNK 0
 #endif
+// 1: capacity layouts with k > 4 use the compacted-route kernels.
+#ifndef MOE_CMB_COMPACT
+#define MOE_CMB_COMPACT 1
+#endif
 
 // Route rows and gates of token t, broadcast from lanes 0..k-1.
 template <int KMAX, bool WEIGHTED>
@@ -317,6 +321,121 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
   }
 }
 
+// Combine backward for capacity layouts (routes may be dropped), G = 1:
+// kept routes compacted onto lanes in route order and taken KC per round;
+// each round walks the row (dout re-read only when a token keeps more than
+// KC routes), writes dY for its routes and reduces their dots to dgate.
+// Per lane the dot of a route sums the same vectors in the same order as
+// combine_bwd_kernel<..., G = 1>, so dgate and dY are the same bits.
+template <typename T, int KC, int UNR>
+__global__ void __launch_bounds__(kThreads) combine_bwd_compact_kernel(
+    const int32_t* __restrict__ row, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ offsets, long long rows, int zero_fill,
+    const float* __restrict__ gate, int s, int k, int e, int nvec,
+    const uint4* __restrict__ dout, const uint4* __restrict__ y, uint4* __restrict__ dY,
+    float* __restrict__ dgate) {
+  constexpr int N = Vec<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  grid_dependency_wait();
+  pdl_trigger_early();
+  for (int t = gw; t < s; t += warps) {
+    const int rl = lane < k ? __ldg(row + (size_t)t * k + lane) : -1;
+    const float gl = lane < k ? __ldg(gate + (size_t)t * k + lane) : 0.f;
+    unsigned kept = __ballot_sync(0xffffffffu, rl >= 0);
+    const int nkept = __popc(kept);
+    if (lane < k && rl < 0) dgate[(size_t)t * k + lane] = 0.f;  // a dropped route
+    // lane c takes the c-th kept route, remembering its route index
+    int cr = -1, cj = 0;
+    float cg = 0.f;
+    for (int c = 0; kept; ++c) {  // warp-uniform: at most k rounds
+      const int src = __ffs(kept) - 1;
+      kept &= kept - 1u;
+      const int rr = __shfl_sync(0xffffffffu, rl, src);
+      const float gg = __shfl_sync(0xffffffffu, gl, src);
+      if (lane == c) {
+        cr = rr;
+        cg = gg;
+        cj = src;
+      }
+    }
+    const uint4* d = dout + (size_t)t * nvec;
+    for (int j0 = 0; j0 < nkept; j0 += KC) {
+      int r[KC];
+      float g[KC];
+      float dot[KC];
+#pragma unroll
+      for (int j = 0; j < KC; ++j) {
+        r[j] = __shfl_sync(0xffffffffu, cr, (j0 + j) & 31);
+        g[j] = __shfl_sync(0xffffffffu, cg, (j0 + j) & 31);
+        if (j0 + j >= nkept) r[j] = -1;
+        dot[j] = 0.f;
+      }
+      for (int v0 = lane; v0 < nvec; v0 += 32 * UNR) {  // no shuffles in here
+        uint4 dv[UNR];
+        uint4 yv[KC][UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+          const int v = v0 + 32 * u;
+          if (v < nvec) dv[u] = ld_stream(d + v);
+        }
+#pragma unroll
+        for (int j = 0; j < KC; ++j) {
+          if (r[j] >= 0) {
+            const uint4* src = y + (size_t)r[j] * nvec;
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+              const int v = v0 + 32 * u;
+              if (v < nvec) yv[j][u] = ld_stream(src + v);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+          const int v = v0 + 32 * u;
+          if (v >= nvec) break;
+          float df[N];
+          Vec<T>::to_float(dv[u], df);
+#pragma unroll
+          for (int j = 0; j < KC; ++j) {
+            if (r[j] >= 0) {
+              float yf[N], pp[N];
+              Vec<T>::to_float(yv[j][u], yf);
+#pragma unroll
+              for (int i = 0; i < N; ++i) {
+                dot[j] = __fmaf_rn(df[i], yf[i], dot[j]);
+                pp[i] = __fmul_rn(g[j], df[i]);
+              }
+              st_stream(dY + (size_t)r[j] * nvec + v, Vec<T>::from_float(pp));
+            }
+          }
+        }
+      }
+      // the round's dots: butterfly, then the route's own dgate slot
+#pragma unroll
+      for (int j = 0; j < KC; ++j) {
+        float v = dot[j];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        const int jj = __shfl_sync(0xffffffffu, cj, (j0 + j) & 31);
+        if (lane == 0 && j0 + j < nkept) dgate[(size_t)t * k + jj] = v;
+      }
+    }
+  }
+  pdl_trigger_late();
+
+  // rows no kept route owns (capacity slots, padding) get zero gradient
+  if (zero_fill) {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (long long rr = gw; rr < rows; rr += warps) {
+      if (row_is_owned(rr, offsets, counts, e)) continue;
+      uint4* dst = dY + (size_t)rr * nvec;
+      for (int v = lane; v < nvec; v += 32) st_stream(dst + v, z);
+    }
+  }
+}
+
 template <typename K>
 int occupancy(K kern) {
   int n = 0;
@@ -398,7 +517,7 @@ cudaError_t combine_bwd_g(const int32_t* row, const int32_t* counts, const int32
 template <typename T, int KMAX>
 cudaError_t combine_bwd_t(const int32_t* row, const int32_t* counts, const int32_t* offsets,
                           long long rows, int zero_fill, const float* gate, int s, int k, int e,
-                          int m, const void* dout, const void* y, void* dY, float* dgate,
+                          int m, const void* dout, const void* y, void* dY, float* dgate, int sparse,
                           const DeviceInfo& di, cudaStream_t st) {
   constexpr int UNR = MOE_CMB_BWD_LOADS / KMAX > 1 ? MOE_CMB_BWD_LOADS / KMAX : 1;
   const int nvec = m / Vec<T>::N;
@@ -406,6 +525,17 @@ cudaError_t combine_bwd_t(const int32_t* row, const int32_t* counts, const int32
   // warps per token for short batches (the dot of the gate gradient is
   // reduced across them in a fixed order, so each G gives fixed results)
   const int G = pieces_for(s, nvec, di, bps, 4, 8);
+  if (MOE_CMB_COMPACT && sparse && k > 4 && G == 1) {
+    constexpr int KC = 4, UNRC = MOE_CMB_BWD_LOADS / KC > 1 ? MOE_CMB_BWD_LOADS / KC : 1;
+    auto kern = combine_bwd_compact_kernel<T, KC, UNRC>;
+    static const int bpsc = occupancy(kern);
+    long long warps = s;
+    if (zero_fill && rows > warps) warps = rows;
+    return launch_pdl(MOE_KERNEL_COMBINE_BWD, kern, dim3(grid_for(warps, di, bpsc)), dim3(kThreads), 0, st,
+                      row, counts, offsets, rows, zero_fill, gate, s, k, e, nvec,
+                      static_cast<const uint4*>(dout), static_cast<const uint4*>(y), static_cast<uint4*>(dY),
+                      dgate);
+  }
 #define MOE_CBWD_G(GG)                                                                            \
   combine_bwd_g<T, KMAX, GG>(row, counts, offsets, rows, zero_fill, gate, s, k, e, nvec, dout, y, dY, \
                              dgate, di, bps, st)
@@ -415,10 +545,6 @@ cudaError_t combine_bwd_t(const int32_t* row, const int32_t* counts, const int32
   return MOE_CBWD_G(1);
 #undef MOE_CBWD_G
 }
-
-#ifndef MOE_CMB_COMPACT
-#define MOE_CMB_COMPACT 1
-#endif
 
 template <typename T>
 cudaError_t combine_compact_t(const int32_t* row, const float* gate, int s, int k, int m, const void* y,
@@ -456,11 +582,11 @@ cudaError_t combine_k(const int32_t* row, const float* gate, int s, int k, int m
 template <typename T>
 cudaError_t combine_bwd_k(const int32_t* row, const int32_t* counts, const int32_t* offsets,
                           long long rows, int zero_fill, const float* gate, int s, int k, int e,
-                          int m, const void* dout, const void* y, void* dY, float* dgate,
+                          int m, const void* dout, const void* y, void* dY, float* dgate, int sparse,
                           const DeviceInfo& di, cudaStream_t st) {
 #define MOE_CBWD(KM)                                                                              \
   combine_bwd_t<T, KM>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout, y, dY, dgate, \
-                       di, st)
+                       sparse, di, st)
   if (k <= 2) return MOE_CBWD(2);
   if (k <= 4) return MOE_CBWD(4);
   if (k <= 8) return MOE_CBWD(8);
@@ -484,12 +610,12 @@ cudaError_t launch_combine(const int32_t* row, const float* gate, int s, int k, 
 cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const int32_t* offsets,
                                long long rows, int zero_fill, const float* gate, int s, int k,
                                int e, int m, int dtype, const void* dout, const void* y, void* dY,
-                               float* dgate, const DeviceInfo& di, cudaStream_t st) {
+                               float* dgate, int sparse, const DeviceInfo& di, cudaStream_t st) {
   if (dtype == 0)
     return combine_bwd_k<float>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout, y, dY,
-                                dgate, di, st);
+                                dgate, sparse, di, st);
   return combine_bwd_k<__nv_bfloat16>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout,
-                                      y, dY, dgate, di, st);
+                                      y, dY, dgate, sparse, di, st);
 }
 
 }  // namespace moe

@@ -98,7 +98,7 @@ cudaError_t launch_combine(const int32_t* row, const float* gate, int s, int k, 
 cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const int32_t* offsets,
                                long long rows, int zero_fill, const float* gate, int s, int k,
                                int e, int m, int dtype, const void* dout, const void* y, void* dY,
-                               float* dgate, const DeviceInfo& di, cudaStream_t st);
+                               float* dgate, int sparse, const DeviceInfo& di, cudaStream_t st);
 
 // --- per-virtual-rank send slots ------------------------------------------
 // rank_slot[t,r] = token-order position of t among the tokens sending to r,
