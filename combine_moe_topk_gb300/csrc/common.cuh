@@ -25,19 +25,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Relaxed 64-bit global accesses at GPU scope.  The look-back words carry
-// their payload in the same 64-bit word as their flag, so no other ordering
-// is needed between a publish and the read that sees it.
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
 // ------------------------------------------- programmatic dependent launch --
 // A kernel launched with programmatic stream serialisation may start while
 // the previous kernel in the stream is still running; it must wait here

@@ -216,7 +216,7 @@ struct Config {
   int piece, npieces, stages, stride, smem, ctas_per_sm;
 };
 
-Config choose(long long row_bytes, const DeviceInfo& di) {
+Config choose(long long row_bytes) {
   Config c;
   const long long kPieceMax = MOE_DSP_PIECE;
   c.npieces = (int)((row_bytes + kPieceMax - 1) / kPieceMax);
@@ -250,7 +250,7 @@ cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, const int
     return e;
   });
   if (err != cudaSuccess) return err;
-  Config c = choose(row_bytes, di);
+  Config c = choose(row_bytes);
   Params p;
   p.x = static_cast<const char*>(x);
   p.X = static_cast<char*>(X);
