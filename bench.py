@@ -55,6 +55,7 @@ KERNEL_FILE = {"topk_gate": "gate.cu", "layout": "layout.cu", "dispatch": "dispa
                "combine_bwd": "combine.cu", "topk_gate_bwd": "gate.cu", "dispatch_bwd": "combine.cu"}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 1024 * 1024  # GB300 L2 (a flush writes twice this)
 SLEEP_CYCLES = 100_000  # ~50 us at 2 GHz: longer than the host's enqueue of one call
 
 
@@ -310,22 +311,21 @@ def run_ours(args, rank: int, world: int, dist):
         run_step()
     barrier()
 
-    # ---- the timed region: exactly K steps, no events inside ----------------
+    # ---- the timed region: exactly K steps ---------------------------------
+    # A step whose working set exceeds twice the L2 leaves nothing useful in
+    # it for the next step: the K steps run back to back with no events
+    # between them.  A smaller one would run from L2, so each step is timed
+    # on its own after a write of more than the L2 (outside its events).
     K = args.steps
+    flush = None if step_total >= 2 * L2_BYTES else torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     launches0 = [B.moe_launch_count(i) for i in range(len(B.KERNELS))]
     with ClockSampler(dev.index) as clk:
         barrier()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for _ in range(K):
-            run_step()
-        t1.record()
+        elapsed_ms = time_loop(run_step, K, flush) * K
         barrier()
     launches = sum(B.moe_launch_count(i) - launches0[i] for i in range(len(B.KERNELS)))
     if graph is not None:
         launches = graph_launches * K
-    elapsed_ms = t0.elapsed_time(t1)
 
     # ---- per-kernel durations: events around each call, eager, own loop -----
     Kr = max(3, min(K, 200))
@@ -382,7 +382,10 @@ def run_ours(args, rank: int, world: int, dist):
             "step": "topk_gate+layout+dispatch+combine+combine_bwd+topk_gate_bwd+dispatch_bwd on the step's handle",
             "launch": launch_mode,
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "l2": f"no flush: step working set {round(step_total / 1e6)} MB algorithmic vs 129 MB L2",
+            "l2": (f"no flush: step working set {round(step_total / 1e6)} MB algorithmic, over twice the 129 MB L2"
+                   if flush is None else
+                   f"L2 flushed before every step (a {2 * L2_BYTES >> 20} MiB write, outside the timing): step "
+                   f"working set {round(step_total / 1e6, 2)} MB; steps timed one by one"),
         },
         "routed_tokens_per_s": round(world * w.s * w.k / (ms_per_step * 1e-3), 1),
         "dispatch_combine": {
@@ -431,6 +434,35 @@ def run_ours(args, rank: int, world: int, dist):
     return line
 
 
+def time_loop(run, n: int, flush=None) -> float:
+    """Mean device time (ms) of n calls of run(): back to back between two
+    events, or, with a flush buffer (a working set that L2 would hold), each
+    call timed on its own after a write of that buffer."""
+    import torch
+
+    if flush is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            run()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        flush.fill_(1)
+        a.record()
+        run()
+        b.record()
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / n
+
+
+def small_working_set(w) -> bool:
+    """Whether a step's inputs and outputs would stay in L2 between steps."""
+    return sum(step_bytes(w, w.s * w.k, w.s).values()) < 2 * L2_BYTES
+
+
 def run_dispatch_combine(w, S, dev, K: int):
     """Dispatch + combine on one handle, as a CUDA graph of the pair replayed
     K times back to back (events around the whole loop): the steady-state
@@ -448,7 +480,7 @@ def run_dispatch_combine(w, S, dev, K: int):
         B.moe_dispatch(h, S["x"], S["X"])
         B.moe_combine(h, S["y"], S["gate"], S["out"])
 
-    how = "graph of dispatch + combine on one handle, replayed back to back"
+    how = "graph of dispatch + combine on one handle"
     try:
         side = torch.cuda.Stream(dev)
         side.wait_stream(torch.cuda.current_stream(dev))
@@ -461,20 +493,17 @@ def run_dispatch_combine(w, S, dev, K: int):
             pair()
         run = g.replay
     except Exception as exc:
-        run, how = pair, f"eager calls back to back (graph capture failed: {type(exc).__name__})"
+        run, how = pair, f"eager calls (graph capture failed: {type(exc).__name__})"
     for _ in range(5):
         run()
     torch.cuda.synchronize()
     n = max(5, min(K, 500))
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(n):
-        run()
-    b.record()
-    torch.cuda.synchronize()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if small_working_set(w) else None
+    ms = time_loop(run, n, flush)
     assert h.status() == 0
     h.destroy()
-    return {"ms": a.elapsed_time(b) / n, "how": f"{how}, {n} pairs"}
+    how += ", each replay timed alone after an L2 flush" if flush is not None else ", replayed back to back"
+    return {"ms": ms, "how": f"{how}, {n} pairs"}
 
 
 def run_replay_step(w, S, dev, K: int):
@@ -498,7 +527,7 @@ def run_replay_step(w, S, dev, K: int):
                             S["dlogits"])
         B.moe_dispatch_bwd(h, S["dY"], S["dx"])
 
-    how = "graph of the step on a saved handle (gate recomputed, no layout), replayed back to back"
+    how = "graph of the step on a saved handle (gate recomputed, no layout)"
     try:
         side = torch.cuda.Stream(dev)
         side.wait_stream(torch.cuda.current_stream(dev))
@@ -517,16 +546,13 @@ def run_replay_step(w, S, dev, K: int):
     torch.cuda.synchronize()
     layouts = B.moe_launch_count("layout")
     n = max(5, min(K, 500))
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(n):
-        run()
-    b.record()
-    torch.cuda.synchronize()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if small_working_set(w) else None
+    ms = time_loop(run, n, flush)
     moved = B.moe_launch_count("layout") - layouts
     assert h.status() == 0
     h.destroy()
-    return {"ms": a.elapsed_time(b) / n, "layout_launches": moved, "how": f"{how}, {n} steps"}
+    how += ", each replay timed alone after an L2 flush" if flush is not None else ", replayed back to back"
+    return {"ms": ms, "layout_launches": moved, "how": f"{how}, {n} steps"}
 
 
 def run_expert_gemm(w, S, dev, reps: int = 10):
