@@ -21,8 +21,7 @@
 // Both forms run on pairs of SMs (grouped_gemm_pair_kernel, below): a
 // cluster of two CTAs computes a 256-row block x 256 columns with
 // tcgen05.mma.cta_group::2, each SM staging only its half of A and of B
-// (the plain form two 64-wide K blocks per stage of a 3-stage ring, the
-// fused form one per stage of a 6-stage ring; see PairCfg).
+// (two 64-wide K blocks per stage of a 3-stage ring).
 // In the fused form the second CTA's gathered rows reach the MMA issuer
 // through a 16-byte shared-to-shared bulk copy that counts on the first
 // CTA's barrier: a per-K-block arrival with cluster-scope release instead
@@ -77,10 +76,11 @@ constexpr int kGatherThreads = 384;  // fused form: + 4 warps gathering the A ro
 #ifndef MOE_GEMM_FUSED_PAIR
 #define MOE_GEMM_FUSED_PAIR 1
 #endif
+// One-SM fused form: stages a gathering warp's arrival trails its copies.
 #ifndef MOE_GEMM_LAG
 #define MOE_GEMM_LAG 2
 #endif
-constexpr int kGatherLag = MOE_GEMM_LAG;  // stages a gather thread's arrivals trail its copies
+constexpr int kGatherLag = MOE_GEMM_LAG;
 static_assert(kGatherLag >= 1 && kGatherLag < 4, "the ring must keep a stage the gather has not yet claimed");
 constexpr int kMaxE = 256;
 // epilogue staging: per epilogue warp 32 rows x 64 bf16 columns, rows padded
@@ -146,6 +146,12 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// One arrival on `bar` once every cp.async this thread issued so far has
+// landed; the barrier's expected count includes it (.noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -488,7 +494,7 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
 // 0 issues tcgen05.mma.cta_group::2 (M256 N256 K16), which reads both
 // CTAs' shared memory at the same offsets and leaves each CTA's 128 rows
 // of the fp32 result in its own TMEM.  Per SM and K-block only 32 KB move
-// (48 KB in the one-SM form), so the ring holds six stages.
+// (48 KB in the one-SM form), so the ring holds six K-blocks.
 //   both ranks, warp 0 lane 0: TMA of its A and B halves; the completion
 //     bytes of both ranks are counted on rank 0's full barrier (the
 //     .cta_group::2 form of the copy lets rank 1 signal it);
@@ -497,21 +503,15 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
 //   both ranks, warp 2: one collective TMEM allocation for the pair;
 //   both ranks, warps 4..7: epilogue of its own rows, then an arrival on
 //     rank 0's tempty barrier (remote for rank 1).
-// A ring stage holds KB 64-wide K blocks of this CTA's A and B halves (16 KB
-// each per block).  The plain form takes two per stage (3 stages: half the
-// barrier round trips per MMA, measured 3-10 % faster); the fused form one
-// (6 stages: its gather warps arrive two stages behind and need the slack).
-template <bool kGather>
-struct PairCfg {
-  static constexpr int KB = kGather ? 1 : 2;
-  static constexpr int Stages = KB == 1 ? 6 : 3;
-};
+// A ring stage holds two 64-wide K blocks of this CTA's A and B halves (16 KB
+// each per block), in a 3-stage ring: half the barrier round trips per MMA
+// of one block per stage (measured 3-10 % faster for the plain form, 10-15 %
+// for the fused one).
 constexpr int kSubA = BM * BK * 2;              // 16 KB: 128 rows x 64 K of A, one swizzle atom column
 constexpr int kSubB = (BN / 2) * BK * 2;        // 16 KB: 128 rows x 64 K of B
-constexpr int kPairMaxStages = 6;
-constexpr int kPairRingBytes = 6 * (kSubA + kSubB);  // both forms: 192 KB
-static_assert(PairCfg<false>::Stages * PairCfg<false>::KB * (kSubA + kSubB) == kPairRingBytes, "ring size");
-static_assert(PairCfg<true>::Stages * PairCfg<true>::KB * (kSubA + kSubB) == kPairRingBytes, "ring size");
+constexpr int kPairKB = 2;
+constexpr int kPairStages = 3;
+constexpr int kPairRingBytes = kPairStages * kPairKB * (kSubA + kSubB);  // 192 KB
 constexpr int kPairSmemBytes = kPairRingBytes + kEpiBytes + 1024;
 constexpr int BM2 = 2 * BM;                     // rows of a pair block
 
@@ -609,14 +609,12 @@ template <bool kGather>
 __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
-  constexpr int kPairKB = PairCfg<kGather>::KB;
-  constexpr int kPairStages = PairCfg<kGather>::Stages;
   constexpr int kPairABytes = kPairKB * kSubA;  // this CTA's 128 rows of A
   constexpr int kPairBBytes = kPairKB * kSubB;  // this CTA's 128 rows of B
   constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full[kPairMaxStages], empty[kPairMaxStages], tfull[2], tempty[2];
-  __shared__ __align__(8) uint64_t gathered[kPairMaxStages];  // fused form, rank 1: its gathered rows landed
+  __shared__ __align__(8) uint64_t full[kPairStages], empty[kPairStages], tfull[2], tempty[2];
+  __shared__ __align__(8) uint64_t gathered[kPairStages];  // fused form, rank 1: its gathered rows landed
   __shared__ __align__(16) uint8_t s_signal[16];             // fused form: source / target of rank 1's signal
   __shared__ uint32_t tmem_base;
   __shared__ int s_off[kMaxE + 1], s_cnt[kMaxE], s_blk[kMaxE + 1];
@@ -625,6 +623,7 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0 or 1 within the pair
   constexpr int kGatherWarps = (kGatherThreads - kThreads) / 32;
+  constexpr int kGatherArrivals = kGatherWarps * 32;  // one per gathering thread and stage
   // identical static layout in both CTAs: the dynamic buffer starts at the
   // same offset, so the MMA's descriptors address the same tiles in both
   uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
@@ -636,10 +635,10 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
     s_err = 0;
     for (int i = 0; i < kPairStages; ++i) {
       // rank 0: its expect_tx arrival (both ranks' TMA bytes, and in the fused
-      // form rank 1's 16-byte signal), plus one arrival per gathering warp
-      mbar_init(&full[i], kGather ? 1 + kGatherWarps : 1);
+      // form rank 1's 16-byte signal), plus its gathering threads' arrivals
+      mbar_init(&full[i], kGather ? 1 + kGatherArrivals : 1);
       mbar_init(&empty[i], 1);  // the MMA commit, multicast to both ranks
-      mbar_init(&gathered[i], kGatherWarps);
+      mbar_init(&gathered[i], kGatherArrivals);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -724,28 +723,42 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
     if (!ok) atomicOr(&s_err, 1);
   } else if (kGather && warp >= kThreads / 32) {
     // ---- A gather (fused form, both ranks): this CTA's 128 rows ------------
-    // As in the one-SM form.  Rank 0's warps arrive on its full barrier;
-    // rank 1's on its own `gathered` barrier, forwarded below.
+    // Each lane copies 16 bytes of 8 rows per K block (8 lanes per 128-byte
+    // row, the swizzle as in the one-SM form), then hands its copies of the
+    // stage to the stage's barrier (cp.async.mbarrier.arrive.noinc: one
+    // arrival once they land) and runs on to the next free stage; waiting
+    // for its own copies two stages later instead held the gather to a
+    // shallow window and the fused GEMM 10-15 % lower.  Rank 0's threads
+    // arrive on its full barrier, rank 1's on its own `gathered` barrier,
+    // forwarded below; the waiter on each fences the async proxy.  A unit's
+    // row-to-token indices are loaded while the previous unit is gathered.
     const int gw = warp - kThreads / 32, chunk = lane & 7;
-    int stage = 0, astage = 0, pending = 0;
+    int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = pair; u < nunits && ok; u += npairs) {
+    // token of each of this lane's 8 rows in unit u; -1 for rows no route owns
+    auto unit_tokens = [&](int u, int* tok) {
       const Unit t = decode_unit(u, ntn, s_blk, s_off, s_cnt, p.e);
       const int i = u / ntn - s_blk[t.x];
       const int r0 = s_off[t.x] + BM2 * i + BM * (int)rank;
       const int left = s_cnt[t.x] - BM2 * i - BM * (int)rank;
-      const __nv_bfloat16* src[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int rr = 32 * gw + 4 * j + (lane >> 3);
-        int tok = 0;  // rows no route owns are skipped below
+        tok[j] = -1;
         if (rr < left) {
           const int v = __ldg(p.inv_row + r0 + rr);
-          tok = (unsigned)v < (unsigned)p.s ? v : 0;
+          tok[j] = (unsigned)v < (unsigned)p.s ? v : 0;
         }
-        src[j] = p.x + (size_t)tok * p.K + chunk * 8;
       }
+    };
+    int tok[8], ntok[8];
+    if (pair < nunits) unit_tokens(pair, tok);
+    for (int u = pair; u < nunits && ok; u += npairs) {
+      if (u + npairs < nunits) unit_tokens(u + npairs, ntok);  // in flight while this unit is gathered
+      const __nv_bfloat16* src[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) src[j] = p.x + (size_t)(tok[j] < 0 ? 0 : tok[j]) * p.K + chunk * 8;
       for (int kb = 0; kb < kblocks; ++kb) {
         bool waited = true;
         if (lane == 0) waited = mbar_wait_bounded(&empty[stage], phase ^ 1u, deadline);
@@ -761,7 +774,7 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
           for (int j = 0; j < 8; ++j) {
             // rows no route owns are not copied (their results are never stored)
             const int rr = 32 * gw + 4 * j + (lane >> 3);
-            if (rr < left) {
+            if (tok[j] >= 0) {
               // columns past K: zeros, nothing read (the row's end may be the buffer's)
               const bool in_k = kx + chunk * 8 < p.K;
               cp_async16_zfill(sa + q * kSubA + rr * 128 + ((chunk ^ (rr & 7)) << 4), in_k ? src[j] + kx : src[j],
@@ -769,32 +782,17 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
             }
           }
         }
-        cp_async_commit();
-        if (++pending > kGatherLag) {
-          cp_async_wait<kGatherLag>();
-          fence_proxy_async_smem();
-          __syncwarp();  // every lane's copies to the stage have landed
-          if (lane == 0) mbar_arrive(rank == 0 ? &full[astage] : &gathered[astage]);
-          --pending;
-          if (++astage == kPairStages) astage = 0;
-        }
+        cp_async_arrive_noinc(rank == 0 ? &full[stage] : &gathered[stage]);
         if (++stage == kPairStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tok[j] = ntok[j];
     }
-    cp_async_wait<0>();  // nothing of this thread's stays in flight
-    if (ok) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      for (; pending > 0; --pending) {
-        if (lane == 0) mbar_arrive(rank == 0 ? &full[astage] : &gathered[astage]);
-        if (++astage == kPairStages) astage = 0;
-      }
-    } else if (lane == 0) {
-      atomicOr(&s_err, 1);
-    }
+    cp_async_wait_all();  // nothing of this thread's stays in flight
+    if (!ok && lane == 0) atomicOr(&s_err, 1);
   } else if (kGather && warp == 1 && lane == 0 && rank == 1) {
     // ---- forwarder (fused form, rank 1) ------------------------------------
     // Once all of this CTA's gathering warps have landed a stage, a 16-byte
@@ -811,6 +809,7 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
           ok = false;
           break;
         }
+        fence_proxy_async_smem();  // the rows landed by cp.async, before the async-proxy signal
         bulk_signal_s2s(sig_dst, s_signal, mapa_shared(smem_addr(&full[stage]), 0));
         if (++stage == kPairStages) {
           stage = 0;
@@ -839,6 +838,7 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
           break;
         }
         tc_fence_after();
+        if (kGather) fence_proxy_async_smem();  // this CTA's rows landed by cp.async
         const uint32_t sa = smem_addr(smem + stage * kPairStageBytes);
 #pragma unroll
         for (int q = 0; q < kPairKB; ++q) {
