@@ -502,7 +502,11 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
 //     barriers of both ranks (multicast);
 //   both ranks, warp 2: one collective TMEM allocation for the pair;
 //   both ranks, warps 4..7: epilogue of its own rows, then an arrival on
-//     rank 0's tempty barrier (remote for rank 1).
+//     rank 0's tempty barrier (remote for rank 1);
+//   fused form, both ranks, warps 8..11: gather the CTA's 128 A rows, each
+//     thread's copies arriving through cp.async.mbarrier.arrive.noinc;
+//   fused form, rank 1, warp 1 lane 0: forwards each gathered stage to
+//     rank 0's full barrier.
 // A ring stage holds two 64-wide K blocks of this CTA's A and B halves (16 KB
 // each per block), in a 3-stage ring: half the barrier round trips per MMA
 // of one block per stage (measured 3-10 % faster for the plain form, 10-15 %
