@@ -89,6 +89,19 @@ def test_edge_shapes(case):
     full_parity(w, DEV)
 
 
+@pytest.mark.parametrize("case", [
+    dict(w=dict(s=1 << 17, m=16, e=256, k=4, dtype="bf16", capacity=0, R=8), priority="token"),
+    dict(w=dict(s=70000, m=16, e=256, k=2, dtype="f32", capacity=300, R=4), priority="kmajor"),
+    dict(w=dict(s=100000, m=8, e=128, k=8, dtype="bf16", capacity=5000, R=8), priority="token"),
+], ids=["dropless-e256", "kmajor-capacity-e256", "capacity-e128"])
+def test_many_subtile_layouts(case):
+    """Batches long enough that each layout tile scans several 256-token
+    sub-tiles (the look-back words are capped at 16384 = tiles x e), so the
+    general sub-tile loop runs rather than the one- and two-sub-tile forms."""
+    w = W.Workload("many-subtiles", seed=11, **case["w"])
+    full_parity(w, DEV, priority=case["priority"])
+
+
 def test_all_logits_equal_ties_and_drops():
     """Every token ties on every expert: all pick experts 0..k-1 (lower index
     wins), and capacity keeps only the first c tokens of each."""
