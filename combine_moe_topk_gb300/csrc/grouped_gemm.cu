@@ -757,6 +757,8 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
       }
     };
     int tok[8], ntok[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ntok[j] = -1;  // after the last unit: nothing
     if (pair < nunits) unit_tokens(pair, tok);
     for (int u = pair; u < nunits && ok; u += npairs) {
       if (u + npairs < nunits) unit_tokens(u + npairs, ntok);  // in flight while this unit is gathered
