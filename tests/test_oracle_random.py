@@ -14,6 +14,10 @@ independently of the oracle's C code:
   scan of the (padded) counts plus the slot; a token counts once for each
   virtual rank that receives one of its kept routes, and its send slot is
   the number of earlier tokens that send to that rank.
+- dispatch, combine and both backwards (the same change's gather and
+  weighted combine; a backward is the other op with the gates applied or
+  dropped): the dense one-hot route mask over the layout's rows, in
+  float64.
 
 The draws cover the degenerate cases the fixed pins do not enumerate: no
 tokens, one expert, k = e, capacity 1, a pad larger than every segment,
@@ -115,3 +119,54 @@ def test_topk_matches_enumeration_with_many_ties(draw):
                 want[beaten_by] = j
         np.testing.assert_array_equal(idx[t], want)
     np.testing.assert_allclose(gate.sum(1), 1.0, rtol=1e-6)
+
+
+@settings(**dict(SETTINGS, max_examples=150))
+@given(routing(), st.integers(0, 5), st.booleans(), st.sampled_from([1, 4]), st.integers(1, 6),
+       st.integers(0, 2**32 - 1))
+def test_payload_ops_match_dense_route_masks(r, cap, kmajor, P, m, seed):
+    """dispatch, combine and both backwards, fp32, on any layout variant:
+    against the dense one-hot route mask M[t, row] (and its gate-weighted
+    twin) in float64 -- X = M^T x, out = G y, dY = G^T dout, dgate[t, j] =
+    <dout[t], y[row]>, dx = M dX; rows no route owns stay zero."""
+    idx, e, R = r
+    if cap:
+        P = 1
+    L = oracle.layout(idx, e, cap, R, priority=1 if kmajor else 0, pad_multiple=P)
+    s, k = idx.shape
+    rows = L["rows"]
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((s, m)).astype(np.float32)
+    y = rng.standard_normal((rows, m)).astype(np.float32)
+    dout = rng.standard_normal((s, m)).astype(np.float32)
+    dX = rng.standard_normal((rows, m)).astype(np.float32)
+    gate = (rng.random((s, k)) + 0.05).astype(np.float32)
+    M = np.zeros((s, rows))
+    G = np.zeros((s, rows))
+    for t in range(s):
+        for j in range(k):
+            if not L["drop"][t, j]:
+                M[t, L["row"][t, j]] = 1.0
+                G[t, L["row"][t, j]] = float(gate[t, j])
+    x64, y64, d64, dX64 = (a.astype(np.float64) for a in (x, y, dout, dX))
+
+    X = oracle.dispatch(L["row"], x, rows)
+    np.testing.assert_array_equal(X.astype(np.float64), M.T @ x64)
+
+    out = oracle.combine(L["row"], gate, y).astype(np.float64)
+    assert np.all(np.abs(out - G @ y64) <= 1e-6 * (G @ np.abs(y64)) + 1e-30)
+
+    dY, dgate = oracle.combine_bwd(L["row"], gate, dout, y)
+    ref = G.T @ d64
+    assert np.all(np.abs(dY.astype(np.float64) - ref) <= 1e-6 * np.abs(ref) + 1e-30)
+    for t in range(s):
+        for j in range(k):
+            if L["drop"][t, j]:
+                assert dgate[t, j] == 0.0
+            else:
+                rr = L["row"][t, j]
+                want = float(d64[t] @ y64[rr])
+                assert abs(dgate[t, j] - want) <= 1e-6 * float(np.abs(d64[t]) @ np.abs(y64[rr])) + 1e-30
+
+    dx = oracle.dispatch_bwd(L["row"], dX).astype(np.float64)
+    assert np.all(np.abs(dx - M @ dX64) <= 1e-6 * (M @ np.abs(dX64)) + 1e-30)
