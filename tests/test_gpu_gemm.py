@@ -180,3 +180,45 @@ def test_fused_pair_is_stable_over_repeated_calls():
         bad += int((Y.view(torch.int16)[own] != ref.view(torch.int16)[own]).any(dim=1).sum().item())
     assert h.status() == 0
     assert bad == 0, f"{bad} rows differed over 40 calls"
+
+
+def _random_gemm_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        e = int(rng.choice([1, 2, 3, 7, 16, 64, 256]))
+        k = int(rng.integers(1, min(e, 8) + 1))
+        s = int(rng.integers(1, 1000))
+        K = 8 * int(rng.integers(8, 81))       # 64 .. 640, any multiple of 8
+        N = 8 * int(rng.integers(1, 81))       # 8 .. 640
+        c = dict(s=s, e=e, k=k, K=K, N=N)
+        r = rng.random()
+        if r < 0.35:
+            c["capacity"] = int(rng.integers(1, max(2, 2 * s * k // e)))
+            if rng.random() < 0.4:
+                c["priority"] = "kmajor"
+        elif r < 0.6:
+            c["pad"] = int(rng.choice([8, 64, 128, 256]))
+        out.append(c)
+    return out
+
+
+@pytest.mark.parametrize("case", _random_gemm_cases(20, seed=1202),
+                         ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_random_shapes_match_float64_and_fused_is_identical(case):
+    """Seeded random layouts and K, N (any multiples of 8): the plain GEMM
+    against a float64 matmul per segment, the fused form bit for bit equal
+    to it, rows no route owns untouched."""
+    c = dict(case)
+    s, e, k, K, N = (c.pop(n) for n in ("s", "e", "k", "K", "N"))
+    h, x, X, OX, L = _setup(s, e, k, K, seed=s + K, **c)
+    g = torch.Generator().manual_seed(N)
+    Wt = (torch.randn(e, N, K, generator=g) / np.sqrt(K)).to(torch.bfloat16)
+    Wd = Wt.to(DEV)
+    Y = B.moe_grouped_gemm(h, X, Wd, _sentinel_out(h.rows, N))
+    Yf = B.moe_dispatch_grouped_gemm(h, x.to(DEV), Wd, _sentinel_out(h.rows, N))
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    _check_float64(Y, OX, Wt, L)
+    np.testing.assert_array_equal(bits(Yf), bits(Y))
+    _check_unowned_untouched(Y, L)
