@@ -49,7 +49,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "dispatch+combine HBM GB/s and routed tokens/s on 1 GB300 vs HBM peak"
-DEFAULT_WORKLOAD = "mixtral-dropless"
+DEFAULT_WORKLOAD = "fine-grained-skewed"  # the largest workload: s=16384, m=4096, e=128, k=8
 OPS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "topk_gate_bwd", "dispatch_bwd"]
 KERNEL_FILE = {"topk_gate": "gate.cu", "layout": "layout.cu", "dispatch": "dispatch.cu", "combine": "combine.cu",
                "combine_bwd": "combine.cu", "topk_gate_bwd": "gate.cu", "dispatch_bwd": "combine.cu"}
@@ -785,6 +785,19 @@ def run_reference(args, rank: int, world: int):
     }
 
 
+def relaunch(n: int) -> int:
+    """Run this command as n processes on one node (one per GPU) under
+    torch.distributed.run; returns their exit status."""
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -802,6 +815,13 @@ def main():
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # one process per GPU: start them (torchrun), each runs this file again
+        sys.exit(relaunch(args.gpus))
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch one process per GPU")
     dist = None
     if args.impl == "reference":
         line = run_reference(args, rank, world)

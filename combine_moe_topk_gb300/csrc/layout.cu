@@ -663,25 +663,35 @@ static __device__ __align__(256) unsigned g_noalloc_lookback[kNoAllocLookbackWor
 namespace {
 
 struct NoAllocSetup {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
+  std::mutex mu;
+  bool done = false;            // set only once every step below succeeded
   unsigned* scratch = nullptr;  // device address of g_noalloc_lookback
   DeviceInfo info;
 };
 NoAllocSetup g_noalloc[64];
 
-// Once per device, with that device current: resolve the scratch array's
-// device address (its host-side name is only a stand-in) and the sizes the
-// tile plan needs.  Allocates nothing.
-void noalloc_setup(int dev) {
+// Per device, with that device current: resolve the scratch array's device
+// address (its host-side name is only a stand-in) and the sizes the tile
+// plan needs.  Allocates nothing.  A failure is returned and not latched, so
+// a later call on the device tries again (a transient error, or a first call
+// issued inside a stream capture, does not poison the device for good).
+cudaError_t noalloc_setup(int dev, const NoAllocSetup** out) {
   NoAllocSetup& st = g_noalloc[dev];
-  void* ptr = nullptr;
-  st.err = cudaGetSymbolAddress(&ptr, g_noalloc_lookback);
-  if (st.err != cudaSuccess) return;
-  st.scratch = static_cast<unsigned*>(ptr);
-  st.err = cudaDeviceGetAttribute(&st.info.sms, cudaDevAttrMultiProcessorCount, dev);
-  if (st.err != cudaSuccess) return;
-  st.info.layout_blocks_per_sm = layout_blocks_per_sm();
+  std::lock_guard<std::mutex> lk(st.mu);
+  if (!st.done) {
+    void* ptr = nullptr;
+    cudaError_t err = cudaGetSymbolAddress(&ptr, g_noalloc_lookback);
+    if (err != cudaSuccess) return err;
+    DeviceInfo info;
+    err = cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    info.layout_blocks_per_sm = layout_blocks_per_sm();
+    st.scratch = static_cast<unsigned*>(ptr);
+    st.info = info;
+    st.done = true;
+  }
+  *out = &st;
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -694,9 +704,10 @@ cudaError_t launch_layout_noalloc(const int32_t* topk_idx, int s, int e, int k, 
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::call_once(g_noalloc[dev].once, noalloc_setup, dev);
-  const NoAllocSetup& setup = g_noalloc[dev];
-  if (setup.err != cudaSuccess) return setup.err;
+  const NoAllocSetup* ps = nullptr;
+  err = noalloc_setup(dev, &ps);
+  if (err != cudaSuccess) return err;
+  const NoAllocSetup& setup = *ps;
 
   const LayoutPlan plan = plan_layout(s, e, setup.info);
   const long long words = (long long)(lookback_bytes(plan, e) / sizeof(unsigned));

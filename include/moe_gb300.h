@@ -198,14 +198,16 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int
  * [R] int32 (ignored when R = 0).  device_status (nullable): an int32 in
  * device memory that gets MOE_DEV_* bits OR-ed in (the caller zeroes it).
  * It calls no allocating routine.  The kernel's scratch (its look-back
- * words, tiles x e of them) is a fixed library array of 16384 32-bit words (64 KB)
- * per device, held until the process exits.  The tile plan keeps tiles x e
- * within 16384 for every accepted size; a plan that would need more returns
+ * words: tiles x (e rounded up to a multiple of 4) of them) is a fixed
+ * library array of 16384 32-bit words (64 KB) per device, held until the
+ * process exits.  The tile plan keeps that product within 16384 for every
+ * accepted size; a plan that would need more returns
  * MOE_ERR_UNSUPPORTED (use moe_dispatch_layout) instead of overrunning it.  Every call shares
  * that array and clears the part it uses, so calls whose work overlaps on the
  * GPU (unordered streams) race; order them.  The first call on each device
  * resolves the array's device address (one-time set-up); make that first call
- * before any stream capture.  The dispatch / combine calls still take a
+ * before any stream capture.  A set-up that fails is not remembered: the
+ * call returns the error and the next call on that device tries again.  The dispatch / combine calls still take a
  * handle, so this suits callers that consume the layout arrays themselves. */
 moe_status moe_dispatch_layout_noalloc(const int32_t* topk_idx, int s, int e, int k, int capacity,
                                        int num_virtual_ranks, int32_t* idx_out, int32_t* loc,

@@ -31,13 +31,12 @@ def bf16_ulp(v: np.ndarray) -> np.ndarray:
 def combine_scale(row: np.ndarray, gate: np.ndarray | None, y: np.ndarray) -> np.ndarray:
     """sum over kept routes of |gate| * |y[row]|, float64 [s, m]."""
     s, k = row.shape
-    ya = np.abs(as_f64(y))
     out = np.zeros((s, y.shape[1]))
     for j in range(k):
         r = row[:, j]
         keep = r >= 0
         g = np.ones(s) if gate is None else np.abs(gate[:, j].astype(np.float64))
-        out[keep] += g[keep, None] * ya[r[keep]]
+        out[keep] += g[keep, None] * np.abs(as_f64(y[r[keep]]))
     return out
 
 
@@ -45,12 +44,11 @@ def dot_scale(row: np.ndarray, dout: np.ndarray, y: np.ndarray) -> np.ndarray:
     """sum_m |dout[t,m] * y[row[t,j],m]|, float64 [s, k]."""
     s, k = row.shape
     da = np.abs(as_f64(dout))
-    ya = np.abs(as_f64(y))
     out = np.zeros((s, k))
     for j in range(k):
         r = row[:, j]
         keep = r >= 0
-        out[keep, j] = np.sum(da[keep] * ya[r[keep]], axis=1)
+        out[keep, j] = np.sum(da[keep] * np.abs(as_f64(y[r[keep]])), axis=1)
     return out
 
 
@@ -77,20 +75,32 @@ def gate_bwd_scale(idx: np.ndarray, gate: np.ndarray, dgate_scale: np.ndarray, e
     return fac * (dg + c)
 
 
-def assert_close(gpu: np.ndarray, ora: np.ndarray, scale: np.ndarray | None, what: str):
-    """Apply the rule for the array's type (uint16 = bf16 bits, float32)."""
+def assert_close(gpu: np.ndarray, ora: np.ndarray, scale, what: str):
+    """Apply the rule for the array's type (uint16 = bf16 bits, float32).
+
+    ``scale`` is the float64 condition scale of every element, or a function
+    of an array of first-axis indices returning the scale of those rows
+    only: then it is evaluated just for the rows that are not bit-identical
+    (the same bar, without building the scale of a multi-GB array whose
+    elements mostly match exactly)."""
     assert gpu.shape == ora.shape, f"{what}: shape {gpu.shape} vs {ora.shape}"
-    g, o = as_f64(gpu), as_f64(ora)
     if np.array_equal(gpu, ora):
         return
+    rows = None
+    if callable(scale):
+        diff = gpu != ora
+        rows = np.unique(np.nonzero(diff.reshape(diff.shape[0], -1))[0])
+        gpu, ora, scale = gpu[rows], ora[rows], (None if ora.dtype == np.uint16 else scale(rows))
+    g, o = as_f64(gpu), as_f64(ora)
     if ora.dtype == np.uint16:
         bad = ~(np.abs(g - o) <= bf16_ulp(o))
     else:
         assert scale is not None
         bad = ~(np.abs(g - o) <= REL_F32 * scale + 1e-30)
     if bad.any():
-        i = tuple(np.argwhere(bad)[0])
-        raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance; first at {i}: "
+        i = tuple(int(v) for v in np.argwhere(bad)[0])
+        at = i if rows is None else (int(rows[i[0]]),) + i[1:]
+        raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance; first at {at}: "
                              f"gpu {g[i]!r} oracle {o[i]!r}")
 
 

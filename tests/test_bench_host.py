@@ -65,7 +65,8 @@ def test_max_over_ranks_with_two_gloo_processes():
 
 def test_reference_arm_prints_only_on_rank_zero():
     env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
-    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1",
                         "--warmup", "1", "--workload", "tiny-capacity", "--ref-seconds", "1"],
                        capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
@@ -94,3 +95,28 @@ def test_traffic_record_is_per_workload_and_tied_to_the_source(tmp_path):
     # the committed record file parses and keys by workload
     committed = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
     assert "mixtral-dropless" in committed and "combine_bwd" in committed["mixtral-dropless"]
+
+
+def test_gpus_flag_must_match_the_process_count():
+    """--gpus N under a launcher that started a different number of ranks is
+    refused instead of silently reporting one replica."""
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "1", "--workload", "tiny-capacity", "--ref-seconds", "1"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode != 0 and "WORLD_SIZE" in r.stderr
+
+
+def test_gpus_flag_starts_one_process_per_gpu():
+    """Without a launcher, --gpus 2 starts two ranks itself (torch.distributed.run
+    on 127.0.0.1); the reference arm then prints one line, from rank 0."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR",
+                                                           "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "1", "--workload", "tiny-capacity", "--ref-seconds", "1"],
+                       capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2

@@ -2,8 +2,8 @@
 
 Reduced sizes run every output of every op element by element, at sizes that
 still span several layout tiles (256 tokens each) and end in a ragged tail.
-The full workload shapes compare every integer output and the gates in
-full, and sampled payload rows / tokens for the floating outputs.
+The full workload shapes are compared in full as well: every integer
+output, gate, dispatched row and every element of the floating outputs.
 """
 import numpy as np
 import pytest
@@ -70,6 +70,45 @@ def test_send_slots_parity(case):
     plain = B.moe_dispatch_layout_ex(to_dev(idx, DEV), case["e"], case["capacity"], case["R"], case["priority"])
     with pytest.raises(B.MoEError):
         plain.rank_slot()
+
+
+def test_tiny_capacity_as_specified_with_the_affine_expert():
+    """The tiny capacity workload exactly as specified, forward only: seed-0
+    logits [256, 8] and x [256, 128] fp32, capacity ceil(1.25*256*2/8) = 80
+    in token order with drops, and the expert output y = 2*X + 1 elementwise
+    on the dispatched buffer (formed in fp32 on the host from the oracle's
+    X, which the GPU's X equals bit for bit).  Gate, layout, dispatch and
+    combine against the oracle, element by element; the combine on the
+    GPU's own gates, fed to both sides."""
+    w = W.WORKLOADS["tiny-capacity"]
+    assert (w.s, w.m, w.e, w.k, w.seed) == (256, 128, 8, 2, 0)
+    assert w.capacity == B.moe_capacity(1.25, w.s, w.k, w.e) == 80
+    inp = W.make_inputs(w, with_grad=False)
+    logits, x = inp["logits"].numpy(), inp["x"].numpy()
+    idx, gate = B.moe_topk_gate(inp["logits"].to(DEV), w.k, w.renorm)
+    oi, og = oracle.topk_gate(logits, w.k, w.renorm)
+    np.testing.assert_array_equal(bits(idx), oi)
+    T.assert_gates_close(bits(gate), og)
+
+    h = B.moe_dispatch_layout(idx, w.e, w.capacity)
+    L = oracle.layout(oi, w.e, w.capacity)
+    check_layout(h, L, oi)
+    assert L["drop"].any(), "capacity 80 drops routes on this workload"
+    X = B.moe_dispatch(h, inp["x"].to(DEV))
+    OX = oracle.dispatch(L["row"], x, L["rows"])
+    np.testing.assert_array_equal(bits(X), OX, err_msg="dispatch")
+
+    y = np.float32(2.0) * OX + np.float32(1.0)  # the expert, on every slot (unused slots hold 1, never read)
+    g = bits(gate)
+    out = B.moe_combine(h, to_dev(y, DEV), gate)
+    ref = oracle.combine(L["row"], g, y)
+    T.assert_close(bits(out), ref, T.combine_scale(L["row"], g, y), "combine")
+    # what the affine expert gives: out[t] = (sum of kept gates) * (2 x[t] + 1)
+    kept_g = np.where(L["row"] >= 0, g.astype(np.float64), 0.0).sum(axis=1, keepdims=True)
+    expect = kept_g * (2.0 * x.astype(np.float64) + 1.0)
+    assert np.all(np.abs(bits(out) - expect) <= 1e-6 * np.abs(kept_g) * np.abs(2.0 * x + 1.0) + 1e-30)
+    assert np.all(bits(out)[(L["row"] < 0).all(axis=1)] == 0), "fully dropped tokens give zeros"
+    assert h.status() == 0
 
 
 def test_tiny_capacity_full_softmax_gates():
@@ -169,15 +208,14 @@ def test_gate_backward_parity(name, renorm):
 
 # ------------------------------------------------------------- full sizes --
 
-def _sample_rows(n, count, gen):
-    return torch.randperm(n, generator=gen)[:count].sort().values.numpy()
-
-
 @pytest.mark.parametrize("name", ["tiny-capacity", "mixtral-dropless", "fine-grained-skewed",
                                   "diffusiongemma-replay", "gshard-capacity"])
 def test_full_size_workloads(name):
     """The exact workload shapes, in the launch configuration the benchmark
-    times: integer outputs and gates in full, payload outputs on samples."""
+    times, compared in full: every index, count, gate, dispatched row (zero
+    tails included), combined token, dY row, dgate and dx token against the
+    oracle on the same inputs (DeepSpeed #8195, Testing: sparse against
+    dense, element by element)."""
     w = W.WORKLOADS[name]
     inp = W.make_inputs(w, device=DEV)
     logits = inp["logits"]
@@ -190,6 +228,7 @@ def test_full_size_workloads(name):
     L = oracle.layout(oi, w.e, w.capacity, w.R)
     check_layout(h, L, oi)
     gd = to_dev(og, DEV)
+    row = L["row"]
 
     X = B.moe_dispatch(h, inp["x"])
     out = B.moe_combine(h, inp["y"], gd)
@@ -198,45 +237,19 @@ def test_full_size_workloads(name):
     torch.cuda.synchronize()
     assert h.status() == 0
 
-    gen = torch.Generator().manual_seed(123)
-    row = L["row"]
-    # dispatch: sampled destination rows, including zero-tail rows in capacity mode
-    rs = _sample_rows(L["rows"], 512, gen)
+    # dispatch: every row, bit-exact (capacity zero tails included)
     xb = bits(inp["x"])
-    owner = np.full(L["rows"], -1, np.int64)
-    kept = row >= 0
-    owner[row[kept]] = np.nonzero(kept)[0]
-    Xs = bits(X[torch.from_numpy(rs).to(DEV)])
-    for i, r in enumerate(rs):
-        if owner[r] >= 0:
-            np.testing.assert_array_equal(Xs[i], xb[owner[r]])
-        else:
-            assert not Xs[i].any(), "unowned rows are zero"
-
-    # combine / combine_bwd / dispatch_bwd on sampled tokens through the oracle
-    ts = _sample_rows(w.s, 256, gen)
-    rsub = row[ts]
-    uniq = np.unique(rsub[rsub >= 0])
-    remap = np.full(L["rows"], -1, np.int64)
-    remap[uniq] = np.arange(len(uniq))
-    rloc = np.where(rsub >= 0, remap[np.maximum(rsub, 0)], -1).astype(np.int32)
-    ysub = bits(inp["y"][torch.from_numpy(uniq).to(DEV)])
-    dsub = bits(inp["dout"][torch.from_numpy(ts).to(DEV)])
-    gsub = np.ascontiguousarray(og[ts])
-    tsd = torch.from_numpy(ts).to(DEV)
-    T.assert_close(bits(out[tsd]), oracle.combine(rloc, gsub, ysub), T.combine_scale(rloc, gsub, ysub), "combine")
-    OdY, Odg = oracle.combine_bwd(rloc, gsub, dsub, ysub)
-    T.assert_close(bits(dgate)[ts], Odg, T.dot_scale(rloc, dsub, ysub), "dgate")
-    dYs = bits(dY[torch.from_numpy(uniq).to(DEV)])
-    T.assert_close(dYs, OdY, np.abs(T.as_f64(OdY)), "dY")
-    T.assert_close(bits(dx[tsd]), oracle.dispatch_bwd(rloc, ysub),
-                   T.combine_scale(rloc, None, ysub), "dispatch_bwd")
-    if w.capacity:
-        # zero tail of dY
-        unowned = np.nonzero(owner < 0)[0]
-        if len(unowned):
-            pick = unowned[_sample_rows(len(unowned), 64, gen)]
-            assert not bits(dY[torch.from_numpy(pick).to(DEV)]).any()
+    np.testing.assert_array_equal(bits(X), oracle.dispatch(row, xb, L["rows"]), err_msg="dispatch")
+    del X, xb
+    yb, db = bits(inp["y"]), bits(inp["dout"])
+    T.assert_close(bits(out), oracle.combine(row, og, yb), lambda ts: T.combine_scale(row[ts], og[ts], yb), "combine")
+    del out
+    OdY, Odg = oracle.combine_bwd(row, og, db, yb)
+    T.assert_close(bits(dY), OdY, lambda rs: np.abs(T.as_f64(OdY[rs])), "dY")
+    T.assert_close(bits(dgate), Odg, lambda ts: T.dot_scale(row[ts], db[ts], yb), "dgate")
+    del dY, OdY
+    T.assert_close(bits(dx), oracle.dispatch_bwd(row, yb), lambda ts: T.combine_scale(row[ts], None, yb),
+                   "dispatch_bwd")
     h.destroy()
 
 

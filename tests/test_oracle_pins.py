@@ -428,6 +428,32 @@ def test_identity_expert_returns_input():
             np.testing.assert_array_equal(out, x)
 
 
+def test_tiny_workload_with_the_affine_expert():
+    """The tiny capacity workload as specified (seed 0, s=256, m=128, e=8,
+    k=2, fp32, capacity 80, token order with drops) with its expert
+    y = 2*X + 1 on the dispatched buffer: the combine must give
+    (sum of the token's kept gates) * (2 x + 1) -- exactly 2 x + 1 (to fp32
+    rounding) where both routes are kept, zero where both are dropped.  A
+    dropped gate still added, a kept one skipped, or the wrong row read
+    fails it."""
+    w = W.WORKLOADS["tiny-capacity"]
+    inp = W.make_inputs(w, with_grad=False)
+    logits, x = inp["logits"].numpy(), inp["x"].numpy()
+    idx, gate = oracle.topk_gate(logits, w.k, w.renorm)
+    L = oracle.layout(idx, w.e, w.capacity)
+    assert L["rows"] == 640 and L["drop"].any() and not L["drop"].all()
+    X = oracle.dispatch(L["row"], x, L["rows"])
+    y = np.float32(2.0) * X + np.float32(1.0)
+    out = oracle.combine(L["row"], gate, y).astype(np.float64)
+    kept = L["row"] >= 0
+    kg = np.where(kept, gate.astype(np.float64), 0.0).sum(axis=1, keepdims=True)
+    affine = 2.0 * x.astype(np.float64) + 1.0
+    assert np.all(np.abs(out - kg * affine) <= 4 * 2.0**-24 * np.abs(kg) * np.abs(affine) + 1e-30)
+    both = kept.all(axis=1)
+    assert both.any() and np.all(np.abs(out[both] - affine[both]) <= 1e-6 * np.abs(affine[both]))
+    assert np.all(out[~kept.any(axis=1)] == 0)
+
+
 def test_fully_dropped_token_gives_zero():
     idx = np.array([[0, 1], [0, 1], [0, 1]], np.int32)
     L = oracle.layout(idx, e=2, capacity=1)

@@ -10,9 +10,11 @@ already run; it passes alone in a fresh process as well.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from combine_moe_topk_gb300 import binding as B
 from combine_moe_topk_gb300 import workloads as W
 
@@ -64,6 +66,16 @@ CASES = [
 ]
 
 
+def assert_oracle_layout(got, idx, e, capacity, R):
+    """The same arrays against the CPU oracle's layout of the same routes."""
+    ids = idx.cpu().numpy()
+    L = oracle.layout(ids, e, capacity, R)
+    np.testing.assert_array_equal(got["idx"].cpu().numpy(), ids, err_msg="idx")
+    for name in ("loc", "row", "drop", "raw_counts", "counts", "offsets") + (("token_in_rank", "rank_counts")
+                                                                              if R else ()):
+        np.testing.assert_array_equal(got[name].cpu().numpy(), L[name], err_msg=name)
+
+
 def test_noalloc_layout_matches_handle_layout_on_consecutive_calls():
     for w in CASES:
         logits = W.make_logits(w, device=DEV)
@@ -72,6 +84,7 @@ def test_noalloc_layout_matches_handle_layout_on_consecutive_calls():
         got = layout_noalloc(idx, w.e, w.capacity, w.R)
         torch.cuda.synchronize()
         assert_same_layout(got, h)
+        assert_oracle_layout(got, idx, w.e, w.capacity, w.R)
         assert h.status() == 0
         h.destroy()
 
