@@ -50,9 +50,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "dispatch+combine HBM GB/s and routed tokens/s on 1 GB300 vs HBM peak"
 DEFAULT_WORKLOAD = "fine-grained-skewed"  # the largest workload: s=16384, m=4096, e=128, k=8
-OPS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "topk_gate_bwd", "dispatch_bwd"]
+OPS = ["topk_gate", "layout", "dispatch", "combine", "combine_gate_bwd", "dispatch_bwd"]
 KERNEL_FILE = {"topk_gate": "gate.cu", "layout": "layout.cu", "dispatch": "dispatch.cu", "combine": "combine.cu",
-               "combine_bwd": "combine.cu", "topk_gate_bwd": "gate.cu", "dispatch_bwd": "combine.cu"}
+               "combine_bwd": "combine.cu", "topk_gate_bwd": ("gate.cu", "router_grad.cuh"),
+               "combine_gate_bwd": ("combine.cu", "router_grad.cuh"), "dispatch_bwd": "combine.cu"}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024  # GB300 L2 (a flush writes twice this)
@@ -69,7 +70,7 @@ def step_bytes(w, kept: int, u: int) -> dict:
     x = s * m * b
     routes = s * k
     meta_r = routes * 4         # reading row[] (or idx)
-    return {
+    out = {
         "topk_gate": s * e * 4 + routes * 8,
         "layout": routes * 4 + routes * 13 + e * 12 + (s * w.R + w.R * 4 if w.R else 0),
         "dispatch": u * m * b + R + meta_r,
@@ -78,6 +79,15 @@ def step_bytes(w, kept: int, u: int) -> dict:
         "topk_gate_bwd": routes * 12 + s * e * 4 + (0 if w.renorm else s * e * 4),
         "dispatch_bwd": kept * m * b + x + meta_r,
     }
+    # fused: the combine backward's bytes, plus the expert ids and the router
+    # gradient written (and the logits without renorm); dgate is not re-read
+    out["combine_gate_bwd"] = out["combine_bwd"] + routes * 4 + s * e * 4 + (0 if w.renorm else s * e * 4)
+    return out
+
+
+def step_sum(nbytes: dict) -> int:
+    """Algorithmic bytes of one step: the ops the step runs."""
+    return sum(nbytes[op] for op in OPS)
 
 
 def payload_bytes(w, kept: int, u: int) -> dict:
@@ -107,10 +117,13 @@ def bf16_peak():
 
 
 def source_sha(op: str) -> str:
-    """Hash of the kernel source file of an op (ties a traffic record to it)."""
-    src = os.path.join(ROOT, "combine_moe_topk_gb300", "csrc", KERNEL_FILE[op])
-    with open(src, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the kernel source file(s) of an op (ties a traffic record to it)."""
+    files = KERNEL_FILE[op] if isinstance(KERNEL_FILE[op], tuple) else (KERNEL_FILE[op],)
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(ROOT, "combine_moe_topk_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_record(op: str, workload: str, path: str | None = None):
@@ -250,15 +263,12 @@ def run_ours(args, rank: int, world: int, dist):
         B.moe_combine(h, b["y"], b["gate"], b["out"])
         mark(3, 1)
         mark(4, 0)
-        B.moe_combine_bwd(h, b["dout"], b["gate"], b["y"], b["dY"], b["dgate"])
+        B.moe_combine_gate_bwd(h, b["dout"], b["gate"], b["y"], b["logits"], w.renorm, b["dY"], b["dgate"],
+                               b["dlogits"])
         mark(4, 1)
         mark(5, 0)
-        B.moe_topk_gate_bwd(None if w.renorm else b["logits"], b["idx"], b["gate"], b["dgate"], w.e, w.renorm,
-                            b["dlogits"])
-        mark(5, 1)
-        mark(6, 0)
         B.moe_dispatch_bwd(h, b["dY"], b["dx"])
-        mark(6, 1)
+        mark(5, 1)
         return h
 
     # kept routes / sending tokens for the byte model (outside any timing)
@@ -270,7 +280,7 @@ def run_ours(args, rank: int, world: int, dist):
     assert h.status() == 0, "device status after the first step"
     h.destroy()
     nbytes = step_bytes(w, kept, u)
-    step_total = sum(nbytes.values())
+    step_total = step_sum(nbytes)
 
     def barrier():
         if dist is not None:
@@ -379,7 +389,8 @@ def run_ours(args, rank: int, world: int, dist):
         "config": {
             "workload": w.name, "s": w.s, "m": w.m, "e": w.e, "k": w.k,
             "mode": f"capacity {w.capacity}" if w.capacity else "dropless", "virtual_ranks": w.R,
-            "step": "topk_gate+layout+dispatch+combine+combine_bwd+topk_gate_bwd+dispatch_bwd on the step's handle",
+            "step": "topk_gate+layout+dispatch+combine+combine_gate_bwd (combine backward with the gate backward "
+                    "fused in)+dispatch_bwd on the step's handle",
             "launch": launch_mode,
             "parallelism": "replicas" if world > 1 else "single GPU",
             "l2": (f"no flush: step working set {round(step_total / 1e6)} MB algorithmic, over twice the 129 MB L2"
@@ -460,7 +471,7 @@ def time_loop(run, n: int, flush=None) -> float:
 
 def small_working_set(w) -> bool:
     """Whether a step's inputs and outputs would stay in L2 between steps."""
-    return sum(step_bytes(w, w.s * w.k, w.s).values()) < 2 * L2_BYTES
+    return step_sum(step_bytes(w, w.s * w.k, w.s)) < 2 * L2_BYTES
 
 
 def run_dispatch_combine(w, S, dev, K: int):
@@ -522,9 +533,8 @@ def run_replay_step(w, S, dev, K: int):
         B.moe_topk_gate(S["logits"], w.k, w.renorm, S["idx"], S["gate"])
         B.moe_dispatch(h, S["x"], S["X"])
         B.moe_combine(h, S["y"], S["gate"], S["out"])
-        B.moe_combine_bwd(h, S["dout"], S["gate"], S["y"], S["dY"], S["dgate"])
-        B.moe_topk_gate_bwd(None if w.renorm else S["logits"], S["idx"], S["gate"], S["dgate"], w.e, w.renorm,
-                            S["dlogits"])
+        B.moe_combine_gate_bwd(h, S["dout"], S["gate"], S["y"], S["logits"], w.renorm, S["dY"], S["dgate"],
+                               S["dlogits"])
         B.moe_dispatch_bwd(h, S["dY"], S["dx"])
 
     how = "graph of the step on a saved handle (gate recomputed, no layout)"
@@ -736,9 +746,9 @@ def cpu_baseline(w, args):
     while not one or (time.perf_counter() - t_start < args.cpu_seconds / 2 and len(one) < 20):
         one.append(oracle_step(ws, inp)[0])
     per1 = statistics.median(one)
-    return {"value": round(sum(nbytes.values()) / per / 1e9, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+    return {"value": round(step_sum(nbytes) / per / 1e9, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{len(times)} full steps of {w.name} (s={w.s}, m={w.m}), median {per:.3f} s each",
-            "single_core": {"value": round(sum(nbytes.values()) / per1 / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "single_core": {"value": round(step_sum(nbytes) / per1 / 1e9, 3), "unit": "GB/s", "cores": 1,
                             "sample": f"{len(one)} full steps, median {per1:.3f} s each"}}
 
 
@@ -769,7 +779,7 @@ def run_reference(args, rank: int, world: int):
         dt, nbytes = oracle_step(ws, inp)
         times.append(dt)
     per = sum(times) / len(times)
-    value = sum(nbytes.values()) / per / 1e9
+    value = step_sum(nbytes) / per / 1e9
     sample = f"{ws.s} of {w.s} tokens of {w.name} (m={w.m}) per step"
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,

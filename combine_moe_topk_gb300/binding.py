@@ -26,7 +26,7 @@ STATUS = {
 MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
 MOE_DEV_NONFINITE, MOE_DEV_BAD_ROUTE, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4
 KERNELS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd", "topk_gate_bwd",
-           "grouped_gemm", "dispatch_gemm", "rank_slots"]
+           "grouped_gemm", "dispatch_gemm", "rank_slots", "combine_gate_bwd"]
 KERNEL_ID = {n: i for i, n in enumerate(KERNELS)}
 
 # every entry point the header declares (checked by the CPU test-suite)
@@ -35,7 +35,7 @@ EXPORTS = [
     "moe_dispatch_bwd", "moe_handle_info", "moe_handle_status", "moe_handle_destroy", "moe_capacity",
     "moe_status_string", "moe_last_error", "moe_launch_count", "moe_debug_hold_layout_tile",
     "moe_dispatch_layout_noalloc", "moe_topk_gate_bwd", "moe_dispatch_layout_ex", "moe_grouped_gemm",
-    "moe_dispatch_grouped_gemm",
+    "moe_dispatch_grouped_gemm", "moe_combine_gate_bwd",
 ]
 
 
@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
             "moe_dispatch": [P, I, I, I, I, P, P, P],
             "moe_combine": [P, I, I, I, I, P, P, P, P],
             "moe_combine_bwd": [P, I, I, I, I, P, P, P, P, P, P],
+            "moe_combine_gate_bwd": [P, I, I, I, I, P, P, P, P, I, P, P, P, P],
             "moe_dispatch_bwd": [P, I, I, I, I, P, P, P],
             "moe_grouped_gemm": [P, I, I, I, P, P, P, P],
             "moe_dispatch_grouped_gemm": [P, I, I, I, I, P, P, P, P],
@@ -350,6 +351,36 @@ def moe_combine_bwd(h: Handle, dout: torch.Tensor, gate: torch.Tensor, y: torch.
                                _ptr(dgate), _stream(dout.device))
     _check(rc, "moe_combine_bwd")
     return dY, dgate
+
+
+def moe_combine_gate_bwd(h: Handle, dout: torch.Tensor, gate: torch.Tensor, y: torch.Tensor,
+                         logits: torch.Tensor | None, renorm: int = 1, dY: torch.Tensor | None = None,
+                         dgate: torch.Tensor | None = None, dlogits: torch.Tensor | None = None):
+    """The combine backward and the top-k gate backward in one kernel:
+    (dY [rows,m], dgate f32 [s,k], dlogits f32 [s,e]); logits f32 [s,e] only
+    needed when renorm = 0."""
+    s, m = _rows2(dout, "dout")
+    rows, my = _rows2(y, "y")
+    if my != m or y.dtype != dout.dtype:
+        raise MoEError(1, "moe_combine_gate_bwd", "dout and y disagree in width or dtype")
+    if gate.dtype != torch.float32 or gate.shape != (h.s, h.k):
+        raise MoEError(1, "moe_combine_gate_bwd", "gate must be float32 [s, k]")
+    if not renorm and (logits is None or logits.dtype != torch.float32 or logits.shape != (h.s, h.e)):
+        raise MoEError(1, "moe_combine_gate_bwd", "logits must be float32 [s, e] when renorm = 0")
+    if dY is None:
+        dY = torch.empty(rows, m, dtype=dout.dtype, device=dout.device)
+    if dgate is None:
+        dgate = torch.empty(h.s, h.k, dtype=torch.float32, device=dout.device)
+    if dlogits is None:
+        dlogits = torch.empty(h.s, h.e, dtype=torch.float32, device=dout.device)
+    if dY.shape != (rows, m) or dY.dtype != dout.dtype or dgate.shape != (h.s, h.k) or \
+            dlogits.shape != (h.s, h.e) or dlogits.dtype != torch.float32:
+        raise MoEError(1, "moe_combine_gate_bwd", "output shapes")
+    rc = lib().moe_combine_gate_bwd(h.raw, s, rows, m, _dtype(dout), _ptr(dout), _ptr(gate), _ptr(y),
+                                    _ptr(None if renorm else logits), int(renorm), _ptr(dY), _ptr(dgate),
+                                    _ptr(dlogits), _stream(dout.device))
+    _check(rc, "moe_combine_gate_bwd")
+    return dY, dgate, dlogits
 
 
 def moe_dispatch_bwd(h: Handle, dX: torch.Tensor, dx: torch.Tensor | None = None) -> torch.Tensor:

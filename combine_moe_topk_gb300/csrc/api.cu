@@ -588,6 +588,50 @@ moe_status moe_combine_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype
   return MOE_OK;
 }
 
+moe_status moe_combine_gate_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype,
+                                const void* dout, const float* gate, const void* y,
+                                const float* logits, int renorm, void* dY, float* dgate,
+                                float* dlogits, void* stream) {
+  MOE_TRY(live_handle(h));
+  MOE_TRY(check_shape(h, s, rows));
+  long long rb = 0;
+  MOE_TRY(check_payload(dtype, m, &rb));
+  if (renorm != 0 && renorm != 1) return fail(MOE_ERR_INVALID_ARG, "renorm must be 0 or 1");
+  if ((long long)s * h->e > 2147483647LL) return fail(MOE_ERR_INVALID_ARG, "s*e must be < 2^31");
+  if (s == 0 && rows == 0) return MOE_OK;
+  if (s > 0) {
+    MOE_TRY(check_ptr(dout, "dout"));
+    MOE_TRY(check_ptr(gate, "gate"));
+    MOE_TRY(check_ptr(dgate, "dgate"));
+    MOE_TRY(check_ptr(dlogits, "dlogits"));
+    if (!renorm) MOE_TRY(check_ptr(logits, "logits"));
+  }
+  if (rows > 0) {
+    MOE_TRY(check_ptr(y, "y"));
+    MOE_TRY(check_ptr(dY, "dY"));
+  }
+  MOE_TRY(handle_device(h));
+  const void* ptrs[7] = {dout, gate, y, dY, dgate, dlogits, renorm ? nullptr : logits};
+  const char* names[7] = {"dout", "gate", "y", "dY", "dgate", "dlogits", "logits"};
+  for (int i = 0; i < 7; ++i) MOE_TRY(check_device_ptr(ptrs[i], names[i], h->device));
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(h->device, &di));
+  cudaError_t err;
+  if (s == 0) {  // nothing to route: only the zero rows of dY
+    err = moe::launch_combine_bwd(h->out.row, h->out.counts, h->out.offsets, h->rows, h->zero_fill, gate,
+                                  s, h->k, h->e, m, dtype == MOE_F32 ? 0 : 1, dout, y, dY, dgate,
+                                  h->capacity > 0, *di, static_cast<cudaStream_t>(stream));
+  } else {
+    err = moe::launch_combine_bwd(h->out.row, h->out.counts, h->out.offsets, h->rows, h->zero_fill, gate,
+                                  s, h->k, h->e, m, dtype == MOE_F32 ? 0 : 1, dout, y, dY, dgate,
+                                  h->capacity > 0, *di, static_cast<cudaStream_t>(stream), h->out.idx,
+                                  renorm ? nullptr : logits, renorm, dlogits);
+  }
+  if (err != cudaSuccess) return cuda_fail(err, "combine_gate_bwd launch");
+  g_launches[s == 0 ? MOE_KERNEL_COMBINE_BWD : MOE_KERNEL_COMBINE_GATE_BWD]++;
+  return MOE_OK;
+}
+
 moe_status moe_dispatch_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype, const void* dX,
                             void* dx, void* stream) {
   MOE_TRY(live_handle(h));

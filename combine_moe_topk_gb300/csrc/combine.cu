@@ -19,6 +19,7 @@
 // partial sums in warp order: fixed for a given batch shape.
 #include "common.cuh"
 #include "internal.h"
+#include "router_grad.cuh"
 
 namespace moe {
 
@@ -46,6 +47,26 @@ constexpr int kThreads = 256;
 #ifndef MOE_CMB_COMPACT
 #define MOE_CMB_COMPACT 1
 #endif
+
+// The gate backward fused into the combine backward: once a token's k gate
+// gradients are reduced, the warp that holds them writes the token's router
+// logits' gradient (router_grad_token, the gate backward kernel's own
+// arithmetic).  idx = the routes' expert ids; logits only without renorm.
+struct RouterGrad {
+  const int32_t* idx;
+  const float* logits;
+  int renorm;
+  float* dlogits;
+};
+constexpr int kRgEpl = 8;  // experts per lane covering e <= 256
+
+// Out of line, so that the router gradient's registers are allocated on
+// their own and do not change the payload loop's allocation (and hence the
+// combine backward's occupancy) in the kernels that call it.
+__device__ __noinline__ void router_grad_call(int t, int lane, int k, int e, const RouterGrad rg, int ij,
+                                              float gj, float dgj) {
+  router_grad_token<kRgEpl>(t, lane, k, e, rg.renorm, ij, gj, dgj, rg.logits, rg.dlogits);
+}
 
 // Route rows and gates of token t, broadcast from lanes 0..k-1.
 template <int KMAX, bool WEIGHTED>
@@ -215,13 +236,13 @@ __global__ void __launch_bounds__(kThreads) combine_compact_kernel(const int32_t
 // row's vectors [w*chunk, (w+1)*chunk); the per-route dots are reduced across
 // the warp's lanes (butterfly), then across the group's warps in warp order
 // through shared memory.  G > 1 gives short batches more warps in flight.
-template <typename T, int KMAX, int UNR, int G>
-__global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
+template <typename T, int KMAX, int UNR, int G, bool RG>
+__device__ __forceinline__ void combine_bwd_body(
     const int32_t* __restrict__ row, const int32_t* __restrict__ counts,
     const int32_t* __restrict__ offsets, long long rows, int zero_fill,
     const float* __restrict__ gate, int s, int k, int e, int nvec, int chunk,
     const uint4* __restrict__ dout, const uint4* __restrict__ y, uint4* __restrict__ dY,
-    float* __restrict__ dgate) {
+    float* __restrict__ dgate, const RouterGrad& rg) {
   constexpr int N = Vec<T>::N;
   constexpr int WPB = kThreads / 32;  // warps per block
   constexpr int TPB = WPB / G;        // tokens per block and round
@@ -240,6 +261,13 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     float dot[KMAX];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) dot[j] = 0.0f;
+    // the router gradient's own copy of the route ids and gates (lanes < k)
+    int rg_id = -1;
+    float rg_g = 0.f;
+    if (RG && live && (G == 1 || w == 0) && lane < k) {
+      rg_id = __ldg(rg.idx + (size_t)t * k + lane);
+      rg_g = __ldg(gate + (size_t)t * k + lane);
+    }
     if (live) {
       token_routes<KMAX, true>(row, gate, t, k, lane, r, g);
       const uint4* d = dout + (size_t)t * nvec;
@@ -294,15 +322,17 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     }
     if (G == 1) {
       if (live && lane < k) dgate[(size_t)t * k + lane] = mine;
+      if (RG && live) router_grad_call(t, lane, k, e, rg, rg_id, rg_g, lane < k ? mine : 0.f);
     } else {
       if (lane < KMAX) s_dot[warp][lane] = mine;
       __syncthreads();
+      float sum = 0.0f;
       if (live && w == 0 && lane < k) {
-        float sum = 0.0f;
 #pragma unroll
         for (int q = 0; q < G; ++q) sum += s_dot[gi * G + q][lane];
         dgate[(size_t)t * k + lane] = sum;
       }
+      if (RG && live && w == 0) router_grad_call(t, lane, k, e, rg, rg_id, rg_g, sum);
       __syncthreads();  // s_dot is rewritten next round
     }
   }
@@ -321,19 +351,42 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
   }
 }
 
+#define MOE_CBWD_PARAMS                                                                         \
+  const int32_t *__restrict__ row, const int32_t *__restrict__ counts,                            \
+      const int32_t *__restrict__ offsets, long long rows, int zero_fill,                         \
+      const float *__restrict__ gate, int s, int k, int e, int nvec, int chunk,                   \
+      const uint4 *__restrict__ dout, const uint4 *__restrict__ y, uint4 *__restrict__ dY,        \
+      float *__restrict__ dgate, const RouterGrad rg
+#define MOE_CBWD_ARGS row, counts, offsets, rows, zero_fill, gate, s, k, e, nvec, chunk, dout, y, dY, dgate, rg
+
+template <typename T, int KMAX, int UNR, int G>
+__global__ void __launch_bounds__(kThreads) combine_bwd_kernel(MOE_CBWD_PARAMS) {
+  combine_bwd_body<T, KMAX, UNR, G, false>(MOE_CBWD_ARGS);
+}
+
+// The combine backward with the gate backward fused in: held to the plain
+// kernel's two blocks per SM (128 registers) for up to 8 routes, so the
+// fusion does not cost the payload loop its occupancy.
+template <typename T, int KMAX, int UNR, int G>
+__global__ void __launch_bounds__(kThreads, KMAX <= 8 ? 2 : 1) combine_gate_bwd_kernel(MOE_CBWD_PARAMS) {
+  combine_bwd_body<T, KMAX, UNR, G, true>(MOE_CBWD_ARGS);
+}
+#undef MOE_CBWD_PARAMS
+#undef MOE_CBWD_ARGS
+
 // Combine backward for capacity layouts (routes may be dropped), G = 1:
 // kept routes compacted onto lanes in route order and taken KC per round;
 // each round walks the row (dout re-read only when a token keeps more than
 // KC routes), writes dY for its routes and reduces their dots to dgate.
 // Per lane the dot of a route sums the same vectors in the same order as
 // combine_bwd_kernel<..., G = 1>, so dgate and dY are the same bits.
-template <typename T, int KC, int UNR>
-__global__ void __launch_bounds__(kThreads) combine_bwd_compact_kernel(
+template <typename T, int KC, int UNR, bool RG>
+__device__ __forceinline__ void combine_bwd_compact_body(
     const int32_t* __restrict__ row, const int32_t* __restrict__ counts,
     const int32_t* __restrict__ offsets, long long rows, int zero_fill,
     const float* __restrict__ gate, int s, int k, int e, int nvec,
     const uint4* __restrict__ dout, const uint4* __restrict__ y, uint4* __restrict__ dY,
-    float* __restrict__ dgate) {
+    float* __restrict__ dgate, const RouterGrad& rg) {
   constexpr int N = Vec<T>::N;
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
@@ -346,6 +399,8 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_compact_kernel(
     unsigned kept = __ballot_sync(0xffffffffu, rl >= 0);
     const int nkept = __popc(kept);
     if (lane < k && rl < 0) dgate[(size_t)t * k + lane] = 0.f;  // a dropped route
+    const int rg_id = (RG && lane < k) ? __ldg(rg.idx + (size_t)t * k + lane) : -1;
+    float rg_dg = 0.f;  // this lane's route's gate gradient (0 when dropped)
     // lane c takes the c-th kept route, remembering its route index
     int cr = -1, cj = 0;
     float cg = 0.f;
@@ -420,8 +475,10 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_compact_kernel(
         for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
         const int jj = __shfl_sync(0xffffffffu, cj, (j0 + j) & 31);
         if (lane == 0 && j0 + j < nkept) dgate[(size_t)t * k + jj] = v;
+        if (RG && lane == jj && j0 + j < nkept) rg_dg = v;
       }
     }
+    if (RG) router_grad_call(t, lane, k, e, rg, rg_id, gl, rg_dg);
   }
   pdl_trigger_late();
 
@@ -434,6 +491,38 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_compact_kernel(
       for (int v = lane; v < nvec; v += 32) st_stream(dst + v, z);
     }
   }
+}
+
+#define MOE_CBWDC_PARAMS                                                                        \
+  const int32_t *__restrict__ row, const int32_t *__restrict__ counts,                            \
+      const int32_t *__restrict__ offsets, long long rows, int zero_fill,                         \
+      const float *__restrict__ gate, int s, int k, int e, int nvec,                              \
+      const uint4 *__restrict__ dout, const uint4 *__restrict__ y, uint4 *__restrict__ dY,        \
+      float *__restrict__ dgate, const RouterGrad rg
+#define MOE_CBWDC_ARGS row, counts, offsets, rows, zero_fill, gate, s, k, e, nvec, dout, y, dY, dgate, rg
+
+template <typename T, int KC, int UNR>
+__global__ void __launch_bounds__(kThreads) combine_bwd_compact_kernel(MOE_CBWDC_PARAMS) {
+  combine_bwd_compact_body<T, KC, UNR, false>(MOE_CBWDC_ARGS);
+}
+
+template <typename T, int KC, int UNR>
+__global__ void __launch_bounds__(kThreads, 2) combine_gate_bwd_compact_kernel(MOE_CBWDC_PARAMS) {
+  combine_bwd_compact_body<T, KC, UNR, true>(MOE_CBWDC_ARGS);
+}
+#undef MOE_CBWDC_PARAMS
+#undef MOE_CBWDC_ARGS
+
+// Kernel of a form: the plain combine backward, or with the gate backward fused.
+template <typename T, int KMAX, int UNR, int G, bool RG>
+constexpr auto cbwd_kernel() {
+  if constexpr (RG) return combine_gate_bwd_kernel<T, KMAX, UNR, G>;
+  else return combine_bwd_kernel<T, KMAX, UNR, G>;
+}
+template <typename T, int KC, int UNR, bool RG>
+constexpr auto cbwd_compact_kernel() {
+  if constexpr (RG) return combine_gate_bwd_compact_kernel<T, KC, UNR>;
+  else return combine_bwd_compact_kernel<T, KC, UNR>;
 }
 
 template <typename K>
@@ -498,47 +587,52 @@ cudaError_t combine_t(const int32_t* row, const float* gate, int s, int k, int m
                     static_cast<const uint4*>(y), static_cast<uint4*>(out));
 }
 
-template <typename T, int KMAX, int G>
+template <typename T, int KMAX, int G, bool RG>
 cudaError_t combine_bwd_g(const int32_t* row, const int32_t* counts, const int32_t* offsets,
                           long long rows, int zero_fill, const float* gate, int s, int k, int e,
                           int nvec, const void* dout, const void* y, void* dY, float* dgate,
-                          const DeviceInfo& di, int bps, cudaStream_t st) {
+                          const RouterGrad& rg, const DeviceInfo& di, int bps, cudaStream_t st) {
   constexpr int UNR = MOE_CMB_BWD_LOADS / KMAX > 1 ? MOE_CMB_BWD_LOADS / KMAX : 1;
-  auto kern = combine_bwd_kernel<T, KMAX, UNR, G>;
+  auto kern = cbwd_kernel<T, KMAX, UNR, G, RG>();
   const int chunk = G == 1 ? nvec : ((nvec + G - 1) / G + 31) / 32 * 32;
   long long warps = (long long)s * G;
   if (zero_fill && rows > warps) warps = rows;
-  return launch_pdl(MOE_KERNEL_COMBINE_BWD, kern, dim3(grid_for(warps, di, bps)), dim3(kThreads), 0, st,
+  return launch_pdl(RG ? MOE_KERNEL_COMBINE_GATE_BWD : MOE_KERNEL_COMBINE_BWD, kern,
+                    dim3(grid_for(warps, di, bps)), dim3(kThreads), 0, st,
                     row, counts, offsets, rows, zero_fill, gate, s, k, e, nvec, chunk,
                     static_cast<const uint4*>(dout), static_cast<const uint4*>(y), static_cast<uint4*>(dY),
-                    dgate);
+                    dgate, rg);
 }
 
-template <typename T, int KMAX>
+template <typename T, int KMAX, bool RG>
 cudaError_t combine_bwd_t(const int32_t* row, const int32_t* counts, const int32_t* offsets,
                           long long rows, int zero_fill, const float* gate, int s, int k, int e,
                           int m, const void* dout, const void* y, void* dY, float* dgate, int sparse,
-                          const DeviceInfo& di, cudaStream_t st) {
+                          const RouterGrad& rg, const DeviceInfo& di, cudaStream_t st) {
   constexpr int UNR = MOE_CMB_BWD_LOADS / KMAX > 1 ? MOE_CMB_BWD_LOADS / KMAX : 1;
   const int nvec = m / Vec<T>::N;
+  // the split below is chosen on the plain kernel's occupancy, so the fused
+  // form splits the same way and computes the same dgate bits
   static const int bps = occupancy(combine_bwd_kernel<T, KMAX, UNR, 1>);
+  static const int bps_launch = occupancy(cbwd_kernel<T, KMAX, UNR, 1, RG>());
   // warps per token for short batches (the dot of the gate gradient is
   // reduced across them in a fixed order, so each G gives fixed results)
   const int G = pieces_for(s, nvec, di, bps, 4, 8);
   if (MOE_CMB_COMPACT && sparse && k > 4 && G == 1) {
     constexpr int KC = 4, UNRC = MOE_CMB_BWD_LOADS / KC > 1 ? MOE_CMB_BWD_LOADS / KC : 1;
-    auto kern = combine_bwd_compact_kernel<T, KC, UNRC>;
+    auto kern = cbwd_compact_kernel<T, KC, UNRC, RG>();
     static const int bpsc = occupancy(kern);
     long long warps = s;
     if (zero_fill && rows > warps) warps = rows;
-    return launch_pdl(MOE_KERNEL_COMBINE_BWD, kern, dim3(grid_for(warps, di, bpsc)), dim3(kThreads), 0, st,
+    return launch_pdl(RG ? MOE_KERNEL_COMBINE_GATE_BWD : MOE_KERNEL_COMBINE_BWD, kern,
+                      dim3(grid_for(warps, di, bpsc)), dim3(kThreads), 0, st,
                       row, counts, offsets, rows, zero_fill, gate, s, k, e, nvec,
                       static_cast<const uint4*>(dout), static_cast<const uint4*>(y), static_cast<uint4*>(dY),
-                      dgate);
+                      dgate, rg);
   }
 #define MOE_CBWD_G(GG)                                                                            \
-  combine_bwd_g<T, KMAX, GG>(row, counts, offsets, rows, zero_fill, gate, s, k, e, nvec, dout, y, dY, \
-                             dgate, di, bps, st)
+  combine_bwd_g<T, KMAX, GG, RG>(row, counts, offsets, rows, zero_fill, gate, s, k, e, nvec, dout, y, dY, \
+                                 dgate, rg, di, bps_launch, st)
   if (G >= 8) return MOE_CBWD_G(8);
   if (G == 4) return MOE_CBWD_G(4);
   if (G == 2) return MOE_CBWD_G(2);
@@ -579,14 +673,14 @@ cudaError_t combine_k(const int32_t* row, const float* gate, int s, int k, int m
   return combine_t<T, 16>(row, gate, s, k, m, y, out, di, st);
 }
 
-template <typename T>
+template <typename T, bool RG>
 cudaError_t combine_bwd_k(const int32_t* row, const int32_t* counts, const int32_t* offsets,
                           long long rows, int zero_fill, const float* gate, int s, int k, int e,
                           int m, const void* dout, const void* y, void* dY, float* dgate, int sparse,
-                          const DeviceInfo& di, cudaStream_t st) {
+                          const RouterGrad& rg, const DeviceInfo& di, cudaStream_t st) {
 #define MOE_CBWD(KM)                                                                              \
-  combine_bwd_t<T, KM>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout, y, dY, dgate, \
-                       sparse, di, st)
+  combine_bwd_t<T, KM, RG>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout, y, dY, dgate, \
+                           sparse, rg, di, st)
   if (k <= 2) return MOE_CBWD(2);
   if (k <= 4) return MOE_CBWD(4);
   if (k <= 8) return MOE_CBWD(8);
@@ -610,12 +704,22 @@ cudaError_t launch_combine(const int32_t* row, const float* gate, int s, int k, 
 cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const int32_t* offsets,
                                long long rows, int zero_fill, const float* gate, int s, int k,
                                int e, int m, int dtype, const void* dout, const void* y, void* dY,
-                               float* dgate, int sparse, const DeviceInfo& di, cudaStream_t st) {
+                               float* dgate, int sparse, const DeviceInfo& di, cudaStream_t st,
+                               const int32_t* rg_idx, const float* rg_logits, int rg_renorm,
+                               float* rg_dlogits) {
+  const RouterGrad rg = {rg_idx, rg_logits, rg_renorm, rg_dlogits};
+  if (rg_dlogits) {
+    if (dtype == 0)
+      return combine_bwd_k<float, true>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout, y, dY,
+                                        dgate, sparse, rg, di, st);
+    return combine_bwd_k<__nv_bfloat16, true>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout,
+                                              y, dY, dgate, sparse, rg, di, st);
+  }
   if (dtype == 0)
-    return combine_bwd_k<float>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout, y, dY,
-                                dgate, sparse, di, st);
-  return combine_bwd_k<__nv_bfloat16>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout,
-                                      y, dY, dgate, sparse, di, st);
+    return combine_bwd_k<float, false>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout, y, dY,
+                                       dgate, sparse, rg, di, st);
+  return combine_bwd_k<__nv_bfloat16, false>(row, counts, offsets, rows, zero_fill, gate, s, k, e, m, dout,
+                                             y, dY, dgate, sparse, rg, di, st);
 }
 
 }  // namespace moe

@@ -214,11 +214,11 @@ __device__ __forceinline__ void bulk_wait_all() {
 // grid_dependency_wait() before reading anything that kernel wrote.
 // Bit mask of the launches that use programmatic serialisation (bit i =
 // kernel id i of moe_launch_count: gate 0, dispatch 2, combine backward 4,
-// dispatch backward 5, gate backward 6).  The combine (3) is left out: its
-// CTAs parked early on the SMs slowed the dispatch they follow, by 6-13 %
-// of a step on every workload measured.
+// dispatch backward 5, gate backward 6, combine + gate backward 10).  The
+// combine (3) is left out: its CTAs parked early on the SMs slowed the
+// dispatch they follow, by 6-13 % of a step on every workload measured.
 #ifndef MOE_PDL_MASK
-#define MOE_PDL_MASK 0x75
+#define MOE_PDL_MASK 0x475
 #endif
 
 template <typename... KArgs, typename... Args>

@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "router_grad.cuh"
 
 namespace moe {
 
@@ -141,8 +142,7 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float* __restrict_
 }
 
 // Gate backward, one warp per token: lanes 0..k-1 hold (expert, gate,
-// dgate) of the selected routes; c = sum_j g_j * dgate_j by a butterfly; each
-// lane then writes the gradient of its experts lane, lane + 32, ...
+// dgate) of the selected routes; router_grad_token does the rest.
 template <int EPL>
 __global__ void __launch_bounds__(256) topk_gate_bwd_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ idx,
@@ -170,55 +170,7 @@ __global__ void __launch_bounds__(256) topk_gate_bwd_kernel(
       n_gj = __ldg(gate + (size_t)tn * k + lane);
       n_dgj = __ldg(dgate + (size_t)tn * k + lane);
     }
-    float c = __fmul_rn(gj, dgj);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
-    // this lane's experts: their dgate (0 if not selected) and gate factor
-    float dg[EPL], fac[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      dg[i] = 0.f;
-      fac[i] = 0.f;
-    }
-    for (int j = 0; j < k; ++j) {
-      const int x = __shfl_sync(0xffffffffu, ij, j);
-      const float g = __shfl_sync(0xffffffffu, gj, j);
-      const float d = __shfl_sync(0xffffffffu, dgj, j);
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        if (lane + 32 * i == x) {
-          dg[i] = d;
-          fac[i] = g;
-        }
-    }
-    if (!renorm) {
-      const float* l = logits + (size_t)t * e;
-      float v[EPL];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int x = lane + 32 * i;
-        v[i] = x < e ? __ldg(l + x) : -INFINITY;
-        mx = fmaxf(mx, v[i]);
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      float z = 0.f;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        if (lane + 32 * i < e) z += expf(v[i] - mx);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) fac[i] = expf(v[i] - mx) / z;  // p_i for every expert
-    }
-    float* out = dlogits + (size_t)t * e;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int x = lane + 32 * i;
-      // an expert outside the top-k gets exactly 0 under renormalisation
-      if (x < e) out[x] = fac[i] == 0.f ? 0.f : __fmul_rn(fac[i], __fsub_rn(dg[i], c));
-    }
+    router_grad_token<EPL>(t, lane, k, e, renorm, ij, gj, dgj, logits, dlogits);
   }
   pdl_trigger_late();
 }

@@ -95,10 +95,15 @@ cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, const int
 cudaError_t launch_combine(const int32_t* row, const float* gate, int s, int k, int m, int dtype,
                            const void* y, void* out, int sparse, const DeviceInfo& di, cudaStream_t st);
 
+// With rg_dlogits != nullptr the top-k gate backward runs fused into the
+// same kernel (rg_idx = the routes' expert ids; rg_logits only when
+// rg_renorm == 0): dlogits as launch_topk_gate_bwd would write from dgate.
 cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const int32_t* offsets,
                                long long rows, int zero_fill, const float* gate, int s, int k,
                                int e, int m, int dtype, const void* dout, const void* y, void* dY,
-                               float* dgate, int sparse, const DeviceInfo& di, cudaStream_t st);
+                               float* dgate, int sparse, const DeviceInfo& di, cudaStream_t st,
+                               const int32_t* rg_idx = nullptr, const float* rg_logits = nullptr,
+                               int rg_renorm = 1, float* rg_dlogits = nullptr);
 
 // --- per-virtual-rank send slots ------------------------------------------
 // rank_slot[t,r] = token-order position of t among the tokens sending to r,

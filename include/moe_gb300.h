@@ -86,7 +86,8 @@ enum {
   MOE_KERNEL_GROUPED_GEMM = 7,
   MOE_KERNEL_DISPATCH_GEMM = 8,
   MOE_KERNEL_RANK_SLOTS = 9,
-  MOE_KERNEL_COUNT = 10
+  MOE_KERNEL_COMBINE_GATE_BWD = 10,
+  MOE_KERNEL_COUNT = 11
 };
 
 /* Opaque layout handle [P1 "How"; P3 description].  Owned by the library:
@@ -264,6 +265,22 @@ moe_status moe_combine(moe_handle h, int s, int rows, int m, moe_dtype dtype,
 moe_status moe_combine_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype,
                            const void* dout, const float* gate, const void* y,
                            void* dY, float* dgate, void* stream);
+
+/* Combine backward with the top-k gate backward fused in [P3 description:
+ * combine-grad = dispatch; P3 review thread: the routing weights' gradient
+ * must reach the router].  Exactly moe_combine_bwd followed by
+ * moe_topk_gate_bwd(logits, idx, gate, dgate, ...) on the handle's own
+ * expert ids (its idx copy), in one kernel: dY [rows,m] and dgate f32 [s,k]
+ * as moe_combine_bwd, and dlogits f32 [s,e] as moe_topk_gate_bwd -- the same
+ * bits as the two calls.  Each token's router gradient is written by the
+ * warp that reduced its gate gradients, so dgate is never re-read.
+ * logits f32 [s,e] is read only when renorm = 0 (may be NULL when renorm =
+ * 1).  Errors as moe_combine_bwd; renorm other than 0 or 1 is
+ * MOE_ERR_INVALID_ARG. */
+moe_status moe_combine_gate_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype,
+                                const void* dout, const float* gate, const void* y,
+                                const float* logits, int renorm, void* dY, float* dgate,
+                                float* dlogits, void* stream);
 
 /* Dispatch backward = a combine with unit weights [P3 description].
  * dX [rows,m] -> dx [s,m]: dx[t] = sum over kept routes, in route order,

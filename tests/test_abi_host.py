@@ -105,6 +105,10 @@ def test_unknown_handles_are_rejected_without_a_gpu(lib):
     assert rc_name(lib.moe_combine(bogus, 4, 8, 8, 1, fake, fake, fake, None)) == "MOE_ERR_HANDLE_MISMATCH"
     assert rc_name(lib.moe_combine_bwd(bogus, 4, 8, 8, 1, fake, fake, fake, fake, fake, None)) == "MOE_ERR_HANDLE_MISMATCH"
     assert rc_name(lib.moe_dispatch_bwd(bogus, 4, 8, 8, 1, fake, fake, None)) == "MOE_ERR_HANDLE_MISMATCH"
+    assert rc_name(lib.moe_combine_gate_bwd(bogus, 4, 8, 8, 1, fake, fake, fake, None, 1, fake, fake, fake,
+                                            None)) == "MOE_ERR_HANDLE_MISMATCH"
+    assert rc_name(lib.moe_combine_gate_bwd(None, 4, 8, 8, 1, fake, fake, fake, None, 1, fake, fake, fake,
+                                            None)) == "MOE_ERR_INVALID_ARG"
     assert rc_name(lib.moe_grouped_gemm(None, 8, 64, 64, fake, fake, fake, None)) == "MOE_ERR_INVALID_ARG"
     assert rc_name(lib.moe_grouped_gemm(bogus, 8, 64, 64, fake, fake, fake, None)) == "MOE_ERR_HANDLE_MISMATCH"
     assert rc_name(lib.moe_dispatch_grouped_gemm(None, 4, 8, 64, 64, fake, fake, fake, None)) == "MOE_ERR_INVALID_ARG"

@@ -30,6 +30,20 @@ def test_byte_model_of_the_mixtral_like_step():
     assert bench.payload_bytes(w, w.s * w.k, w.s) == {"dispatch": 3 * x, "combine": 3 * x}
 
 
+def test_byte_model_of_the_fused_backward_and_the_step():
+    """The fused combine + gate backward moves the combine backward's bytes
+    plus the expert ids read and the router gradient written; a step counts
+    each op it runs once (not the separate backward ops as well)."""
+    w = W.WORKLOADS["fine-grained-skewed"]
+    b = bench.step_bytes(w, kept=w.s * w.k, u=w.s)
+    assert b["combine_gate_bwd"] == b["combine_bwd"] + w.s * w.k * 4 + w.s * w.e * 4
+    assert bench.step_sum(b) == sum(b[op] for op in
+                                    ("topk_gate", "layout", "dispatch", "combine", "combine_gate_bwd", "dispatch_bwd"))
+    wn = W.WORKLOADS["tiny-capacity"].replace(renorm=0)
+    bn = bench.step_bytes(wn, kept=100, u=60)
+    assert bn["combine_gate_bwd"] == bn["combine_bwd"] + wn.s * wn.k * 4 + 2 * wn.s * wn.e * 4
+
+
 def test_byte_model_counts_the_capacity_zero_tail():
     w = W.WORKLOADS["gshard-capacity"]
     kept, u = 150000, 30000

@@ -206,6 +206,43 @@ def test_gate_backward_parity(name, renorm):
         assert np.all(got[~sel] == 0)
 
 
+@pytest.mark.parametrize("renorm", [1, 0])
+@pytest.mark.parametrize("name", list(REDUCED) + ["edge-k16", "edge-capacity-k6"])
+def test_combine_gate_bwd_fused(name, renorm):
+    """The combine backward with the gate backward fused in: dY and dgate
+    against the oracle's combine backward, dlogits against the oracle's gate
+    backward fed the kernel's own dgate (each op on identical inputs), and
+    all three bit for bit equal to the two separate calls."""
+    w = {"edge-k16": W.Workload("edge", s=301, m=64, e=64, k=16, dtype="bf16", capacity=0, R=0, seed=8),
+         "edge-capacity-k6": W.Workload("edge", s=777, m=96, e=16, k=6, dtype="f32", capacity=200, R=0,
+                                        seed=9)}.get(name) or REDUCED[name]
+    inp = W.make_inputs(w)
+    g = {k_: v.to(DEV) for k_, v in inp.items()}
+    logits = inp["logits"].numpy()
+    oi, og = oracle.topk_gate(logits, w.k, renorm)
+    h = B.moe_dispatch_layout(to_dev(oi, DEV), w.e, w.capacity, w.R)
+    L = oracle.layout(oi, w.e, w.capacity, w.R)
+    gd = to_dev(og, DEV)
+    dY, dgate, dl = B.moe_combine_gate_bwd(h, g["dout"], gd, g["y"], g["logits"], renorm)
+    yb, db = bits(inp["y"]), bits(inp["dout"])
+    row = L["row"]
+    OdY, Odg = oracle.combine_bwd(row, og, db, yb)
+    T.assert_close(bits(dY), OdY, np.abs(T.as_f64(OdY)), "dY")
+    T.assert_close(bits(dgate), Odg, T.dot_scale(row, db, yb), "dgate")
+    gdg = bits(dgate)
+    Odl = oracle.topk_gate_bwd(logits, oi, og, gdg, w.e, renorm)
+    T.assert_close(bits(dl), Odl, T.gate_bwd_scale(oi, og, gdg, w.e, renorm, logits), "dlogits")
+    # the same bits as the two separate calls
+    dY2, dgate2 = B.moe_combine_bwd(h, g["dout"], gd, g["y"])
+    dl2 = B.moe_topk_gate_bwd(g["logits"] if not renorm else None, to_dev(oi, DEV), gd, dgate2, w.e, renorm)
+    assert torch.equal(dY, dY2) and torch.equal(dgate, dgate2)
+    assert torch.equal(dl.view(torch.int32), dl2.view(torch.int32))
+    n = B.moe_launch_count("combine_gate_bwd")
+    B.moe_combine_gate_bwd(h, g["dout"], gd, g["y"], g["logits"], renorm)
+    assert B.moe_launch_count("combine_gate_bwd") == n + 1
+    assert h.status() == 0
+
+
 # ------------------------------------------------------------- full sizes --
 
 @pytest.mark.parametrize("name", ["tiny-capacity", "mixtral-dropless", "fine-grained-skewed",
