@@ -2,10 +2,10 @@
 """Benchmark of the MoE token path on GB300.
 
 One step = one pass of the whole path over one batch of seeded synthetic
-input: top-k gate -> dispatch layout -> dispatch -> combine -> combine
-backward (gate-scaled dispatch + gate gradient) -> gate backward (router
-logits' gradient) -> dispatch backward, all on the layout handle the step
-built, then the handle is released.
+input: top-k gate + dispatch layout (one kernel) -> dispatch -> combine ->
+combine backward (gate-scaled dispatch + gate gradient) with the gate
+backward (router logits' gradient) in the same kernel -> dispatch backward,
+all on the layout handle the step built.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the CPU oracle, on a bounded sample
@@ -26,6 +26,8 @@ inserted between steps.  Further keys:
   back to back (the cached-replay case);
 - ``replay``: the step on a saved handle (gate recomputed, no layout), and
   the layout launches seen meanwhile (must be 0);
+- the step's handle is created once and rebuilt in place by each step's
+  fused gate + layout kernel (no allocation or memset per step);
 - ``routing``: drop fraction, and the dedup ratio over virtual ranks;
 - ``e2e``: the same metric with every step's inputs copied from pinned
   host memory and its results copied back inside the timed region;
@@ -50,8 +52,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "dispatch+combine HBM GB/s and routed tokens/s on 1 GB300 vs HBM peak"
 DEFAULT_WORKLOAD = "fine-grained-skewed"  # the largest workload: s=16384, m=4096, e=128, k=8
-OPS = ["topk_gate", "layout", "dispatch", "combine", "combine_gate_bwd", "dispatch_bwd"]
-KERNEL_FILE = {"topk_gate": "gate.cu", "layout": "layout.cu", "dispatch": "dispatch.cu", "combine": "combine.cu",
+OPS = ["gate_layout", "dispatch", "combine", "combine_gate_bwd", "dispatch_bwd"]
+KERNEL_FILE = {"topk_gate": "gate.cu", "layout": "layout.cu", "gate_layout": ("layout.cu", "gate_core.cuh"),
+               "dispatch": "dispatch.cu", "combine": "combine.cu",
                "combine_bwd": "combine.cu", "topk_gate_bwd": ("gate.cu", "router_grad.cuh"),
                "combine_gate_bwd": ("combine.cu", "router_grad.cuh"), "dispatch_bwd": "combine.cu"}
 FALLBACK_HBM_GBS = 6800.0
@@ -82,6 +85,9 @@ def step_bytes(w, kept: int, u: int) -> dict:
     # fused: the combine backward's bytes, plus the expert ids and the router
     # gradient written (and the logits without renorm); dgate is not re-read
     out["combine_gate_bwd"] = out["combine_bwd"] + routes * 4 + s * e * 4 + (0 if w.renorm else s * e * 4)
+    # fused gate + layout: the gate's logits in and ids + gates out, the
+    # layout's outputs; the ids are not read back
+    out["gate_layout"] = out["topk_gate"] + out["layout"] - routes * 4
     return out
 
 
@@ -234,41 +240,43 @@ def run_ours(args, rank: int, world: int, dist):
             dlogits=torch.empty(w.s, w.e, dtype=torch.float32, device=dev))
 
     S = buffers(w.seed + 1000 * rank)
+    # the layout handle: created once (its memory allocated and zeroed), then
+    # rebuilt in place by every step's gate + layout, with no allocation
+    H = {0: B.moe_layout_create(w.s, w.e, w.k, w.capacity, w.R, device=dev)}
 
     pad = getattr(torch.cuda, "_sleep", None)
 
-    def step(b=S, ev=None):
-        """One pass of the path: gate, layout, dispatch, combine, combine
-        backward, gate backward, dispatch backward on the step's handle.
-        With ev (pairs of events per op), each op is bracketed by its own
-        events, preceded by a short GPU sleep so that the host has enqueued
-        the op before the start event is reached: the pair then times the
-        kernel, not the host's launch overhead."""
+    def step(b=S, ev=None, slot=0):
+        """One pass of the path on a layout handle rebuilt from this step's
+        logits: the top-k gate fused into the layout build, dispatch,
+        combine, the combine backward with the gate backward fused in, and
+        the dispatch backward.  With ev (pairs of events per op), each op is
+        bracketed by its own events, preceded by a short GPU sleep so that
+        the host has enqueued the op before the start event is reached: the
+        pair then times the kernel, not the host's launch overhead."""
         def mark(i, j):
             if ev is not None:
                 if j == 0 and pad is not None:
                     pad(SLEEP_CYCLES)
                 ev[i][j].record()
 
+        h = H[slot]
         mark(0, 0)
-        B.moe_topk_gate(b["logits"], w.k, w.renorm, b["idx"], b["gate"])
+        B.moe_topk_gate_layout(h, b["logits"], w.renorm, b["idx"], b["gate"])
         mark(0, 1)
         mark(1, 0)
-        h = B.moe_dispatch_layout(b["idx"], w.e, w.capacity, w.R)
+        B.moe_dispatch(h, b["x"], b["X"])
         mark(1, 1)
         mark(2, 0)
-        B.moe_dispatch(h, b["x"], b["X"])
+        B.moe_combine(h, b["y"], b["gate"], b["out"])
         mark(2, 1)
         mark(3, 0)
-        B.moe_combine(h, b["y"], b["gate"], b["out"])
-        mark(3, 1)
-        mark(4, 0)
         B.moe_combine_gate_bwd(h, b["dout"], b["gate"], b["y"], b["logits"], w.renorm, b["dY"], b["dgate"],
                                b["dlogits"])
-        mark(4, 1)
-        mark(5, 0)
+        mark(3, 1)
+        mark(4, 0)
         B.moe_dispatch_bwd(h, b["dY"], b["dx"])
-        mark(5, 1)
+        mark(4, 1)
         return h
 
     # kept routes / sending tokens for the byte model (outside any timing)
@@ -278,7 +286,6 @@ def run_ours(args, rank: int, world: int, dist):
     u = int((drop == 0).any(dim=1).sum().item())
     rank_sum = int(h.rank_counts().sum().item()) if w.R else 0
     assert h.status() == 0, "device status after the first step"
-    h.destroy()
     nbytes = step_bytes(w, kept, u)
     step_total = step_sum(nbytes)
 
@@ -295,13 +302,13 @@ def run_ours(args, rank: int, world: int, dist):
             side.wait_stream(torch.cuda.current_stream(dev))
             with torch.cuda.stream(side):
                 for _ in range(2):
-                    step().destroy()
+                    step()
             torch.cuda.current_stream(dev).wait_stream(side)
             torch.cuda.synchronize()
             c0 = sum(B.moe_launch_count(i) for i in range(len(B.KERNELS)))
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph):
-                step().destroy()
+                step()
             graph_launches = sum(B.moe_launch_count(i) for i in range(len(B.KERNELS))) - c0
             graph.replay()
             torch.cuda.synchronize()
@@ -315,7 +322,7 @@ def run_ours(args, rank: int, world: int, dist):
         if graph is not None:
             graph.replay()
         else:
-            step().destroy()
+            step()
 
     for _ in range(args.warmup):
         run_step()
@@ -341,7 +348,7 @@ def run_ours(args, rank: int, world: int, dist):
     Kr = max(3, min(K, 200))
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in OPS] for _ in range(Kr)]
     for i in range(Kr):
-        step(ev=evs[i]).destroy()
+        step(ev=evs[i])
     torch.cuda.synchronize()
     samples = {op: sorted(evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(Kr)) for j, op in enumerate(OPS)}
     per_op = {op: statistics.mean(v) for op, v in samples.items()}
@@ -554,11 +561,11 @@ def run_replay_step(w, S, dev, K: int):
     for _ in range(5):
         run()
     torch.cuda.synchronize()
-    layouts = B.moe_launch_count("layout")
+    layouts = B.moe_launch_count("layout") + B.moe_launch_count("gate_layout")
     n = max(5, min(K, 500))
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if small_working_set(w) else None
     ms = time_loop(run, n, flush)
-    moved = B.moe_launch_count("layout") - layouts
+    moved = B.moe_launch_count("layout") + B.moe_launch_count("gate_layout") - layouts
     assert h.status() == 0
     h.destroy()
     how += ", each replay timed alone after an L2 flush" if flush is not None else ", replayed back to back"
@@ -654,7 +661,7 @@ def run_e2e(w, S, step, buffers, dev, K, warmup):
                 s_cmp.wait_event(ev_in[j])
                 if i >= 2:
                     s_cmp.wait_event(ev_out[j])  # its previous results have left
-                step(b).destroy()
+                step(b)
                 ev_cmp[j].record(s_cmp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_cmp[j])

@@ -26,7 +26,7 @@ STATUS = {
 MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
 MOE_DEV_NONFINITE, MOE_DEV_BAD_ROUTE, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4
 KERNELS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd", "topk_gate_bwd",
-           "grouped_gemm", "dispatch_gemm", "rank_slots", "combine_gate_bwd"]
+           "grouped_gemm", "dispatch_gemm", "rank_slots", "combine_gate_bwd", "gate_layout"]
 KERNEL_ID = {n: i for i, n in enumerate(KERNELS)}
 
 # every entry point the header declares (checked by the CPU test-suite)
@@ -35,7 +35,8 @@ EXPORTS = [
     "moe_dispatch_bwd", "moe_handle_info", "moe_handle_status", "moe_handle_destroy", "moe_capacity",
     "moe_status_string", "moe_last_error", "moe_launch_count", "moe_debug_hold_layout_tile",
     "moe_dispatch_layout_noalloc", "moe_topk_gate_bwd", "moe_dispatch_layout_ex", "moe_grouped_gemm",
-    "moe_dispatch_grouped_gemm", "moe_combine_gate_bwd",
+    "moe_dispatch_grouped_gemm", "moe_combine_gate_bwd", "moe_layout_create", "moe_layout_rebuild",
+    "moe_topk_gate_layout",
 ]
 
 
@@ -79,6 +80,9 @@ def lib() -> ctypes.CDLL:
             "moe_topk_gate_bwd": [P, P, P, P, I, I, I, I, P, P],
             "moe_dispatch_layout": [P, I, I, I, I, I, P, ctypes.POINTER(P)],
             "moe_dispatch_layout_ex": [P, I, I, I, ctypes.POINTER(LayoutOptions), P, ctypes.POINTER(P)],
+            "moe_layout_create": [I, I, I, ctypes.POINTER(LayoutOptions), P, ctypes.POINTER(P)],
+            "moe_layout_rebuild": [P, P, P],
+            "moe_topk_gate_layout": [P, P, I, P, P, P],
             "moe_dispatch": [P, I, I, I, I, P, P, P],
             "moe_combine": [P, I, I, I, I, P, P, P, P],
             "moe_combine_bwd": [P, I, I, I, I, P, P, P, P, P, P],
@@ -297,6 +301,49 @@ def moe_dispatch_layout_ex(topk_idx: torch.Tensor, e: int, capacity: int = 0, nu
                                       ctypes.byref(raw))
     _check(rc, "moe_dispatch_layout_ex")
     return Handle(raw, dev)
+
+
+def moe_layout_create(s: int, e: int, k: int, capacity: int = 0, num_virtual_ranks: int = 0,
+                      priority: str = "token", pad_multiple: int = 1, send_slots: bool = False,
+                      device: torch.device | None = None) -> Handle:
+    """An empty handle for [s, k] routes over e experts with these layout
+    options, to be built (and rebuilt) in place by moe_layout_rebuild or
+    moe_topk_gate_layout without allocating."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    opt = LayoutOptions(int(capacity), int(num_virtual_ranks), PRIORITY[priority], int(pad_multiple),
+                        int(bool(send_slots)))
+    raw = ctypes.c_void_p()
+    with torch.cuda.device(dev):
+        rc = lib().moe_layout_create(int(s), int(e), int(k), ctypes.byref(opt), _stream(dev), ctypes.byref(raw))
+    _check(rc, "moe_layout_create")
+    return Handle(raw, dev)
+
+
+def moe_layout_rebuild(h: Handle, topk_idx: torch.Tensor) -> Handle:
+    """Rebuild h's layout in place from new expert ids i32 [s, k]."""
+    if topk_idx.dtype != torch.int32 or tuple(topk_idx.shape) != (h.s, h.k):
+        raise MoEError(1, "moe_layout_rebuild", "topk_idx must be int32 [s, k] of the handle's shape")
+    _check(lib().moe_layout_rebuild(h.raw, _ptr(topk_idx), _stream(topk_idx.device)), "moe_layout_rebuild")
+    return h
+
+
+def moe_topk_gate_layout(h: Handle, logits: torch.Tensor, renorm: int = 1, topk_idx: torch.Tensor | None = None,
+                         topk_gate: torch.Tensor | None = None):
+    """The top-k gate and the layout build in one kernel: logits f32 [s, e]
+    -> (topk_idx i32 [s, k], topk_gate f32 [s, k]), h rebuilt on those ids."""
+    if logits.dtype != torch.float32 or tuple(logits.shape) != (h.s, h.e):
+        raise MoEError(1, "moe_topk_gate_layout", "logits must be float32 [s, e] of the handle's shape")
+    dev = logits.device
+    if topk_idx is None:
+        topk_idx = torch.empty(h.s, h.k, dtype=torch.int32, device=dev)
+    if topk_gate is None:
+        topk_gate = torch.empty(h.s, h.k, dtype=torch.float32, device=dev)
+    if tuple(topk_idx.shape) != (h.s, h.k) or tuple(topk_gate.shape) != (h.s, h.k) or \
+            topk_idx.dtype != torch.int32 or topk_gate.dtype != torch.float32:
+        raise MoEError(1, "moe_topk_gate_layout", "output shapes")
+    rc = lib().moe_topk_gate_layout(h.raw, _ptr(logits), int(renorm), _ptr(topk_idx), _ptr(topk_gate), _stream(dev))
+    _check(rc, "moe_topk_gate_layout")
+    return topk_idx, topk_gate
 
 
 def _rows2(t: torch.Tensor, name: str) -> tuple[int, int]:

@@ -25,9 +25,11 @@ struct moe_handle_s {
   int zero_fill;  // the dispatched buffer has rows no route owns
   void* blob;
   size_t blob_bytes;
+  size_t clear_bytes;  // the blob's leading status word and rank counts
   moe::LayoutOut out;
   int32_t* rank_slot;  // [s,R] send slots, or NULL
   moe::LayoutPlan plan;
+  int builds;          // layout builds enqueued so far (0: created, no layout yet)
 };
 
 namespace {
@@ -104,6 +106,13 @@ moe_status live_handle(moe_handle h) {
   if (!h) return fail(MOE_ERR_INVALID_ARG, "handle is NULL");
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_live.count(h)) return fail(MOE_ERR_HANDLE_MISMATCH, "handle is unknown or destroyed");
+  return MOE_OK;
+}
+
+// A handle from moe_layout_create has no layout until its first build.
+moe_status built_handle(moe_handle h) {
+  MOE_TRY(live_handle(h));
+  if (h->builds == 0) return fail(MOE_ERR_INVALID_ARG, "the handle has no layout yet (build it first)");
   return MOE_OK;
 }
 
@@ -266,8 +275,13 @@ moe_status moe_topk_gate_bwd(const float* logits, const int32_t* topk_idx, const
   return MOE_OK;
 }
 
-moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
-                                  const moe_layout_options* options, void* stream, moe_handle* out) {
+namespace {
+
+// Validates the sizes and options, allocates the handle's blob from the
+// device's pool on `stream` and zeroes its leading part (status word, rank
+// counts, look-back words).  No layout yet.
+moe_status create_handle(int s, int e, int k, const moe_layout_options* options, void* stream,
+                         moe_handle* out, const int32_t* topk_idx = nullptr) {
   if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (!options) return fail(MOE_ERR_INVALID_ARG, "options is NULL");
@@ -292,11 +306,13 @@ moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
   const long long rows = capacity > 0 ? (long long)e * capacity : routes + (long long)e * (pad - 1);
   if (routes > 2147483647LL || rows > 2147483647LL)
     return fail(MOE_ERR_INVALID_ARG, "s*k and the row count must be < 2^31");
-  if (s > 0) MOE_TRY(check_ptr(topk_idx, "topk_idx"));
+  if ((long long)s * e > 2147483647LL) return fail(MOE_ERR_INVALID_ARG, "s*e must be < 2^31");
+
+  if (topk_idx && s > 0) MOE_TRY(check_ptr(topk_idx, "topk_idx"));
 
   int dev = 0;
   MOE_TRY(current_device(&dev));
-  if (s > 0) MOE_TRY(check_device_ptr(topk_idx, "topk_idx", dev));
+  if (topk_idx && s > 0) MOE_TRY(check_device_ptr(topk_idx, "topk_idx", dev));
   const moe::DeviceInfo* di = nullptr;
   MOE_TRY(device_state(dev, &di));
 
@@ -312,6 +328,7 @@ moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
   h->priority = priority;
   h->pad = pad;
   h->zero_fill = capacity > 0 || pad > 1;
+  h->builds = 0;
   // the scan runs over s*k one-route units in k-major order
   h->plan = moe::plan_layout(priority == MOE_PRIORITY_KMAJOR ? s * k : s, e, *di);
 
@@ -320,6 +337,7 @@ moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
   size_t off = 0;
   const size_t o_status = off; off = align_up(off + 4, A);
   const size_t o_rank = off;   off = align_up(off + 4 * (size_t)(R > 0 ? R : 1), A);
+  h->clear_bytes = off;
   const size_t o_lb = off;     off = align_up(off + moe::lookback_bytes(h->plan, e), A);
   const size_t zero_bytes = off;
   const size_t o_idx = off;    off = align_up(off + 4 * (size_t)routes, A);
@@ -355,6 +373,52 @@ moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
   h->rank_slot = send_slots ? reinterpret_cast<int32_t*>(base + o_slot) : nullptr;
 
   err = cudaMemsetAsync(base, 0, zero_bytes, h->stream);
+  if (err != cudaSuccess) {
+    cudaFreeAsync(h->blob, h->stream);
+    delete h;
+    return cuda_fail(err, "handle zeroing");
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_live.insert(h);
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+// Enqueues one build of h's layout on `stream`: from expert ids, or (logits
+// != nullptr) with the top-k gate fused in, writing the ids and gates to
+// gate_idx / gate_val.  Nothing here depends on how many builds came before
+// (the kernel finds its look-back parity on the device and clears the status
+// word and rank counts itself), so a CUDA graph may capture a build and
+// replay it.
+moe_status build_handle(moe_handle h, const int32_t* topk_idx, const float* logits, int renorm,
+                        int32_t* gate_idx, float* gate_val, void* stream) {
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  moe::LayoutBuild build;
+  build.clear_status = 1;
+  cudaError_t err = cudaSuccess;
+  if (logits && !moe::layout_can_fuse_gate(h->plan, h->priority)) {
+    // the layout variant cannot select in its first pass: the gate kernel
+    // first, then the layout on its ids (status cleared before the gate
+    // reports into it)
+    const moe::DeviceInfo* di = nullptr;
+    MOE_TRY(device_state(h->device, &di));
+    err = cudaMemsetAsync(h->blob, 0, h->clear_bytes, st);
+    if (err == cudaSuccess)
+      err = moe::launch_topk_gate(logits, h->s, h->e, h->k, renorm, gate_idx, gate_val, h->out.status, *di, st);
+    if (err != cudaSuccess) return cuda_fail(err, "topk_gate launch");
+    g_launches[MOE_KERNEL_TOPK_GATE]++;
+    topk_idx = gate_idx;
+    logits = nullptr;
+    build.clear_status = 0;
+  }
+  if (logits) {
+    build.logits = logits;
+    build.renorm = renorm;
+    build.gate_idx = gate_idx;
+    build.gate_val = gate_val;
+  }
   int hold = -1;
   long long timeout_ns = kDefaultTimeoutNs;
   {
@@ -365,30 +429,82 @@ moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
       g_hold_tile = -1;
     }
   }
-  if (err == cudaSuccess)
-    err = moe::launch_layout(topk_idx, s, e, k, capacity, R, priority, pad, h->plan, h->out, hold,
-                             timeout_ns, h->stream);
-  if (err != cudaSuccess) {
-    cudaFreeAsync(h->blob, h->stream);
-    delete h;
-    return cuda_fail(err, "layout launch");
-  }
-  g_launches[MOE_KERNEL_LAYOUT]++;
-  if (h->rank_slot && s > 0) {
-    err = moe::launch_rank_slots(h->out.token_in_rank, s, R, h->rank_slot, h->stream);
-    if (err != cudaSuccess) {
-      cudaFreeAsync(h->blob, h->stream);
-      delete h;
-      return cuda_fail(err, "rank_slots launch");
-    }
+  err = moe::launch_layout(topk_idx, h->s, h->e, h->k, h->capacity, h->R, h->priority, h->pad, h->plan, h->out,
+                           hold, timeout_ns, st, build);
+  if (err != cudaSuccess) return cuda_fail(err, "layout launch");
+  g_launches[logits ? MOE_KERNEL_GATE_LAYOUT : MOE_KERNEL_LAYOUT]++;
+  h->builds++;
+  h->stream = st;  // the handle's latest writer: its memory is freed on this stream
+  if (h->rank_slot && h->s > 0) {
+    err = moe::launch_rank_slots(h->out.token_in_rank, h->s, h->R, h->rank_slot, st);
+    if (err != cudaSuccess) return cuda_fail(err, "rank_slots launch");
     g_launches[MOE_KERNEL_RANK_SLOTS]++;
   }
+  return MOE_OK;
+}
+
+// Device-pointer checks of a build's inputs and outputs.
+moe_status check_build_ptrs(moe_handle h, const int32_t* topk_idx, const float* logits, int32_t* gate_idx,
+                            float* gate_val) {
+  if (h->s == 0) return MOE_OK;
+  MOE_TRY(handle_device(h));
+  if (!logits) {
+    MOE_TRY(check_ptr(topk_idx, "topk_idx"));
+    return check_device_ptr(topk_idx, "topk_idx", h->device);
+  }
+  MOE_TRY(check_ptr(logits, "logits"));
+  MOE_TRY(check_ptr(gate_idx, "topk_idx"));
+  MOE_TRY(check_ptr(gate_val, "topk_gate"));
+  MOE_TRY(check_device_ptr(logits, "logits", h->device));
+  MOE_TRY(check_device_ptr(gate_idx, "topk_idx", h->device));
+  return check_device_ptr(gate_val, "topk_gate", h->device);
+}
+
+// Removes a handle that failed its first build.
+void discard_handle(moe_handle h) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    g_live.insert(h);
+    g_live.erase(h);
+  }
+  cudaFreeAsync(h->blob, h->stream);
+  delete h;
+}
+
+}  // namespace
+
+moe_status moe_dispatch_layout_ex(const int32_t* topk_idx, int s, int e, int k,
+                                  const moe_layout_options* options, void* stream, moe_handle* out) {
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (s > 0 && !topk_idx) return fail(MOE_ERR_INVALID_ARG, "topk_idx is NULL");
+  moe_handle h = nullptr;
+  MOE_TRY(create_handle(s, e, k, options, stream, &h, topk_idx));
+  const moe_status st = build_handle(h, topk_idx, nullptr, 1, nullptr, nullptr, stream);
+  if (st != MOE_OK) {
+    discard_handle(h);
+    return st;
   }
   *out = h;
   return MOE_OK;
+}
+
+moe_status moe_layout_create(int s, int e, int k, const moe_layout_options* options, void* stream,
+                             moe_handle* out) {
+  return create_handle(s, e, k, options, stream, out);
+}
+
+moe_status moe_layout_rebuild(moe_handle h, const int32_t* topk_idx, void* stream) {
+  MOE_TRY(live_handle(h));
+  MOE_TRY(check_build_ptrs(h, topk_idx, nullptr, nullptr, nullptr));
+  return build_handle(h, topk_idx, nullptr, 1, nullptr, nullptr, stream);
+}
+
+moe_status moe_topk_gate_layout(moe_handle h, const float* logits, int renorm, int32_t* topk_idx,
+                                float* topk_gate, void* stream) {
+  MOE_TRY(live_handle(h));
+  if (renorm != 0 && renorm != 1) return fail(MOE_ERR_INVALID_ARG, "renorm must be 0 or 1");
+  MOE_TRY(check_build_ptrs(h, nullptr, logits, topk_idx, topk_gate));
+  return build_handle(h, nullptr, logits, renorm, topk_idx, topk_gate, stream);
 }
 
 moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity,
@@ -433,7 +549,7 @@ moe_status gemm_result(cudaError_t err, const char* where, int kernel) {
 
 moe_status moe_grouped_gemm(moe_handle h, int rows, int K, int N, const void* X, const void* W,
                             void* Y, void* stream) {
-  MOE_TRY(live_handle(h));
+  MOE_TRY(built_handle(h));
   MOE_TRY(check_gemm(h, rows, K, N, X, "X", rows, W, Y));
   if (rows == 0) return MOE_OK;
   const moe::DeviceInfo* di = nullptr;
@@ -445,7 +561,7 @@ moe_status moe_grouped_gemm(moe_handle h, int rows, int K, int N, const void* X,
 
 moe_status moe_dispatch_grouped_gemm(moe_handle h, int s, int rows, int K, int N, const void* x,
                                      const void* W, void* Y, void* stream) {
-  MOE_TRY(live_handle(h));
+  MOE_TRY(built_handle(h));
   MOE_TRY(check_shape(h, s, rows));
   MOE_TRY(check_gemm(h, rows, K, N, x, "x", s, W, Y));
   if (rows == 0 || s == 0) return MOE_OK;
@@ -514,7 +630,7 @@ moe_status moe_handle_destroy(moe_handle h) {
 
 moe_status moe_dispatch(moe_handle h, int s, int rows, int m, moe_dtype dtype, const void* x,
                         void* X, void* stream) {
-  MOE_TRY(live_handle(h));
+  MOE_TRY(built_handle(h));
   MOE_TRY(check_shape(h, s, rows));
   long long rb = 0;
   MOE_TRY(check_payload(dtype, m, &rb));
@@ -536,7 +652,7 @@ moe_status moe_dispatch(moe_handle h, int s, int rows, int m, moe_dtype dtype, c
 
 moe_status moe_combine(moe_handle h, int s, int rows, int m, moe_dtype dtype, const void* y,
                        const float* gate, void* out, void* stream) {
-  MOE_TRY(live_handle(h));
+  MOE_TRY(built_handle(h));
   MOE_TRY(check_shape(h, s, rows));
   long long rb = 0;
   MOE_TRY(check_payload(dtype, m, &rb));
@@ -559,7 +675,7 @@ moe_status moe_combine(moe_handle h, int s, int rows, int m, moe_dtype dtype, co
 
 moe_status moe_combine_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype, const void* dout,
                            const float* gate, const void* y, void* dY, float* dgate, void* stream) {
-  MOE_TRY(live_handle(h));
+  MOE_TRY(built_handle(h));
   MOE_TRY(check_shape(h, s, rows));
   long long rb = 0;
   MOE_TRY(check_payload(dtype, m, &rb));
@@ -592,7 +708,7 @@ moe_status moe_combine_gate_bwd(moe_handle h, int s, int rows, int m, moe_dtype 
                                 const void* dout, const float* gate, const void* y,
                                 const float* logits, int renorm, void* dY, float* dgate,
                                 float* dlogits, void* stream) {
-  MOE_TRY(live_handle(h));
+  MOE_TRY(built_handle(h));
   MOE_TRY(check_shape(h, s, rows));
   long long rb = 0;
   MOE_TRY(check_payload(dtype, m, &rb));
@@ -634,7 +750,7 @@ moe_status moe_combine_gate_bwd(moe_handle h, int s, int rows, int m, moe_dtype 
 
 moe_status moe_dispatch_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype, const void* dX,
                             void* dx, void* stream) {
-  MOE_TRY(live_handle(h));
+  MOE_TRY(built_handle(h));
   MOE_TRY(check_shape(h, s, rows));
   long long rb = 0;
   MOE_TRY(check_payload(dtype, m, &rb));

@@ -8,32 +8,19 @@
 // exactly as the forward did, so selection is a pure comparison on the
 // logits (no exp rounding can change it) with a fixed tie-break.
 //
-// Each lane holds the logits of experts lane, lane+32, ... (EPL per lane) as
-// order-preserving 32-bit keys, sorted within the lane.  Each of the k rounds
-// is two warp reductions (redux.sync): the largest head key, then the lowest
-// expert id among the lanes holding it; that lane pops its head, and lane r
-// keeps round r's winner.  The softmax max is round 0's value; the
-// denominator is a butterfly sum, so every lane sees the same bits.
+// The selection of one token by one warp is topk_gate_kernel's loop body,
+// topk_token (gate_core.cuh); this file adds the launch shape (a warp per
+// token, the next token's logits loaded one token ahead) and the backward.
 #include <math.h>
 
 #include "common.cuh"
+#include "gate_core.cuh"
 #include "internal.h"
 #include "router_grad.cuh"
 
 namespace moe {
 
 namespace {
-
-// Order-preserving 32-bit key of a float: a larger value gets a larger key,
-// and -0.0 and +0.0 get the same key (adding +0.0 turns -0.0 into +0.0).
-__device__ __forceinline__ uint32_t order_key(float v) {
-  const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float key_value(uint32_t key) {
-  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
-}
 
 template <int EPL>
 __global__ void __launch_bounds__(256) topk_gate_kernel(const float* __restrict__ logits, int s,
@@ -64,78 +51,12 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float* __restrict_
       const int j = lane + 32 * i;
       nxt[i] = (tn < s && j < e) ? __ldg(logits + (size_t)tn * e + j) : 0.0f;
     }
-    // this lane's candidates, experts lane + 32*i; key 0 marks padding (below -inf)
-    uint32_t key[EPL];
-    int id[EPL];
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int j = lane + 32 * i;
-      const float v = cur[i];
-      if (j < e && !isfinite(v)) bad = true;
-      key[i] = j < e ? order_key(v) : 0u;
-      id[i] = j;
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_status(status, MOE_DEV_NONFINITE);
-    // stable sort of the lane's candidates, largest key first (equal keys keep
-    // their ascending expert order)
-#pragma unroll
-    for (int a = 0; a < EPL; ++a)
-#pragma unroll
-      for (int b = EPL - 1; b > a; --b)
-        if (key[b] > key[b - 1]) {
-          const uint32_t tk = key[b];
-          key[b] = key[b - 1];
-          key[b - 1] = tk;
-          const int ti = id[b];
-          id[b] = id[b - 1];
-          id[b - 1] = ti;
-        }
-    // the lane's values, kept for the full-softmax sum before the selection
-    // consumes them; the first `nvalid` sorted entries are real experts
-    const int nvalid = min(EPL, max(0, (e - lane + 31) / 32));
-    float all_v[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) all_v[i] = key_value(key[i]);
-    uint32_t top_key = 0;
-    uint32_t sel_key = 0;
-    int sel_id = 0;
-    // k rounds: the warp's largest head key, ties to the lower expert id
-    for (int r = 0; r < k; ++r) {
-      const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
-      const uint32_t cand = key[0] == m ? (uint32_t)id[0] : 0xffffffffu;
-      const uint32_t j = __reduce_min_sync(0xffffffffu, cand);
-      if (key[0] == m && (uint32_t)id[0] == j) {  // the winner pops its head
-#pragma unroll
-        for (int i = 0; i + 1 < EPL; ++i) {
-          key[i] = key[i + 1];
-          id[i] = id[i + 1];
-        }
-        key[EPL - 1] = 0u;
-      }
-      if (lane == r) {
-        sel_key = m;
-        sel_id = (int)j;
-      }
-      if (r == 0) top_key = m;
-    }
-    const float top = key_value(top_key);
-    const float sel_v = key_value(sel_key);
-
-    float z = 0.f;
-    if (renorm) {
-      if (lane < k) z = expf(sel_v - top);
-    } else {
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        if (i < nvalid) z += expf(all_v[i] - top);
-    }
-    float den = z;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    int sel_id;
+    float g;
+    if (topk_token<EPL>(cur, lane, e, k, renorm, &sel_id, &g) && lane == 0) raise_status(status, MOE_DEV_NONFINITE);
     if (lane < k) {
       idx[(size_t)t * k + lane] = sel_id;
-      gate[(size_t)t * k + lane] = expf(sel_v - top) / den;
+      gate[(size_t)t * k + lane] = g;
     }
   }
   pdl_trigger_late();

@@ -67,12 +67,28 @@ struct LayoutOut {
   int32_t* inv_row = nullptr;    // [rows]: token of each kept route's row (optional)
 };
 
+// One build of a layout into its arrays (the look-back words must have been
+// zeroed once, or left by an earlier build of the same plan: the kernel
+// takes the other parity from each tile's own row).  clear_status: the
+// kernel itself zeroes the status word and the rank counts (so a rebuild
+// needs no memset).  logits != nullptr: the top-k gate runs fused in the
+// same kernel (renorm; the ids to gate_idx, the gates to gate_val); only
+// when layout_can_fuse_gate(plan, priority).
+struct LayoutBuild {
+  int clear_status = 0;
+  const float* logits = nullptr;
+  int renorm = 1;
+  int32_t* gate_idx = nullptr;
+  float* gate_val = nullptr;
+};
+bool layout_can_fuse_gate(const LayoutPlan& plan, int priority);
+
 // priority 0 = token order, 1 = k-major; pad_multiple >= 1 pads dropless
 // expert segments.  The plan must be made for s units (s * k when k-major).
 cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity, int R,
                           int priority, int pad_multiple, const LayoutPlan& plan,
                           const LayoutOut& out, int hold_tile, long long timeout_ns,
-                          cudaStream_t st);
+                          cudaStream_t st, const LayoutBuild& build);
 
 // Allocation-free layout: the look-back scratch is a file-scope device array
 // of noalloc_lookback_words() words; returns cudaErrorInvalidValue (and sets

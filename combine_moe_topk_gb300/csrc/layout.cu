@@ -32,9 +32,26 @@
 // records MOE_DEV_TIMEOUT and carries on with what it has (no hang, no trap).
 // All tiles are co-resident (cooperative launch), which is what makes the
 // wait for the last tile safe.
+//
+// Rebuilds.  A handle's layout can be rebuilt in place from new routes with
+// no allocation and no memset: a look-back word counts as published when its
+// top bit equals the build's parity, and every build rewrites every tile's
+// row, so the previous build's rows read as unpublished.  The parity is
+// found on the device, not passed in (so a CUDA graph that replays a build
+// stays right): each tile reads the top bit of its own row, which only it
+// writes -- zero after the allocation's memset, else the previous build's
+// parity -- and takes the other value.  Tile 0 clears the status word and
+// the rank counts before it publishes; every other tile reads tile 0's row
+// before its own atomics.
+//
+// Fused gate.  With router logits instead of expert ids, phase A first runs
+// the top-k gate (gate_core.cuh, the gate kernel's own arithmetic) for the
+// tile's tokens -- each warp its 32 tokens of a sub-tile, one at a time, the
+// next token's logits loaded ahead -- and writes the ids and gates out.
 #include <mutex>
 
 #include "common.cuh"
+#include "gate_core.cuh"
 #include "internal.h"
 
 namespace moe {
@@ -73,6 +90,13 @@ struct Params {
   LayoutOut out;
   int hold_tile;
   long long timeout_ns;
+  int clear_status;      // tile 0 clears the status word and the rank counts
+  // fused gate (layout_kernel with EPL > 0): router logits [s, e] in, the
+  // caller's ids [s, k] and gates [s, k] out
+  const float* logits;
+  int renorm;
+  int32_t* gate_idx;
+  float* gate_val;
 };
 
 // Index of unit v's first route in the caller's [s_tok, k_tok] arrays.
@@ -91,12 +115,20 @@ __device__ __forceinline__ uint4 ld_relaxed_v4(const uint4* p) {
   return v;
 }
 
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void st_relaxed_u32(unsigned* p, unsigned v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ bool all_published(const uint4& w) {
-  return (w.x & w.y & w.z & w.w & kPublished) != 0;
+// All four words carry this build's publish bit (pub = kPublished or 0).
+__device__ __forceinline__ bool all_published(const uint4& w, unsigned pub) {
+  const unsigned x = pub ? (w.x & w.y & w.z & w.w) : ~(w.x | w.y | w.z | w.w);
+  return (x & kPublished) != 0;
 }
 
 // Load token t's k expert ids (16- or 8-byte loads when k allows) and mark
@@ -158,13 +190,16 @@ __device__ __forceinline__ void mark_routes(const Params& p, unsigned (*mask)[kM
 // of every tile read.  Waits are bounded; a time-out sets *timed_out and the
 // missing rows count as empty.
 __device__ void lookback(const Params& p, int tile, int nread, const int* s_agg, int* s_excl,
-                         int* s_tot, uint64_t deadline, bool* timed_out) {
+                         int* s_tot, unsigned pub, uint64_t deadline, bool* timed_out) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int e4 = padded_e(p.e);
   unsigned* rows = reinterpret_cast<unsigned*>(p.out.lookback);
+  // release: this tile's earlier writes (tile 0's cleared status word and
+  // rank counts) before its published row
+  __threadfence();
   if (tile != p.hold_tile)
     for (int x = tid; x < e4; x += kThreads)
-      st_relaxed_u32(rows + (size_t)tile * e4 + x, kPublished | (unsigned)(x < p.e ? s_agg[x] : 0));
+      st_relaxed_u32(rows + (size_t)tile * e4 + x, pub | (unsigned)(x < p.e ? s_agg[x] : 0));
 
   const int quads = e4 / 4;
   const int groups = kThreads / quads;  // threads (g, q) read tiles g, g + groups, ...
@@ -178,18 +213,18 @@ __device__ void lookback(const Params& p, int tile, int nread, const int* s_agg,
       for (int u = 0; u < kLookbackLoads; ++u) {
         const int b = b0 + groups * u;
         w[u] = (b < nread && b != tile) ? ld_relaxed_v4(col + (size_t)b * quads)
-                                         : make_uint4(kPublished, kPublished, kPublished, kPublished);
+                                         : make_uint4(pub, pub, pub, pub);
       }
 #pragma unroll
       for (int u = 0; u < kLookbackLoads; ++u) {
         const int b = b0 + groups * u;
         if (b >= nread || b == tile) continue;
-        for (uint32_t it = 0; !all_published(w[u]) && !*timed_out; ++it) {
+        for (uint32_t it = 0; !all_published(w[u], pub) && !*timed_out; ++it) {
           __nanosleep(32);
           if ((it & 15) == 15 && globaltimer_ns() > deadline) *timed_out = true;
           w[u] = ld_relaxed_v4(col + (size_t)b * quads);
         }
-        if (*timed_out && !all_published(w[u])) continue;
+        if (*timed_out && !all_published(w[u], pub)) continue;
         const unsigned v[4] = {w[u].x & ~kPublished, w[u].y & ~kPublished, w[u].z & ~kPublished,
                                w[u].w & ~kPublished};
 #pragma unroll
@@ -199,6 +234,15 @@ __device__ void lookback(const Params& p, int tile, int nread, const int* s_agg,
         }
       }
     }
+  }
+  // acquire: the rows read (tile 0's above all) before this tile's atomics
+  __threadfence();
+  // a held tile (test hook) publishes only after its own deadline, so that
+  // every build still rewrites every row
+  if (tile == p.hold_tile) {
+    while (globaltimer_ns() <= deadline) __nanosleep(1000);
+    for (int x = tid; x < e4; x += kThreads)
+      st_relaxed_u32(rows + (size_t)tile * e4 + x, pub | (unsigned)(x < p.e ? s_agg[x] : 0));
   }
   // sum the lanes of the warp that read the same column (xor shuffles, when
   // the column count is a power of two), then shared atomics per column
@@ -355,11 +399,52 @@ __device__ __forceinline__ void count_ranks(unsigned long long ranks, int lane, 
   }
 }
 
+// Fused gate: warp `warp` selects the top-k experts of tokens base .. base+31
+// (those below s), one token at a time with the next token's logits loaded
+// ahead, writes the ids and gates to the caller's arrays and the ids to
+// s_ids[i][j] (token base + i, route j) for the slot pass.  Returns whether
+// any of the tokens had a non-finite logit.
+template <int EPL>
+__device__ bool gate_warp_tokens(const Params& p, int base, int lane, uint8_t (*s_ids)[kMaxK]) {
+  const int n = min(32, p.s - base);
+  bool bad = false;
+  float nxt[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int j = lane + 32 * i;
+    nxt[i] = (n > 0 && j < p.e) ? __ldg(p.logits + (size_t)base * p.e + j) : 0.0f;
+  }
+  for (int i = 0; i < n; ++i) {
+    const int t = base + i;
+    float cur[EPL];
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) cur[q] = nxt[q];
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+      const int j = lane + 32 * q;
+      nxt[q] = (i + 1 < n && j < p.e) ? __ldg(p.logits + (size_t)(t + 1) * p.e + j) : 0.0f;
+    }
+    int sel;
+    float g;
+    bad |= topk_token<EPL>(cur, lane, p.e, p.k, p.renorm, &sel, &g);
+    if (lane < p.k) {
+      p.gate_idx[(size_t)t * p.k + lane] = sel;
+      p.gate_val[(size_t)t * p.k + lane] = g;
+      s_ids[i][lane] = (uint8_t)sel;
+    }
+  }
+  __syncwarp();
+  return bad;
+}
+
 // One CTA per tile; TPT > 0: the tile is exactly TPT sub-tiles and each
 // thread keeps its TPT tokens' routes in registers from the histogram to the
 // slot pass; TPT == 0: any number of sub-tiles, routes reloaded per pass.
-template <int TPT>
+// EPL > 0: the fused gate (router logits in, EPL logits per lane; TPT > 0
+// only, since the routes stay in registers between the passes).
+template <int TPT, int EPL>
 __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
+  static_assert(EPL == 0 || TPT > 0, "the fused gate keeps its routes in registers");
   constexpr int NM = TPT > 0 ? TPT : 1;
   __shared__ unsigned s_mask[NM][kWarps][kMaxE];
   __shared__ int s_wbase[NM][kWarps][kMaxE];
@@ -368,7 +453,9 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   __shared__ int s_tot[kMaxE];
   __shared__ int s_off[kMaxE + 1];
   __shared__ int s_rank[kMaxR];
-  __shared__ int s_flags;  // bit 0: a bad route; bit 1: a wait timed out
+  __shared__ int s_flags;  // bit 0: a bad route; bit 1: a wait timed out; bit 2: a non-finite logit
+  __shared__ unsigned s_pub;  // this build's publish bit
+  __shared__ uint8_t s_ids[EPL > 0 ? kWarps : 1][32][kMaxK];  // fused gate: ids of the warp's tokens
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x;
@@ -385,7 +472,19 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
     s_excl[x] = 0;
   }
   if (tid < kMaxR) s_rank[tid] = 0;
-  if (tid == 0) s_flags = 0;
+  if (tid == 0) {
+    s_flags = 0;
+    // this tile's own row, as the previous build (or the zeroing) left it
+    const unsigned own = ld_relaxed_u32(reinterpret_cast<const unsigned*>(p.out.lookback) +
+                                        (size_t)tile * padded_e(p.e));
+    s_pub = (own & kPublished) ? 0u : kPublished;
+  }
+  // a rebuild: tile 0 clears what the kernel accumulates into (published
+  // with its look-back row, which every other tile reads before its atomics)
+  if (p.clear_status && tile == 0) {
+    if (tid == 0 && p.out.status) *p.out.status = 0;
+    if (p.out.rank_counts && tid < p.R_tok) p.out.rank_counts[tid] = 0;
+  }
   __syncthreads();
 
   // ---- A: token masks and the tile histogram -------------------------------
@@ -397,9 +496,25 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
     for (int r = 0; r < NM; ++r) {
       const int t = (sub0 + r) * kThreads + tid;
       valid[r] = 0;
+      if (EPL > 0 && sub0 + r < sub1) {
+        // the warp's 32 tokens of this sub-tile: select, then each thread
+        // takes its own token's ids
+        constexpr int GE = EPL > 0 ? EPL : 1;
+        if (gate_warp_tokens<GE>(p, (sub0 + r) * kThreads + warp * 32, lane, s_ids[warp]) && lane == 0)
+          atomicOr(&s_flags, 4);
+        if (t < p.s) {
+#pragma unroll
+          for (int j = 0; j < kMaxK; ++j)
+            if (j < p.k) xs[r][j] = s_ids[warp][lane][j];
+          valid[r] = (1u << p.k) - 1u;  // k distinct ids in [0, e)
+        }
+        __syncwarp();
+      }
       if (sub0 + r < sub1 && t < p.s) {
-        valid[r] = load_routes(p, t, xs[r]);
-        bad |= valid[r] != (1u << p.k) - 1u;
+        if (EPL == 0) {
+          valid[r] = load_routes(p, t, xs[r]);
+          bad |= valid[r] != (1u << p.k) - 1u;
+        }
         store_route_ints(p.out.idx + unit_base(p, t), xs[r], p.k);
         mark_routes(p, s_mask[r], warp, lane, xs[r], valid[r]);
       }
@@ -448,7 +563,7 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   const bool last = tile == p.tiles - 1;
   const int nread = (p.capacity == 0 || last) ? p.tiles : tile;
   bool timed_out = false;
-  lookback(p, tile, nread, s_agg, s_excl, s_tot, deadline, &timed_out);
+  lookback(p, tile, nread, s_agg, s_excl, s_tot, s_pub, deadline, &timed_out);
   if (timed_out) atomicOr(&s_flags, 2);
   __syncthreads();
   if (p.capacity == 0 || last) {
@@ -510,6 +625,7 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
     int bits = 0;
     if (s_flags & 1) bits |= MOE_DEV_BAD_ROUTE;
     if (s_flags & 2) bits |= MOE_DEV_TIMEOUT;
+    if (s_flags & 4) bits |= MOE_DEV_NONFINITE;
     raise_status(p.out.status, bits);
   }
 }
@@ -581,16 +697,27 @@ size_t lookback_bytes(const LayoutPlan& plan, int e) {
 // The fewest co-resident blocks per SM over the kernel variants, so that a
 // plan fits whichever variant runs it.
 int layout_blocks_per_sm() {
-  int a = blocks_per_sm((const void*)layout_kernel<0>);
-  int b = blocks_per_sm((const void*)layout_kernel<1>);
-  int c = blocks_per_sm((const void*)layout_kernel<2>);
-  return a < b ? (a < c ? a : c) : (b < c ? b : c);
+  const void* kerns[] = {
+      (const void*)layout_kernel<0, 0>, (const void*)layout_kernel<1, 0>, (const void*)layout_kernel<2, 0>,
+      (const void*)layout_kernel<1, 1>, (const void*)layout_kernel<1, 2>, (const void*)layout_kernel<1, 4>,
+      (const void*)layout_kernel<1, 8>, (const void*)layout_kernel<2, 1>, (const void*)layout_kernel<2, 2>,
+      (const void*)layout_kernel<2, 4>, (const void*)layout_kernel<2, 8>};
+  int n = 1 << 30;
+  for (const void* k : kerns) {
+    const int b = blocks_per_sm(k);
+    if (b < n) n = b;
+  }
+  return n;
+}
+
+bool layout_can_fuse_gate(const LayoutPlan& plan, int priority) {
+  return priority == 0 && plan.subtiles_per_tile >= 1 && plan.subtiles_per_tile <= 2;
 }
 
 cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity, int R,
                           int priority, int pad_multiple, const LayoutPlan& plan,
                           const LayoutOut& out, int hold_tile, long long timeout_ns,
-                          cudaStream_t st) {
+                          cudaStream_t st, const LayoutBuild& build) {
   Params p;
   p.topk_idx = topk_idx;
   p.kmajor = priority == 1;
@@ -608,6 +735,12 @@ cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capa
   p.out = out;
   p.hold_tile = hold_tile;
   p.timeout_ns = timeout_ns;
+  p.clear_status = build.clear_status;
+  p.logits = build.logits;
+  p.renorm = build.renorm;
+  p.gate_idx = build.gate_idx;
+  p.gate_val = build.gate_val;
+  if (p.logits && !layout_can_fuse_gate(plan, priority)) return cudaErrorInvalidValue;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.tiles);
@@ -620,12 +753,23 @@ cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capa
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t err;
-  if (plan.subtiles_per_tile == 1)
-    err = cudaLaunchKernelEx(&cfg, layout_kernel<1>, p);
-  else if (plan.subtiles_per_tile == 2)
-    err = cudaLaunchKernelEx(&cfg, layout_kernel<2>, p);
-  else
-    err = cudaLaunchKernelEx(&cfg, layout_kernel<0>, p);
+  const int tpt = plan.subtiles_per_tile;
+  if (p.logits) {
+    const int epl = (e + 31) / 32;
+#define MOE_LAYOUT_GATE(T)                                             \
+  (epl == 1   ? cudaLaunchKernelEx(&cfg, layout_kernel<T, 1>, p)      \
+   : epl == 2 ? cudaLaunchKernelEx(&cfg, layout_kernel<T, 2>, p)      \
+   : epl <= 4 ? cudaLaunchKernelEx(&cfg, layout_kernel<T, 4>, p)      \
+              : cudaLaunchKernelEx(&cfg, layout_kernel<T, 8>, p))
+    err = tpt == 1 ? MOE_LAYOUT_GATE(1) : MOE_LAYOUT_GATE(2);
+#undef MOE_LAYOUT_GATE
+  } else if (tpt == 1) {
+    err = cudaLaunchKernelEx(&cfg, layout_kernel<1, 0>, p);
+  } else if (tpt == 2) {
+    err = cudaLaunchKernelEx(&cfg, layout_kernel<2, 0>, p);
+  } else {
+    err = cudaLaunchKernelEx(&cfg, layout_kernel<0, 0>, p);
+  }
   if (err != cudaSuccess || !p.kmajor || s == 0) return err;
   constexpr int kMaxPostBlocks = 1024;  // grid-stride beyond this
   int blocks = (s + kThreads - 1) / kThreads;
@@ -720,7 +864,8 @@ cudaError_t launch_layout_noalloc(const int32_t* topk_idx, int s, int e, int k, 
   if (err == cudaSuccess && R > 0)
     err = cudaMemsetAsync(out.rank_counts, 0, (size_t)R * sizeof(int32_t), st);
   if (err != cudaSuccess) return err;
-  return launch_layout(topk_idx, s, e, k, capacity, R, 0, 1, plan, out, -1, 2000000000LL, st);
+  LayoutBuild build;  // status: the caller's word, OR-ed into
+  return launch_layout(topk_idx, s, e, k, capacity, R, 0, 1, plan, out, -1, 2000000000LL, st, build);
 }
 
 }  // namespace moe

@@ -87,15 +87,22 @@ enum {
   MOE_KERNEL_DISPATCH_GEMM = 8,
   MOE_KERNEL_RANK_SLOTS = 9,
   MOE_KERNEL_COMBINE_GATE_BWD = 10,
-  MOE_KERNEL_COUNT = 11
+  MOE_KERNEL_GATE_LAYOUT = 11,
+  MOE_KERNEL_COUNT = 12
 };
 
 /* Opaque layout handle [P1 "How"; P3 description].  Owned by the library:
- * built by moe_dispatch_layout, immutable afterwards, replayable any number
- * of times by dispatch / combine and their backwards, alive until
- * moe_handle_destroy (so a backward issued after later forwards still finds
- * it).  Its device arrays come from a library memory pool, allocated and
- * freed in stream order on the stream it was built on. */
+ * built by moe_dispatch_layout, replayable any number of times by dispatch /
+ * combine and their backwards, alive until moe_handle_destroy (so a backward
+ * issued after later forwards still finds it).  Its device arrays come from a
+ * library memory pool, allocated in stream order on the stream it was
+ * created on and freed on the stream of its latest build.  A handle can also
+ * be created empty (moe_layout_create) and built in place, again and again,
+ * from new routes of the same shape (moe_layout_rebuild,
+ * moe_topk_gate_layout): a build replaces the layout in stream order, so
+ * work enqueued before it sees the old layout and work after it the new
+ * one; builds of one handle must be ordered with each other and with every
+ * use of the handle (one stream, or events). */
 typedef struct moe_handle_s* moe_handle;
 
 /* Capacity priority of moe_dispatch_layout_ex. */
@@ -186,6 +193,37 @@ moe_status moe_topk_gate_bwd(const float* logits, const int32_t* topk_idx, const
  * row = -1.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_OOM, MOE_ERR_CUDA. */
 moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity,
                                int num_virtual_ranks, void* stream, moe_handle* out);
+
+/* An empty layout handle for s tokens, e experts, k routes per token and the
+ * layout options of moe_dispatch_layout_ex: its device arrays are allocated
+ * (and their flags zeroed) on `stream`, but it holds no layout until the
+ * first moe_layout_rebuild or moe_topk_gate_layout; payload calls on it
+ * before that return MOE_ERR_INVALID_ARG.  For per-step builds that should
+ * not allocate [P1 description: the layout is recomputed every step].
+ * Errors as moe_dispatch_layout_ex. */
+moe_status moe_layout_create(int s, int e, int k, const moe_layout_options* options, void* stream,
+                             moe_handle* out);
+
+/* Build (or rebuild) h's layout in place from new expert ids topk_idx
+ * i32 [h.s, h.k]: the same arrays, counts and status as
+ * moe_dispatch_layout_ex with h's options would give, written into h's own
+ * memory with no allocation and no memset (the layout kernel clears the
+ * status word and rank counts itself).  See moe_handle on ordering.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_HANDLE_MISMATCH, MOE_ERR_CUDA. */
+moe_status moe_layout_rebuild(moe_handle h, const int32_t* topk_idx, void* stream);
+
+/* Top-k gating fused into the layout build [P4 change 1; P1 description].
+ * logits f32 [h.s, h.e] -> topk_idx i32 [h.s, h.k] and topk_gate f32
+ * [h.s, h.k] exactly as moe_topk_gate(logits, ..., renorm) writes them, and
+ * h's layout built from those ids as moe_layout_rebuild would: one kernel,
+ * in which each tile selects its own tokens' experts before counting them.
+ * Non-finite logits set MOE_DEV_NONFINITE in h's status word.  Layouts with
+ * k-major priority, and batches long enough that a layout tile spans more
+ * than two sub-tiles of 256 tokens, run the gate kernel and then the layout
+ * kernel instead (the same results).  Errors as moe_layout_rebuild;
+ * renorm other than 0 or 1 is MOE_ERR_INVALID_ARG. */
+moe_status moe_topk_gate_layout(moe_handle h, const float* logits, int renorm, int32_t* topk_idx,
+                                float* topk_gate, void* stream);
 
 /* Allocation-free dispatch layout.  The paper has no counterpart: an
  * addition of this library for callers that cannot allocate device memory

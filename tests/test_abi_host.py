@@ -95,6 +95,13 @@ def test_layout_rejects_bad_sizes_without_a_gpu(lib):
     assert rc_name(lib.moe_dispatch_layout_ex(fake, 4, 8, 2, ctypes.byref(opt), None, ctypes.byref(out))) \
         == "MOE_ERR_INVALID_ARG"
     assert out.value is None
+    # an empty handle for in-place builds: the same checks, before any CUDA call
+    assert rc_name(lib.moe_layout_create(4, 8, 2, ctypes.byref(B.LayoutOptions(0, 3, 0, 1, 0)), None,
+                                         ctypes.byref(out))) == "MOE_ERR_INVALID_ARG"
+    assert rc_name(lib.moe_layout_create(4, 8, 9, ctypes.byref(B.LayoutOptions(0, 0, 0, 1, 0)), None,
+                                         ctypes.byref(out))) == "MOE_ERR_INVALID_ARG"
+    assert rc_name(lib.moe_layout_create(4, 8, 2, None, None, ctypes.byref(out))) == "MOE_ERR_INVALID_ARG"
+    assert out.value is None
 
 
 def test_unknown_handles_are_rejected_without_a_gpu(lib):
@@ -109,6 +116,9 @@ def test_unknown_handles_are_rejected_without_a_gpu(lib):
                                             None)) == "MOE_ERR_HANDLE_MISMATCH"
     assert rc_name(lib.moe_combine_gate_bwd(None, 4, 8, 8, 1, fake, fake, fake, None, 1, fake, fake, fake,
                                             None)) == "MOE_ERR_INVALID_ARG"
+    assert rc_name(lib.moe_layout_rebuild(bogus, fake, None)) == "MOE_ERR_HANDLE_MISMATCH"
+    assert rc_name(lib.moe_layout_rebuild(None, fake, None)) == "MOE_ERR_INVALID_ARG"
+    assert rc_name(lib.moe_topk_gate_layout(bogus, fake, 1, fake, fake, None)) == "MOE_ERR_HANDLE_MISMATCH"
     assert rc_name(lib.moe_grouped_gemm(None, 8, 64, 64, fake, fake, fake, None)) == "MOE_ERR_INVALID_ARG"
     assert rc_name(lib.moe_grouped_gemm(bogus, 8, 64, 64, fake, fake, fake, None)) == "MOE_ERR_HANDLE_MISMATCH"
     assert rc_name(lib.moe_dispatch_grouped_gemm(None, 4, 8, 64, 64, fake, fake, fake, None)) == "MOE_ERR_INVALID_ARG"
