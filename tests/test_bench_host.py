@@ -32,13 +32,15 @@ def test_byte_model_of_the_mixtral_like_step():
 
 def test_byte_model_of_the_fused_backward_and_the_step():
     """The fused combine + gate backward moves the combine backward's bytes
-    plus the expert ids read and the router gradient written; a step counts
-    each op it runs once (not the separate backward ops as well)."""
+    plus the expert ids read and the router gradient written; the fused gate
+    + layout the two ops' bytes less the ids read back; a step counts each
+    op it runs once (not the separate ops as well)."""
     w = W.WORKLOADS["fine-grained-skewed"]
     b = bench.step_bytes(w, kept=w.s * w.k, u=w.s)
     assert b["combine_gate_bwd"] == b["combine_bwd"] + w.s * w.k * 4 + w.s * w.e * 4
+    assert b["gate_layout"] == b["topk_gate"] + b["layout"] - w.s * w.k * 4  # the ids are not read back
     assert bench.step_sum(b) == sum(b[op] for op in
-                                    ("topk_gate", "layout", "dispatch", "combine", "combine_gate_bwd", "dispatch_bwd"))
+                                    ("gate_layout", "dispatch", "combine", "combine_gate_bwd", "dispatch_bwd"))
     wn = W.WORKLOADS["tiny-capacity"].replace(renorm=0)
     bn = bench.step_bytes(wn, kept=100, u=60)
     assert bn["combine_gate_bwd"] == bn["combine_bwd"] + wn.s * wn.k * 4 + 2 * wn.s * wn.e * 4
