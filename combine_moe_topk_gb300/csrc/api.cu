@@ -150,7 +150,10 @@ void init_device(int dev) {
   cudaError_t err = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
   if (err == cudaSuccess)
     err = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (err == cudaSuccess) di.layout_blocks_per_sm = moe::layout_blocks_per_sm();
+  if (err == cudaSuccess) {
+    di.layout_blocks_per_sm = moe::layout_blocks_per_sm();
+    di.gate_layout_blocks_per_sm = moe::gate_layout_blocks_per_sm();
+  }
   if (err == cudaSuccess) {
     cudaMemPoolProps props = {};
     props.allocType = cudaMemAllocationTypePinned;
@@ -398,12 +401,12 @@ moe_status build_handle(moe_handle h, const int32_t* topk_idx, const float* logi
   moe::LayoutBuild build;
   build.clear_status = 1;
   cudaError_t err = cudaSuccess;
-  if (logits && !moe::layout_can_fuse_gate(h->plan, h->priority)) {
-    // the layout variant cannot select in its first pass: the gate kernel
-    // first, then the layout on its ids (status cleared before the gate
-    // reports into it)
-    const moe::DeviceInfo* di = nullptr;
-    MOE_TRY(device_state(h->device, &di));
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(h->device, &di));
+  if (logits && !moe::layout_can_fuse_gate(h->plan, h->priority, h->e, *di)) {
+    // the layout kernel cannot select in its first pass here: the gate
+    // kernel first, then the layout on its ids (the status word cleared
+    // before the gate reports into it)
     err = cudaMemsetAsync(h->blob, 0, h->clear_bytes, st);
     if (err == cudaSuccess)
       err = moe::launch_topk_gate(logits, h->s, h->e, h->k, renorm, gate_idx, gate_val, h->out.status, *di, st);

@@ -115,3 +115,87 @@ __device__ __forceinline__ bool topk_token(const float (&cur)[EPL], int lane, in
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// The warp's butterfly sum (xor offsets 16, 8, 4, 2, 1; each lane adds its
+// partner's value to its own) of v[0..31], as one thread: IEEE addition is
+// commutative, so every lane of the warp ends with exactly this tree.
+__device__ __forceinline__ float butterfly_tree32(const float (&v)[32]) {
+  float a[16], b[8], c[4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = v[i] + v[i + 16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) b[i] = a[i] + a[i + 8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = b[i] + b[i + 4];
+  return (c[0] + c[2]) + (c[1] + c[3]);
+}
+
+// topk_token<1> (e <= 32: expert j on lane j) computed by one thread for one
+// token: the same k ids in the same order (largest key first, the lower id
+// on equal keys) and the same gate bits (the same expf terms, summed in the
+// warp's butterfly order).  row = the token's e logits (16-byte aligned when
+// e is a multiple of 4).  Returns whether a logit is NaN or infinite.
+__device__ __forceinline__ bool topk_token_thread(const float* __restrict__ row, int e, int k, int renorm,
+                                                  int* ids, float* gates) {
+  float v[32];
+  if ((e & 3) == 0) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (4 * q < e) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(row) + q);
+        v[4 * q] = f.x;
+        v[4 * q + 1] = f.y;
+        v[4 * q + 2] = f.z;
+        v[4 * q + 3] = f.w;
+      }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < e) v[j] = __ldg(row + j);
+  }
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (j < e && !isfinite(v[j])) bad = true;
+  uint32_t taken = 0, top_key = 0;
+  uint32_t sel_key[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    sel_key[r] = 0;
+    if (r < k) {
+      uint32_t best = 0;
+      int bj = -1;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < e && !((taken >> j) & 1u)) {
+          const uint32_t kj = order_key(v[j]);
+          if (bj < 0 || kj > best) {  // ascending j: equal keys keep the lower id
+            best = kj;
+            bj = j;
+          }
+        }
+      taken |= 1u << bj;
+      ids[r] = bj;
+      sel_key[r] = best;
+      if (r == 0) top_key = best;
+    }
+  }
+  const float top = key_value(top_key);
+  float z[32];
+  if (renorm) {
+#pragma unroll
+    for (int r = 0; r < 32; ++r) z[r] = (r < 16 && r < k) ? expf(key_value(sel_key[r < 16 ? r : 0]) - top) : 0.f;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) z[j] = j < e ? expf(key_value(order_key(v[j])) - top) : 0.f;
+  }
+  const float den = butterfly_tree32(z);
+#pragma unroll
+  for (int r = 0; r < 16; ++r)
+    if (r < k) gates[r] = expf(key_value(sel_key[r]) - top) / den;
+  return bad;
+}
+
+}  // namespace moe

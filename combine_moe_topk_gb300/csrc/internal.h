@@ -30,6 +30,7 @@ struct OncePerDevice {
 struct DeviceInfo {
   int sms = 0;                 // streaming multiprocessors
   int layout_blocks_per_sm = 0;
+  int gate_layout_blocks_per_sm = 0;  // the layout kernel with the gate fused in
   int max_smem_optin = 0;      // bytes of dynamic shared memory a block may opt into
 };
 
@@ -73,7 +74,7 @@ struct LayoutOut {
 // kernel itself zeroes the status word and the rank counts (so a rebuild
 // needs no memset).  logits != nullptr: the top-k gate runs fused in the
 // same kernel (renorm; the ids to gate_idx, the gates to gate_val); only
-// when layout_can_fuse_gate(plan, priority).
+// when layout_can_fuse_gate(plan, priority, e, di).
 struct LayoutBuild {
   int clear_status = 0;
   const float* logits = nullptr;
@@ -81,7 +82,8 @@ struct LayoutBuild {
   int32_t* gate_idx = nullptr;
   float* gate_val = nullptr;
 };
-bool layout_can_fuse_gate(const LayoutPlan& plan, int priority);
+bool layout_can_fuse_gate(const LayoutPlan& plan, int priority, int e, const DeviceInfo& di);
+int gate_layout_blocks_per_sm();
 
 // priority 0 = token order, 1 = k-major; pad_multiple >= 1 pads dropless
 // expert segments.  The plan must be made for s units (s * k when k-major).

@@ -44,10 +44,14 @@
 // the rank counts before it publishes; every other tile reads tile 0's row
 // before its own atomics.
 //
-// Fused gate.  With router logits instead of expert ids, phase A first runs
-// the top-k gate (gate_core.cuh, the gate kernel's own arithmetic) for the
-// tile's tokens -- each warp its 32 tokens of a sub-tile, one at a time, the
-// next token's logits loaded ahead -- and writes the ids and gates out.
+// Fused gate (e <= 32).  With router logits instead of expert ids, phase A
+// first selects each token's experts in the token's own thread (all the
+// tile's logits loaded at once; topk_token_thread gives the gate kernel's
+// ids and gate bits) and writes the ids and gates out.  For more experts a
+// thread per token holds too many logits, and a warp per token inside a
+// tile selects its 32 tokens one after another: measured slower than the
+// gate kernel followed by the layout kernel, which is what runs there.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -399,52 +403,28 @@ __device__ __forceinline__ void count_ranks(unsigned long long ranks, int lane, 
   }
 }
 
-// Fused gate: warp `warp` selects the top-k experts of tokens base .. base+31
-// (those below s), one token at a time with the next token's logits loaded
-// ahead, writes the ids and gates to the caller's arrays and the ids to
-// s_ids[i][j] (token base + i, route j) for the slot pass.  Returns whether
-// any of the tokens had a non-finite logit.
-template <int EPL>
-__device__ bool gate_warp_tokens(const Params& p, int base, int lane, uint8_t (*s_ids)[kMaxK]) {
-  const int n = min(32, p.s - base);
-  bool bad = false;
-  float nxt[EPL];
+// Fused gate: thread t's token selects its experts (topk_token_thread, the
+// gate kernel's ids and gate bits for e <= 32) and writes the ids and gates
+// to the caller's arrays.  Returns whether a logit was not finite.
+__device__ __forceinline__ bool gate_thread_token(const Params& p, int t, int* xs) {
+  float g[kMaxK];
+  const bool bad = topk_token_thread(p.logits + (size_t)t * p.e, p.e, p.k, p.renorm, xs, g);
+  store_route_ints(p.gate_idx + (size_t)t * p.k, xs, p.k);
+  float* gd = p.gate_val + (size_t)t * p.k;
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int j = lane + 32 * i;
-    nxt[i] = (n > 0 && j < p.e) ? __ldg(p.logits + (size_t)base * p.e + j) : 0.0f;
-  }
-  for (int i = 0; i < n; ++i) {
-    const int t = base + i;
-    float cur[EPL];
-#pragma unroll
-    for (int q = 0; q < EPL; ++q) cur[q] = nxt[q];
-#pragma unroll
-    for (int q = 0; q < EPL; ++q) {
-      const int j = lane + 32 * q;
-      nxt[q] = (i + 1 < n && j < p.e) ? __ldg(p.logits + (size_t)(t + 1) * p.e + j) : 0.0f;
-    }
-    int sel;
-    float g;
-    bad |= topk_token<EPL>(cur, lane, p.e, p.k, p.renorm, &sel, &g);
-    if (lane < p.k) {
-      p.gate_idx[(size_t)t * p.k + lane] = sel;
-      p.gate_val[(size_t)t * p.k + lane] = g;
-      s_ids[i][lane] = (uint8_t)sel;
-    }
-  }
-  __syncwarp();
+  for (int j = 0; j < kMaxK; ++j)
+    if (j < p.k) gd[j] = g[j];
   return bad;
 }
 
 // One CTA per tile; TPT > 0: the tile is exactly TPT sub-tiles and each
 // thread keeps its TPT tokens' routes in registers from the histogram to the
 // slot pass; TPT == 0: any number of sub-tiles, routes reloaded per pass.
-// EPL > 0: the fused gate (router logits in, EPL logits per lane; TPT > 0
-// only, since the routes stay in registers between the passes).
-template <int TPT, int EPL>
+// GATE: the fused gate (router logits in, e <= 32; TPT > 0 only, since the
+// routes stay in registers between the passes).
+template <int TPT, bool GATE>
 __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
-  static_assert(EPL == 0 || TPT > 0, "the fused gate keeps its routes in registers");
+  static_assert(!GATE || TPT > 0, "the fused gate keeps its routes in registers");
   constexpr int NM = TPT > 0 ? TPT : 1;
   __shared__ unsigned s_mask[NM][kWarps][kMaxE];
   __shared__ int s_wbase[NM][kWarps][kMaxE];
@@ -455,7 +435,6 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   __shared__ int s_rank[kMaxR];
   __shared__ int s_flags;  // bit 0: a bad route; bit 1: a wait timed out; bit 2: a non-finite logit
   __shared__ unsigned s_pub;  // this build's publish bit
-  __shared__ uint8_t s_ids[EPL > 0 ? kWarps : 1][32][kMaxK];  // fused gate: ids of the warp's tokens
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x;
@@ -496,22 +475,11 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
     for (int r = 0; r < NM; ++r) {
       const int t = (sub0 + r) * kThreads + tid;
       valid[r] = 0;
-      if (EPL > 0 && sub0 + r < sub1) {
-        // the warp's 32 tokens of this sub-tile: select, then each thread
-        // takes its own token's ids
-        constexpr int GE = EPL > 0 ? EPL : 1;
-        if (gate_warp_tokens<GE>(p, (sub0 + r) * kThreads + warp * 32, lane, s_ids[warp]) && lane == 0)
-          atomicOr(&s_flags, 4);
-        if (t < p.s) {
-#pragma unroll
-          for (int j = 0; j < kMaxK; ++j)
-            if (j < p.k) xs[r][j] = s_ids[warp][lane][j];
-          valid[r] = (1u << p.k) - 1u;  // k distinct ids in [0, e)
-        }
-        __syncwarp();
-      }
       if (sub0 + r < sub1 && t < p.s) {
-        if (EPL == 0) {
+        if (GATE) {
+          if (gate_thread_token(p, t, xs[r])) atomicOr(&s_flags, 4);
+          valid[r] = (1u << p.k) - 1u;  // k distinct ids in [0, e)
+        } else {
           valid[r] = load_routes(p, t, xs[r]);
           bad |= valid[r] != (1u << p.k) - 1u;
         }
@@ -697,21 +665,24 @@ size_t lookback_bytes(const LayoutPlan& plan, int e) {
 // The fewest co-resident blocks per SM over the kernel variants, so that a
 // plan fits whichever variant runs it.
 int layout_blocks_per_sm() {
-  const void* kerns[] = {
-      (const void*)layout_kernel<0, 0>, (const void*)layout_kernel<1, 0>, (const void*)layout_kernel<2, 0>,
-      (const void*)layout_kernel<1, 1>, (const void*)layout_kernel<1, 2>, (const void*)layout_kernel<1, 4>,
-      (const void*)layout_kernel<1, 8>, (const void*)layout_kernel<2, 1>, (const void*)layout_kernel<2, 2>,
-      (const void*)layout_kernel<2, 4>, (const void*)layout_kernel<2, 8>};
-  int n = 1 << 30;
-  for (const void* k : kerns) {
-    const int b = blocks_per_sm(k);
-    if (b < n) n = b;
-  }
-  return n;
+  const int a = blocks_per_sm((const void*)layout_kernel<0, false>);
+  const int b = blocks_per_sm((const void*)layout_kernel<1, false>);
+  const int c = blocks_per_sm((const void*)layout_kernel<2, false>);
+  return a < b ? (a < c ? a : c) : (b < c ? b : c);
 }
 
-bool layout_can_fuse_gate(const LayoutPlan& plan, int priority) {
-  return priority == 0 && plan.subtiles_per_tile >= 1 && plan.subtiles_per_tile <= 2;
+// Co-resident CTAs per SM of the fused-gate variants.
+int gate_layout_blocks_per_sm() {
+  const int a = blocks_per_sm((const void*)layout_kernel<1, true>);
+  const int b = blocks_per_sm((const void*)layout_kernel<2, true>);
+  return a < b ? a : b;
+}
+
+std::atomic<bool> g_coop_pdl{true};  // the cooperative launch also takes programmatic serialisation
+
+bool layout_can_fuse_gate(const LayoutPlan& plan, int priority, int e, const DeviceInfo& di) {
+  return priority == 0 && e <= 32 && plan.subtiles_per_tile >= 1 && plan.subtiles_per_tile <= 2 &&
+         plan.tiles <= di.sms * di.gate_layout_blocks_per_sm;
 }
 
 cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity, int R,
@@ -740,35 +711,44 @@ cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capa
   p.renorm = build.renorm;
   p.gate_idx = build.gate_idx;
   p.gate_val = build.gate_val;
-  if (p.logits && !layout_can_fuse_gate(plan, priority)) return cudaErrorInvalidValue;
+  if (p.logits && (priority != 0 || e > 32 || plan.subtiles_per_tile < 1 || plan.subtiles_per_tile > 2))
+    return cudaErrorInvalidValue;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.tiles);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  // cooperative (every tile co-resident), and with programmatic stream
+  // serialisation where the driver takes both: the tiles may be scheduled
+  // while the previous kernel drains; each waits for it (griddepcontrol.wait)
+  // before its first read, and nothing that kernel runs waits on a tile.
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = (MOE_PDL != 0 && ((MOE_PDL_MASK >> MOE_KERNEL_LAYOUT) & 1) && g_coop_pdl.load()) ? 2 : 1;
   cudaError_t err;
   const int tpt = plan.subtiles_per_tile;
   if (p.logits) {
-    const int epl = (e + 31) / 32;
-#define MOE_LAYOUT_GATE(T)                                             \
-  (epl == 1   ? cudaLaunchKernelEx(&cfg, layout_kernel<T, 1>, p)      \
-   : epl == 2 ? cudaLaunchKernelEx(&cfg, layout_kernel<T, 2>, p)      \
-   : epl <= 4 ? cudaLaunchKernelEx(&cfg, layout_kernel<T, 4>, p)      \
-              : cudaLaunchKernelEx(&cfg, layout_kernel<T, 8>, p))
-    err = tpt == 1 ? MOE_LAYOUT_GATE(1) : MOE_LAYOUT_GATE(2);
-#undef MOE_LAYOUT_GATE
+    err = tpt == 1 ? cudaLaunchKernelEx(&cfg, layout_kernel<1, true>, p)
+                   : cudaLaunchKernelEx(&cfg, layout_kernel<2, true>, p);
   } else if (tpt == 1) {
-    err = cudaLaunchKernelEx(&cfg, layout_kernel<1, 0>, p);
+    err = cudaLaunchKernelEx(&cfg, layout_kernel<1, false>, p);
   } else if (tpt == 2) {
-    err = cudaLaunchKernelEx(&cfg, layout_kernel<2, 0>, p);
+    err = cudaLaunchKernelEx(&cfg, layout_kernel<2, false>, p);
   } else {
-    err = cudaLaunchKernelEx(&cfg, layout_kernel<0, 0>, p);
+    err = cudaLaunchKernelEx(&cfg, layout_kernel<0, false>, p);
+  }
+  if (err != cudaSuccess && cfg.numAttrs == 2) {
+    // the driver refused the pair of attributes: launch cooperative only,
+    // from now on
+    cudaGetLastError();
+    g_coop_pdl.store(false);
+    return launch_layout(topk_idx, s, e, k, capacity, R, priority, pad_multiple, plan, out, hold_tile, timeout_ns,
+                         st, build);
   }
   if (err != cudaSuccess || !p.kmajor || s == 0) return err;
   constexpr int kMaxPostBlocks = 1024;  // grid-stride beyond this

@@ -215,13 +215,14 @@ moe_status moe_layout_rebuild(moe_handle h, const int32_t* topk_idx, void* strea
 /* Top-k gating fused into the layout build [P4 change 1; P1 description].
  * logits f32 [h.s, h.e] -> topk_idx i32 [h.s, h.k] and topk_gate f32
  * [h.s, h.k] exactly as moe_topk_gate(logits, ..., renorm) writes them, and
- * h's layout built from those ids as moe_layout_rebuild would: one kernel,
- * in which each tile selects its own tokens' experts before counting them.
- * Non-finite logits set MOE_DEV_NONFINITE in h's status word.  Layouts with
- * k-major priority, and batches long enough that a layout tile spans more
- * than two sub-tiles of 256 tokens, run the gate kernel and then the layout
- * kernel instead (the same results).  Errors as moe_layout_rebuild;
- * renorm other than 0 or 1 is MOE_ERR_INVALID_ARG. */
+ * h's layout built from those ids as moe_layout_rebuild would.  With up to
+ * 32 experts (token priority, batches whose layout tiles span at most two
+ * sub-tiles of 256 tokens) this is one kernel, in which each token's thread
+ * selects its experts before the tile counts them; otherwise it is the gate
+ * kernel followed by the layout kernel (measured faster there than a fused
+ * form), with the same results.  No allocation and no memset either way.
+ * Non-finite logits set MOE_DEV_NONFINITE in h's status word.  Errors as
+ * moe_layout_rebuild; renorm other than 0 or 1 is MOE_ERR_INVALID_ARG. */
 moe_status moe_topk_gate_layout(moe_handle h, const float* logits, int renorm, int32_t* topk_idx,
                                 float* topk_gate, void* stream);
 

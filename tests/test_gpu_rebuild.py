@@ -92,7 +92,7 @@ def test_gate_fused_into_the_layout(name, renorm):
     bit-exact against the oracle's layout of those ids; twice in a row."""
     w = SHAPES[name].replace(s=W.WORKLOADS[name].s)  # the workload's own token count
     h = B.moe_layout_create(w.s, w.e, w.k, w.capacity, w.R, device=DEV)
-    n_fused = B.moe_launch_count("gate_layout")
+    n_fused, n_gate = B.moe_launch_count("gate_layout"), B.moe_launch_count("topk_gate")
     for seed in (w.seed, w.seed + 1):
         logits = W.make_logits(w, seed=seed)
         idx, gate = B.moe_topk_gate_layout(h, logits.to(DEV), renorm)
@@ -103,14 +103,18 @@ def test_gate_fused_into_the_layout(name, renorm):
         assert torch.equal(idx, idx2) and torch.equal(gate.view(torch.int32), gate2.view(torch.int32))
         check_layout(h, _oracle_layout(oi, w), oi)
         assert h.status() == 0
-    assert B.moe_launch_count("gate_layout") == n_fused + 2
+    # one kernel up to 32 experts; the gate kernel then the layout beyond
+    fused = 2 if w.e <= 32 else 0
+    assert B.moe_launch_count("gate_layout") == n_fused + fused
+    assert B.moe_launch_count("topk_gate") == n_gate + 4 - fused  # + the two separate calls above
     h.destroy()
 
 
 @pytest.mark.parametrize("case", [
-    dict(s=5000, e=64, k=6, capacity=400, R=4, priority="kmajor"),   # k-major: gate kernel, then layout
-    dict(s=1 << 17, e=256, k=4, capacity=0, R=8, priority="token"),  # tiles span 8 sub-tiles
-], ids=["kmajor", "many-subtiles"])
+    dict(s=5000, e=16, k=6, capacity=400, R=4, priority="kmajor"),   # k-major: gate kernel, then layout
+    dict(s=1 << 17, e=32, k=4, capacity=0, R=8, priority="token"),   # tiles span several sub-tiles
+    dict(s=3001, e=64, k=4, capacity=0, R=0, priority="token"),      # more than 32 experts
+], ids=["kmajor", "many-subtiles", "e64"])
 def test_gate_layout_where_the_layout_cannot_select(case):
     """Where the layout kernel cannot run the gate itself, the same entry
     point launches the gate kernel and then the layout: the same results."""
@@ -127,6 +131,32 @@ def test_gate_layout_where_the_layout_cannot_select(case):
         check_layout(h, _oracle_layout(oi, w, priority=1 if case["priority"] == "kmajor" else 0), oi)
         assert h.status() == 0
     assert B.moe_launch_count("topk_gate") == n_gate + 2
+    h.destroy()
+
+
+@pytest.mark.parametrize("case", [
+    dict(s=1000, e=32, k=16), dict(s=777, e=7, k=3), dict(s=300, e=1, k=1), dict(s=513, e=30, k=5),
+], ids=lambda c: f"e{c['e']}-k{c['k']}")
+@pytest.mark.parametrize("renorm", [1, 0])
+def test_fused_gate_edges_and_ties(case, renorm):
+    """The fused gate's thread-per-token selection at the edges of its range
+    (e = 32 with k = 16, odd e without 16-byte rows, e = 1), with logits on a
+    small grid so that ties are everywhere: the gate kernel's bits."""
+    s, e, k = case["s"], case["e"], case["k"]
+    g = torch.Generator().manual_seed(e * 100 + k)
+    logits = (torch.randint(-3, 4, (s, e), generator=g).float() * 0.5)
+    logits[::7] = -logits[::7]  # -0.0 against +0.0 as well
+    h = B.moe_layout_create(s, e, k, device=DEV)
+    n_fused = B.moe_launch_count("gate_layout")
+    idx, gate = B.moe_topk_gate_layout(h, logits.to(DEV), renorm)
+    assert B.moe_launch_count("gate_layout") == n_fused + 1
+    idx2, gate2 = B.moe_topk_gate(logits.to(DEV), k, renorm)
+    assert torch.equal(idx, idx2) and torch.equal(gate.view(torch.int32), gate2.view(torch.int32))
+    oi, og = oracle.topk_gate(logits.numpy(), k, renorm)
+    np.testing.assert_array_equal(bits(idx), oi)
+    T.assert_gates_close(bits(gate), og)
+    check_layout(h, oracle.layout(oi, e), oi)
+    assert h.status() == 0
     h.destroy()
 
 
