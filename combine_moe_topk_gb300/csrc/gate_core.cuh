@@ -136,7 +136,9 @@ __device__ __forceinline__ float butterfly_tree32(const float (&v)[32]) {
 // token: the same k ids in the same order (largest key first, the lower id
 // on equal keys) and the same gate bits (the same expf terms, summed in the
 // warp's butterfly order).  row = the token's e logits (16-byte aligned when
-// e is a multiple of 4).  Returns whether a logit is NaN or infinite.
+// e is a multiple of 4); KM >= k bounds the rounds, so the code a thread runs
+// through once stays short.  Returns whether a logit is NaN or infinite.
+template <int KM>
 __device__ __forceinline__ bool topk_token_thread(const float* __restrict__ row, int e, int k, int renorm,
                                                   int* ids, float* gates) {
   float v[32];
@@ -156,45 +158,49 @@ __device__ __forceinline__ bool topk_token_thread(const float* __restrict__ row,
       if (j < e) v[j] = __ldg(row + j);
   }
   bool bad = false;
+  uint32_t key[32];
 #pragma unroll
-  for (int j = 0; j < 32; ++j)
+  for (int j = 0; j < 32; ++j) {
     if (j < e && !isfinite(v[j])) bad = true;
-  uint32_t taken = 0, top_key = 0;
-  uint32_t sel_key[16];
+    key[j] = j < e ? order_key(v[j]) : 0u;
+  }
+  uint32_t taken = 0;
+  uint32_t sel_key[KM];
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
+  for (int r = 0; r < KM; ++r) {
     sel_key[r] = 0;
+    ids[r] = 0;
     if (r < k) {
       uint32_t best = 0;
       int bj = -1;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (j < e && !((taken >> j) & 1u)) {
-          const uint32_t kj = order_key(v[j]);
-          if (bj < 0 || kj > best) {  // ascending j: equal keys keep the lower id
-            best = kj;
-            bj = j;
-          }
+        if (j < e && !((taken >> j) & 1u) && (bj < 0 || key[j] > best)) {  // equal keys keep the lower id
+          best = key[j];
+          bj = j;
         }
       taken |= 1u << bj;
       ids[r] = bj;
       sel_key[r] = best;
-      if (r == 0) top_key = best;
     }
   }
-  const float top = key_value(top_key);
+  const float top = key_value(sel_key[0]);
   float z[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) z[j] = 0.f;
   if (renorm) {
 #pragma unroll
-    for (int r = 0; r < 32; ++r) z[r] = (r < 16 && r < k) ? expf(key_value(sel_key[r < 16 ? r : 0]) - top) : 0.f;
+    for (int r = 0; r < KM; ++r)
+      if (r < k) z[r] = expf(key_value(sel_key[r]) - top);
   } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) z[j] = j < e ? expf(key_value(order_key(v[j])) - top) : 0.f;
+    for (int j = 0; j < 32; ++j)
+      if (j < e) z[j] = expf(key_value(key[j]) - top);
   }
   const float den = butterfly_tree32(z);
 #pragma unroll
-  for (int r = 0; r < 16; ++r)
-    if (r < k) gates[r] = expf(key_value(sel_key[r]) - top) / den;
+  for (int r = 0; r < KM; ++r)
+    if (r < k) gates[r] = (renorm ? z[r] : expf(key_value(sel_key[r]) - top)) / den;
   return bad;
 }
 

@@ -52,6 +52,7 @@
 // tile selects its 32 tokens one after another: measured slower than the
 // gate kernel followed by the layout kernel, which is what runs there.
 #include <atomic>
+#include <initializer_list>
 #include <mutex>
 
 #include "common.cuh"
@@ -138,11 +139,12 @@ __device__ __forceinline__ bool all_published(const uint4& w, unsigned pub) {
 // Load token t's k expert ids (16- or 8-byte loads when k allows) and mark
 // which routes are valid: in range and not a repeat of an earlier route of
 // the same token.
+template <int KM>
 __device__ __forceinline__ unsigned load_routes(const Params& p, int t, int* xs) {
   const int32_t* src = p.topk_idx + unit_base(p, t);
   if ((p.k & 3) == 0) {
 #pragma unroll
-    for (int j4 = 0; j4 < kMaxK / 4; ++j4)
+    for (int j4 = 0; j4 < (KM / 4); ++j4)
       if (4 * j4 < p.k) {
         const int4 v = __ldg(reinterpret_cast<const int4*>(src) + j4);
         xs[4 * j4] = v.x;
@@ -152,7 +154,7 @@ __device__ __forceinline__ unsigned load_routes(const Params& p, int t, int* xs)
       }
   } else if ((p.k & 1) == 0) {
 #pragma unroll
-    for (int j2 = 0; j2 < kMaxK / 2; ++j2)
+    for (int j2 = 0; j2 < (KM / 2); ++j2)
       if (2 * j2 < p.k) {
         const int2 v = __ldg(reinterpret_cast<const int2*>(src) + j2);
         xs[2 * j2] = v.x;
@@ -160,12 +162,12 @@ __device__ __forceinline__ unsigned load_routes(const Params& p, int t, int* xs)
       }
   } else {
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
+    for (int j = 0; j < KM; ++j)
       if (j < p.k) xs[j] = __ldg(src + j);
   }
   unsigned valid = 0;
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
+  for (int j = 0; j < KM; ++j) {
     if (j < p.k) {
       const int x = xs[j];
       bool ok = x >= 0 && x < p.e;
@@ -179,10 +181,11 @@ __device__ __forceinline__ unsigned load_routes(const Params& p, int t, int* xs)
 }
 
 // Set bit `lane` of the warp's token mask of every valid route's expert.
+template <int KM>
 __device__ __forceinline__ void mark_routes(const Params& p, unsigned (*mask)[kMaxE], int warp,
                                             int lane, const int* xs, unsigned valid) {
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j)
+  for (int j = 0; j < KM; ++j)
     if ((valid >> j) & 1u) atomicOr(&mask[warp][xs[j]], 1u << lane);
 }
 
@@ -316,19 +319,20 @@ __device__ void expert_offsets(const Params& p, const int* s_tot, int* s_off, bo
 }
 
 // Store k int32 values of one token (16- or 8-byte stores when k allows).
+template <int KM>
 __device__ __forceinline__ void store_route_ints(int32_t* dst, const int* v, int k) {
   if ((k & 3) == 0) {
 #pragma unroll
-    for (int j4 = 0; j4 < kMaxK / 4; ++j4)
+    for (int j4 = 0; j4 < (KM / 4); ++j4)
       if (4 * j4 < k)
         reinterpret_cast<int4*>(dst)[j4] = make_int4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
   } else if ((k & 1) == 0) {
 #pragma unroll
-    for (int j2 = 0; j2 < kMaxK / 2; ++j2)
+    for (int j2 = 0; j2 < (KM / 2); ++j2)
       if (2 * j2 < k) reinterpret_cast<int2*>(dst)[j2] = make_int2(v[2 * j2], v[2 * j2 + 1]);
   } else {
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
+    for (int j = 0; j < KM; ++j)
       if (j < k) dst[j] = v[j];
   }
 }
@@ -337,6 +341,7 @@ __device__ __forceinline__ void store_route_ints(int32_t* dst, const int* v, int
 // virtual-rank set; with inv_row, the token number at each kept row.
 // base[x] is the slot of this warp's first token routed
 // to x; mask[x] the warp's token mask for x.  Returns the token's rank set.
+template <int KM>
 __device__ __forceinline__ unsigned long long write_routes(const Params& p, int t, int lane,
                                                            const int* xs, unsigned valid,
                                                            const int* base, const unsigned* mask,
@@ -344,10 +349,12 @@ __device__ __forceinline__ unsigned long long write_routes(const Params& p, int 
   const unsigned below = (1u << lane) - 1u;
   const int per_rank = p.R > 0 ? p.e / p.R : 1;
   unsigned long long ranks = 0;
-  int loc[kMaxK], row[kMaxK];
-  uint32_t dropw[kMaxK / 4] = {0, 0, 0, 0};
+  int loc[KM], row[KM];
+  uint32_t dropw[(KM + 3) / 4];
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
+  for (int q = 0; q < (KM + 3) / 4; ++q) dropw[q] = 0;
+#pragma unroll
+  for (int j = 0; j < KM; ++j) {
     loc[j] = -1;
     row[j] = -1;
     if (j < p.k && ((valid >> j) & 1u)) {
@@ -367,19 +374,19 @@ __device__ __forceinline__ unsigned long long write_routes(const Params& p, int 
   if (p.out.inv_row) {
     const int token = p.kmajor ? t - (t / p.s_tok) * p.s_tok : t;
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
+    for (int j = 0; j < KM; ++j)
       if (j < p.k && row[j] >= 0) p.out.inv_row[row[j]] = token;
   }
-  store_route_ints(p.out.loc + q0, loc, p.k);
-  store_route_ints(p.out.row + q0, row, p.k);
+  store_route_ints<KM>(p.out.loc + q0, loc, p.k);
+  store_route_ints<KM>(p.out.row + q0, row, p.k);
   uint8_t* dr = p.out.drop + q0;
   if ((p.k & 3) == 0) {
 #pragma unroll
-    for (int j4 = 0; j4 < kMaxK / 4; ++j4)
+    for (int j4 = 0; j4 < (KM / 4); ++j4)
       if (4 * j4 < p.k) reinterpret_cast<uint32_t*>(dr)[j4] = dropw[j4];
   } else {
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
+    for (int j = 0; j < KM; ++j)
       if (j < p.k) dr[j] = (uint8_t)((dropw[j / 4] >> (8 * (j % 4))) & 0xffu);
   }
   if (p.R > 0) {
@@ -406,13 +413,14 @@ __device__ __forceinline__ void count_ranks(unsigned long long ranks, int lane, 
 // Fused gate: thread t's token selects its experts (topk_token_thread, the
 // gate kernel's ids and gate bits for e <= 32) and writes the ids and gates
 // to the caller's arrays.  Returns whether a logit was not finite.
+template <int KM>
 __device__ __forceinline__ bool gate_thread_token(const Params& p, int t, int* xs) {
-  float g[kMaxK];
-  const bool bad = topk_token_thread(p.logits + (size_t)t * p.e, p.e, p.k, p.renorm, xs, g);
-  store_route_ints(p.gate_idx + (size_t)t * p.k, xs, p.k);
+  float g[KM];
+  const bool bad = topk_token_thread<KM>(p.logits + (size_t)t * p.e, p.e, p.k, p.renorm, xs, g);
+  store_route_ints<KM>(p.gate_idx + (size_t)t * p.k, xs, p.k);
   float* gd = p.gate_val + (size_t)t * p.k;
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j)
+  for (int j = 0; j < KM; ++j)
     if (j < p.k) gd[j] = g[j];
   return bad;
 }
@@ -422,7 +430,7 @@ __device__ __forceinline__ bool gate_thread_token(const Params& p, int t, int* x
 // slot pass; TPT == 0: any number of sub-tiles, routes reloaded per pass.
 // GATE: the fused gate (router logits in, e <= 32; TPT > 0 only, since the
 // routes stay in registers between the passes).
-template <int TPT, bool GATE>
+template <int TPT, bool GATE, int KM>
 __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   static_assert(!GATE || TPT > 0, "the fused gate keeps its routes in registers");
   constexpr int NM = TPT > 0 ? TPT : 1;
@@ -467,7 +475,7 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   __syncthreads();
 
   // ---- A: token masks and the tile histogram -------------------------------
-  int xs[NM][kMaxK];
+  int xs[NM][KM];
   unsigned valid[NM];
   bool bad = false;
   if (TPT > 0) {
@@ -477,14 +485,14 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
       valid[r] = 0;
       if (sub0 + r < sub1 && t < p.s) {
         if (GATE) {
-          if (gate_thread_token(p, t, xs[r])) atomicOr(&s_flags, 4);
+          if (gate_thread_token<KM>(p, t, xs[r])) atomicOr(&s_flags, 4);
           valid[r] = (1u << p.k) - 1u;  // k distinct ids in [0, e)
         } else {
-          valid[r] = load_routes(p, t, xs[r]);
+          valid[r] = load_routes<KM>(p, t, xs[r]);
           bad |= valid[r] != (1u << p.k) - 1u;
         }
-        store_route_ints(p.out.idx + unit_base(p, t), xs[r], p.k);
-        mark_routes(p, s_mask[r], warp, lane, xs[r], valid[r]);
+        store_route_ints<KM>(p.out.idx + unit_base(p, t), xs[r], p.k);
+        mark_routes<KM>(p, s_mask[r], warp, lane, xs[r], valid[r]);
       }
     }
     __syncthreads();
@@ -502,13 +510,13 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   } else {
     for (int sb = sub0; sb < sub1; ++sb) {
       const int t = sb * kThreads + tid;
-      int ys[kMaxK];
+      int ys[KM];
       unsigned vy = 0;
       if (t < p.s) {
-        vy = load_routes(p, t, ys);
+        vy = load_routes<KM>(p, t, ys);
         bad |= vy != (1u << p.k) - 1u;
-        store_route_ints(p.out.idx + unit_base(p, t), ys, p.k);
-        mark_routes(p, s_mask[0], warp, lane, ys, vy);
+        store_route_ints<KM>(p.out.idx + unit_base(p, t), ys, p.k);
+        mark_routes<KM>(p, s_mask[0], warp, lane, ys, vy);
       }
       __syncthreads();
       for (int x = tid; x < p.e; x += kThreads) {
@@ -553,7 +561,7 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
       const int t = (sub0 + r) * kThreads + tid;
       unsigned long long ranks = 0;
       if (sub0 + r < sub1 && t < p.s)
-        ranks = write_routes(p, t, lane, xs[r], valid[r], s_wbase[r][warp], s_mask[r][warp], s_off);
+        ranks = write_routes<KM>(p, t, lane, xs[r], valid[r], s_wbase[r][warp], s_mask[r][warp], s_off);
       if (p.R > 0) count_ranks(ranks, lane, s_rank);
     }
   } else {
@@ -561,11 +569,11 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
     __syncthreads();
     for (int sb = sub0; sb < sub1; ++sb) {
       const int t = sb * kThreads + tid;
-      int ys[kMaxK];
+      int ys[KM];
       unsigned vy = 0;
       if (t < p.s) {
-        vy = load_routes(p, t, ys);
-        mark_routes(p, s_mask[0], warp, lane, ys, vy);
+        vy = load_routes<KM>(p, t, ys);
+        mark_routes<KM>(p, s_mask[0], warp, lane, ys, vy);
       }
       __syncthreads();
       for (int x = tid; x < p.e; x += kThreads) {
@@ -579,7 +587,7 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
       }
       __syncthreads();
       unsigned long long ranks = 0;
-      if (t < p.s) ranks = write_routes(p, t, lane, ys, vy, s_wbase[0][warp], s_mask[0][warp], s_off);
+      if (t < p.s) ranks = write_routes<KM>(p, t, lane, ys, vy, s_wbase[0][warp], s_mask[0][warp], s_off);
       if (p.R > 0) count_ranks(ranks, lane, s_rank);
       __syncthreads();
       for (int i = tid; i < kWarps * kMaxE; i += kThreads) (&s_mask[0][0][0])[i] = 0u;
@@ -662,20 +670,45 @@ size_t lookback_bytes(const LayoutPlan& plan, int e) {
   return sizeof(unsigned) * (size_t)plan.tiles * (size_t)padded_e(e);
 }
 
+// The kernel variant of a sub-tile count (0 = any), a fused gate or not and
+// the routes per unit rounded up to 1, 2, 4, 8 or 16.
+template <int TPT, bool GATE>
+const void* layout_variant(int k) {
+  if (k <= 1) return (const void*)layout_kernel<TPT, GATE, 1>;
+  if (k <= 2) return (const void*)layout_kernel<TPT, GATE, 2>;
+  if (k <= 4) return (const void*)layout_kernel<TPT, GATE, 4>;
+  if (k <= 8) return (const void*)layout_kernel<TPT, GATE, 8>;
+  return (const void*)layout_kernel<TPT, GATE, 16>;
+}
+
+int min_blocks(std::initializer_list<const void*> kerns) {
+  int n = 1 << 30;
+  for (const void* k : kerns) {
+    const int b = blocks_per_sm(k);
+    if (b < n) n = b;
+  }
+  return n;
+}
+
 // The fewest co-resident blocks per SM over the kernel variants, so that a
 // plan fits whichever variant runs it.
 int layout_blocks_per_sm() {
-  const int a = blocks_per_sm((const void*)layout_kernel<0, false>);
-  const int b = blocks_per_sm((const void*)layout_kernel<1, false>);
-  const int c = blocks_per_sm((const void*)layout_kernel<2, false>);
-  return a < b ? (a < c ? a : c) : (b < c ? b : c);
+  int n = 1 << 30;
+  for (int k : {1, 2, 4, 8, 16}) {
+    const int b = min_blocks({layout_variant<0, false>(k), layout_variant<1, false>(k), layout_variant<2, false>(k)});
+    if (b < n) n = b;
+  }
+  return n;
 }
 
 // Co-resident CTAs per SM of the fused-gate variants.
 int gate_layout_blocks_per_sm() {
-  const int a = blocks_per_sm((const void*)layout_kernel<1, true>);
-  const int b = blocks_per_sm((const void*)layout_kernel<2, true>);
-  return a < b ? a : b;
+  int n = 1 << 30;
+  for (int k : {1, 2, 4, 8, 16}) {
+    const int b = min_blocks({layout_variant<1, true>(k), layout_variant<2, true>(k)});
+    if (b < n) n = b;
+  }
+  return n;
 }
 
 std::atomic<bool> g_coop_pdl{true};  // the cooperative launch also takes programmatic serialisation
@@ -732,16 +765,12 @@ cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capa
   cfg.numAttrs = (MOE_PDL != 0 && ((MOE_PDL_MASK >> MOE_KERNEL_LAYOUT) & 1) && g_coop_pdl.load()) ? 2 : 1;
   cudaError_t err;
   const int tpt = plan.subtiles_per_tile;
-  if (p.logits) {
-    err = tpt == 1 ? cudaLaunchKernelEx(&cfg, layout_kernel<1, true>, p)
-                   : cudaLaunchKernelEx(&cfg, layout_kernel<2, true>, p);
-  } else if (tpt == 1) {
-    err = cudaLaunchKernelEx(&cfg, layout_kernel<1, false>, p);
-  } else if (tpt == 2) {
-    err = cudaLaunchKernelEx(&cfg, layout_kernel<2, false>, p);
-  } else {
-    err = cudaLaunchKernelEx(&cfg, layout_kernel<0, false>, p);
-  }
+  const void* kern = p.logits ? (tpt == 1 ? layout_variant<1, true>(p.k) : layout_variant<2, true>(p.k))
+                   : tpt == 1   ? layout_variant<1, false>(p.k)
+                   : tpt == 2   ? layout_variant<2, false>(p.k)
+                                : layout_variant<0, false>(p.k);
+  void* args[] = {&p};
+  err = cudaLaunchKernelExC(&cfg, kern, args);
   if (err != cudaSuccess && cfg.numAttrs == 2) {
     // the driver refused the pair of attributes: launch cooperative only,
     // from now on
