@@ -112,7 +112,7 @@ def test_gate_fused_into_the_layout(name, renorm):
 
 @pytest.mark.parametrize("case", [
     dict(s=5000, e=16, k=6, capacity=400, R=4, priority="kmajor"),   # k-major: gate kernel, then layout
-    dict(s=1 << 17, e=32, k=4, capacity=0, R=8, priority="token"),   # tiles span several sub-tiles
+    dict(s=1 << 18, e=32, k=4, capacity=0, R=8, priority="token"),   # tiles span four sub-tiles
     dict(s=3001, e=64, k=4, capacity=0, R=0, priority="token"),      # more than 32 experts
 ], ids=["kmajor", "many-subtiles", "e64"])
 def test_gate_layout_where_the_layout_cannot_select(case):
