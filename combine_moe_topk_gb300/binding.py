@@ -26,7 +26,8 @@ STATUS = {
 MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
 MOE_DEV_NONFINITE, MOE_DEV_BAD_ROUTE, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4
 KERNELS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd", "topk_gate_bwd",
-           "grouped_gemm", "dispatch_gemm", "rank_slots", "combine_gate_bwd", "gate_layout"]
+           "grouped_gemm", "dispatch_gemm", "rank_slots", "combine_gate_bwd", "gate_layout", "ep_pack", "ep_unpack",
+           "ep_dispatch", "ep_combine"]
 KERNEL_ID = {n: i for i, n in enumerate(KERNELS)}
 
 # every entry point the header declares (checked by the CPU test-suite)
@@ -36,7 +37,7 @@ EXPORTS = [
     "moe_status_string", "moe_last_error", "moe_launch_count", "moe_debug_hold_layout_tile",
     "moe_dispatch_layout_noalloc", "moe_topk_gate_bwd", "moe_dispatch_layout_ex", "moe_grouped_gemm",
     "moe_dispatch_grouped_gemm", "moe_combine_gate_bwd", "moe_layout_create", "moe_layout_rebuild",
-    "moe_topk_gate_layout",
+    "moe_topk_gate_layout", "moe_ep_pack", "moe_ep_dispatch", "moe_ep_combine", "moe_ep_unpack_dgate",
 ]
 
 
@@ -49,7 +50,7 @@ class MoEError(RuntimeError):
 
 class LayoutOptions(ctypes.Structure):
     _fields_ = [("capacity", ctypes.c_int32), ("num_virtual_ranks", ctypes.c_int32), ("priority", ctypes.c_int32),
-                ("pad_multiple", ctypes.c_int32), ("send_slots", ctypes.c_int32)]
+                ("pad_multiple", ctypes.c_int32), ("send_slots", ctypes.c_int32), ("absent_routes", ctypes.c_int32)]
 
 
 PRIORITY = {"token": 0, "kmajor": 1}
@@ -83,6 +84,10 @@ def lib() -> ctypes.CDLL:
             "moe_layout_create": [I, I, I, ctypes.POINTER(LayoutOptions), P, ctypes.POINTER(P)],
             "moe_layout_rebuild": [P, P, P],
             "moe_topk_gate_layout": [P, P, I, P, P, P],
+            "moe_ep_pack": [P, P, I, P, P, P, P],
+            "moe_ep_dispatch": [P, P, I, I, I, P, P, P],
+            "moe_ep_combine": [P, P, I, I, I, P, P, P],
+            "moe_ep_unpack_dgate": [P, P, I, P, P, P],
             "moe_dispatch": [P, I, I, I, I, P, P, P],
             "moe_combine": [P, I, I, I, I, P, P, P, P],
             "moe_combine_bwd": [P, I, I, I, I, P, P, P, P, P, P],
@@ -285,16 +290,18 @@ def moe_dispatch_layout(topk_idx: torch.Tensor, e: int, capacity: int = 0, num_v
 
 
 def moe_dispatch_layout_ex(topk_idx: torch.Tensor, e: int, capacity: int = 0, num_virtual_ranks: int = 0,
-                           priority: str = "token", pad_multiple: int = 1, send_slots: bool = False) -> Handle:
+                           priority: str = "token", pad_multiple: int = 1, send_slots: bool = False,
+                           absent_routes: bool = False) -> Handle:
     """Layout with a capacity priority ("token" or "kmajor"), per-expert
-    padding of the dropless rows (handle.rows is then an upper bound) and,
-    with send_slots, each token's token-order slot per virtual rank
-    (handle.rank_slot())."""
+    padding of the dropless rows (handle.rows is then an upper bound),
+    with send_slots each token's token-order slot per virtual rank
+    (handle.rank_slot()), and with absent_routes expert id -1 taken as a
+    route that does not exist."""
     if topk_idx.dim() != 2 or topk_idx.dtype != torch.int32:
         raise ValueError("topk_idx must be int32 [s, k]")
     s, k = topk_idx.shape
     opt = LayoutOptions(int(capacity), int(num_virtual_ranks), PRIORITY[priority], int(pad_multiple),
-                        int(bool(send_slots)))
+                        int(bool(send_slots)), int(bool(absent_routes)))
     raw = ctypes.c_void_p()
     dev = topk_idx.device
     rc = lib().moe_dispatch_layout_ex(_ptr(topk_idx), s, int(e), k, ctypes.byref(opt), _stream(dev),
@@ -305,13 +312,13 @@ def moe_dispatch_layout_ex(topk_idx: torch.Tensor, e: int, capacity: int = 0, nu
 
 def moe_layout_create(s: int, e: int, k: int, capacity: int = 0, num_virtual_ranks: int = 0,
                       priority: str = "token", pad_multiple: int = 1, send_slots: bool = False,
-                      device: torch.device | None = None) -> Handle:
+                      device: torch.device | None = None, absent_routes: bool = False) -> Handle:
     """An empty handle for [s, k] routes over e experts with these layout
     options, to be built (and rebuilt) in place by moe_layout_rebuild or
     moe_topk_gate_layout without allocating."""
     dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
     opt = LayoutOptions(int(capacity), int(num_virtual_ranks), PRIORITY[priority], int(pad_multiple),
-                        int(bool(send_slots)))
+                        int(bool(send_slots)), int(bool(absent_routes)))
     raw = ctypes.c_void_p()
     with torch.cuda.device(dev):
         rc = lib().moe_layout_create(int(s), int(e), int(k), ctypes.byref(opt), _stream(dev), ctypes.byref(raw))
@@ -441,6 +448,69 @@ def moe_dispatch_bwd(h: Handle, dX: torch.Tensor, dx: torch.Tensor | None = None
     _check(lib().moe_dispatch_bwd(h.raw, s, rows, m, _dtype(dX), _ptr(dX), _ptr(dx), _stream(dX.device)),
            "moe_dispatch_bwd")
     return dx
+
+
+# ---------------------------------------------------- expert parallelism --
+
+def moe_ep_pack(h: Handle, gate: torch.Tensor, rows_sent: int, send_row: torch.Tensor | None = None,
+                meta_idx: torch.Tensor | None = None, meta_gate: torch.Tensor | None = None):
+    """The send map of a source handle (built with send slots over R ranks):
+    (send_row i32 [s,R], meta_idx i32 [rows_sent,k], meta_gate f32 [rows_sent,k])."""
+    dev = gate.device
+    if gate.dtype != torch.float32 or tuple(gate.shape) != (h.s, h.k):
+        raise MoEError(1, "moe_ep_pack", "gate must be float32 [s, k]")
+    if send_row is None:
+        send_row = torch.empty(h.s, h.R, dtype=torch.int32, device=dev)
+    if meta_idx is None:
+        meta_idx = torch.empty(rows_sent, h.k, dtype=torch.int32, device=dev)
+    if meta_gate is None:
+        meta_gate = torch.empty(rows_sent, h.k, dtype=torch.float32, device=dev)
+    if tuple(send_row.shape) != (h.s, h.R) or tuple(meta_idx.shape) != (rows_sent, h.k) or \
+            tuple(meta_gate.shape) != (rows_sent, h.k):
+        raise MoEError(1, "moe_ep_pack", "output shapes")
+    _check(lib().moe_ep_pack(h.raw, _ptr(gate), int(rows_sent), _ptr(send_row), _ptr(meta_idx), _ptr(meta_gate),
+                             _stream(dev)), "moe_ep_pack")
+    return send_row, meta_idx, meta_gate
+
+
+def moe_ep_dispatch(h: Handle, send_row: torch.Tensor, rows_sent: int, x: torch.Tensor,
+                    X_send: torch.Tensor | None = None) -> torch.Tensor:
+    """The send buffer [rows_sent, m]: each token row once per destination rank."""
+    s, m = _rows2(x, "x")
+    if X_send is None:
+        X_send = torch.empty(rows_sent, m, dtype=x.dtype, device=x.device)
+    if tuple(X_send.shape) != (rows_sent, m) or X_send.dtype != x.dtype or s != h.s:
+        raise MoEError(1, "moe_ep_dispatch", "shapes")
+    _check(lib().moe_ep_dispatch(h.raw, _ptr(send_row), int(rows_sent), m, _dtype(x), _ptr(x), _ptr(X_send),
+                                 _stream(x.device)), "moe_ep_dispatch")
+    return X_send
+
+
+def moe_ep_combine(h: Handle, send_row: torch.Tensor, rows_sent: int, P: torch.Tensor,
+                   out: torch.Tensor | None = None) -> torch.Tensor:
+    """out [s, m] = the returned partials P [rows_sent, m] summed over ranks in rank order."""
+    rows, m = _rows2(P, "P")
+    if rows != rows_sent:
+        raise MoEError(1, "moe_ep_combine", "P must have rows_sent rows")
+    if out is None:
+        out = torch.empty(h.s, m, dtype=P.dtype, device=P.device)
+    if tuple(out.shape) != (h.s, m) or out.dtype != P.dtype:
+        raise MoEError(1, "moe_ep_combine", "output shape")
+    _check(lib().moe_ep_combine(h.raw, _ptr(send_row), int(rows_sent), m, _dtype(P), _ptr(P), _ptr(out),
+                                _stream(P.device)), "moe_ep_combine")
+    return out
+
+
+def moe_ep_unpack_dgate(h: Handle, send_row: torch.Tensor, rows_sent: int, dgate_back: torch.Tensor,
+                        dgate: torch.Tensor | None = None) -> torch.Tensor:
+    """dgate f32 [s, k] from the gate gradients returned per sent row [rows_sent, k]."""
+    if tuple(dgate_back.shape) != (rows_sent, h.k) or dgate_back.dtype != torch.float32:
+        raise MoEError(1, "moe_ep_unpack_dgate", "dgate_back must be float32 [rows_sent, k]")
+    if dgate is None:
+        dgate = torch.empty(h.s, h.k, dtype=torch.float32, device=dgate_back.device)
+    _check(lib().moe_ep_unpack_dgate(h.raw, _ptr(send_row), int(rows_sent), _ptr(dgate_back), _ptr(dgate),
+                                     _stream(dgate_back.device)), "moe_ep_unpack_dgate")
+    return dgate
 
 
 def moe_grouped_gemm(h: Handle, X: torch.Tensor, W: torch.Tensor, Y: torch.Tensor | None = None) -> torch.Tensor:

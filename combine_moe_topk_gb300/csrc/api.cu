@@ -30,6 +30,7 @@ struct moe_handle_s {
   int32_t* rank_slot;  // [s,R] send slots, or NULL
   moe::LayoutPlan plan;
   int builds;          // layout builds enqueued so far (0: created, no layout yet)
+  int absent;          // expert id -1 = an absent route
 };
 
 namespace {
@@ -298,9 +299,13 @@ moe_status create_handle(int s, int e, int k, const moe_layout_options* options,
   if (pad > 65536) return fail(MOE_ERR_INVALID_ARG, "pad_multiple must be <= 65536");
   const int send_slots = options->send_slots;
   if (send_slots != 0 && send_slots != 1) return fail(MOE_ERR_INVALID_ARG, "send_slots must be 0 or 1");
+  if (options->absent_routes != 0 && options->absent_routes != 1)
+    return fail(MOE_ERR_INVALID_ARG, "absent_routes must be 0 or 1");
   if (send_slots && options->num_virtual_ranks <= 0)
     return fail(MOE_ERR_INVALID_ARG, "send_slots needs num_virtual_ranks > 0");
-  if (s < 0 || e < 1 || e > kMaxE || k < 1 || k > e || k > kMaxK)
+  // with absent routes a token may list more routes than there are experts
+  // (at most e of them present)
+  if (s < 0 || e < 1 || e > kMaxE || k < 1 || (k > e && !options->absent_routes) || k > kMaxK)
     return fail(MOE_ERR_INVALID_ARG, "need s >= 0, 1 <= e <= 256, 1 <= k <= min(e, 16)");
   if (capacity < 0) return fail(MOE_ERR_INVALID_ARG, "capacity must be >= 0 (0 = dropless)");
   if (R < 0 || R > kMaxR || (R > 0 && e % R != 0))
@@ -332,6 +337,7 @@ moe_status create_handle(int s, int e, int k, const moe_layout_options* options,
   h->pad = pad;
   h->zero_fill = capacity > 0 || pad > 1;
   h->builds = 0;
+  h->absent = options->absent_routes != 0;
   // the scan runs over s*k one-route units in k-major order
   h->plan = moe::plan_layout(priority == MOE_PRIORITY_KMAJOR ? s * k : s, e, *di);
 
@@ -400,6 +406,7 @@ moe_status build_handle(moe_handle h, const int32_t* topk_idx, const float* logi
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   moe::LayoutBuild build;
   build.clear_status = 1;
+  build.absent_ok = h->absent;
   cudaError_t err = cudaSuccess;
   const moe::DeviceInfo* di = nullptr;
   MOE_TRY(device_state(h->device, &di));
@@ -518,6 +525,7 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int
   opt.priority = MOE_PRIORITY_TOKEN;
   opt.pad_multiple = 1;
   opt.send_slots = 0;
+  opt.absent_routes = 0;
   return moe_dispatch_layout_ex(topk_idx, s, e, k, &opt, stream, out);
 }
 
@@ -574,6 +582,108 @@ moe_status moe_dispatch_grouped_gemm(moe_handle h, int s, int rows, int K, int N
                                                K, N, x, W, Y, h->out.status, *di,
                                                static_cast<cudaStream_t>(stream)),
                      "dispatch_grouped_gemm launch", MOE_KERNEL_DISPATCH_GEMM);
+}
+
+namespace {
+
+// An expert-parallel source handle and its send map: built, with send slots
+// over 1..32 ranks, rows_sent in range, pointers on the handle's device.
+moe_status check_ep(moe_handle h, int rows_sent, const void* send_row) {
+  MOE_TRY(built_handle(h));
+  if (h->R < 1 || h->R > 32) return fail(MOE_ERR_INVALID_ARG, "expert-parallel calls need 1 <= R <= 32 ranks");
+  if (!h->rank_slot) return fail(MOE_ERR_INVALID_ARG, "the handle was built without send_slots");
+  if (rows_sent < 0 || (long long)rows_sent > (long long)h->s * h->R)
+    return fail(MOE_ERR_INVALID_ARG, "rows_sent must be in [0, s*R]");
+  if (h->s > 0) {
+    MOE_TRY(check_ptr(send_row, "send_row"));
+    MOE_TRY(handle_device(h));
+    MOE_TRY(check_device_ptr(send_row, "send_row", h->device));
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+moe_status moe_ep_pack(moe_handle h, const float* gate, int rows_sent, int32_t* send_row, int32_t* meta_idx,
+                       float* meta_gate, void* stream) {
+  MOE_TRY(check_ep(h, rows_sent, send_row));
+  if ((long long)rows_sent * h->k > 2147483647LL) return fail(MOE_ERR_INVALID_ARG, "rows_sent*k must be < 2^31");
+  if (h->s == 0) return MOE_OK;
+  MOE_TRY(check_ptr(gate, "gate"));
+  MOE_TRY(check_device_ptr(gate, "gate", h->device));
+  if (rows_sent > 0) {
+    MOE_TRY(check_ptr(meta_idx, "meta_idx"));
+    MOE_TRY(check_ptr(meta_gate, "meta_gate"));
+    MOE_TRY(check_device_ptr(meta_idx, "meta_idx", h->device));
+    MOE_TRY(check_device_ptr(meta_gate, "meta_gate", h->device));
+  }
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(h->device, &di));
+  cudaError_t err = moe::launch_ep_pack(h->out.idx, h->out.row, gate, h->rank_slot, h->out.rank_counts, h->s, h->k,
+                                        h->e, h->R, rows_sent, send_row, meta_idx, meta_gate, h->out.status, *di,
+                                        static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "ep_pack launch");
+  g_launches[MOE_KERNEL_EP_PACK]++;
+  return MOE_OK;
+}
+
+moe_status moe_ep_dispatch(moe_handle h, const int32_t* send_row, int rows_sent, int m, moe_dtype dtype,
+                           const void* x, void* X_send, void* stream) {
+  MOE_TRY(check_ep(h, rows_sent, send_row));
+  long long rb = 0;
+  MOE_TRY(check_payload(dtype, m, &rb));
+  if (h->s == 0 || rows_sent == 0) return MOE_OK;
+  MOE_TRY(check_ptr(x, "x"));
+  MOE_TRY(check_ptr(X_send, "X_send"));
+  MOE_TRY(check_device_ptr(x, "x", h->device));
+  MOE_TRY(check_device_ptr(X_send, "X_send", h->device));
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(h->device, &di));
+  cudaError_t err = moe::launch_dispatch(send_row, nullptr, nullptr, h->s, h->R, 1, 0, rows_sent, 0, x, X_send, rb,
+                                         h->out.status, *di, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "ep_dispatch launch");
+  g_launches[MOE_KERNEL_EP_DISPATCH]++;
+  return MOE_OK;
+}
+
+moe_status moe_ep_combine(moe_handle h, const int32_t* send_row, int rows_sent, int m, moe_dtype dtype,
+                          const void* P, void* out, void* stream) {
+  MOE_TRY(check_ep(h, rows_sent, send_row));
+  long long rb = 0;
+  MOE_TRY(check_payload(dtype, m, &rb));
+  if (h->s == 0) return MOE_OK;
+  if (rows_sent > 0) {
+    MOE_TRY(check_ptr(P, "P"));
+    MOE_TRY(check_device_ptr(P, "P", h->device));
+  }
+  MOE_TRY(check_ptr(out, "out"));
+  MOE_TRY(check_device_ptr(out, "out", h->device));
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(h->device, &di));
+  cudaError_t err = moe::launch_combine(send_row, nullptr, h->s, h->R, m, dtype == MOE_F32 ? 0 : 1, P, out, 1, *di,
+                                        static_cast<cudaStream_t>(stream), rows_sent);
+  if (err != cudaSuccess) return cuda_fail(err, "ep_combine launch");
+  g_launches[MOE_KERNEL_EP_COMBINE]++;
+  return MOE_OK;
+}
+
+moe_status moe_ep_unpack_dgate(moe_handle h, const int32_t* send_row, int rows_sent, const float* dgate_back,
+                               float* dgate, void* stream) {
+  MOE_TRY(check_ep(h, rows_sent, send_row));
+  if (h->s == 0) return MOE_OK;
+  if (rows_sent > 0) {
+    MOE_TRY(check_ptr(dgate_back, "dgate_back"));
+    MOE_TRY(check_device_ptr(dgate_back, "dgate_back", h->device));
+  }
+  MOE_TRY(check_ptr(dgate, "dgate"));
+  MOE_TRY(check_device_ptr(dgate, "dgate", h->device));
+  const moe::DeviceInfo* di = nullptr;
+  MOE_TRY(device_state(h->device, &di));
+  cudaError_t err = moe::launch_ep_unpack_dgate(h->out.idx, h->out.row, send_row, dgate_back, h->s, h->k, h->e, h->R,
+                                                rows_sent, dgate, *di, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "ep_unpack_dgate launch");
+  g_launches[MOE_KERNEL_EP_UNPACK]++;
+  return MOE_OK;
 }
 
 moe_status moe_handle_info(moe_handle h, moe_layout_info* info) {
@@ -670,7 +780,7 @@ moe_status moe_combine(moe_handle h, int s, int rows, int m, moe_dtype dtype, co
   const moe::DeviceInfo* di = nullptr;
   MOE_TRY(device_state(h->device, &di));
   cudaError_t err = moe::launch_combine(h->out.row, gate, s, h->k, m, dtype == MOE_F32 ? 0 : 1, y, out, h->capacity > 0,
-                                        *di, static_cast<cudaStream_t>(stream));
+                                        *di, static_cast<cudaStream_t>(stream), h->rows);
   if (err != cudaSuccess) return cuda_fail(err, "combine launch");
   g_launches[MOE_KERNEL_COMBINE]++;
   return MOE_OK;
@@ -766,7 +876,7 @@ moe_status moe_dispatch_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtyp
   const moe::DeviceInfo* di = nullptr;
   MOE_TRY(device_state(h->device, &di));
   cudaError_t err = moe::launch_combine(h->out.row, nullptr, s, h->k, m, dtype == MOE_F32 ? 0 : 1, dX, dx, h->capacity > 0,
-                                        *di, static_cast<cudaStream_t>(stream));
+                                        *di, static_cast<cudaStream_t>(stream), h->rows);
   if (err != cudaSuccess) return cuda_fail(err, "dispatch_bwd launch");
   g_launches[MOE_KERNEL_DISPATCH_BWD]++;
   return MOE_OK;

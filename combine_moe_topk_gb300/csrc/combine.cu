@@ -69,11 +69,14 @@ __device__ __noinline__ void router_grad_call(int t, int lane, int k, int e, con
 }
 
 // Route rows and gates of token t, broadcast from lanes 0..k-1.
+// A row index outside [0, rows) counts as a dropped route: nothing past the
+// buffer is read.
 template <int KMAX, bool WEIGHTED>
 __device__ __forceinline__ void token_routes(const int32_t* __restrict__ row,
-                                             const float* __restrict__ gate, int t, int k,
+                                             const float* __restrict__ gate, int t, int k, long long rows,
                                              int lane, int (&r)[KMAX], float (&g)[KMAX]) {
-  const int rl = lane < k ? __ldg(row + (size_t)t * k + lane) : -1;
+  int rl = lane < k ? __ldg(row + (size_t)t * k + lane) : -1;
+  if (rl >= rows) rl = -1;
   const float gl = (WEIGHTED && lane < k) ? __ldg(gate + (size_t)t * k + lane) : 1.0f;
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
@@ -85,7 +88,7 @@ __device__ __forceinline__ void token_routes(const int32_t* __restrict__ row,
 template <typename T, int KMAX, int UNR, bool WEIGHTED>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __restrict__ row,
                                                            const float* __restrict__ gate, int s,
-                                                           int k, int nvec, int chunk, int nchunks,
+                                                           int k, long long rows, int nvec, int chunk, int nchunks,
                                                            const uint4* __restrict__ y,
                                                            uint4* __restrict__ out) {
   constexpr int N = Vec<T>::N;
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __rest
     const int c1 = min(nvec, c0 + chunk);
     int r[KMAX];
     float g[KMAX];
-    token_routes<KMAX, WEIGHTED>(row, gate, t, k, lane, r, g);
+    token_routes<KMAX, WEIGHTED>(row, gate, t, k, rows, lane, r, g);
     uint4* o = out + (size_t)t * nvec;
     for (int v0 = c0 + lane; v0 < c1; v0 += 32 * UNR) {
       uint4 val[KMAX][UNR];
@@ -148,7 +151,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __rest
 template <typename T, int KC, int UNR, bool WEIGHTED>
 __global__ void __launch_bounds__(kThreads) combine_compact_kernel(const int32_t* __restrict__ row,
                                                                    const float* __restrict__ gate, int s,
-                                                                   int k, int nvec, int chunk, int nchunks,
+                                                                   int k, long long rows, int nvec, int chunk,
+                                                                   int nchunks,
                                                                    const uint4* __restrict__ y,
                                                                    uint4* __restrict__ out) {
   constexpr int N = Vec<T>::N;
@@ -161,7 +165,8 @@ __global__ void __launch_bounds__(kThreads) combine_compact_kernel(const int32_t
     const int t = (int)(u / nchunks);
     const int c0 = (int)(u - (long long)t * nchunks) * chunk;
     const int c1 = min(nvec, c0 + chunk);
-    const int rl = lane < k ? __ldg(row + (size_t)t * k + lane) : -1;
+    int rl = lane < k ? __ldg(row + (size_t)t * k + lane) : -1;
+    if (rl >= rows) rl = -1;  // past the buffer: read nothing
     const float gl = (WEIGHTED && lane < k) ? __ldg(gate + (size_t)t * k + lane) : 1.0f;
     unsigned kept = __ballot_sync(0xffffffffu, rl >= 0);
     const int nkept = __popc(kept);
@@ -269,7 +274,7 @@ __device__ __forceinline__ void combine_bwd_body(
       rg_g = __ldg(gate + (size_t)t * k + lane);
     }
     if (live) {
-      token_routes<KMAX, true>(row, gate, t, k, lane, r, g);
+      token_routes<KMAX, true>(row, gate, t, k, rows, lane, r, g);
       const uint4* d = dout + (size_t)t * nvec;
       for (int v0 = c0 + lane; v0 < c1; v0 += 32 * UNR) {
         uint4 dv[UNR];
@@ -394,7 +399,8 @@ __device__ __forceinline__ void combine_bwd_compact_body(
   grid_dependency_wait();
   pdl_trigger_early();
   for (int t = gw; t < s; t += warps) {
-    const int rl = lane < k ? __ldg(row + (size_t)t * k + lane) : -1;
+    int rl = lane < k ? __ldg(row + (size_t)t * k + lane) : -1;
+    if (rl >= rows) rl = -1;  // past the buffer: read nothing
     const float gl = lane < k ? __ldg(gate + (size_t)t * k + lane) : 0.f;
     unsigned kept = __ballot_sync(0xffffffffu, rl >= 0);
     const int nkept = __popc(kept);
@@ -554,7 +560,7 @@ int pieces_for(long long s, int nvec, const DeviceInfo& di, int blocks_per_sm, i
 }
 
 template <typename T, int KMAX>
-cudaError_t combine_t(const int32_t* row, const float* gate, int s, int k, int m, const void* y,
+cudaError_t combine_t(const int32_t* row, const float* gate, int s, int k, long long rows, int m, const void* y,
                       void* out, const DeviceInfo& di, cudaStream_t st) {
   // two routes: 8 loads per lane already keep enough bytes in flight, and
   // the lower register count doubles the resident warps
@@ -580,10 +586,10 @@ cudaError_t combine_t(const int32_t* row, const float* gate, int s, int k, int m
   const long long units = (long long)s * nchunks;
   if (gate)
     return launch_pdl(MOE_KERNEL_COMBINE, kern_w, dim3(grid_for(units, di, bps)), dim3(kThreads), 0, st,
-                      row, gate, s, k, nvec, chunk, nchunks, static_cast<const uint4*>(y),
+                      row, gate, s, k, rows, nvec, chunk, nchunks, static_cast<const uint4*>(y),
                       static_cast<uint4*>(out));
   return launch_pdl(MOE_KERNEL_DISPATCH_BWD, kern_u, dim3(grid_for(units, di, bps)), dim3(kThreads), 0, st,
-                    row, static_cast<const float*>(nullptr), s, k, nvec, chunk, nchunks,
+                    row, static_cast<const float*>(nullptr), s, k, rows, nvec, chunk, nchunks,
                     static_cast<const uint4*>(y), static_cast<uint4*>(out));
 }
 
@@ -641,8 +647,8 @@ cudaError_t combine_bwd_t(const int32_t* row, const int32_t* counts, const int32
 }
 
 template <typename T>
-cudaError_t combine_compact_t(const int32_t* row, const float* gate, int s, int k, int m, const void* y,
-                              void* out, const DeviceInfo& di, cudaStream_t st) {
+cudaError_t combine_compact_t(const int32_t* row, const float* gate, int s, int k, long long rows, int m,
+                              const void* y, void* out, const DeviceInfo& di, cudaStream_t st) {
   constexpr int KC = 4, UNR = 2;
   const int nvec = m / Vec<T>::N;
   auto kern_w = combine_compact_kernel<T, KC, UNR, true>;
@@ -657,20 +663,20 @@ cudaError_t combine_compact_t(const int32_t* row, const float* gate, int s, int 
   const long long units = (long long)s * nchunks;
   if (gate)
     return launch_pdl(MOE_KERNEL_COMBINE, kern_w, dim3(grid_for(units, di, bps)), dim3(kThreads), 0, st,
-                      row, gate, s, k, nvec, chunk, nchunks, static_cast<const uint4*>(y),
+                      row, gate, s, k, rows, nvec, chunk, nchunks, static_cast<const uint4*>(y),
                       static_cast<uint4*>(out));
   return launch_pdl(MOE_KERNEL_DISPATCH_BWD, kern_u, dim3(grid_for(units, di, bps)), dim3(kThreads), 0, st,
-                    row, static_cast<const float*>(nullptr), s, k, nvec, chunk, nchunks,
+                    row, static_cast<const float*>(nullptr), s, k, rows, nvec, chunk, nchunks,
                     static_cast<const uint4*>(y), static_cast<uint4*>(out));
 }
 
 template <typename T>
-cudaError_t combine_k(const int32_t* row, const float* gate, int s, int k, int m, const void* y,
+cudaError_t combine_k(const int32_t* row, const float* gate, int s, int k, long long rows, int m, const void* y,
                       void* out, const DeviceInfo& di, cudaStream_t st) {
-  if (k <= 2) return combine_t<T, 2>(row, gate, s, k, m, y, out, di, st);
-  if (k <= 4) return combine_t<T, 4>(row, gate, s, k, m, y, out, di, st);
-  if (k <= 8) return combine_t<T, 8>(row, gate, s, k, m, y, out, di, st);
-  return combine_t<T, 16>(row, gate, s, k, m, y, out, di, st);
+  if (k <= 2) return combine_t<T, 2>(row, gate, s, k, rows, m, y, out, di, st);
+  if (k <= 4) return combine_t<T, 4>(row, gate, s, k, rows, m, y, out, di, st);
+  if (k <= 8) return combine_t<T, 8>(row, gate, s, k, rows, m, y, out, di, st);
+  return combine_t<T, 16>(row, gate, s, k, rows, m, y, out, di, st);
 }
 
 template <typename T, bool RG>
@@ -691,14 +697,15 @@ cudaError_t combine_bwd_k(const int32_t* row, const int32_t* counts, const int32
 }  // namespace
 
 cudaError_t launch_combine(const int32_t* row, const float* gate, int s, int k, int m, int dtype,
-                           const void* y, void* out, int sparse, const DeviceInfo& di, cudaStream_t st) {
+                           const void* y, void* out, int sparse, const DeviceInfo& di, cudaStream_t st,
+                           long long rows) {
   // capacity layouts (routes may be dropped) with more routes than a round holds
   if (MOE_CMB_COMPACT && sparse && k > 4) {
-    if (dtype == 0) return combine_compact_t<float>(row, gate, s, k, m, y, out, di, st);
-    return combine_compact_t<__nv_bfloat16>(row, gate, s, k, m, y, out, di, st);
+    if (dtype == 0) return combine_compact_t<float>(row, gate, s, k, rows, m, y, out, di, st);
+    return combine_compact_t<__nv_bfloat16>(row, gate, s, k, rows, m, y, out, di, st);
   }
-  if (dtype == 0) return combine_k<float>(row, gate, s, k, m, y, out, di, st);
-  return combine_k<__nv_bfloat16>(row, gate, s, k, m, y, out, di, st);
+  if (dtype == 0) return combine_k<float>(row, gate, s, k, rows, m, y, out, di, st);
+  return combine_k<__nv_bfloat16>(row, gate, s, k, rows, m, y, out, di, st);
 }
 
 cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const int32_t* offsets,

@@ -215,11 +215,11 @@ __device__ __forceinline__ void bulk_wait_all() {
 // Bit mask of the launches that use programmatic serialisation (bit i =
 // kernel id i of moe_launch_count: gate 0, layout 1, dispatch 2, combine
 // backward 4, dispatch backward 5, gate backward 6, combine + gate backward
-// 10).  The combine (3) is left out: its CTAs parked early on the SMs
+// 10, the expert-parallel pack 12 and gate-gradient unpack 13).  The combine (3) is left out: its CTAs parked early on the SMs
 // slowed the dispatch they follow, by 6-13 % of a step on every workload
 // measured.
 #ifndef MOE_PDL_MASK
-#define MOE_PDL_MASK 0x477
+#define MOE_PDL_MASK 0x3477
 #endif
 
 template <typename... KArgs, typename... Args>

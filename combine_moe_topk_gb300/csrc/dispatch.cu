@@ -41,7 +41,7 @@ namespace {
 
 constexpr int kMaxStages = 8;
 constexpr int kBatch = 32;   // tokens of routing metadata staged at a time
-constexpr int kMaxK = 16;
+constexpr int kMaxK = 32;   // routes per token: k, or the ranks of an expert-parallel send
 constexpr int kMaxE = 256;
 
 struct Params {
@@ -106,8 +106,15 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const Params p) {
         __syncwarp();
         if (lane < blen) {
           unsigned mk = 0;
-          for (int j = 0; j < p.k; ++j)
-            if (b_rows[lane * p.k + j] >= 0) mk |= 1u << j;
+          for (int j = 0; j < p.k; ++j) {
+            const int r = b_rows[lane * p.k + j];
+            if (r >= 0 && r < p.rows) {
+              mk |= 1u << j;
+            } else if (r >= 0) {  // a row past the buffer: written nowhere, reported
+              b_rows[lane * p.k + j] = -1;
+              raise_status(p.status, MOE_DEV_BAD_ROUTE);
+            }
+          }
           b_mask[lane] = mk;
         }
         __syncwarp();

@@ -77,6 +77,7 @@ struct LayoutOut {
 // when layout_can_fuse_gate(plan, priority, e, di).
 struct LayoutBuild {
   int clear_status = 0;
+  int absent_ok = 0;  // expert id -1 = no route (row -1, drop 1, no status bit)
   const float* logits = nullptr;
   int renorm = 1;
   int32_t* gate_idx = nullptr;
@@ -110,8 +111,10 @@ cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, const int
 // --- combine family -----------------------------------------------------
 // dtype: 0 = f32, 1 = bf16.  gate == nullptr means unit weights.
 // sparse: the layout may have dropped routes (capacity mode)
+// rows: rows of y; a row index at or past it counts as a dropped route.
 cudaError_t launch_combine(const int32_t* row, const float* gate, int s, int k, int m, int dtype,
-                           const void* y, void* out, int sparse, const DeviceInfo& di, cudaStream_t st);
+                           const void* y, void* out, int sparse, const DeviceInfo& di, cudaStream_t st,
+                           long long rows);
 
 // With rg_dlogits != nullptr the top-k gate backward runs fused into the
 // same kernel (rg_idx = the routes' expert ids; rg_logits only when
@@ -128,6 +131,17 @@ cudaError_t launch_combine_bwd(const int32_t* row, const int32_t* counts, const 
 // -1 where token_in_rank[t,r] = 0.  [s,R] int32, one CTA per rank.
 cudaError_t launch_rank_slots(const uint8_t* token_in_rank, int s, int R, int32_t* rank_slot,
                               cudaStream_t st);
+
+// --- expert-parallel exchange: send map and gate gradients ---------------
+// send_row [s,R], meta_idx / meta_gate [rows_sent,k] (see ep.cu).
+cudaError_t launch_ep_pack(const int32_t* idx, const int32_t* row, const float* gate, const int32_t* rank_slot,
+                           const int32_t* rank_counts, int s, int k, int e, int R, long long rows_sent,
+                           int32_t* send_row, int32_t* meta_idx, float* meta_gate, int32_t* status,
+                           const DeviceInfo& di, cudaStream_t st);
+// dgate[t,j] = dgate_back[send_row[t, idx[t,j]/E], j] for kept routes, else 0.
+cudaError_t launch_ep_unpack_dgate(const int32_t* idx, const int32_t* row, const int32_t* send_row,
+                                   const float* dgate_back, int s, int k, int e, int R, long long rows_sent,
+                                   float* dgate, const DeviceInfo& di, cudaStream_t st);
 
 // --- expert-grouped GEMM on the tensor cores -----------------------------
 // Y[r] = X[r] . W[x]^T over the 128-row blocks of each expert segment that a

@@ -96,6 +96,7 @@ struct Params {
   int hold_tile;
   long long timeout_ns;
   int clear_status;      // tile 0 clears the status word and the rank counts
+  int absent_ok;         // an expert id of -1 is a route that does not exist (not an error)
   // fused gate (layout_kernel with EPL > 0): router logits [s, e] in, the
   // caller's ids [s, k] and gates [s, k] out
   const float* logits;
@@ -140,7 +141,7 @@ __device__ __forceinline__ bool all_published(const uint4& w, unsigned pub) {
 // which routes are valid: in range and not a repeat of an earlier route of
 // the same token.
 template <int KM>
-__device__ __forceinline__ unsigned load_routes(const Params& p, int t, int* xs) {
+__device__ __forceinline__ unsigned load_routes(const Params& p, int t, int* xs, unsigned* absent) {
   const int32_t* src = p.topk_idx + unit_base(p, t);
   if ((p.k & 3) == 0) {
 #pragma unroll
@@ -165,7 +166,7 @@ __device__ __forceinline__ unsigned load_routes(const Params& p, int t, int* xs)
     for (int j = 0; j < KM; ++j)
       if (j < p.k) xs[j] = __ldg(src + j);
   }
-  unsigned valid = 0;
+  unsigned valid = 0, none = 0;
 #pragma unroll
   for (int j = 0; j < KM; ++j) {
     if (j < p.k) {
@@ -175,8 +176,10 @@ __device__ __forceinline__ unsigned load_routes(const Params& p, int t, int* xs)
       for (int jj = 0; jj < j; ++jj)
         if (xs[jj] == x) ok = false;
       if (ok) valid |= 1u << j;
+      if (p.absent_ok && x == -1) none |= 1u << j;
     }
   }
+  *absent = none;
   return valid;
 }
 
@@ -488,8 +491,9 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
           if (gate_thread_token<KM>(p, t, xs[r])) atomicOr(&s_flags, 4);
           valid[r] = (1u << p.k) - 1u;  // k distinct ids in [0, e)
         } else {
-          valid[r] = load_routes<KM>(p, t, xs[r]);
-          bad |= valid[r] != (1u << p.k) - 1u;
+          unsigned none;
+          valid[r] = load_routes<KM>(p, t, xs[r], &none);
+          bad |= (valid[r] | none) != (1u << p.k) - 1u;
         }
         store_route_ints<KM>(p.out.idx + unit_base(p, t), xs[r], p.k);
         mark_routes<KM>(p, s_mask[r], warp, lane, xs[r], valid[r]);
@@ -513,8 +517,9 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
       int ys[KM];
       unsigned vy = 0;
       if (t < p.s) {
-        vy = load_routes<KM>(p, t, ys);
-        bad |= vy != (1u << p.k) - 1u;
+        unsigned none;
+        vy = load_routes<KM>(p, t, ys, &none);
+        bad |= (vy | none) != (1u << p.k) - 1u;
         store_route_ints<KM>(p.out.idx + unit_base(p, t), ys, p.k);
         mark_routes<KM>(p, s_mask[0], warp, lane, ys, vy);
       }
@@ -572,7 +577,8 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
       int ys[KM];
       unsigned vy = 0;
       if (t < p.s) {
-        vy = load_routes<KM>(p, t, ys);
+        unsigned none;
+        vy = load_routes<KM>(p, t, ys, &none);
         mark_routes<KM>(p, s_mask[0], warp, lane, ys, vy);
       }
       __syncthreads();
@@ -631,7 +637,7 @@ __global__ void __launch_bounds__(kThreads) token_ranks_kernel(const Params p) {
           if (__ldg(p.out.row + (size_t)t * p.k_tok + j) >= 0) ranks |= 1ull << (xs[j] / per_rank);
 #pragma unroll
           for (int jj = 0; jj < j; ++jj)
-            if (xs[jj] == xs[j]) bad = true;
+            if (xs[jj] == xs[j] && !(p.absent_ok && xs[j] == -1)) bad = true;
         }
       if (p.R_tok > 0) {
         uint8_t* tir = p.out.token_in_rank + (size_t)t * p.R_tok;
@@ -740,6 +746,7 @@ cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capa
   p.hold_tile = hold_tile;
   p.timeout_ns = timeout_ns;
   p.clear_status = build.clear_status;
+  p.absent_ok = build.absent_ok;
   p.logits = build.logits;
   p.renorm = build.renorm;
   p.gate_idx = build.gate_idx;

@@ -88,7 +88,11 @@ enum {
   MOE_KERNEL_RANK_SLOTS = 9,
   MOE_KERNEL_COMBINE_GATE_BWD = 10,
   MOE_KERNEL_GATE_LAYOUT = 11,
-  MOE_KERNEL_COUNT = 12
+  MOE_KERNEL_EP_PACK = 12,
+  MOE_KERNEL_EP_UNPACK = 13,
+  MOE_KERNEL_EP_DISPATCH = 14,
+  MOE_KERNEL_EP_COMBINE = 15,
+  MOE_KERNEL_COUNT = 16
 };
 
 /* Opaque layout handle [P1 "How"; P3 description].  Owned by the library:
@@ -119,6 +123,10 @@ typedef struct {
   int32_t pad_multiple;      /* dropless only: each expert's rows padded to a
                                 multiple of this; 1 (or 0) = no padding            */
   int32_t send_slots;        /* 1: also build rank_slot (needs num_virtual_ranks > 0) */
+  int32_t absent_routes;     /* 1: an expert id of -1 is a route that does not exist
+                                (row -1, drop 1, no status bit): the layout of the
+                                arrivals on an expert-parallel rank, whose routes to
+                                other ranks are absent                             */
 } moe_layout_options;
 
 /* Host view of a handle: sizes and read-only device pointers. */
@@ -326,6 +334,57 @@ moe_status moe_combine_gate_bwd(moe_handle h, int s, int rows, int m, moe_dtype 
  * accumulated in fp32 as in moe_combine. */
 moe_status moe_dispatch_bwd(moe_handle h, int s, int rows, int m, moe_dtype dtype,
                             const void* dX, void* dx, void* stream);
+
+/* ---- Expert-parallel exchange [P3 description: a token goes to each
+ * destination rank once, not once per selected expert; the transport
+ * replicates it, groups the arrivals by expert and reduces in its combine;
+ * P3 review thread: the routing weights travel with the tokens and are
+ * applied on the expert's rank, their gradient returns to the router].
+ * Rank r of R owns experts [r*E, (r+1)*E), E = e/R.  On the source rank,
+ * h is the layout of its routes built with num_virtual_ranks = R and
+ * send_slots = 1 (1 <= R <= 32).  The send buffer holds R destination
+ * segments in rank order, segment r = the tokens with a kept route to rank
+ * r in token order, rows_sent = sum of h's rank_counts (a host integer the
+ * caller obtains once per layout, e.g. with the all-to-all of the counts
+ * that sizes the exchange).  The all-to-all itself is the caller's (NCCL);
+ * these calls are the per-rank steps around it.  On the destination, the
+ * arrivals (segments from source 0, 1, ...) get their own layout from the
+ * received meta_idx with absent_routes = 1 and go through moe_dispatch /
+ * moe_combine(gate = the received meta_gate) / their backwards as any
+ * batch does; each arrival's combined row is its partial, sent back.
+ * Errors: MOE_ERR_INVALID_ARG (no send slots, R outside [1, 32], sizes,
+ * pointers), MOE_ERR_HANDLE_MISMATCH, MOE_ERR_CUDA. */
+
+/* send_row i32 [s,R]: send_row[t,r] = the row of token t in the send
+ * buffer's segment r, or -1; and, per sent row q, the token's k routes as
+ * the destination sees them: meta_idx i32 [rows_sent,k] = local expert id
+ * (idx - r*E) of a kept route to rank r, else -1; meta_gate f32
+ * [rows_sent,k] = its gate, else 0.  A send slot at or past rows_sent is
+ * not sent and sets MOE_DEV_BAD_ROUTE in h's status word. */
+moe_status moe_ep_pack(moe_handle h, const float* gate, int rows_sent, int32_t* send_row,
+                       int32_t* meta_idx, float* meta_gate, void* stream);
+
+/* The send buffer: X_send[send_row[t,r]] = x[t] for every r with
+ * send_row[t,r] >= 0 -- each token row read once, written once per
+ * destination rank (the dispatch kernel over the send map).  x [s,m],
+ * X_send [rows_sent,m]; rows at or past rows_sent are never written. */
+moe_status moe_ep_dispatch(moe_handle h, const int32_t* send_row, int rows_sent, int m, moe_dtype dtype,
+                           const void* x, void* X_send, void* stream);
+
+/* The source's reduction of the partials that came back (P [rows_sent,m],
+ * each at the row its token was sent from): out[t] = sum over r in rank
+ * order of P[send_row[t,r]], accumulated in fp32 and rounded once; a token
+ * that sent nothing gets zeros.  Also the backward of moe_ep_dispatch
+ * (dx from the returned gradients). */
+moe_status moe_ep_combine(moe_handle h, const int32_t* send_row, int rows_sent, int m, moe_dtype dtype,
+                          const void* P, void* out, void* stream);
+
+/* The gate gradients that came back (dgate_back f32 [rows_sent,k], row q =
+ * the destination's gradients of the sent token's k routes) to the
+ * source's routes: dgate[t,j] = dgate_back[send_row[t, idx[t,j]/E], j] for
+ * a kept route, 0 for a dropped one. */
+moe_status moe_ep_unpack_dgate(moe_handle h, const int32_t* send_row, int rows_sent, const float* dgate_back,
+                               float* dgate, void* stream);
 
 /* Expert-grouped GEMM over the dispatched buffer, on the tensor cores
  * [P3 description: the dispatch groups arrivals by expert for the grouped
