@@ -344,6 +344,17 @@ def run_ours(args, rank: int, world: int, dist):
     if graph is not None:
         launches = graph_launches * K
 
+    if args.only_step:
+        elapsed_ms = max_over_ranks([elapsed_ms], dist, dev)[0]
+        if rank != 0:
+            return None
+        ms = elapsed_ms / K
+        return {"metric": METRIC, "value": round(job_gbs(world, step_total, ms), 1), "unit": "GB/s", "n_gpus": world,
+                "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+                "config": {"workload": w.name, "launch": launch_mode, "legs": "step only (profiling run)"},
+                "gpu_launches": launches, "clocks": clk.summary()}
+
     # ---- per-kernel durations: events around each call, eager, own loop -----
     Kr = max(3, min(K, 200))
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in OPS] for _ in range(Kr)]
@@ -827,6 +838,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gemm", action="store_true", help="skip the expert_gemm figures")
     ap.add_argument("--eager", action="store_true", help="time eager calls instead of a CUDA graph of the step")
+    ap.add_argument("--only-step", action="store_true",
+                    help="time the step alone: no per-op, pair, replay, end-to-end, GEMM or CPU legs (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
