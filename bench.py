@@ -53,7 +53,7 @@ sys.path.insert(0, ROOT)
 METRIC = "dispatch+combine HBM GB/s and routed tokens/s on 1 GB300 vs HBM peak"
 DEFAULT_WORKLOAD = "fine-grained-skewed"  # the largest workload: s=16384, m=4096, e=128, k=8
 OPS = ["gate_layout", "dispatch", "combine", "combine_gate_bwd", "dispatch_bwd"]
-KERNEL_FILE = {"topk_gate": "gate.cu", "layout": "layout.cu", "gate_layout": ("layout.cu", "gate_core.cuh"),
+KERNEL_FILE = {"topk_gate": "gate.cu", "layout": "layout.cu", "gate_layout": ("layout.cu", "gate.cu", "gate_core.cuh"),
                "dispatch": "dispatch.cu", "combine": "combine.cu",
                "combine_bwd": "combine.cu", "topk_gate_bwd": ("gate.cu", "router_grad.cuh"),
                "combine_gate_bwd": ("combine.cu", "router_grad.cuh"), "dispatch_bwd": "combine.cu"}

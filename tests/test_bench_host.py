@@ -110,7 +110,7 @@ def test_traffic_record_is_per_workload_and_tied_to_the_source(tmp_path):
     assert bench.traffic_record("combine", "wl-b", str(path)) is None  # taken on another source
     # the committed record file parses and keys by workload
     committed = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
-    assert "mixtral-dropless" in committed and "combine_bwd" in committed["mixtral-dropless"]
+    assert "fine-grained-skewed" in committed and "combine_gate_bwd" in committed["fine-grained-skewed"]
 
 
 def test_gpus_flag_must_match_the_process_count():
