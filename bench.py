@@ -623,18 +623,32 @@ def run_expert_gemm(w, S, dev, reps: int = 10):
     h.destroy()
     flops = 2.0 * kept * w.m * N
     peak, src = bf16_peak()
+    hbm, hsrc = peaks()
     tf = lambda ms: flops / (ms * 1e-3) / 1e12
+    # the bytes a GEMM must move at least: its rows in, every expert's weights
+    # once, its outputs; with many experts and few rows each, streaming the
+    # weights takes longer than the MMAs
+    gemm_bytes = kept * w.m * 2 + w.e * N * w.m * 2 + kept * N * 2
+    t_tensor = flops / (peak * 1e12)
+    t_hbm = gemm_bytes / (hbm * 1e9)
+    bound = "tensor" if t_tensor >= t_hbm else "hbm"
+    t_bound_ms = max(t_tensor, t_hbm) * 1e3
     return {
-        "N": N, "K": w.m, "rows": int(Y.shape[0]), "kept_rows": kept, "flops": flops,
+        "N": N, "K": w.m, "rows": int(Y.shape[0]), "kept_rows": kept, "flops": flops, "min_bytes": gemm_bytes,
         "us_dispatch": round(t_d * 1e3, 1), "us_gemm": round(t_g * 1e3, 1),
         "us_fused_dispatch_gemm": round(t_f * 1e3, 1),
         "tflops_gemm": round(tf(t_g), 1), "tflops_fused": round(tf(t_f), 1),
         "tflops_dispatch_then_gemm": round(tf(t_d + t_g), 1),
-        "roofline": {"bound": "tensor", "peak": peak, "unit": "TFLOP/s",
+        "roofline": {"bound": bound, "peak": peak, "unit": "TFLOP/s",
                      "peak_source": f"{src} bf16 dense (burst, kernel timed alone)",
-                     "frac_gemm": round(tf(t_g) / peak, 4), "frac_fused": round(tf(t_f) / peak, 4)},
+                     "hbm_peak_gbs": hbm, "hbm_peak_source": hsrc,
+                     "us_at_bound": round(t_bound_ms * 1e3, 1),
+                     "frac_gemm": round(tf(t_g) / peak, 4), "frac_fused": round(tf(t_f) / peak, 4),
+                     "frac_of_bound_gemm": round(t_bound_ms / t_g, 4),
+                     "frac_of_bound_fused": round(t_bound_ms / t_f, 4)},
         "note": "synthetic N(0,1)/sqrt(m) expert weights; events around single calls, median of "
-                f"{reps}; not included in value",
+                f"{reps}; not included in value; the bound is the longer of the FLOPs at the bf16 peak and "
+                "min_bytes (rows in, each expert's weights once, outputs) at the copy bandwidth",
     }
 
 

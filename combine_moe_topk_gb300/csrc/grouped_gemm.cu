@@ -25,29 +25,14 @@
 // In the fused form the second CTA's gathered rows reach the MMA issuer
 // through a 16-byte shared-to-shared bulk copy that counts on the first
 // CTA's barrier: a per-K-block arrival with cluster-scope release instead
-// held the paired fused GEMM to 0.56 PFLOP/s.  The one-SM kernel below
-// (grouped_gemm_kernel, built when MOE_GEMM_PAIR / MOE_GEMM_FUSED_PAIR are
-// 0) has the same roles on one CTA per SM, persistent over the units:
-//   warp 0 lane 0  -- TMA producer: B (256 x 64) K-blocks, and in the plain
-//                     form A (128 x 64) as one tile load, into a 4-stage
-//                     SWIZZLE_128B ring, mbarrier complete_tx;
-//   warps 8..11    -- fused form only: gather the A rows with 16-byte
-//                     cp.async in the same swizzle, each warp arriving on
-//                     a stage once its lanes' copies have landed (a TMA
-//                     tile::gather4 of four rows per request was tried
-//                     first: correct, but at 33 copy requests per K-block
-//                     it held the GEMM to a third of the tensor rate);
-//   warp 1 lane 0  -- MMA issuer: four tcgen05.mma (M128 N256 K16) per
-//                     K-block into one of two 256-column TMEM accumulators,
-//                     tcgen05.commit frees the ring stage / hands over the tile;
-//   warp 2         -- allocates (and at the end frees) 512 TMEM columns;
-//   warp 3         -- the per-expert block prefix, once;
-//   warps 4..7     -- epilogue: tcgen05.ld 32 lanes x 32 columns at a time,
-//                     fp32 -> bf16 (nearest-even), staged through shared
-//                     memory so each store instruction writes 4 rows x 128
-//                     bytes; only the block's owned rows are stored (a
-//                     block's tail may belong to the next segment or to no
-//                     route).
+// held the paired fused GEMM to 0.56 PFLOP/s.  A TMA tile::gather4 of four
+// rows per request was tried first for the fused form's A: correct, but at
+// 33 copy requests per K-block it held the GEMM to a third of the tensor
+// rate.  (A one-SM form with 128-row blocks came before the pairs and was
+// measured 2-12 % slower on every shape; it is gone.  Short expert segments
+// waste the tail of a 256-row block, but a 128-row block wastes the same
+// tail rows, and where segments are short -- many experts, few rows each --
+// streaming each expert's weights once bounds the GEMM anyway.)
 // Every mbarrier wait is bounded on the global timer; a time-out records
 // MOE_DEV_TIMEOUT and the roles wind down to the TMEM release.
 #include <cuda.h>
@@ -61,34 +46,15 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK * 2;  // 16 KB
-constexpr int kBBytes = BN * BK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTmemCols = 2 * BN;     // two fp32 accumulators of 128 lanes x 256 columns
 constexpr int kThreads = 256;        // tile-fed form
 constexpr int kGatherThreads = 384;  // fused form: + 4 warps gathering the A rows
-// Plain GEMM: 1 = the two-SM (cta_group::2) kernel, 0 = the one-SM kernel.
-#ifndef MOE_GEMM_PAIR
-#define MOE_GEMM_PAIR 1
-#endif
-// Fused GEMM: 1 = the two-SM kernel, 0 = the one-SM kernel.
-#ifndef MOE_GEMM_FUSED_PAIR
-#define MOE_GEMM_FUSED_PAIR 1
-#endif
-// One-SM fused form: stages a gathering warp's arrival trails its copies.
-#ifndef MOE_GEMM_LAG
-#define MOE_GEMM_LAG 2
-#endif
-constexpr int kGatherLag = MOE_GEMM_LAG;
-static_assert(kGatherLag >= 1 && kGatherLag < 4, "the ring must keep a stage the gather has not yet claimed");
 constexpr int kMaxE = 256;
 // epilogue staging: per epilogue warp 32 rows x 64 bf16 columns, rows padded
 // to 144 bytes (conflict-free 16-byte writes by row and reads by column)
 constexpr int kStageRowBytes = 64 * 2 + 16;
 constexpr int kEpiWarpBytes = 32 * kStageRowBytes;
 constexpr int kEpiBytes = 4 * kEpiWarpBytes;
-constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + 1024;  // + alignment slack
 
 struct GemmParams {
   const __nv_bfloat16* x;  // gather mode: token rows [s, K]
@@ -102,18 +68,6 @@ struct GemmParams {
   long long timeout_ns;
 };
 
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A
-// and B, both K-major, M = 128, N = 256.
-__device__ __forceinline__ uint32_t mma_idesc() {
-  uint32_t d = 0;
-  d |= 1u << 4;                        // accumulator format: f32
-  d |= 1u << 7;                        // A format: bf16
-  d |= 1u << 10;                       // B format: bf16
-  d |= (uint32_t)(BN >> 3) << 17;      // N / 8
-  d |= (uint32_t)(BM >> 4) << 24;      // M / 16
-  return d;
-}
-
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle (as TMA writes
 // it), 8-row groups 1024 bytes apart.  The tile base is 1024-byte aligned.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
@@ -126,26 +80,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
   return d;
 }
 
-__device__ __forceinline__ void tma_load_2d(void* sdst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(sdst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
-}
-
 // 16-byte asynchronous copy global -> shared (L2 only): copies src_bytes
 // (0 or 16) from gsrc and fills the rest of the 16 bytes with zeros; with 0
 // nothing is read.
 __device__ __forceinline__ void cp_async16_zfill(uint32_t sdst, const void* gsrc, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sdst), "l"(gsrc), "r"(src_bytes)
                : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // One arrival on `bar` once every cp.async this thread issued so far has
@@ -158,23 +98,6 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, int accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_addr(bar))
-      : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -260,233 +183,6 @@ __device__ __forceinline__ Unit decode_unit(int u, int ntn, const int* s_blk, co
   return t;
 }
 
-template <bool kGather>
-__global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
-  __shared__ uint32_t tmem_base;
-  __shared__ int s_off[kMaxE + 1], s_cnt[kMaxE], s_blk[kMaxE + 1];
-  __shared__ int s_err;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
-  const uint64_t deadline = globaltimer_ns() + (uint64_t)p.timeout_ns;
-
-  for (int x = threadIdx.x; x <= p.e; x += blockDim.x) s_off[x] = __ldg(p.offsets + x);
-  for (int x = threadIdx.x; x < p.e; x += blockDim.x) s_cnt[x] = __ldg(p.counts + x);
-  if (threadIdx.x == 0) {
-    s_err = 0;
-    for (int i = 0; i < kStages; ++i) {
-      // the B tile's expect_tx arrival, plus one per gathering warp
-      mbar_init(&full[i], kGather ? 1 + (kGatherThreads - kThreads) / 32 : 1);
-      mbar_init(&empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 128);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
-  if (warp == 2) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_addr(&tmem_base)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  } else if (warp == 3) {
-    // exclusive prefix over experts of their 128-row block counts
-    int carry = 0;
-    for (int x0 = 0; x0 < p.e; x0 += 32) {
-      const int x = x0 + lane;
-      const int c = x < p.e ? s_cnt[x] : 0;
-      int v = c > 0 ? (c + BM - 1) / BM : 0;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int w = __shfl_up_sync(0xffffffffu, v, d);
-        if (lane >= d) v += w;
-      }
-      const int blocks = x < p.e ? (c > 0 ? (c + BM - 1) / BM : 0) : 0;
-      if (x < p.e) s_blk[x] = carry + v - blocks;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-    if (lane == 0) s_blk[p.e] = carry;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = tmem_base;
-
-  const int ntn = (p.N + BN - 1) / BN;  // the last column tile may be partial
-  const int nunits = s_blk[p.e] * ntn;
-  const int kblocks = (p.K + BK - 1) / BK;  // columns past K read as zeros
-
-  if (warp == 0 && lane == 0) {
-    // ---- TMA producer: B always, A in the tile-fed form ------------------
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-      const Unit t = decode_unit(u, ntn, s_blk, s_off, s_cnt, p.e);
-      for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, deadline)) {
-          ok = false;
-          break;
-        }
-        uint8_t* sa = smem + stage * kStageBytes;
-        mbar_arrive_expect_tx(&full[stage], kGather ? kBBytes : kStageBytes);
-        tma_load_2d(sa + kABytes, &tmB, kb * BK, t.x * p.N + t.n0, &full[stage]);
-        if (!kGather) tma_load_2d(sa, &tmA, kb * BK, t.r0, &full[stage]);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-    if (!ok) atomicOr(&s_err, 1);
-  } else if (kGather && warp >= kThreads / 32) {
-    // ---- A gather (fused form): 128 threads, 16-byte cp.async ------------
-    // Warp gw copies rows 32*gw .. 32*gw+31 of the block; per instruction 8
-    // lanes cover one row's 128 bytes (4 rows at a time), written in the
-    // 128-byte swizzle the MMA descriptor reads (16-byte chunk c of row r at
-    // chunk c ^ (r & 7)).  Each lane waits for its copies to a stage (kGatherLag
-    // stages behind its issue) and fences them for the tensor cores; then one
-    // lane arrives on the stage's full barrier for the warp.
-    const int gw = warp - kThreads / 32, chunk = lane & 7;
-    int stage = 0, astage = 0, pending = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-      const Unit t = decode_unit(u, ntn, s_blk, s_off, s_cnt, p.e);
-      const __nv_bfloat16* src[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int rr = 32 * gw + 4 * i + (lane >> 3);
-        int tok = 0;  // rows no route owns are skipped below
-        if (rr < t.nvalid) {
-          const int v = __ldg(p.inv_row + t.r0 + rr);
-          tok = (unsigned)v < (unsigned)p.s ? v : 0;
-        }
-        src[i] = p.x + (size_t)tok * p.K + chunk * 8;
-      }
-      for (int kb = 0; kb < kblocks; ++kb) {
-        bool waited = true;
-        if (lane == 0) waited = mbar_wait_bounded(&empty[stage], phase ^ 1u, deadline);
-        if (!__shfl_sync(0xffffffffu, waited ? 1 : 0, 0)) {
-          ok = false;
-          break;
-        }
-        const uint32_t sa = smem_addr(smem + stage * kStageBytes);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          // rows no route owns are not copied: an output row depends only on
-          // its own A row, and theirs are never stored
-          const int rr = 32 * gw + 4 * i + (lane >> 3);
-          if (rr < t.nvalid) {
-            // columns past K: zeros, nothing read (the row's end may be the buffer's)
-            const bool in_k = kb * BK + chunk * 8 < p.K;
-            cp_async16_zfill(sa + rr * 128 + ((chunk ^ (rr & 7)) << 4), in_k ? src[i] + kb * BK : src[i],
-                             in_k ? 16u : 0u);
-          }
-        }
-        cp_async_commit();
-        if (++pending > kGatherLag) {
-          cp_async_wait<kGatherLag>();
-          fence_proxy_async_smem();
-          __syncwarp();  // every lane's copies to the stage have landed
-          if (lane == 0) mbar_arrive(&full[astage]);
-          --pending;
-          if (++astage == kStages) astage = 0;
-        }
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-    cp_async_wait<0>();  // nothing of this thread's stays in flight
-    if (ok) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      for (; pending > 0; --pending) {
-        if (lane == 0) mbar_arrive(&full[astage]);
-        if (++astage == kStages) astage = 0;
-      }
-    } else if (lane == 0) {
-      atomicOr(&s_err, 1);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer ------------------------------------------------------
-    const uint32_t idesc = mma_idesc();
-    int stage = 0, acc = 0;
-    uint32_t phase = 0, tphase[2] = {0u, 0u};
-    bool ok = true;
-    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-      if (!mbar_wait_bounded(&tempty[acc], tphase[acc] ^ 1u, deadline)) {
-        ok = false;
-        break;
-      }
-      tphase[acc] ^= 1u;
-      tc_fence_after();
-      const uint32_t dt = tbase + (uint32_t)(acc * BN);
-      for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait_bounded(&full[stage], phase, deadline)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sa = smem_addr(smem + stage * kStageBytes);
-        const uint64_t ad = smem_desc(sa), bd = smem_desc(sa + kABytes);
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 per MMA: advance 32 bytes in the swizzled row
-          mma_bf16(dt, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (kb | kk) != 0);
-        mma_commit(&empty[stage]);  // the ring stage is free once these MMAs have read it
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-      if (!ok) break;
-      mma_commit(&tfull[acc]);  // the accumulator is complete
-      acc ^= 1;
-    }
-    if (!ok) atomicOr(&s_err, 1);
-  } else if (warp >= 4 && warp < 8) {
-    // ---- epilogue: TMEM -> registers -> bf16 -> Y ------------------------
-    const int ew = warp - 4;  // TMEM lanes 32*ew .. 32*ew+31
-    int acc = 0;
-    uint32_t tphase[2] = {0u, 0u};
-    bool ok = true;
-    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-      const Unit t = decode_unit(u, ntn, s_blk, s_off, s_cnt, p.e);
-      // every lane waits (and acquires) itself; the warp leaves together
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull[acc], tphase[acc], deadline))) {
-        ok = false;
-        break;
-      }
-      tphase[acc] ^= 1u;
-      tc_fence_after();
-      store_accumulator(tbase + ((uint32_t)(32 * ew) << 16) + (uint32_t)(acc * BN), ew, lane,
-                        smem + kStages * kStageBytes + ew * kEpiWarpBytes, p.Y, p.N, t.r0, t.n0, t.nvalid);
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
-      acc ^= 1;
-    }
-    if (!ok) atomicOr(&s_err, 1);
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 2)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),
-                 "r"(kTmemCols)
-                 : "memory");
-  if (threadIdx.x == 0 && s_err) raise_status(p.status, MOE_DEV_TIMEOUT);
-}
-
 // ---- two-SM form (cta_group::2) ------------------------------------------
 // A cluster of two CTAs on two SMs computes one 256 x 256 tile: CTA rank c
 // holds rows 128c .. 128c+127 of the 256-row block (its A half) and columns
@@ -558,13 +254,14 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t dtmem, uint64_t adesc, ui
       : "memory");
 }
 
-// Arrive on the barrier at this offset in both CTAs of the pair once the
-// issuing thread's earlier MMAs have completed.
-__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+// Arrive on the barrier at this offset in the CTAs of the pair that `mask`
+// names (bit c = rank c) once the issuing thread's earlier MMAs have
+// completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t mask = 0x3) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;" ::"r"(smem_addr(bar)),
-      "h"((uint16_t)0x3)
+      "h"(mask)
       : "memory");
 }
 
@@ -619,6 +316,7 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[kPairStages], empty[kPairStages], tfull[2], tempty[2];
   __shared__ __align__(8) uint64_t gathered[kPairStages];  // fused form, rank 1: its gathered rows landed
+  __shared__ __align__(8) uint64_t mma_drain;               // rank 0, after a time-out: its MMAs are done
   __shared__ __align__(16) uint8_t s_signal[16];             // fused form: source / target of rank 1's signal
   __shared__ uint32_t tmem_base;
   __shared__ int s_off[kMaxE + 1], s_cnt[kMaxE], s_blk[kMaxE + 1];
@@ -648,6 +346,7 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 2 * 4);  // rank 0: the epilogue warps of both ranks
     }
+    mbar_init(&mma_drain, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -863,7 +562,15 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
       mma_commit_pair(&tfull[acc]);
       acc ^= 1;
     }
-    if (!ok) atomicOr(&s_err, 1);
+    if (!ok) {
+      // a wait ran out: before this CTA (and, at the cluster barrier below,
+      // its partner) leaves, let every MMA issued so far finish reading both
+      // CTAs' shared memory -- one more commit, to this CTA only, arrives
+      // after all of them and after the commits before it (bounded wait)
+      mma_commit_pair(&mma_drain, 0x1);
+      mbar_wait_bounded(&mma_drain, 0, globaltimer_ns() + (uint64_t)p.timeout_ns);
+      atomicOr(&s_err, 1);
+    }
   } else if (warp >= 4 && warp < 8) {
     // ---- epilogue (both ranks): own 128 rows ------------------------------
     const int ew = warp - 4;
@@ -937,30 +644,6 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
 }
 
 template <bool kGather>
-cudaError_t enable_smem() {
-  static OncePerDevice once;
-  return once.run([] {
-    return cudaFuncSetAttribute(grouped_gemm_kernel<kGather>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSmemBytes);
-  });
-}
-
-template <bool kGather>
-cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
-                   const DeviceInfo& di, cudaStream_t st) {
-  cudaError_t err = enable_smem<kGather>();
-  if (err != cudaSuccess) return err;
-  // units: at most ceil(rows / 128) + e row blocks (one partial block per
-  // segment), times the column tiles; the kernel reads the exact count
-  const long long blocks = ((long long)p.rows + BM - 1) / BM + p.e;
-  const long long nunits = blocks * ((p.N + BN - 1) / BN);
-  int grid = (long long)di.sms < nunits ? di.sms : (int)nunits;
-  if (grid < 1) grid = 1;
-  grouped_gemm_kernel<kGather><<<grid, kGather ? kGatherThreads : kThreads, kSmemBytes, st>>>(ma, mb, p);
-  return cudaGetLastError();
-}
-
-template <bool kGather>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
                         const DeviceInfo& di, cudaStream_t st) {
   static OncePerDevice once;
@@ -1013,16 +696,10 @@ cudaError_t launch_grouped_gemm(const int32_t* offsets, const int32_t* counts, i
                                 int N, const void* X, const void* W, void* Y, int32_t* status,
                                 const DeviceInfo& di, cudaStream_t st) {
   CUtensorMap ma, mb;
-  if (MOE_GEMM_PAIR) {
-    if (!make_map(&ma, X, (uint64_t)K, (uint64_t)rows, BM) ||
-        !make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN / 2))
-      return cudaErrorInvalidValue;
-    return launch_pair<false>(ma, mb, params(offsets, counts, e, rows, K, N, Y, status), di, st);
-  }
   if (!make_map(&ma, X, (uint64_t)K, (uint64_t)rows, BM) ||
-      !make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN))
+      !make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN / 2))
     return cudaErrorInvalidValue;
-  return launch<false>(ma, mb, params(offsets, counts, e, rows, K, N, Y, status), di, st);
+  return launch_pair<false>(ma, mb, params(offsets, counts, e, rows, K, N, Y, status), di, st);
 }
 
 cudaError_t launch_dispatch_gemm(const int32_t* offsets, const int32_t* counts, const int32_t* inv_row,
@@ -1033,12 +710,8 @@ cudaError_t launch_dispatch_gemm(const int32_t* offsets, const int32_t* counts, 
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.inv_row = inv_row;
   p.s = s;
-  if (MOE_GEMM_FUSED_PAIR) {
-    if (!make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN / 2)) return cudaErrorInvalidValue;
-    return launch_pair<true>(mb, mb, p, di, st);  // A is gathered by threads: no A map
-  }
-  if (!make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN)) return cudaErrorInvalidValue;
-  return launch<true>(mb, mb, p, di, st);
+  if (!make_map(&mb, W, (uint64_t)K, (uint64_t)e * (uint64_t)N, BN / 2)) return cudaErrorInvalidValue;
+  return launch_pair<true>(mb, mb, p, di, st);  // A is gathered by threads: no A map
 }
 
 }  // namespace moe
