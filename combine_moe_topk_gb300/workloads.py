@@ -18,7 +18,9 @@ routing traces are available, so N(0, 1) router logits stand in for them):
   expert bias b_j = -1.2*log(j+1) (the log of a Zipf(1.2) weight)
 
 Draw order per seed: logits, x, y (expert output, dispatched shape), dout.
-bf16 tensors are fp32 N(0, 1) draws rounded to nearest-even.
+The logits always come from the CPU generator (the routing of a seed is the
+same on every device); on a GPU the payloads come from that device's
+generator.  bf16 tensors are fp32 N(0, 1) draws rounded to nearest-even.
 """
 from __future__ import annotations
 
@@ -88,24 +90,32 @@ def _gen(device, seed: int) -> torch.Generator:
 
 
 def make_logits(w: Workload, device="cpu", seed: int | None = None) -> torch.Tensor:
-    g = _gen(device, w.seed if seed is None else seed)
-    logits = torch.randn(w.s, w.e, generator=g, device=device, dtype=torch.float32)
+    """Router logits [s,e] f32, drawn on the CPU whatever the device, so a seed
+    gives the same routing everywhere (plus the workload's expert bias)."""
+    g = _gen("cpu", w.seed if seed is None else seed)
+    logits = torch.randn(w.s, w.e, generator=g, dtype=torch.float32)
     if w.zipf_alpha:
         bias = torch.tensor([-w.zipf_alpha * math.log(j + 1) for j in range(w.e)], dtype=torch.float32)
-        logits += bias.to(device)
-    return logits
+        logits += bias
+    return logits.to(device)
 
 
 def make_inputs(w: Workload, device="cpu", seed: int | None = None, with_grad: bool = True,
                 rows: int | None = None) -> dict:
     """Draw logits [s,e] f32, x [s,m], y [rows,m] and dout [s,m] from one seed
-    (rows defaults to the workload's; a padded layout needs more)."""
+    (rows defaults to the workload's; a padded layout needs more).  The
+    logits come first from the seed's CPU generator, so the routing is the
+    same on every device; the payloads continue on the device's generator
+    (on the CPU that is the same generator, so a CPU draw is one stream)."""
     seed = w.seed if seed is None else seed
-    g = _gen(device, seed)
-    logits = torch.randn(w.s, w.e, generator=g, device=device, dtype=torch.float32)
+    g = _gen("cpu", seed)
+    logits = torch.randn(w.s, w.e, generator=g, dtype=torch.float32)
     if w.zipf_alpha:
         bias = torch.tensor([-w.zipf_alpha * math.log(j + 1) for j in range(w.e)], dtype=torch.float32)
-        logits += bias.to(device)
+        logits += bias
+    logits = logits.to(device)
+    if torch.device(device).type != "cpu":
+        g = _gen(device, seed)
     dt = w.torch_dtype
     x = torch.randn(w.s, w.m, generator=g, device=device, dtype=torch.float32).to(dt)
     out = dict(logits=logits, x=x)
