@@ -187,3 +187,42 @@ def test_ep_calls_reject_a_handle_without_send_slots():
     hs = B.moe_dispatch_layout_ex(idx, 8, 0, 2, send_slots=True)
     with pytest.raises(B.MoEError):
         B.moe_ep_pack(hs, torch.ones(64, 2, device=DEV), 64 * 2 + 1)  # more rows than s*R
+
+
+def test_expert_parallel_layer_on_a_one_rank_group():
+    """ExpertParallelMoE end to end over a real (one-rank, NCCL) process
+    group: with one rank it must give the one-GPU path's bits -- forward,
+    input gradient and gate gradients."""
+    import socket
+
+    import torch.distributed as dist
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                            device_id=DEV)
+    try:
+        w = W.Workload("ep1", s=700, m=128, e=16, k=4, dtype="bf16", capacity=0, R=1, seed=21)
+        inp = W.make_inputs(w, device=DEV)
+        idx, gate = B.moe_topk_gate(inp["logits"], w.k, 1)
+        layer = EP.ExpertParallelMoE(w.e)
+        assert (layer.R, layer.E) == (1, 16)
+        h, plan = layer.layout(idx)
+        assert plan.rows_sent == plan.rows_recv == w.s
+        fwd = lambda recv: expert_gpu(recv.X, recv.h, 0)
+        bwd = lambda recv, dY: expert_gpu(dY, recv.h, 0)  # the expert is a per-expert scale: its own adjoint
+        out, saved = layer.forward(h, plan, inp["x"], gate, fwd)
+        dx, dgate = layer.backward(h, plan, saved, inp["dout"], bwd)
+        # the one-GPU path on the same routes
+        h1 = B.moe_dispatch_layout(idx, w.e)
+        X = B.moe_dispatch(h1, inp["x"])
+        y = expert_gpu(X, h1, 0)
+        ref = B.moe_combine(h1, y, gate)
+        dY, dg = B.moe_combine_bwd(h1, inp["dout"], gate, y)
+        dxr = B.moe_dispatch_bwd(h1, expert_gpu(dY, h1, 0))
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref) and torch.equal(dx, dxr)
+        assert torch.equal(dgate.view(torch.int32), dg.view(torch.int32))
+    finally:
+        dist.destroy_process_group()
