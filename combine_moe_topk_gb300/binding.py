@@ -24,7 +24,7 @@ STATUS = {
     8: "MOE_ERR_NONFINITE", 9: "MOE_ERR_BAD_ROUTE",
 }
 MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
-MOE_DEV_NONFINITE, MOE_DEV_BAD_ROUTE, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4
+MOE_DEV_NONFINITE, MOE_DEV_BAD_ROUTE, MOE_DEV_TIMEOUT, MOE_DEV_ROWS_EXCEEDED = 0x1, 0x2, 0x4, 0x8
 KERNELS = ["topk_gate", "layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd", "topk_gate_bwd",
            "grouped_gemm", "dispatch_gemm", "rank_slots", "combine_gate_bwd", "gate_layout", "ep_pack", "ep_unpack",
            "ep_dispatch", "ep_combine"]
@@ -50,7 +50,8 @@ class MoEError(RuntimeError):
 
 class LayoutOptions(ctypes.Structure):
     _fields_ = [("capacity", ctypes.c_int32), ("num_virtual_ranks", ctypes.c_int32), ("priority", ctypes.c_int32),
-                ("pad_multiple", ctypes.c_int32), ("send_slots", ctypes.c_int32), ("absent_routes", ctypes.c_int32)]
+                ("pad_multiple", ctypes.c_int32), ("send_slots", ctypes.c_int32), ("absent_routes", ctypes.c_int32),
+                ("rows_bound", ctypes.c_int32)]
 
 
 PRIORITY = {"token": 0, "kmajor": 1}
@@ -291,17 +292,18 @@ def moe_dispatch_layout(topk_idx: torch.Tensor, e: int, capacity: int = 0, num_v
 
 def moe_dispatch_layout_ex(topk_idx: torch.Tensor, e: int, capacity: int = 0, num_virtual_ranks: int = 0,
                            priority: str = "token", pad_multiple: int = 1, send_slots: bool = False,
-                           absent_routes: bool = False) -> Handle:
+                           absent_routes: bool = False, rows_bound: int = 0) -> Handle:
     """Layout with a capacity priority ("token" or "kmajor"), per-expert
     padding of the dropless rows (handle.rows is then an upper bound),
     with send_slots each token's token-order slot per virtual rank
-    (handle.rank_slot()), and with absent_routes expert id -1 taken as a
-    route that does not exist."""
+    (handle.rank_slot()), with absent_routes expert id -1 taken as a
+    route that does not exist, and with rows_bound (dropless) the caller's
+    bound on the kept routes as the handle's rows."""
     if topk_idx.dim() != 2 or topk_idx.dtype != torch.int32:
         raise ValueError("topk_idx must be int32 [s, k]")
     s, k = topk_idx.shape
     opt = LayoutOptions(int(capacity), int(num_virtual_ranks), PRIORITY[priority], int(pad_multiple),
-                        int(bool(send_slots)), int(bool(absent_routes)))
+                        int(bool(send_slots)), int(bool(absent_routes)), int(rows_bound))
     raw = ctypes.c_void_p()
     dev = topk_idx.device
     rc = lib().moe_dispatch_layout_ex(_ptr(topk_idx), s, int(e), k, ctypes.byref(opt), _stream(dev),
@@ -312,13 +314,14 @@ def moe_dispatch_layout_ex(topk_idx: torch.Tensor, e: int, capacity: int = 0, nu
 
 def moe_layout_create(s: int, e: int, k: int, capacity: int = 0, num_virtual_ranks: int = 0,
                       priority: str = "token", pad_multiple: int = 1, send_slots: bool = False,
-                      device: torch.device | None = None, absent_routes: bool = False) -> Handle:
+                      device: torch.device | None = None, absent_routes: bool = False,
+                      rows_bound: int = 0) -> Handle:
     """An empty handle for [s, k] routes over e experts with these layout
     options, to be built (and rebuilt) in place by moe_layout_rebuild or
     moe_topk_gate_layout without allocating."""
     dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
     opt = LayoutOptions(int(capacity), int(num_virtual_ranks), PRIORITY[priority], int(pad_multiple),
-                        int(bool(send_slots)), int(bool(absent_routes)))
+                        int(bool(send_slots)), int(bool(absent_routes)), int(rows_bound))
     raw = ctypes.c_void_p()
     with torch.cuda.device(dev):
         rc = lib().moe_layout_create(int(s), int(e), int(k), ctypes.byref(opt), _stream(dev), ctypes.byref(raw))

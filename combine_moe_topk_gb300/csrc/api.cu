@@ -311,10 +311,16 @@ moe_status create_handle(int s, int e, int k, const moe_layout_options* options,
   if (R < 0 || R > kMaxR || (R > 0 && e % R != 0))
     return fail(MOE_ERR_INVALID_ARG, "num_virtual_ranks must be in [0, 64] and divide e");
   const long long routes = (long long)s * k;
-  const long long rows = capacity > 0 ? (long long)e * capacity : routes + (long long)e * (pad - 1);
+  long long rows = capacity > 0 ? (long long)e * capacity : routes + (long long)e * (pad - 1);
   if (routes > 2147483647LL || rows > 2147483647LL)
     return fail(MOE_ERR_INVALID_ARG, "s*k and the row count must be < 2^31");
   if ((long long)s * e > 2147483647LL) return fail(MOE_ERR_INVALID_ARG, "s*e must be < 2^31");
+  if (options->rows_bound != 0) {
+    if (capacity > 0 || pad > 1) return fail(MOE_ERR_INVALID_ARG, "rows_bound applies to the unpadded dropless layout");
+    if (options->rows_bound < 0 || options->rows_bound > routes)
+      return fail(MOE_ERR_INVALID_ARG, "rows_bound must be in [0, s*k]");
+    rows = options->rows_bound;
+  }
 
   if (topk_idx && s > 0) MOE_TRY(check_ptr(topk_idx, "topk_idx"));
 
@@ -439,8 +445,8 @@ moe_status build_handle(moe_handle h, const int32_t* topk_idx, const float* logi
       g_hold_tile = -1;
     }
   }
-  err = moe::launch_layout(topk_idx, h->s, h->e, h->k, h->capacity, h->R, h->priority, h->pad, h->plan, h->out,
-                           hold, timeout_ns, st, build);
+  err = moe::launch_layout(topk_idx, h->s, h->e, h->k, h->capacity, h->R, h->priority, h->pad, h->rows, h->plan,
+                           h->out, hold, timeout_ns, st, build);
   if (err != cudaSuccess) return cuda_fail(err, "layout launch");
   g_launches[logits ? MOE_KERNEL_GATE_LAYOUT : MOE_KERNEL_LAYOUT]++;
   h->builds++;
@@ -526,6 +532,7 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, int s, int e, int k, int
   opt.pad_multiple = 1;
   opt.send_slots = 0;
   opt.absent_routes = 0;
+  opt.rows_bound = 0;
   return moe_dispatch_layout_ex(topk_idx, s, e, k, &opt, stream, out);
 }
 

@@ -88,8 +88,10 @@ int gate_layout_blocks_per_sm();
 
 // priority 0 = token order, 1 = k-major; pad_multiple >= 1 pads dropless
 // expert segments.  The plan must be made for s units (s * k when k-major).
+// rows: the dispatched buffer's rows; a dropless route whose row would fall at
+// or past it gets none (MOE_DEV_ROWS_EXCEEDED), and counts / offsets are cut there.
 cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity, int R,
-                          int priority, int pad_multiple, const LayoutPlan& plan,
+                          int priority, int pad_multiple, int rows, const LayoutPlan& plan,
                           const LayoutOut& out, int hold_tile, long long timeout_ns,
                           cudaStream_t st, const LayoutBuild& build);
 

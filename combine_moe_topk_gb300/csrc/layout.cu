@@ -97,6 +97,7 @@ struct Params {
   long long timeout_ns;
   int clear_status;      // tile 0 clears the status word and the rank counts
   int absent_ok;         // an expert id of -1 is a route that does not exist (not an error)
+  int rows;              // rows of the dispatched buffer: no route gets a row at or past it
   // fused gate (layout_kernel with EPL > 0): router logits [s, e] in, the
   // caller's ids [s, k] and gates [s, k] out
   const float* logits;
@@ -307,9 +308,12 @@ __device__ void expert_offsets(const Params& p, const int* s_tot, int* s_off, bo
       const int off = p.capacity > 0 ? x * p.capacity : run;
       s_off[x] = off;
       if (write_out) {
+        // a segment is cut at the buffer's rows (a dropless bound below the
+        // routes: the routes past it get no row, write_routes reports them)
+        const int o = min(off, p.rows);
         p.out.raw_counts[x] = raw[i];
-        p.out.counts[x] = v[i];
-        p.out.offsets[x] = off;
+        p.out.counts[x] = min(v[i], p.rows - o);
+        p.out.offsets[x] = o;
       }
     }
     run += (v[i] + p.pad - 1) / p.pad * p.pad;
@@ -317,7 +321,7 @@ __device__ void expert_offsets(const Params& p, const int* s_tot, int* s_off, bo
   if (lane == 31) {
     const int end = p.capacity > 0 ? p.e * p.capacity : run;
     s_off[p.e] = end;
-    if (write_out) p.out.offsets[p.e] = end;
+    if (write_out) p.out.offsets[p.e] = min(end, p.rows);
   }
 }
 
@@ -348,7 +352,7 @@ template <int KM>
 __device__ __forceinline__ unsigned long long write_routes(const Params& p, int t, int lane,
                                                            const int* xs, unsigned valid,
                                                            const int* base, const unsigned* mask,
-                                                           const int* s_off) {
+                                                           const int* s_off, bool* over) {
   const unsigned below = (1u << lane) - 1u;
   const int per_rank = p.R > 0 ? p.e / p.R : 1;
   unsigned long long ranks = 0;
@@ -368,6 +372,10 @@ __device__ __forceinline__ unsigned long long write_routes(const Params& p, int 
         if (l < p.capacity) row[j] = x * p.capacity + l;
       } else {
         row[j] = s_off[x] + l;
+        if (row[j] >= p.rows) {  // past the caller's bound on the rows: not kept, reported
+          row[j] = -1;
+          *over = true;
+        }
       }
       if (row[j] >= 0) ranks |= 1ull << (x / per_rank);
     }
@@ -444,7 +452,7 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   __shared__ int s_tot[kMaxE];
   __shared__ int s_off[kMaxE + 1];
   __shared__ int s_rank[kMaxR];
-  __shared__ int s_flags;  // bit 0: a bad route; bit 1: a wait timed out; bit 2: a non-finite logit
+  __shared__ int s_flags;  // bit 0: a bad route; 1: a wait timed out; 2: a non-finite logit; 3: rows exceeded
   __shared__ unsigned s_pub;  // this build's publish bit
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -553,6 +561,7 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   }
 
   // ---- C: token-order slots, rows, drops, dedup ----------------------------
+  bool over = false;  // a route's row fell at or past the buffer's rows
   if (TPT > 0) {
 #pragma unroll
     for (int r = 0; r < NM; ++r) {
@@ -566,7 +575,7 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
       const int t = (sub0 + r) * kThreads + tid;
       unsigned long long ranks = 0;
       if (sub0 + r < sub1 && t < p.s)
-        ranks = write_routes<KM>(p, t, lane, xs[r], valid[r], s_wbase[r][warp], s_mask[r][warp], s_off);
+        ranks = write_routes<KM>(p, t, lane, xs[r], valid[r], s_wbase[r][warp], s_mask[r][warp], s_off, &over);
       if (p.R > 0) count_ranks(ranks, lane, s_rank);
     }
   } else {
@@ -593,13 +602,14 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
       }
       __syncthreads();
       unsigned long long ranks = 0;
-      if (t < p.s) ranks = write_routes<KM>(p, t, lane, ys, vy, s_wbase[0][warp], s_mask[0][warp], s_off);
+      if (t < p.s) ranks = write_routes<KM>(p, t, lane, ys, vy, s_wbase[0][warp], s_mask[0][warp], s_off, &over);
       if (p.R > 0) count_ranks(ranks, lane, s_rank);
       __syncthreads();
       for (int i = tid; i < kWarps * kMaxE; i += kThreads) (&s_mask[0][0][0])[i] = 0u;
       __syncthreads();
     }
   }
+  if (over) atomicOr(&s_flags, 8);
   __syncthreads();
   pdl_trigger_late();
   if (p.R > 0 && tid < p.R && s_rank[tid]) atomicAdd(&p.out.rank_counts[tid], s_rank[tid]);
@@ -608,6 +618,7 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
     if (s_flags & 1) bits |= MOE_DEV_BAD_ROUTE;
     if (s_flags & 2) bits |= MOE_DEV_TIMEOUT;
     if (s_flags & 4) bits |= MOE_DEV_NONFINITE;
+    if (s_flags & 8) bits |= MOE_DEV_ROWS_EXCEEDED;
     raise_status(p.out.status, bits);
   }
 }
@@ -725,7 +736,7 @@ bool layout_can_fuse_gate(const LayoutPlan& plan, int priority, int e, const Dev
 }
 
 cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capacity, int R,
-                          int priority, int pad_multiple, const LayoutPlan& plan,
+                          int priority, int pad_multiple, int rows, const LayoutPlan& plan,
                           const LayoutOut& out, int hold_tile, long long timeout_ns,
                           cudaStream_t st, const LayoutBuild& build) {
   Params p;
@@ -747,6 +758,7 @@ cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capa
   p.timeout_ns = timeout_ns;
   p.clear_status = build.clear_status;
   p.absent_ok = build.absent_ok;
+  p.rows = rows;
   p.logits = build.logits;
   p.renorm = build.renorm;
   p.gate_idx = build.gate_idx;
@@ -783,8 +795,8 @@ cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capa
     // from now on
     cudaGetLastError();
     g_coop_pdl.store(false);
-    return launch_layout(topk_idx, s, e, k, capacity, R, priority, pad_multiple, plan, out, hold_tile, timeout_ns,
-                         st, build);
+    return launch_layout(topk_idx, s, e, k, capacity, R, priority, pad_multiple, rows, plan, out, hold_tile,
+                         timeout_ns, st, build);
   }
   if (err != cudaSuccess || !p.kmajor || s == 0) return err;
   constexpr int kMaxPostBlocks = 1024;  // grid-stride beyond this
@@ -881,7 +893,8 @@ cudaError_t launch_layout_noalloc(const int32_t* topk_idx, int s, int e, int k, 
     err = cudaMemsetAsync(out.rank_counts, 0, (size_t)R * sizeof(int32_t), st);
   if (err != cudaSuccess) return err;
   LayoutBuild build;  // status: the caller's word, OR-ed into
-  return launch_layout(topk_idx, s, e, k, capacity, R, 0, 1, plan, out, -1, 2000000000LL, st, build);
+  const long long rows = capacity > 0 ? (long long)e * capacity : (long long)s * k;
+  return launch_layout(topk_idx, s, e, k, capacity, R, 0, 1, (int)rows, plan, out, -1, 2000000000LL, st, build);
 }
 
 }  // namespace moe

@@ -50,8 +50,9 @@ from . import binding as B
 @dataclasses.dataclass
 class Plan:
     """Sizes of one layout's exchange on this rank (host integers)."""
-    send_counts: list   # rows to each destination rank, in rank order
-    recv_counts: list   # rows from each source rank, in rank order
+    send_counts: list   # rows (tokens) to each destination rank, in rank order
+    recv_counts: list   # rows (tokens) from each source rank, in rank order
+    recv_routes: list | None = None  # kept routes from each source to this rank's experts
 
     @property
     def rows_sent(self) -> int:
@@ -61,17 +62,31 @@ class Plan:
     def rows_recv(self) -> int:
         return sum(self.recv_counts)
 
+    @property
+    def routes_recv(self) -> int:
+        """Rows of this rank's grouped buffer (0 when not exchanged)."""
+        return sum(self.recv_routes) if self.recv_routes is not None else 0
 
-def exchange_counts(rank_counts: torch.Tensor, group=None) -> Plan:
+
+def route_counts(h: B.Handle) -> torch.Tensor:
+    """Kept routes to each virtual rank's experts ([R], from the handle's counts)."""
+    return h.counts().view(h.R, h.e // h.R).sum(dim=1)
+
+
+def exchange_counts(rank_counts: torch.Tensor, group=None, routes: torch.Tensor | None = None) -> Plan:
     """All-to-all of this rank's per-destination token counts ([R] int32,
-    e.g. a layout handle's rank_counts) into a Plan.  Reads the counts on
-    the host once (the exchange is sized by them)."""
+    e.g. a layout handle's rank_counts) -- and, given, its kept routes to
+    each destination -- into a Plan.  Reads the counts on the host once
+    (the exchange and the receiving buffers are sized by them)."""
     import torch.distributed as dist
 
-    send = rank_counts.to(torch.int64).contiguous()
+    cols = [rank_counts.to(torch.int64)] + ([routes.to(torch.int64)] if routes is not None else [])
+    send = torch.stack(cols, dim=1).contiguous()  # [R, 1 or 2]: row r goes to rank r
     recv = torch.empty_like(send)
     dist.all_to_all_single(recv, send, group=group)
-    return Plan(send_counts=[int(v) for v in send.tolist()], recv_counts=[int(v) for v in recv.tolist()])
+    s, r = send.tolist(), recv.tolist()
+    return Plan(send_counts=[int(v[0]) for v in s], recv_counts=[int(v[0]) for v in r],
+                recv_routes=[int(v[1]) for v in r] if routes is not None else None)
 
 
 def all_to_all(t: torch.Tensor, plan: Plan, group=None, back: bool = False) -> torch.Tensor:
@@ -114,9 +129,12 @@ class Recv:
     meta_gate: torch.Tensor   # [arrivals, k] the routes' gates
 
 
-def dest_receive(rows: torch.Tensor, meta_idx: torch.Tensor, meta_gate: torch.Tensor, E: int) -> Recv:
-    """Group the arrivals (from source 0, 1, ... in order) by local expert."""
-    hr = B.moe_dispatch_layout_ex(meta_idx, E, absent_routes=True)
+def dest_receive(rows: torch.Tensor, meta_idx: torch.Tensor, meta_gate: torch.Tensor, E: int,
+                 routes: int = 0) -> Recv:
+    """Group the arrivals (from source 0, 1, ... in order) by local expert;
+    routes (the plan's routes_recv) sizes the grouped buffer exactly, else it
+    is the bound arrivals * k."""
+    hr = B.moe_dispatch_layout_ex(meta_idx, E, absent_routes=True, rows_bound=routes)
     return Recv(h=hr, X=B.moe_dispatch(hr, rows), meta_gate=meta_gate)
 
 
@@ -170,14 +188,14 @@ class ExpertParallelMoE:
 
     def layout(self, idx: torch.Tensor, capacity: int = 0) -> tuple[B.Handle, Plan]:
         h = B.moe_dispatch_layout_ex(idx, self.e, capacity, self.R, send_slots=True)
-        return h, exchange_counts(h.rank_counts(), self.group)
+        return h, exchange_counts(h.rank_counts(), self.group, route_counts(h))
 
     def forward(self, h: B.Handle, plan: Plan, x: torch.Tensor, gate: torch.Tensor, expert_fwd):
         send = source_send(h, x, gate, plan)
         rows = all_to_all(send.X_send, plan, self.group)
         ids = all_to_all(send.meta_idx, plan, self.group)
         gates = all_to_all(send.meta_gate, plan, self.group)
-        recv = dest_receive(rows, ids, gates, self.E)
+        recv = dest_receive(rows, ids, gates, self.E, plan.routes_recv)
         y = expert_fwd(recv)
         P = dest_partial(recv, y)
         out = source_reduce(h, send, all_to_all(P, plan, self.group, back=True))

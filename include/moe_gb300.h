@@ -73,6 +73,7 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_F16 = 2 /* always rejected */ } mo
 #define MOE_DEV_NONFINITE 0x1
 #define MOE_DEV_BAD_ROUTE 0x2
 #define MOE_DEV_TIMEOUT 0x4
+#define MOE_DEV_ROWS_EXCEEDED 0x8 /* dropless routes past the layout's rows_bound got no row */
 
 /* Kernel ids for moe_launch_count. */
 enum {
@@ -127,6 +128,13 @@ typedef struct {
                                 (row -1, drop 1, no status bit): the layout of the
                                 arrivals on an expert-parallel rank, whose routes to
                                 other ranks are absent                             */
+  int32_t rows_bound;        /* dropless without padding: the caller's bound on the
+                                kept routes, used as the handle's rows instead of
+                                s*k (e.g. an expert-parallel rank's route count,
+                                known from the exchange of counts); 0 = s*k.  Routes
+                                past it get no row (MOE_DEV_ROWS_EXCEEDED) and the
+                                segments are cut there, so nothing reads or writes
+                                past the rows                                       */
 } moe_layout_options;
 
 /* Host view of a handle: sizes and read-only device pointers. */

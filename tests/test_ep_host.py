@@ -50,7 +50,8 @@ def _rank_main(rank, R, port, args, q):
         t = torch.from_numpy
         # source: the layout's counts sized by one all-to-all, the send map
         sp = OEP.send_plan(idx, e, R)
-        plan = EP.exchange_counts(t(sp["rank_counts"].astype(np.int32)))
+        per_dst = np.array([sum(1 for tt in range(s) for j in range(k) if idx[tt, j] // E == d) for d in range(R)])
+        plan = EP.exchange_counts(t(sp["rank_counts"].astype(np.int32)), routes=t(per_dst.astype(np.int32)))
         assert plan.rows_sent == sp["rows_sent"]
         mi, mg = OEP.send_meta(sp, idx, gate, e, R)
         rows = EP.all_to_all(t(oracle.dispatch(sp["send_row"], x, sp["rows_sent"])), plan).numpy()
@@ -59,6 +60,7 @@ def _rank_main(rank, R, port, args, q):
         assert len(rows) == plan.rows_recv
         # destination: the arrivals grouped, the expert, the weighted partials
         loc = OEP.recv_layout(ids, E)
+        assert loc["rows"] == plan.routes_recv  # the exchanged route counts size the grouped rows exactly
         X = oracle.dispatch(loc["row"], rows, loc["rows"])
         y = expert(X, loc["offsets"], loc["counts"], rank * E)
         P = oracle.combine(loc["row"], gts, y)

@@ -77,13 +77,15 @@ def run_case(R, s, m, e, k, dtype, capacity=0, seed=0, zipf=0.0, skip_rank=None)
     # ---- forward, rank by rank with the exchange between the phases
     hs = [B.moe_dispatch_layout_ex(idx[r], e, capacity, R, send_slots=True) for r in range(R)]
     counts = torch.stack([h.rank_counts() for h in hs]).cpu().numpy().astype(np.int64)  # [src, dst]
-    plans = [EP.Plan(send_counts=[int(v) for v in counts[r]], recv_counts=[int(v) for v in counts[:, r]])
-             for r in range(R)]
+    routes = torch.stack([EP.route_counts(h) for h in hs]).cpu().numpy().astype(np.int64)  # [src, dst]
+    plans = [EP.Plan(send_counts=[int(v) for v in counts[r]], recv_counts=[int(v) for v in counts[:, r]],
+                     recv_routes=[int(v) for v in routes[:, r]]) for r in range(R)]
     sends = [EP.source_send(hs[r], xs[r], gate[r], plans[r]) for r in range(R)]
     rows = emulated_all_to_all([sd.X_send for sd in sends], plans)
     ids = emulated_all_to_all([sd.meta_idx for sd in sends], plans)
     gts = emulated_all_to_all([sd.meta_gate for sd in sends], plans)
-    recvs = [EP.dest_receive(rows[d], ids[d], gts[d], E) for d in range(R)]
+    # the grouped buffers sized exactly by the exchanged route counts
+    recvs = [EP.dest_receive(rows[d], ids[d], gts[d], E, plans[d].routes_recv) for d in range(R)]
     ys = [expert_gpu(recvs[d].X, recvs[d].h, d * E) for d in range(R)]
     P = [EP.dest_partial(recvs[d], ys[d]) for d in range(R)]
     P_back = emulated_all_to_all(P, plans, back=True)
@@ -119,9 +121,8 @@ def run_case(R, s, m, e, k, dtype, capacity=0, seed=0, zipf=0.0, skip_rank=None)
         np.testing.assert_array_equal(bits(recvs[d].h.row()), lr, err_msg="arrivals' rows")
         np.testing.assert_array_equal(bits(recvs[d].h.counts()), loc["counts"], err_msg="arrivals' counts")
         np.testing.assert_array_equal(bits(recvs[d].h.offsets()), loc["offsets"], err_msg="arrivals' offsets")
-        # the grouped buffer has the host bound arrivals*k rows; rows past
-        # offsets[E] belong to no route and are not written
         lrows = loc["rows"]
+        assert recvs[d].h.rows == lrows == plans[d].routes_recv  # sized exactly from the exchanged counts
         X = bits(recvs[d].X)[:lrows]
         np.testing.assert_array_equal(X, st["X"][d], err_msg="grouped rows")
         y = bits(ys[d])[:lrows]
@@ -226,3 +227,30 @@ def test_expert_parallel_layer_on_a_one_rank_group():
         assert torch.equal(dgate.view(torch.int32), dg.view(torch.int32))
     finally:
         dist.destroy_process_group()
+
+
+def test_rows_bound_below_the_routes_cuts_and_reports():
+    """A dropless bound smaller than the routes: the routes past it get no
+    row, the segments are cut at the bound, the status says so, and the
+    dispatch writes nothing past the buffer."""
+    s, e, k = 500, 8, 2
+    idx = W.random_routes(s, e, k, device=DEV, seed=4)
+    bound = s * k - 137
+    h = B.moe_dispatch_layout_ex(idx, e, rows_bound=bound)
+    assert h.rows == bound
+    assert h.status() & B.MOE_DEV_ROWS_EXCEEDED
+    L = __import__("oracle").layout(bits(idx), e)
+    row = bits(h.row())
+    full = L["row"]
+    np.testing.assert_array_equal(row, np.where(full < bound, full, -1))
+    off = bits(h.offsets())
+    cnt = bits(h.counts())
+    assert off[-1] == bound and np.all(off[:-1] + cnt <= bound)
+    np.testing.assert_array_equal(off, np.minimum(L["offsets"], bound))
+    x = torch.randn(s, 16, device=DEV)
+    guard = torch.full((bound + 64, 16), 7.0, device=DEV)
+    B.moe_dispatch(h, x, guard[:bound])
+    torch.cuda.synchronize()
+    assert torch.all(guard[bound:] == 7.0)  # nothing past the rows
+    exact = B.moe_dispatch_layout_ex(idx, e, rows_bound=s * k)
+    assert exact.status() == 0 and exact.rows == s * k
