@@ -32,8 +32,11 @@ inserted between steps.  Further keys:
 - ``e2e``: the same metric with every step's inputs copied from pinned
   host memory and its results copied back inside the timed region;
 - ``expert_gemm``: the grouped GEMM consuming the dispatched rows, plain
-  and fused with the dispatch, in TFLOP/s against the measured bf16 peak
-  (outside ``value``);
+  and fused with the dispatch, in TFLOP/s against the longer of its FLOP and
+  weight-streaming bounds (outside ``value``);
+- ``expert_parallel`` (workloads with virtual ranks): the expert-parallel
+  layer's per-rank kernels, R ranks emulated on this GPU, per phase
+  (outside ``value``; the exchange between GPUs is not measured here);
 - ``cpu_baseline``: the oracle on the host's cores (and on one core).
 """
 from __future__ import annotations
@@ -378,6 +381,9 @@ def run_ours(args, rank: int, world: int, dist):
     # ---- the tensor-core consumer of the dispatched rows (outside value) ------
     gemm = None if args.no_gemm else run_expert_gemm(w, S, dev)
 
+    # ---- the expert-parallel layer's per-rank kernels (outside value) --------
+    epl = run_expert_parallel(w, dev) if (w.R and not args.no_ep) else None
+
     elapsed_ms, e2e["ms"], dc["ms"], rp["ms"] = max_over_ranks([elapsed_ms, e2e["ms"], dc["ms"], rp["ms"]], dist,
                                                                dev)
     if rank != 0:
@@ -458,6 +464,8 @@ def run_ours(args, rank: int, world: int, dist):
     }
     if gemm is not None:
         line["expert_gemm"] = gemm
+    if epl is not None:
+        line["expert_parallel"] = epl
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args)
     return line
@@ -649,6 +657,103 @@ def run_expert_gemm(w, S, dev, reps: int = 10):
         "note": "synthetic N(0,1)/sqrt(m) expert weights; events around single calls, median of "
                 f"{reps}; not included in value; the bound is the longer of the FLOPs at the bf16 peak and "
                 "min_bytes (rows in, each expert's weights once, outputs) at the copy bandwidth",
+    }
+
+
+def run_expert_parallel(w, dev, reps: int = 3):
+    """The expert-parallel layer's per-rank kernels (outside value): R ranks
+    of this workload (rank r's tokens from seed + r, experts [r*E, (r+1)*E)),
+    all emulated on this GPU, forward and backward with an identity expert.
+    Each phase of each rank is timed with events (median of reps); the
+    all-to-alls between the ranks are device copies here, timed apart --
+    the exchange between GPUs is not measured on one GPU."""
+    import torch
+
+    from combine_moe_topk_gb300 import binding as B
+    from combine_moe_topk_gb300 import ep as EP
+    from combine_moe_topk_gb300 import workloads as W
+
+    R, E, b = w.R, w.e // w.R, w.elem_bytes
+    srcs = []
+    for r in range(R):
+        inp = W.make_inputs(w, device=dev, seed=w.seed + r, with_grad=False)
+        idx, gate = B.moe_topk_gate(inp["logits"], w.k, w.renorm)
+        srcs.append(dict(x=inp["x"], idx=idx, gate=gate, dout=inp["x"]))  # the upstream gradient: any rows
+
+    def a2a(bufs, plans, back=False):
+        if not back:
+            pieces = [torch.split(bufs[i], plans[i].send_counts) for i in range(R)]
+            return [torch.cat([pieces[i][j] for i in range(R)]) for j in range(R)]
+        pieces = [torch.split(bufs[j], plans[j].recv_counts) for j in range(R)]
+        return [torch.cat([pieces[j][i] for j in range(R)]) for i in range(R)]
+
+    times = {}
+
+    def timed(name, fn):
+        out = None
+        ts = []
+        for _ in range(reps):
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            out = fn()
+            c.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(c))
+        times.setdefault(name, []).append(statistics.median(ts))
+        return out
+
+    hs = [timed("layout", lambda r=r: B.moe_dispatch_layout_ex(srcs[r]["idx"], w.e, w.capacity, R, send_slots=True))
+          for r in range(R)]
+    counts = torch.stack([h.rank_counts() for h in hs]).cpu().tolist()
+    routes = torch.stack([EP.route_counts(h) for h in hs]).cpu().tolist()
+    plans = [EP.Plan([int(v) for v in counts[r]], [int(counts[i][r]) for i in range(R)],
+                     [int(routes[i][r]) for i in range(R)]) for r in range(R)]
+    sends = [timed("pack+send", lambda r=r: EP.source_send(hs[r], srcs[r]["x"], srcs[r]["gate"], plans[r]))
+             for r in range(R)]
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    rows = a2a([sd.X_send for sd in sends], plans)
+    ids = a2a([sd.meta_idx for sd in sends], plans)
+    gts = a2a([sd.meta_gate for sd in sends], plans)
+    torch.cuda.synchronize()
+    ex_fwd = time.perf_counter() - t0
+    recvs = [timed("receive", lambda d=d: EP.dest_receive(rows[d], ids[d], gts[d], E, plans[d].routes_recv))
+             for d in range(R)]
+    P = [timed("partial", lambda d=d: EP.dest_partial(recvs[d], recvs[d].X)) for d in range(R)]
+    Pb = a2a(P, plans, back=True)
+    outs = [timed("reduce", lambda r=r: EP.source_reduce(hs[r], sends[r], Pb[r])) for r in range(R)]
+    dPs = [timed("send_grad", lambda r=r: EP.source_send_grad(hs[r], sends[r], srcs[r]["dout"])) for r in range(R)]
+    dP = a2a(dPs, plans)
+    cb = [timed("combine_bwd", lambda d=d: EP.dest_combine_bwd(recvs[d], dP[d], recvs[d].X)) for d in range(R)]
+    dgb = a2a([c[1] for c in cb], plans, back=True)
+    timed_dg = [timed("dgate", lambda r=r: EP.source_dgate(hs[r], sends[r], dgb[r])) for r in range(R)]
+    dxp = [timed("dispatch_bwd", lambda d=d: EP.dest_dispatch_bwd(recvs[d], cb[d][0])) for d in range(R)]
+    dxb = a2a(dxp, plans, back=True)
+    [timed("reduce_grad", lambda r=r: EP.source_reduce(hs[r], sends[r], dxb[r])) for r in range(R)]
+    torch.cuda.synchronize()
+    for h in hs + [rc.h for rc in recvs]:
+        assert h.status() == 0
+    sent = sum(sum(p.send_counts) for p in plans)
+    nroutes = sum(p.routes_recv for p in plans)
+    row = w.m * b
+    # bytes per phase over all ranks: payload rows only (metadata is < 1 %)
+    pb = {"pack+send": sum(w.s for _ in range(R)) * row + sent * row,
+          "receive": sent * row + nroutes * row, "partial": nroutes * row + sent * row,
+          "reduce": sent * row + R * w.s * row, "send_grad": R * w.s * row + sent * row,
+          "combine_bwd": sent * row + 2 * nroutes * row, "dispatch_bwd": nroutes * row + sent * row,
+          "reduce_grad": sent * row + R * w.s * row}
+    per = {k: round(sum(v) * 1e3, 1) for k, v in times.items()}
+    hbm, _ = peaks()
+    return {
+        "ranks": R, "experts_per_rank": E, "tokens_per_rank": w.s,
+        "rows_sent": sent, "routes": nroutes, "routes_per_sent_row": round(nroutes / max(1, sent), 3),
+        "us_per_phase_all_ranks": per,
+        "gbs_per_phase": {k: round(pb[k] / (per[k] * 1e-6) / 1e9, 1) for k in pb if per.get(k)},
+        "busiest_rank_routes": max(p.routes_recv for p in plans),
+        "emulated_exchange_ms": round(ex_fwd * 1e3, 2),
+        "how": f"{R} ranks emulated on one GPU, each phase of each rank timed alone (median of {reps}), summed over "
+               "ranks; identity expert; the all-to-all is a device copy here and the exchange between GPUs is "
+               f"unmeasured; copy peak {hbm} GB/s",
     }
 
 
@@ -851,6 +956,7 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=120.0, help="total oracle work of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-gemm", action="store_true", help="skip the expert_gemm figures")
+    ap.add_argument("--no-ep", action="store_true", help="skip the expert_parallel figures")
     ap.add_argument("--eager", action="store_true", help="time eager calls instead of a CUDA graph of the step")
     ap.add_argument("--only-step", action="store_true",
                     help="time the step alone: no per-op, pair, replay, end-to-end, GEMM or CPU legs (profiling runs)")
