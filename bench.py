@@ -688,12 +688,15 @@ def run_expert_parallel(w, dev, reps: int = 3):
         return [torch.cat([pieces[j][i] for j in range(R)]) for i in range(R)]
 
     times = {}
+    pad = getattr(torch.cuda, "_sleep", None)
 
     def timed(name, fn):
         out = None
         ts = []
         for _ in range(reps):
             a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if pad is not None:
+                pad(SLEEP_CYCLES)  # the host enqueues the phase while the GPU sleeps
             a.record()
             out = fn()
             c.record()
@@ -751,7 +754,8 @@ def run_expert_parallel(w, dev, reps: int = 3):
         "gbs_per_phase": {k: round(pb[k] / (per[k] * 1e-6) / 1e9, 1) for k in pb if per.get(k)},
         "busiest_rank_routes": max(p.routes_recv for p in plans),
         "emulated_exchange_ms": round(ex_fwd * 1e3, 2),
-        "how": f"{R} ranks emulated on one GPU, each phase of each rank timed alone (median of {reps}), summed over "
+        "how": f"{R} ranks emulated on one GPU, each phase of each rank timed alone after a GPU sleep (median of "
+               f"{reps}), summed over "
                "ranks; identity expert; the all-to-all is a device copy here and the exchange between GPUs is "
                f"unmeasured; copy peak {hbm} GB/s",
     }

@@ -68,12 +68,6 @@ __device__ __noinline__ void router_grad_call(int t, int lane, int k, int e, con
   router_grad_token<kRgEpl>(t, lane, k, e, rg.renorm, ij, gj, dgj, rg.logits, rg.dlogits);
 }
 
-// Barrier of the `threads` threads (whole warps) of warp group gi: hardware
-// barrier 1 + gi (0 is the block's own), shared-memory ordering among them.
-__device__ __forceinline__ void group_sync(int gi, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(1 + gi), "r"(threads) : "memory");
-}
-
 // Route rows and gates of token t, broadcast from lanes 0..k-1.
 // A row index outside [0, rows) counts as a dropped route: nothing past the
 // buffer is read.
@@ -246,9 +240,10 @@ __global__ void __launch_bounds__(kThreads) combine_compact_kernel(const int32_t
 // G warps per token (G = 1, 2, 4 or 8): warp w of a token's group takes the
 // row's vectors [w*chunk, (w+1)*chunk); the per-route dots are reduced across
 // the warp's lanes (butterfly), then across the group's warps in warp order
-// through shared memory, the group alone meeting at a named barrier (a
-// block-wide one cost 2.4 of 13.6 stall cycles per instruction on the
-// Mixtral-like shape).  G > 1 gives short batches more warps in flight.
+// through shared memory (a block-wide barrier: per-group named barriers,
+// tried because the block barrier is 2.4 of 13.6 stall cycles per
+// instruction on the Mixtral-like shape, made that kernel 3 % slower).
+// G > 1 gives short batches more warps in flight.
 template <typename T, int KMAX, int UNR, int G, bool RG>
 __device__ __forceinline__ void combine_bwd_body(
     const int32_t* __restrict__ row, const int32_t* __restrict__ counts,
@@ -338,7 +333,7 @@ __device__ __forceinline__ void combine_bwd_body(
       if (RG && live) router_grad_call(t, lane, k, e, rg, rg_id, rg_g, lane < k ? mine : 0.f);
     } else {
       if (lane < KMAX) s_dot[warp][lane] = mine;
-      group_sync(gi, 32 * G);  // only the token's G warps share s_dot
+      __syncthreads();
       float sum = 0.0f;
       if (live && w == 0 && lane < k) {
 #pragma unroll
@@ -346,7 +341,7 @@ __device__ __forceinline__ void combine_bwd_body(
         dgate[(size_t)t * k + lane] = sum;
       }
       if (RG && live && w == 0) router_grad_call(t, lane, k, e, rg, rg_id, rg_g, sum);
-      group_sync(gi, 32 * G);  // s_dot is rewritten next round
+      __syncthreads();  // s_dot is rewritten next round
     }
   }
   pdl_trigger_late();

@@ -26,6 +26,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxR = 64;
 
+// One thread per (token, destination rank): send_row[t, r] (coalesced), and
+// for a sent pair its metadata row.  The token's k routes are read once per
+// thread (the R threads of a token hit the same lines).
 __global__ void __launch_bounds__(kThreads) ep_pack_kernel(
     const int32_t* __restrict__ idx, const int32_t* __restrict__ row, const float* __restrict__ gate,
     const int32_t* __restrict__ rank_slot, const int32_t* __restrict__ rank_counts, int s, int k, int e,
@@ -44,22 +47,23 @@ __global__ void __launch_bounds__(kThreads) ep_pack_kernel(
   pdl_trigger_late();
   const int E = e / R;
   bool bad = false;
-  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < s; t += (long long)gridDim.x * blockDim.x) {
-    for (int r = 0; r < R; ++r) {
-      const int slot = __ldg(rank_slot + t * R + r);
-      long long q = slot >= 0 ? s_off[r] + slot : -1;
-      if (q >= rows_sent) {  // send slots that disagree with the row count given: send nothing
-        bad = true;
-        q = -1;
-      }
-      send_row[t * R + r] = (int32_t)q;
-      if (q < 0) continue;
-      for (int j = 0; j < k; ++j) {
-        const int x = __ldg(idx + t * k + j);
-        const bool on = __ldg(row + t * k + j) >= 0 && x / E == r;
-        meta_idx[q * k + j] = on ? x - r * E : -1;
-        meta_gate[q * k + j] = on ? __ldg(gate + t * k + j) : 0.f;
-      }
+  const long long n = (long long)s * R;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long t = i / R;
+    const int r = (int)(i - t * R);
+    const int slot = __ldg(rank_slot + i);
+    long long q = slot >= 0 ? s_off[r] + slot : -1;
+    if (q >= rows_sent) {  // send slots that disagree with the row count given: send nothing
+      bad = true;
+      q = -1;
+    }
+    send_row[i] = (int32_t)q;
+    if (q < 0) continue;
+    for (int j = 0; j < k; ++j) {
+      const int x = __ldg(idx + t * k + j);
+      const bool on = __ldg(row + t * k + j) >= 0 && x / E == r;
+      meta_idx[q * k + j] = on ? x - r * E : -1;
+      meta_gate[q * k + j] = on ? __ldg(gate + t * k + j) : 0.f;
     }
   }
   if (bad) raise_status(status, MOE_DEV_BAD_ROUTE);
@@ -99,7 +103,8 @@ cudaError_t launch_ep_pack(const int32_t* idx, const int32_t* row, const float* 
                            const int32_t* rank_counts, int s, int k, int e, int R, long long rows_sent,
                            int32_t* send_row, int32_t* meta_idx, float* meta_gate, int32_t* status,
                            const DeviceInfo& di, cudaStream_t st) {
-  return launch_pdl(MOE_KERNEL_EP_PACK, ep_pack_kernel, dim3(grid_of(s, di)), dim3(kThreads), 0, st, idx, row, gate,
+  return launch_pdl(MOE_KERNEL_EP_PACK, ep_pack_kernel, dim3(grid_of((long long)s * R, di)), dim3(kThreads), 0, st,
+                    idx, row, gate,
                     rank_slot, rank_counts, s, k, e, R, rows_sent, send_row, meta_idx, meta_gate, status);
 }
 
