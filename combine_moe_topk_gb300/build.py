@@ -50,7 +50,9 @@ def stale() -> bool:
 
 def _compile(src: str, ptxas_verbose: bool) -> tuple[str, str]:
     obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+    # MOE_NVCC_FLAGS: extra nvcc flags (e.g. -DMOE_DSP_STAGES=3 for a tuning
+    # sweep); rebuild with build(force=True) when they change
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *os.environ.get("MOE_NVCC_FLAGS", "").split(), "-c", src, "-o", obj]
     if ptxas_verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)

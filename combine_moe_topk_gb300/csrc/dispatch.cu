@@ -39,10 +39,14 @@ namespace {
 #define MOE_DSP_MAX_CTAS 16
 #endif
 
-constexpr int kMaxStages = 8;
-constexpr int kBatch = 32;   // tokens of routing metadata staged at a time
-constexpr int kMaxK = 32;   // routes per token: k, or the ranks of an expert-parallel send
+constexpr int kMaxStages = MOE_DSP_STAGES;
+constexpr int kBatch = 32;       // tokens of routing metadata staged at a time (at most)
+constexpr int kMaxK = 32;        // routes per token: k, or the ranks of an expert-parallel send
+constexpr int kRowBudget = 512;  // staged route rows: a batch holds min(32, 512 / k) tokens
 constexpr int kMaxE = 256;
+// The static shared memory stays under 5 KB so that six CTAs with a 4-stage
+// ring of 8 KB rows fit on an SM (at 7.4 KB, with 32 x 32 staged routes, only
+// five did: 2 % of the dispatch's time on the fine-grained workload).
 
 struct Params {
   const char* x;
@@ -68,7 +72,7 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const Params p) {
   __shared__ int desc_rows[kMaxStages][kMaxK];
   __shared__ int desc_t[kMaxStages];
   __shared__ int desc_p[kMaxStages];
-  __shared__ int b_rows[kBatch * kMaxK];
+  __shared__ int b_rows[kRowBudget];
   __shared__ unsigned b_mask[kBatch];
   __shared__ int s_counts[kMaxE];
   __shared__ int s_offsets[kMaxE + 1];
@@ -98,7 +102,7 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const Params p) {
       if (ti == blen) {
         tb += blen;
         if (tb >= t1) return false;
-        blen = min(kBatch, t1 - tb);
+        blen = min(min(kBatch, kRowBudget / p.k), t1 - tb);
         ti = 0;
         pi = 0;
         __syncwarp();
