@@ -50,7 +50,7 @@ def stale() -> bool:
 
 def _compile(src: str, ptxas_verbose: bool) -> tuple[str, str]:
     obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    # MOE_NVCC_FLAGS: extra nvcc flags (e.g. -DMOE_DSP_STAGES=3 for a tuning
+    # MOE_NVCC_FLAGS: extra nvcc flags (e.g. -DMOE_DSP_UNR=4 for a tuning
     # sweep); rebuild with build(force=True) when they change
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *os.environ.get("MOE_NVCC_FLAGS", "").split(), "-c", src, "-o", obj]
     if ptxas_verbose:

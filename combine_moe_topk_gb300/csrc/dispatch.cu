@@ -1,5 +1,4 @@
-// dispatch.cu -- gather token rows into the expert-grouped buffer with 1-D
-// bulk (TMA) copies staged through shared memory.
+// dispatch.cu -- gather token rows into the expert-grouped buffer.
 //
 // DeepSpeed #8195 "MoE dispatch: fix silent Tutel + TP corruption, speed up
 // native and Tutel paths", change 3: route each token through its slot
@@ -11,16 +10,20 @@
 // expansion and replicates them itself -- here each token row is read from
 // HBM once and written to each of its kept routes.
 //
-// One warp per CTA, several CTAs per SM, each CTA owning a contiguous token
-// range.  A ring of `stages` shared-memory buffers: lane 0 loads a token row
-// (or a piece of it) with cp.async.bulk global->shared, completion counted
-// on the stage's mbarrier; once it lands, lane j issues the bulk
-// shared->global store for route j, and every lane commits one bulk group
-// per unit, so `wait_group.read 1` tells when the previous unit's buffer may
-// be refilled.  In capacity mode the CTA then writes the zero tail of its
-// share of the [e, c] slots from a zeroed buffer.  All mbarrier waits are
-// bounded; on time-out the kernel records MOE_DEV_TIMEOUT, waits (bounded)
-// for its loads in flight and for its stores, and returns.
+// A warp per token, or per piece of a token row when the batch is short of
+// 8x the resident warps.  Each lane loads UNR 16-byte vectors of the piece
+// (all loads in flight before the first store), then stores them to every
+// kept route's row: each store instruction writes 512 contiguous bytes.
+// The routes are read by lanes 0..k-1 and broadcast by shuffle; a token
+// with no kept route reads nothing.  Rows no route owns (capacity slots
+// past the counts, per-expert padding) are zeroed afterwards, a warp per
+// row.  Nothing waits on anything but the previous kernel (the programmatic
+// launch dependency), so the kernel has no time-out path.
+//
+// An earlier form moved the rows with 1-D bulk (TMA) copies through a
+// shared-memory ring, one warp per CTA; at the same bytes it was 9 % slower
+// on the GShard capacity workload and 25 % slower on the 256-token one,
+// and no faster elsewhere.
 #include "common.cuh"
 #include "internal.h"
 
@@ -28,219 +31,111 @@ namespace moe {
 
 namespace {
 
-// Tuning: ring depth, largest bulk piece in bytes, cap on CTAs per SM.
-#ifndef MOE_DSP_STAGES
-#define MOE_DSP_STAGES 4
+// Tuning: 16-byte vectors in flight per lane, cap on CTAs (of 256 threads)
+// per SM below what the registers allow.
+#ifndef MOE_DSP_UNR
+#define MOE_DSP_UNR 8
 #endif
-#ifndef MOE_DSP_PIECE
-#define MOE_DSP_PIECE 16384
-#endif
-#ifndef MOE_DSP_MAX_CTAS
-#define MOE_DSP_MAX_CTAS 16
+#ifndef MOE_DSP_BPS
+#define MOE_DSP_BPS 8
 #endif
 
-constexpr int kMaxStages = MOE_DSP_STAGES;
-constexpr int kBatch = 32;       // tokens of routing metadata staged at a time (at most)
-constexpr int kMaxK = 32;        // routes per token: k, or the ranks of an expert-parallel send
-constexpr int kRowBudget = 512;  // staged route rows: a batch holds min(32, 512 / k) tokens
-constexpr int kMaxE = 256;
-// The static shared memory stays under 5 KB so that six CTAs with a 4-stage
-// ring of 8 KB rows fit on an SM (at 7.4 KB, with 32 x 32 staged routes, only
-// five did: 2 % of the dispatch's time on the fine-grained workload).
-
-struct Params {
-  const char* x;
-  char* X;
-  const int32_t* row;
-  const int32_t* counts;
-  const int32_t* offsets;
-  int s, k, e, capacity;
-  long long rows;   // rows of X
-  int zero_fill;    // X has rows no route owns (capacity slots, padding): zero them
-  long long row_bytes;
-  int piece;       // bytes per unit (multiple of 16)
-  int npieces;     // units per token row
-  int stages;
-  int stage_stride;
-  int32_t* status;
-  long long timeout_ns;
-};
-
-__global__ void __launch_bounds__(32) dispatch_kernel(const Params p) {
-  extern __shared__ __align__(128) unsigned char buf[];
-  __shared__ __align__(8) uint64_t bar[kMaxStages];
-  __shared__ int desc_rows[kMaxStages][kMaxK];
-  __shared__ int desc_t[kMaxStages];
-  __shared__ int desc_p[kMaxStages];
-  __shared__ int b_rows[kRowBudget];
-  __shared__ unsigned b_mask[kBatch];
-  __shared__ int s_counts[kMaxE];
-  __shared__ int s_offsets[kMaxE + 1];
-
-  const int lane = threadIdx.x;
-  const long long G = gridDim.x, b = blockIdx.x;
-  const int t0 = (int)((long long)p.s * b / G);
-  const int t1 = (int)((long long)p.s * (b + 1) / G);
-  const uint64_t deadline = globaltimer_ns() + (uint64_t)p.timeout_ns;
-
-  if (lane == 0) {
-    for (int st = 0; st < p.stages; ++st) mbar_init(&bar[st], 1);
-    fence_barrier_init();
-  }
+// KMAX: routes per token rounded up to a power of two (k, or the ranks of an
+// expert-parallel send, at most 32).  A unit is (token, piece); a piece is
+// `chunk` vectors of the row, a multiple of 32.
+template <int KMAX, int UNR>
+__global__ void __launch_bounds__(256) dispatch_kernel(
+    const int32_t* __restrict__ row, const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+    int s, int k, int e, long long rows, int zero_fill, int nvec, int chunk, int nchunks,
+    const uint4* __restrict__ x, uint4* __restrict__ X, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long units = (long long)s * nchunks;
   grid_dependency_wait();
   pdl_trigger_early();
-  if (p.zero_fill) {
-    for (int x = lane; x < p.e; x += 32) s_counts[x] = __ldg(p.counts + x);
-    for (int x = lane; x <= p.e; x += 32) s_offsets[x] = __ldg(p.offsets + x);
-  }
-  __syncwarp();
-
-  // ---- unit iterator (uniform across the warp) ----------------------------
-  int tb = t0, blen = 0, ti = 0, pi = 0;
-  auto next_unit = [&](int st) -> bool {
-    for (;;) {
-      if (ti == blen) {
-        tb += blen;
-        if (tb >= t1) return false;
-        blen = min(min(kBatch, kRowBudget / p.k), t1 - tb);
-        ti = 0;
-        pi = 0;
-        __syncwarp();
-        for (int i = lane; i < blen * p.k; i += 32) b_rows[i] = __ldg(p.row + (size_t)tb * p.k + i);
-        __syncwarp();
-        if (lane < blen) {
-          unsigned mk = 0;
-          for (int j = 0; j < p.k; ++j) {
-            const int r = b_rows[lane * p.k + j];
-            if (r >= 0 && r < p.rows) {
-              mk |= 1u << j;
-            } else if (r >= 0) {  // a row past the buffer: written nowhere, reported
-              b_rows[lane * p.k + j] = -1;
-              raise_status(p.status, MOE_DEV_BAD_ROUTE);
-            }
+  bool bad = false;
+  for (long long u = gw; u < units; u += warps) {
+    const int t = (int)(u / nchunks);
+    const int c0 = (int)(u - (long long)t * nchunks) * chunk;
+    const int c1 = min(nvec, c0 + chunk);
+    int rl = lane < k ? __ldg(row + (size_t)t * k + lane) : -1;
+    if (rl >= rows) {  // a row past the buffer: written nowhere, reported
+      bad = true;
+      rl = -1;
+    }
+    if (!__any_sync(0xffffffffu, rl >= 0)) continue;  // every route dropped: nothing to read
+    int r[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) r[j] = __shfl_sync(0xffffffffu, rl, j);
+    const uint4* src = x + (size_t)t * nvec;
+    for (int v0 = c0 + lane; v0 < c1; v0 += 32 * UNR) {
+      uint4 val[UNR];
+#pragma unroll
+      for (int q = 0; q < UNR; ++q) {
+        const int v = v0 + 32 * q;
+        if (v < c1) val[q] = ld_stream(src + v);
+      }
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k && r[j] >= 0) {
+          uint4* dst = X + (size_t)r[j] * nvec;
+#pragma unroll
+          for (int q = 0; q < UNR; ++q) {
+            const int v = v0 + 32 * q;
+            if (v < c1) st_stream(dst + v, val[q]);
           }
-          b_mask[lane] = mk;
         }
-        __syncwarp();
       }
-      if (b_mask[ti] == 0) {  // every route of this token was dropped
-        ++ti;
-        continue;
-      }
-      break;
     }
-    const int t = tb + ti;
-    const int pc = pi;
-    if (lane < p.k) desc_rows[st][lane] = b_rows[ti * p.k + lane];
-    if (lane == 0) {
-      desc_t[st] = t;
-      desc_p[st] = pc;
-    }
-    __syncwarp();
-    if (lane == 0) {
-      const long long off = (long long)pc * p.piece;
-      const uint32_t bytes = (uint32_t)min((long long)p.piece, p.row_bytes - off);
-      mbar_arrive_expect_tx(&bar[st], bytes);
-      bulk_g2s(buf + (size_t)st * p.stage_stride, p.x + (size_t)t * p.row_bytes + off, bytes,
-               &bar[st]);
-    }
-    if (++pi == p.npieces) {
-      pi = 0;
-      ++ti;
-    }
-    return true;
-  };
-
-  // ---- pipeline -------------------------------------------------------------
-  long long issued = 0, done = 0;
-  for (int st = 0; st < p.stages; ++st) {
-    if (!next_unit(st)) break;
-    ++issued;
   }
-  uint32_t parity = 0;
-  bool ok = true;
-  while (done < issued) {
-    const int st = (int)(done % p.stages);
-    if (!mbar_wait_bounded(&bar[st], (parity >> st) & 1u, deadline)) {
-      ok = false;
-      break;
-    }
-    parity ^= 1u << st;
-    const int t = desc_t[st];
-    const long long off = (long long)desc_p[st] * p.piece;
-    const uint32_t bytes = (uint32_t)min((long long)p.piece, p.row_bytes - off);
-    (void)t;
-    if (lane < p.k) {
-      const int r = desc_rows[st][lane];
-      if (r >= 0) bulk_s2g(p.X + (size_t)r * p.row_bytes + off, buf + (size_t)st * p.stage_stride, bytes);
-    }
-    bulk_commit();
-    if (done >= 1) {
-      // the unit before this one has finished reading its buffer: refill it
-      bulk_wait_read<1>();
-      __syncwarp();
-      const int prev = (int)((done - 1) % p.stages);
-      if (next_unit(prev)) ++issued;
-    }
-    ++done;
-  }
-
-  if (!ok) {
-    pdl_trigger_late();
-    if (lane == 0) raise_status(p.status, MOE_DEV_TIMEOUT);
-    // let the loads still in flight land before the CTA's shared memory goes
-    const uint64_t drain = globaltimer_ns() + (uint64_t)p.timeout_ns;
-    for (long long u = done; u < issued; ++u) {
-      const int st = (int)(u % p.stages);
-      if (!mbar_wait_bounded(&bar[st], (parity >> st) & 1u, drain)) break;
-      parity ^= 1u << st;
-    }
-    bulk_wait_all();
-    return;
-  }
-
   pdl_trigger_late();
-  // ---- rows no route owns: capacity slots past counts, padding ------------
-  if (p.zero_fill) {
-    bulk_wait_all();
-    __syncwarp();
-    uint4* z = reinterpret_cast<uint4*>(buf);
-    for (int i = lane; i < p.stage_stride / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
-    __syncwarp();
-    const long long r0 = p.rows * b / G, r1 = p.rows * (b + 1) / G;
-    for (long long r = r0 + lane; r < r1; r += 32) {
-      if (row_is_owned(r, s_offsets, s_counts, p.e)) continue;
-      for (int pc = 0; pc < p.npieces; ++pc) {
-        const long long off = (long long)pc * p.piece;
-        const uint32_t bytes = (uint32_t)min((long long)p.piece, p.row_bytes - off);
-        bulk_s2g(p.X + (size_t)r * p.row_bytes + off, buf, bytes);
-      }
+  if (bad) raise_status(status, MOE_DEV_BAD_ROUTE);
+  if (zero_fill) {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (long long rr = gw; rr < rows; rr += warps) {
+      if (row_is_owned(rr, offsets, counts, e)) continue;
+      uint4* dst = X + (size_t)rr * nvec;
+      for (int v = lane; v < nvec; v += 32) st_stream(dst + v, z);
     }
-    bulk_commit();
   }
-  bulk_wait_all();
 }
 
-
-struct Config {
-  int piece, npieces, stages, stride, smem, ctas_per_sm;
-};
-
-Config choose(long long row_bytes) {
-  Config c;
-  const long long kPieceMax = MOE_DSP_PIECE;
-  c.npieces = (int)((row_bytes + kPieceMax - 1) / kPieceMax);
-  long long piece = (row_bytes + c.npieces - 1) / c.npieces;
-  piece = (piece + 15) / 16 * 16;
-  c.piece = (int)piece;
-  c.stride = (int)((piece + 127) / 128 * 128);
-  c.stages = MOE_DSP_STAGES;
-  c.smem = c.stages * c.stride;
-  int n = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dispatch_kernel, 32, c.smem);
-  c.ctas_per_sm = n < 1 ? 1 : (n > MOE_DSP_MAX_CTAS ? MOE_DSP_MAX_CTAS : n);
-  return c;
+template <int KMAX>
+cudaError_t launch(const int32_t* row, const int32_t* counts, const int32_t* offsets, int s, int k, int e,
+                   long long rows, int zero_fill, const void* x, void* X, long long row_bytes, int32_t* status,
+                   const DeviceInfo& di, cudaStream_t st) {
+  auto kern = dispatch_kernel<KMAX, MOE_DSP_UNR>;
+  static OncePerDevice occ_once;
+  static int bps[kOnceDevices];
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = occ_once.run([&] {
+    int n = 0;
+    cudaError_t e2 = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 256, 0);
+    if (n > MOE_DSP_BPS) n = MOE_DSP_BPS;
+    if (e2 == cudaSuccess) bps[dev] = n < 1 ? 1 : n;
+    return e2;
+  });
+  if (err != cudaSuccess) return err;
+  const int nvec = (int)(row_bytes / 16);
+  // pieces of a row (a power of two, each at least 32 vectors) while the
+  // units number fewer than 8x the resident warps
+  const long long resident = (long long)di.sms * bps[dev] * 8;
+  int pieces = 1;
+  while (pieces < 8 && (long long)s * pieces < 8 * resident && nvec / (2 * pieces) >= 32) pieces *= 2;
+  const int chunk = pieces > 1 ? ((nvec + pieces - 1) / pieces + 31) / 32 * 32 : nvec;
+  const int nchunks = (nvec + chunk - 1) / chunk;
+  long long warps = (long long)s * nchunks;
+  if (zero_fill && rows > warps) warps = rows;
+  long long blocks = (warps * 32 + 255) / 256;
+  const long long cap = (long long)di.sms * bps[dev];
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(MOE_KERNEL_DISPATCH, kern, dim3((unsigned)blocks), dim3(256), 0, st, row, counts, offsets, s, k,
+                    e, rows, zero_fill, nvec, chunk, nchunks, static_cast<const uint4*>(x), static_cast<uint4*>(X),
+                    status);
 }
 
 }  // namespace
@@ -249,48 +144,12 @@ cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, const int
                             int k, int e, int capacity, long long rows, int zero_fill, const void* x,
                             void* X, long long row_bytes, int32_t* status, const DeviceInfo& di,
                             cudaStream_t st) {
-  // allow the kernel the device's whole opt-in shared memory (less its static
-  // part) once per device; occupancy still follows the dynamic size launched
-  static OncePerDevice opt_in;
-  cudaError_t err = opt_in.run([&] {
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, dispatch_kernel);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               di.max_smem_optin - (int)fa.sharedSizeBytes);
-    return e;
-  });
-  if (err != cudaSuccess) return err;
-  Config c = choose(row_bytes);
-  Params p;
-  p.x = static_cast<const char*>(x);
-  p.X = static_cast<char*>(X);
-  p.row = row;
-  p.counts = counts;
-  p.offsets = offsets;
-  p.rows = rows;
-  p.zero_fill = zero_fill;
-  p.s = s;
-  p.k = k;
-  p.e = e;
-  p.capacity = capacity;
-  p.row_bytes = row_bytes;
-  p.piece = c.piece;
-  p.npieces = c.npieces;
-  p.stages = c.stages;
-  p.stage_stride = c.stride;
-  p.status = status;
-  p.timeout_ns = 2000000000LL;
-
-  long long work = s;
-  if (zero_fill) {
-    const long long zero_groups = (rows + 31) / 32;
-    if (zero_groups > work) work = zero_groups;
-  }
-  long long grid = (long long)di.sms * c.ctas_per_sm;
-  if (grid > work) grid = work;
-  if (grid < 1) grid = 1;
-  return launch_pdl(MOE_KERNEL_DISPATCH, dispatch_kernel, dim3((unsigned)grid), dim3(32), (size_t)c.smem, st, p);
+  (void)capacity;
+  if (k <= 2) return launch<2>(row, counts, offsets, s, k, e, rows, zero_fill, x, X, row_bytes, status, di, st);
+  if (k <= 4) return launch<4>(row, counts, offsets, s, k, e, rows, zero_fill, x, X, row_bytes, status, di, st);
+  if (k <= 8) return launch<8>(row, counts, offsets, s, k, e, rows, zero_fill, x, X, row_bytes, status, di, st);
+  if (k <= 16) return launch<16>(row, counts, offsets, s, k, e, rows, zero_fill, x, X, row_bytes, status, di, st);
+  return launch<32>(row, counts, offsets, s, k, e, rows, zero_fill, x, X, row_bytes, status, di, st);
 }
 
 }  // namespace moe

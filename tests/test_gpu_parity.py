@@ -119,7 +119,7 @@ def test_tiny_capacity_full_softmax_gates():
     dict(s=1, m=8, e=1, k=1, dtype="bf16", capacity=0, R=0),
     dict(s=1, m=4, e=4, k=4, dtype="f32", capacity=1, R=2),
     dict(s=37, m=8, e=256, k=16, dtype="bf16", capacity=0, R=64),
-    dict(s=300, m=12288, e=16, k=3, dtype="bf16", capacity=0, R=4),   # rows split into 2 bulk pieces
+    dict(s=300, m=12288, e=16, k=3, dtype="bf16", capacity=0, R=4),   # a short batch: rows split into 8 pieces
     dict(s=513, m=36, e=5, k=2, dtype="f32", capacity=7, R=5),        # heavy drops, odd widths
     dict(s=2049, m=64, e=64, k=6, dtype="bf16", capacity=200, R=8),
 ])
