@@ -136,15 +136,18 @@ __device__ __forceinline__ float butterfly_tree32(const float (&v)[32]) {
 // token: the same k ids in the same order (largest key first, the lower id
 // on equal keys) and the same gate bits (the same expf terms, summed in the
 // warp's butterfly order).  row = the token's e logits (16-byte aligned when
-// e is a multiple of 4); KM >= k bounds the rounds, so the code a thread runs
-// through once stays short.  Returns whether a logit is NaN or infinite.
-template <int KM>
+// e is a multiple of 4); KM >= k bounds the rounds and EM >= e (8 or 32) the
+// experts, so the code a thread runs through once stays short (the terms
+// past EM are zeros in the same tree).  Returns whether a logit is NaN or
+// infinite.
+template <int KM, int EM = 32>
 __device__ __forceinline__ bool topk_token_thread(const float* __restrict__ row, int e, int k, int renorm,
                                                   int* ids, float* gates) {
+  static_assert(EM == 8 || EM == 16 || EM == 32, "EM: 8, 16 or 32 experts");
   float v[32];
   if ((e & 3) == 0) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
+    for (int q = 0; q < EM / 4; ++q)
       if (4 * q < e) {
         const float4 f = __ldg(reinterpret_cast<const float4*>(row) + q);
         v[4 * q] = f.x;
@@ -154,13 +157,13 @@ __device__ __forceinline__ bool topk_token_thread(const float* __restrict__ row,
       }
   } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
+    for (int j = 0; j < EM; ++j)
       if (j < e) v[j] = __ldg(row + j);
   }
   bool bad = false;
   uint32_t key[32];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
+  for (int j = 0; j < EM; ++j) {
     if (j < e && !isfinite(v[j])) bad = true;
     key[j] = j < e ? order_key(v[j]) : 0u;
   }
@@ -174,7 +177,7 @@ __device__ __forceinline__ bool topk_token_thread(const float* __restrict__ row,
       uint32_t best = 0;
       int bj = -1;
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
+      for (int j = 0; j < EM; ++j)
         if (j < e && !((taken >> j) & 1u) && (bj < 0 || key[j] > best)) {  // equal keys keep the lower id
           best = key[j];
           bj = j;
@@ -194,7 +197,7 @@ __device__ __forceinline__ bool topk_token_thread(const float* __restrict__ row,
       if (r < k) z[r] = expf(key_value(sel_key[r]) - top);
   } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
+    for (int j = 0; j < EM; ++j)
       if (j < e) z[j] = expf(key_value(key[j]) - top);
   }
   const float den = butterfly_tree32(z);

@@ -47,7 +47,10 @@
 // Fused gate (e <= 32).  With router logits instead of expert ids, phase A
 // first selects each token's experts in the token's own thread (all the
 // tile's logits loaded at once; topk_token_thread gives the gate kernel's
-// ids and gate bits) and writes the ids and gates out.  For more experts a
+// ids and gate bits) and writes the ids and gates out.  It is instantiated
+// for e <= 8 and e <= 32, so a small router's thread runs through 8-wide
+// loops (the fused kernel took 9.6 us alone on 256 tokens over 8 experts
+// with 32-wide ones, 8.0 us with 8-wide).  For more experts a
 // thread per token holds too many logits, and a warp per token inside a
 // tile selects its 32 tokens one after another: measured slower than the
 // gate kernel followed by the layout kernel, which is what runs there.
@@ -205,9 +208,10 @@ __device__ void lookback(const Params& p, int tile, int nread, const int* s_agg,
   const int tid = threadIdx.x, lane = tid & 31;
   const int e4 = padded_e(p.e);
   unsigned* rows = reinterpret_cast<unsigned*>(p.out.lookback);
-  // release: this tile's earlier writes (tile 0's cleared status word and
-  // rank counts) before its published row
-  __threadfence();
+  // release: tile 0's cleared status word and rank counts before its
+  // published row (no other tile publishes anything another tile reads, and
+  // a lone tile's clears and atomics are the same thread's, same address)
+  if (tile == 0 && p.clear_status && p.tiles > 1) __threadfence();
   if (tile != p.hold_tile)
     for (int x = tid; x < e4; x += kThreads)
       st_relaxed_u32(rows + (size_t)tile * e4 + x, pub | (unsigned)(x < p.e ? s_agg[x] : 0));
@@ -246,12 +250,13 @@ __device__ void lookback(const Params& p, int tile, int nread, const int* s_agg,
       }
     }
   }
-  // acquire: the rows read (tile 0's above all) before this tile's atomics
-  __threadfence();
-  // a held tile (test hook) publishes only after its own deadline, so that
-  // every build still rewrites every row
+  // a held tile (test hook) publishes one more time-out after its own
+  // deadline -- well after every waiting tile has given up, whatever the
+  // skew of the tiles' start times -- so that every build still rewrites
+  // every row
   if (tile == p.hold_tile) {
-    while (globaltimer_ns() <= deadline) __nanosleep(1000);
+    const uint64_t release_at = deadline + (uint64_t)p.timeout_ns;
+    while (globaltimer_ns() <= release_at) __nanosleep(1000);
     for (int x = tid; x < e4; x += kThreads)
       st_relaxed_u32(rows + (size_t)tile * e4 + x, pub | (unsigned)(x < p.e ? s_agg[x] : 0));
   }
@@ -424,10 +429,10 @@ __device__ __forceinline__ void count_ranks(unsigned long long ranks, int lane, 
 // Fused gate: thread t's token selects its experts (topk_token_thread, the
 // gate kernel's ids and gate bits for e <= 32) and writes the ids and gates
 // to the caller's arrays.  Returns whether a logit was not finite.
-template <int KM>
+template <int KM, int EM>
 __device__ __forceinline__ bool gate_thread_token(const Params& p, int t, int* xs) {
   float g[KM];
-  const bool bad = topk_token_thread<KM>(p.logits + (size_t)t * p.e, p.e, p.k, p.renorm, xs, g);
+  const bool bad = topk_token_thread<KM, EM>(p.logits + (size_t)t * p.e, p.e, p.k, p.renorm, xs, g);
   store_route_ints<KM>(p.gate_idx + (size_t)t * p.k, xs, p.k);
   float* gd = p.gate_val + (size_t)t * p.k;
 #pragma unroll
@@ -439,11 +444,11 @@ __device__ __forceinline__ bool gate_thread_token(const Params& p, int t, int* x
 // One CTA per tile; TPT > 0: the tile is exactly TPT sub-tiles and each
 // thread keeps its TPT tokens' routes in registers from the histogram to the
 // slot pass; TPT == 0: any number of sub-tiles, routes reloaded per pass.
-// GATE: the fused gate (router logits in, e <= 32; TPT > 0 only, since the
-// routes stay in registers between the passes).
-template <int TPT, bool GATE, int KM>
+// GATE: 0, or the fused gate for e <= GATE experts (8 or 32; router logits
+// in; TPT > 0 only, since the routes stay in registers between the passes).
+template <int TPT, int GATE, int KM>
 __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
-  static_assert(!GATE || TPT > 0, "the fused gate keeps its routes in registers");
+  static_assert(GATE == 0 || TPT > 0, "the fused gate keeps its routes in registers");
   constexpr int NM = TPT > 0 ? TPT : 1;
   __shared__ unsigned s_mask[NM][kWarps][kMaxE];
   __shared__ int s_wbase[NM][kWarps][kMaxE];
@@ -470,13 +475,12 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
     s_excl[x] = 0;
   }
   if (tid < kMaxR) s_rank[tid] = 0;
-  if (tid == 0) {
-    s_flags = 0;
-    // this tile's own row, as the previous build (or the zeroing) left it
-    const unsigned own = ld_relaxed_u32(reinterpret_cast<const unsigned*>(p.out.lookback) +
-                                        (size_t)tile * padded_e(p.e));
-    s_pub = (own & kPublished) ? 0u : kPublished;
-  }
+  // this tile's own row, as the previous build (or the zeroing) left it:
+  // loaded now, used at the publication (its latency hides behind phase A)
+  const unsigned own = tid == 0 ? ld_relaxed_u32(reinterpret_cast<const unsigned*>(p.out.lookback) +
+                                                 (size_t)tile * padded_e(p.e))
+                                : 0u;
+  if (tid == 0) s_flags = 0;
   // a rebuild: tile 0 clears what the kernel accumulates into (published
   // with its look-back row, which every other tile reads before its atomics)
   if (p.clear_status && tile == 0) {
@@ -495,8 +499,8 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
       const int t = (sub0 + r) * kThreads + tid;
       valid[r] = 0;
       if (sub0 + r < sub1 && t < p.s) {
-        if (GATE) {
-          if (gate_thread_token<KM>(p, t, xs[r])) atomicOr(&s_flags, 4);
+        if (GATE > 0) {
+          if (gate_thread_token<KM, (GATE > 0 ? GATE : 8)>(p, t, xs[r])) atomicOr(&s_flags, 4);
           valid[r] = (1u << p.k) - 1u;  // k distinct ids in [0, e)
         } else {
           unsigned none;
@@ -544,6 +548,7 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
     }
   }
   if (bad) atomicOr(&s_flags, 1);
+  if (tid == 0) s_pub = (own & kPublished) ? 0u : kPublished;
   __syncthreads();
   for (int x = tid; x < p.e; x += kThreads) s_tot[x] = s_agg[x];
   __syncthreads();
@@ -612,7 +617,11 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   if (over) atomicOr(&s_flags, 8);
   __syncthreads();
   pdl_trigger_late();
-  if (p.R > 0 && tid < p.R && s_rank[tid]) atomicAdd(&p.out.rank_counts[tid], s_rank[tid]);
+  // acquire: tile 0's row, read in the look-back, before this tile's atomics
+  // on what tile 0 cleared (tile 0's own atomics follow its own clears)
+  const bool rank_add = p.R > 0 && tid < p.R && s_rank[tid];
+  if (tile != 0 && (rank_add || (tid == 0 && s_flags))) __threadfence();
+  if (rank_add) atomicAdd(&p.out.rank_counts[tid], s_rank[tid]);
   if (tid == 0 && s_flags) {
     int bits = 0;
     if (s_flags & 1) bits |= MOE_DEV_BAD_ROUTE;
@@ -689,7 +698,7 @@ size_t lookback_bytes(const LayoutPlan& plan, int e) {
 
 // The kernel variant of a sub-tile count (0 = any), a fused gate or not and
 // the routes per unit rounded up to 1, 2, 4, 8 or 16.
-template <int TPT, bool GATE>
+template <int TPT, int GATE>
 const void* layout_variant(int k) {
   if (k <= 1) return (const void*)layout_kernel<TPT, GATE, 1>;
   if (k <= 2) return (const void*)layout_kernel<TPT, GATE, 2>;
@@ -712,7 +721,7 @@ int min_blocks(std::initializer_list<const void*> kerns) {
 int layout_blocks_per_sm() {
   int n = 1 << 30;
   for (int k : {1, 2, 4, 8, 16}) {
-    const int b = min_blocks({layout_variant<0, false>(k), layout_variant<1, false>(k), layout_variant<2, false>(k)});
+    const int b = min_blocks({layout_variant<0, 0>(k), layout_variant<1, 0>(k), layout_variant<2, 0>(k)});
     if (b < n) n = b;
   }
   return n;
@@ -722,7 +731,8 @@ int layout_blocks_per_sm() {
 int gate_layout_blocks_per_sm() {
   int n = 1 << 30;
   for (int k : {1, 2, 4, 8, 16}) {
-    const int b = min_blocks({layout_variant<1, true>(k), layout_variant<2, true>(k)});
+    const int b = min_blocks({layout_variant<1, 8>(k), layout_variant<2, 8>(k), layout_variant<1, 32>(k),
+                              layout_variant<2, 32>(k)});
     if (b < n) n = b;
   }
   return n;
@@ -784,10 +794,11 @@ cudaError_t launch_layout(const int32_t* topk_idx, int s, int e, int k, int capa
   cfg.numAttrs = (MOE_PDL != 0 && ((MOE_PDL_MASK >> MOE_KERNEL_LAYOUT) & 1) && g_coop_pdl.load()) ? 2 : 1;
   cudaError_t err;
   const int tpt = plan.subtiles_per_tile;
-  const void* kern = p.logits ? (tpt == 1 ? layout_variant<1, true>(p.k) : layout_variant<2, true>(p.k))
-                   : tpt == 1   ? layout_variant<1, false>(p.k)
-                   : tpt == 2   ? layout_variant<2, false>(p.k)
-                                : layout_variant<0, false>(p.k);
+  const void* kern = p.logits && e <= 8 ? (tpt == 1 ? layout_variant<1, 8>(p.k) : layout_variant<2, 8>(p.k))
+                   : p.logits           ? (tpt == 1 ? layout_variant<1, 32>(p.k) : layout_variant<2, 32>(p.k))
+                   : tpt == 1           ? layout_variant<1, 0>(p.k)
+                   : tpt == 2           ? layout_variant<2, 0>(p.k)
+                                        : layout_variant<0, 0>(p.k);
   void* args[] = {&p};
   err = cudaLaunchKernelExC(&cfg, kern, args);
   if (err != cudaSuccess && cfg.numAttrs == 2) {

@@ -463,9 +463,9 @@ const char* moe_last_error(void);
 uint64_t moe_launch_count(int kernel_id);
 
 /* Test hook for the bounded waits: the next layout build whose tile count
- * exceeds `tile` leaves that tile's look-back words unpublished, so every
- * later tile's wait runs out (after timeout_ms) and sets MOE_DEV_TIMEOUT in
- * the handle's status word.  The hook disarms itself after one build;
+ * exceeds `tile` leaves that tile's look-back words unpublished for twice
+ * timeout_ms, so every tile that waits on it gives up (after timeout_ms) and
+ * sets MOE_DEV_TIMEOUT in the handle's status word.  The hook disarms itself after one build;
  * tile = -1 disarms it.  Never used on the product path. */
 moe_status moe_debug_hold_layout_tile(int tile, int timeout_ms);
 
