@@ -216,6 +216,18 @@ __device__ void lookback(const Params& p, int tile, int nread, const int* s_agg,
     for (int x = tid; x < e4; x += kThreads)
       st_relaxed_u32(rows + (size_t)tile * e4 + x, pub | (unsigned)(x < p.e ? s_agg[x] : 0));
 
+  // a held tile (test hook) publishes one more time-out after its own
+  // deadline -- well after every waiting tile has given up, whatever the
+  // skew of the tiles' start times -- so that every build still rewrites
+  // every row
+  if (tile == p.hold_tile) {
+    const uint64_t release_at = deadline + (uint64_t)p.timeout_ns;
+    while (globaltimer_ns() <= release_at) __nanosleep(1000);
+    for (int x = tid; x < e4; x += kThreads)
+      st_relaxed_u32(rows + (size_t)tile * e4 + x, pub | (unsigned)(x < p.e ? s_agg[x] : 0));
+  }
+  // nothing to read: this tile's totals are its own, no earlier routes
+  if (nread <= (tile < nread ? 1 : 0)) return;
   const int quads = e4 / 4;
   const int groups = kThreads / quads;  // threads (g, q) read tiles g, g + groups, ...
   const int g = tid / quads, q = tid - (tid / quads) * quads;
@@ -249,16 +261,6 @@ __device__ void lookback(const Params& p, int tile, int nread, const int* s_agg,
         }
       }
     }
-  }
-  // a held tile (test hook) publishes one more time-out after its own
-  // deadline -- well after every waiting tile has given up, whatever the
-  // skew of the tiles' start times -- so that every build still rewrites
-  // every row
-  if (tile == p.hold_tile) {
-    const uint64_t release_at = deadline + (uint64_t)p.timeout_ns;
-    while (globaltimer_ns() <= release_at) __nanosleep(1000);
-    for (int x = tid; x < e4; x += kThreads)
-      st_relaxed_u32(rows + (size_t)tile * e4 + x, pub | (unsigned)(x < p.e ? s_agg[x] : 0));
   }
   // sum the lanes of the warp that read the same column (xor shuffles, when
   // the column count is a power of two), then shared atomics per column
@@ -297,7 +299,7 @@ __device__ void expert_offsets(const Params& p, const int* s_tot, int* s_off, bo
     const int x = lane * 8 + i;
     raw[i] = x < p.e ? s_tot[x] : 0;
     v[i] = p.capacity > 0 ? min(raw[i], p.capacity) : raw[i];
-    sum += (v[i] + p.pad - 1) / p.pad * p.pad;  // rows of the expert's segment
+    sum += p.pad > 1 ? (v[i] + p.pad - 1) / p.pad * p.pad : v[i];  // rows of the expert's segment
   }
   int incl = sum;
 #pragma unroll
@@ -321,7 +323,7 @@ __device__ void expert_offsets(const Params& p, const int* s_tot, int* s_off, bo
         p.out.offsets[x] = o;
       }
     }
-    run += (v[i] + p.pad - 1) / p.pad * p.pad;
+    run += p.pad > 1 ? (v[i] + p.pad - 1) / p.pad * p.pad : v[i];
   }
   if (lane == 31) {
     const int end = p.capacity > 0 ? p.e * p.capacity : run;
@@ -351,15 +353,18 @@ __device__ __forceinline__ void store_route_ints(int32_t* dst, const int* v, int
 
 // Write one token's routes: token-order slot, row, drop flag, and its
 // virtual-rank set; with inv_row, the token number at each kept row.
-// base[x] is the slot of this warp's first token routed
-// to x; mask[x] the warp's token mask for x.  Returns the token's rank set.
+// base[x] (+ excl[x] when given: the routes of earlier tiles) is the slot of
+// this warp's first token routed to x; mask[x] the warp's token mask for x.
+// Returns the token's rank set.
 template <int KM>
 __device__ __forceinline__ unsigned long long write_routes(const Params& p, int t, int lane,
                                                            const int* xs, unsigned valid,
-                                                           const int* base, const unsigned* mask,
-                                                           const int* s_off, bool* over) {
+                                                           const int* base, const int* excl,
+                                                           const unsigned* mask, const int* s_off, bool* over) {
   const unsigned below = (1u << lane) - 1u;
+  // experts per virtual rank, as a shift when a power of two
   const int per_rank = p.R > 0 ? p.e / p.R : 1;
+  const int rank_shift = (per_rank & (per_rank - 1)) == 0 ? __ffs(per_rank) - 1 : -1;
   unsigned long long ranks = 0;
   int loc[KM], row[KM];
   uint32_t dropw[(KM + 3) / 4];
@@ -371,7 +376,7 @@ __device__ __forceinline__ unsigned long long write_routes(const Params& p, int 
     row[j] = -1;
     if (j < p.k && ((valid >> j) & 1u)) {
       const int x = xs[j];
-      const int l = base[x] + __popc(mask[x] & below);
+      const int l = base[x] + (excl ? excl[x] : 0) + __popc(mask[x] & below);
       loc[j] = l;
       if (p.capacity > 0) {
         if (l < p.capacity) row[j] = x * p.capacity + l;
@@ -382,7 +387,7 @@ __device__ __forceinline__ unsigned long long write_routes(const Params& p, int 
           *over = true;
         }
       }
-      if (row[j] >= 0) ranks |= 1ull << (x / per_rank);
+      if (p.R > 0 && row[j] >= 0) ranks |= 1ull << (rank_shift >= 0 ? x >> rank_shift : x / per_rank);
     }
     if (row[j] < 0) dropw[j / 4] |= 1u << (8 * (j % 4));
   }
@@ -465,11 +470,16 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   const int nsub = (p.s + kThreads - 1) / kThreads;
   const int sub0 = tile * p.subtiles_per_tile;
   const int sub1 = min(nsub, sub0 + p.subtiles_per_tile);
-  const uint64_t deadline = globaltimer_ns() + (uint64_t)p.timeout_ns;
-
   grid_dependency_wait();
   pdl_trigger_early();
-  for (int i = tid; i < NM * kWarps * kMaxE; i += kThreads) (&s_mask[0][0][0])[i] = 0u;
+  // the waits are bounded from here (not from the launch: a programmatic
+  // launch may start this grid long before the previous kernel ends)
+  const uint64_t deadline = globaltimer_ns() + (uint64_t)p.timeout_ns;
+  if (p.e <= 32) {  // only the columns a route can touch
+    for (int i = tid; i < NM * kWarps * 32; i += kThreads) (&s_mask[0][0][0])[(i >> 5) * kMaxE + (i & 31)] = 0u;
+  } else {
+    for (int i = tid; i < NM * kWarps * kMaxE; i += kThreads) (&s_mask[0][0][0])[i] = 0u;
+  }
   for (int x = tid; x < kMaxE; x += kThreads) {
     s_agg[x] = 0;
     s_excl[x] = 0;
@@ -522,6 +532,7 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
           run += __popc(s_mask[r][w][x]);
         }
       s_agg[x] = run;
+      s_tot[x] = run;
     }
   } else {
     for (int sb = sub0; sb < sub1; ++sb) {
@@ -546,11 +557,10 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
       for (int i = tid; i < kWarps * kMaxE; i += kThreads) (&s_mask[0][0][0])[i] = 0u;
       __syncthreads();
     }
+    for (int x = tid; x < p.e; x += kThreads) s_tot[x] = s_agg[x];
   }
   if (bad) atomicOr(&s_flags, 1);
   if (tid == 0) s_pub = (own & kPublished) ? 0u : kPublished;
-  __syncthreads();
-  for (int x = tid; x < p.e; x += kThreads) s_tot[x] = s_agg[x];
   __syncthreads();
 
   // ---- B: look-back over every earlier tile (all tiles when totals are needed)
@@ -570,17 +580,11 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   if (TPT > 0) {
 #pragma unroll
     for (int r = 0; r < NM; ++r) {
-      for (int x = tid; x < p.e; x += kThreads)
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) s_wbase[r][w][x] += s_excl[x];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < NM; ++r) {
       const int t = (sub0 + r) * kThreads + tid;
       unsigned long long ranks = 0;
       if (sub0 + r < sub1 && t < p.s)
-        ranks = write_routes<KM>(p, t, lane, xs[r], valid[r], s_wbase[r][warp], s_mask[r][warp], s_off, &over);
+        ranks = write_routes<KM>(p, t, lane, xs[r], valid[r], s_wbase[r][warp], s_excl, s_mask[r][warp], s_off,
+                                 &over);
       if (p.R > 0) count_ranks(ranks, lane, s_rank);
     }
   } else {
@@ -607,7 +611,8 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
       }
       __syncthreads();
       unsigned long long ranks = 0;
-      if (t < p.s) ranks = write_routes<KM>(p, t, lane, ys, vy, s_wbase[0][warp], s_mask[0][warp], s_off, &over);
+      if (t < p.s)
+        ranks = write_routes<KM>(p, t, lane, ys, vy, s_wbase[0][warp], nullptr, s_mask[0][warp], s_off, &over);
       if (p.R > 0) count_ranks(ranks, lane, s_rank);
       __syncthreads();
       for (int i = tid; i < kWarps * kMaxE; i += kThreads) (&s_mask[0][0][0])[i] = 0u;
