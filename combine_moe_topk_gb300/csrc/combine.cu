@@ -258,6 +258,7 @@ __device__ __forceinline__ void combine_bwd_body(
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gi = warp / G, w = warp - gi * G;  // token slot in the block, warp in the group
   const int c0 = w * chunk, c1 = min(nvec, c0 + chunk);
+  __shared__ SegmentStage seg;
   grid_dependency_wait();
   pdl_trigger_early();
   // every warp of a block runs the same number of rounds (block-uniform loop)
@@ -348,11 +349,13 @@ __device__ __forceinline__ void combine_bwd_body(
 
   // rows no kept route owns (capacity slots, padding) get zero gradient
   if (zero_fill) {
+    stage_segments(seg, offsets, counts, e);  // one round trip, not a chain per row
+    __syncthreads();
     const long long warps = (gridDim.x * blockDim.x) >> 5;
     const long long gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (long long rr = gw; rr < rows; rr += warps) {
-      if (row_is_owned(rr, offsets, counts, e)) continue;
+      if (row_is_owned(rr, seg.offsets, seg.counts, e)) continue;
       uint4* dst = dY + (size_t)rr * nvec;
       for (int v = lane; v < nvec; v += 32) st_stream(dst + v, z);
     }
@@ -399,6 +402,7 @@ __device__ __forceinline__ void combine_bwd_compact_body(
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  __shared__ SegmentStage seg;
   grid_dependency_wait();
   pdl_trigger_early();
   for (int t = gw; t < s; t += warps) {
@@ -493,9 +497,11 @@ __device__ __forceinline__ void combine_bwd_compact_body(
 
   // rows no kept route owns (capacity slots, padding) get zero gradient
   if (zero_fill) {
+    stage_segments(seg, offsets, counts, e);  // one round trip, not a chain per row
+    __syncthreads();
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (long long rr = gw; rr < rows; rr += warps) {
-      if (row_is_owned(rr, offsets, counts, e)) continue;
+      if (row_is_owned(rr, seg.offsets, seg.counts, e)) continue;
       uint4* dst = dY + (size_t)rr * nvec;
       for (int v = lane; v < nvec; v += 32) st_stream(dst + v, z);
     }

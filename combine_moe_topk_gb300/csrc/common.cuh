@@ -69,6 +69,23 @@ __device__ __forceinline__ bool row_is_owned(long long r, const P* offsets, cons
   return r - (long long)offsets[lo] < (long long)counts[lo];
 }
 
+// The per-expert segments (e + 1 offsets, e counts; e <= 256) staged in
+// shared memory for a zero tail: one load per thread, all in flight at once,
+// so the tail's ownership tests read shared memory instead of each running a
+// chain of dependent global loads; read only after a block barrier.
+struct SegmentStage {
+  int offsets[257];
+  int counts[256];
+};
+
+__device__ __forceinline__ void stage_segments(SegmentStage& st, const int32_t* offsets, const int32_t* counts,
+                                               int e) {
+  for (int x = threadIdx.x; x <= e; x += blockDim.x) {
+    st.offsets[x] = __ldg(offsets + x);
+    if (x < e) st.counts[x] = __ldg(counts + x);
+  }
+}
+
 // ------------------------------------------------------ 16-byte vectors ----
 
 template <typename T>

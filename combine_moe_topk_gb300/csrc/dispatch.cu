@@ -17,7 +17,7 @@
 // The routes are read by lanes 0..k-1 and broadcast by shuffle; a token
 // with no kept route reads nothing.  Rows no route owns (capacity slots
 // past the counts, per-expert padding) are zeroed afterwards, a warp per
-// row.  Nothing waits on anything but the previous kernel (the programmatic
+// row, against the segments the block stages in shared memory first.  Nothing waits on anything but the previous kernel (the programmatic
 // launch dependency), so the kernel has no time-out path.
 //
 // An earlier form moved the rows with 1-D bulk (TMA) copies through a
@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
   const long long warps = ((long long)gridDim.x * blockDim.x) >> 5;
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long units = (long long)s * nchunks;
+  __shared__ SegmentStage seg;
   grid_dependency_wait();
   pdl_trigger_early();
   bool bad = false;
@@ -92,9 +93,11 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
   pdl_trigger_late();
   if (bad) raise_status(status, MOE_DEV_BAD_ROUTE);
   if (zero_fill) {
+    stage_segments(seg, offsets, counts, e);  // one round trip, not a chain per row
+    __syncthreads();
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (long long rr = gw; rr < rows; rr += warps) {
-      if (row_is_owned(rr, offsets, counts, e)) continue;
+      if (row_is_owned(rr, seg.offsets, seg.counts, e)) continue;
       uint4* dst = X + (size_t)rr * nvec;
       for (int v = lane; v < nvec; v += 32) st_stream(dst + v, z);
     }
