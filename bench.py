@@ -596,7 +596,7 @@ def run_expert_gemm(w, S, dev, reps: int = 10):
     or of ``value``): synthetic expert weights W [e, N, m], N = m, bf16.
     Times dispatch, the grouped GEMM on the dispatched rows, and the fused
     dispatch + GEMM that gathers the token rows itself (CUDA events, one
-    call each, median of ``reps``)."""
+    call each, the three in turn, median of ``reps``; the SM clocks seen)."""
     import torch
 
     from combine_moe_topk_gb300 import binding as B
@@ -611,22 +611,24 @@ def run_expert_gemm(w, S, dev, reps: int = 10):
     Y = torch.empty(h.rows, N, dtype=torch.bfloat16, device=dev)
     kept = int(h.counts().sum().item())
 
-    def timed(fn):
+    # the three calls take turns within each repetition, so that the GPU's
+    # warming (and its power cap) over the block weighs on each alike
+    calls = [lambda: B.moe_dispatch(h, S["x"], X), lambda: B.moe_grouped_gemm(h, X, Wt, Y),
+             lambda: B.moe_dispatch_grouped_gemm(h, S["x"], Wt, Y)]
+    for fn in calls:
         for _ in range(2):
             fn()
-        ts = []
+    ts = [[], [], []]
+    with ClockSampler(dev.index) as clk:
         for _ in range(reps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
-
-    t_d = timed(lambda: B.moe_dispatch(h, S["x"], X))
-    t_g = timed(lambda: B.moe_grouped_gemm(h, X, Wt, Y))
-    t_f = timed(lambda: B.moe_dispatch_grouped_gemm(h, S["x"], Wt, Y))
+            for i, fn in enumerate(calls):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                torch.cuda.synchronize()
+                ts[i].append(a.elapsed_time(b))
+    t_d, t_g, t_f = (statistics.median(t) for t in ts)
     assert h.status() == 0
     h.destroy()
     flops = 2.0 * kept * w.m * N
@@ -654,9 +656,11 @@ def run_expert_gemm(w, S, dev, reps: int = 10):
                      "frac_gemm": round(tf(t_g) / peak, 4), "frac_fused": round(tf(t_f) / peak, 4),
                      "frac_of_bound_gemm": round(t_bound_ms / t_g, 4),
                      "frac_of_bound_fused": round(t_bound_ms / t_f, 4)},
-        "note": "synthetic N(0,1)/sqrt(m) expert weights; events around single calls, median of "
-                f"{reps}; not included in value; the bound is the longer of the FLOPs at the bf16 peak and "
-                "min_bytes (rows in, each expert's weights once, outputs) at the copy bandwidth",
+        "clocks": clk.summary(),
+        "note": "synthetic N(0,1)/sqrt(m) expert weights; events around single calls, the three calls "
+                f"in turn, median of {reps}; not included in value; the bound is the longer of the FLOPs at "
+                "the bf16 peak and min_bytes (rows in, each expert's weights once, outputs) at the copy "
+                "bandwidth",
     }
 
 
