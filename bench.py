@@ -64,6 +64,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024  # GB300 L2 (a flush writes twice this)
 SLEEP_CYCLES = 100_000  # ~50 us at 2 GHz: longer than the host's enqueue of one call
+EP_SLEEP_CYCLES = 1_000_000  # ~0.5 ms: an expert-parallel phase enqueues several calls and allocations
 
 
 # ------------------------------------------------------------ byte model --
@@ -700,7 +701,7 @@ def run_expert_parallel(w, dev, reps: int = 3):
         for _ in range(reps):
             a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             if pad is not None:
-                pad(SLEEP_CYCLES)  # the host enqueues the phase while the GPU sleeps
+                pad(EP_SLEEP_CYCLES)  # the host enqueues the phase while the GPU sleeps
             a.record()
             out = fn()
             c.record()

@@ -17,7 +17,8 @@
 // The routes are read by lanes 0..k-1 and broadcast by shuffle; a token
 // with no kept route reads nothing.  Rows no route owns (capacity slots
 // past the counts, per-expert padding) are zeroed afterwards, a warp per
-// row, against the segments the block stages in shared memory first.  Nothing waits on anything but the previous kernel (the programmatic
+// row, against the segments the block stages in shared memory first.
+// Nothing waits on anything but the previous kernel (the programmatic
 // launch dependency), so the kernel has no time-out path.
 //
 // An earlier form moved the rows with 1-D bulk (TMA) copies through a
