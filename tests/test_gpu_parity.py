@@ -121,6 +121,8 @@ def test_tiny_capacity_full_softmax_gates():
     dict(s=37, m=8, e=256, k=16, dtype="bf16", capacity=0, R=64),
     dict(s=300, m=12288, e=16, k=3, dtype="bf16", capacity=0, R=4),   # a short batch: rows split into 8 pieces
     dict(s=513, m=36, e=5, k=2, dtype="f32", capacity=7, R=5),        # heavy drops, odd widths
+    dict(s=700, m=16, e=12, k=3, dtype="f32", capacity=0, R=4),       # 3 experts per rank (not a power of 2)
+    dict(s=1500, m=32, e=96, k=6, dtype="bf16", capacity=150, R=8),   # 12 experts per rank, drops
     dict(s=2049, m=64, e=64, k=6, dtype="bf16", capacity=200, R=8),
 ])
 def test_edge_shapes(case):

@@ -136,11 +136,14 @@ def test_gate_layout_where_the_layout_cannot_select(case):
 
 @pytest.mark.parametrize("case", [
     dict(s=1000, e=32, k=16), dict(s=777, e=7, k=3), dict(s=300, e=1, k=1), dict(s=513, e=30, k=5),
+    # the 8-expert form's edges (k = e; 16-byte rows of 4) and the 32-expert form's smallest e
+    dict(s=600, e=8, k=8), dict(s=900, e=4, k=2), dict(s=450, e=9, k=2),
 ], ids=lambda c: f"e{c['e']}-k{c['k']}")
 @pytest.mark.parametrize("renorm", [1, 0])
 def test_fused_gate_edges_and_ties(case, renorm):
     """The fused gate's thread-per-token selection at the edges of its range
-    (e = 32 with k = 16, odd e without 16-byte rows, e = 1), with logits on a
+    (e = 32 with k = 16, odd e without 16-byte rows, e = 1; the 8-expert
+    form at k = e and e = 4, the 32-expert form at e = 9), with logits on a
     small grid so that ties are everywhere: the gate kernel's bits."""
     s, e, k = case["s"], case["e"], case["k"]
     g = torch.Generator().manual_seed(e * 100 + k)
