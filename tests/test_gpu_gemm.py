@@ -127,6 +127,49 @@ def test_grouped_gemm_matches_float64_matmul_and_fused_is_identical(case):
     _check_unowned_untouched(Y, L)
 
 
+SEGMENT_COUNTS = [0, 1, 127, 128, 129, 255, 256, 257, 383, 384, 385, 511, 640]
+
+
+@pytest.mark.parametrize("weights", ["identity", "random"])
+def test_segments_around_the_block_edges(weights):
+    """Expert segments of every size class at the 128- and 256-row block
+    edges of the pair kernel's 256-row blocks (each CTA's 128-row half):
+    empty, full blocks only (256), a last block whose second half holds
+    1..127 rows (129, 255, 257 .. 511) or none (1, 127, 128, 384, 640);
+    plain and fused, every owned row against the oracle, the rest untouched."""
+    e = len(SEGMENT_COUNTS)
+    ids = np.repeat(np.arange(e), SEGMENT_COUNTS)
+    rng = np.random.default_rng(17)
+    rng.shuffle(ids)  # token order across experts
+    s, K = len(ids), 128
+    idx = torch.from_numpy(ids.astype(np.int32)).view(s, 1)
+    h = B.moe_dispatch_layout(idx.to(DEV), e)
+    L = oracle.layout(idx.numpy(), e)
+    np.testing.assert_array_equal(np.asarray(L["counts"]), SEGMENT_COUNTS)
+    g = torch.Generator().manual_seed(19)
+    x = torch.randn(s, K, generator=g).to(torch.bfloat16)
+    X = B.moe_dispatch(h, x.to(DEV))
+    OX = oracle.dispatch(L["row"], bits(x), L["rows"])
+    if weights == "identity":
+        N = K
+        Wt = torch.eye(K, dtype=torch.bfloat16).expand(e, K, K).contiguous()
+    else:
+        N = 264  # a partial second column tile
+        Wt = (torch.randn(e, N, K, generator=g) / np.sqrt(K)).to(torch.bfloat16)
+    Wd = Wt.to(DEV)
+    Y = B.moe_grouped_gemm(h, X, Wd, _sentinel_out(h.rows, N))
+    Yf = B.moe_dispatch_grouped_gemm(h, x.to(DEV), Wd, _sentinel_out(h.rows, N))
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    if weights == "identity":
+        r = _owned_rows(L)
+        np.testing.assert_array_equal(bits(Y)[r], OX[r])
+    else:
+        _check_float64(Y, OX, Wt, L)
+    np.testing.assert_array_equal(bits(Yf), bits(Y))
+    _check_unowned_untouched(Y, L)
+
+
 def test_inv_row_names_the_token_of_every_owned_row():
     s, e, k = 5000, 32, 4
     for kw in (dict(capacity=500), dict(capacity=0), dict(capacity=600, priority="kmajor")):
