@@ -646,7 +646,7 @@ moe_status moe_ep_dispatch(moe_handle h, const int32_t* send_row, int rows_sent,
   MOE_TRY(check_device_ptr(X_send, "X_send", h->device));
   const moe::DeviceInfo* di = nullptr;
   MOE_TRY(device_state(h->device, &di));
-  cudaError_t err = moe::launch_dispatch(send_row, nullptr, nullptr, h->s, h->R, 1, 0, rows_sent, 0, x, X_send, rb,
+  cudaError_t err = moe::launch_dispatch(send_row, nullptr, nullptr, h->s, h->R, 1, rows_sent, 0, x, X_send, rb,
                                          h->out.status, *di, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "ep_dispatch launch");
   g_launches[MOE_KERNEL_EP_DISPATCH]++;
@@ -762,8 +762,8 @@ moe_status moe_dispatch(moe_handle h, int s, int rows, int m, moe_dtype dtype, c
   if (rows == 0) return MOE_OK;
   const moe::DeviceInfo* di = nullptr;
   MOE_TRY(device_state(h->device, &di));
-  cudaError_t err = moe::launch_dispatch(h->out.row, h->out.counts, h->out.offsets, s, h->k, h->e,
-                                         h->capacity, h->rows, h->zero_fill, x, X, rb, h->out.status, *di,
+  cudaError_t err = moe::launch_dispatch(h->out.row, h->out.counts, h->out.offsets, s, h->k, h->e, h->rows,
+                                         h->zero_fill, x, X, rb, h->out.status, *di,
                                          static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "dispatch launch");
   g_launches[MOE_KERNEL_DISPATCH]++;

@@ -145,10 +145,9 @@ cudaError_t launch(const int32_t* row, const int32_t* counts, const int32_t* off
 }  // namespace
 
 cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, const int32_t* offsets, int s,
-                            int k, int e, int capacity, long long rows, int zero_fill, const void* x,
+                            int k, int e, long long rows, int zero_fill, const void* x,
                             void* X, long long row_bytes, int32_t* status, const DeviceInfo& di,
                             cudaStream_t st) {
-  (void)capacity;
   if (k <= 2) return launch<2>(row, counts, offsets, s, k, e, rows, zero_fill, x, X, row_bytes, status, di, st);
   if (k <= 4) return launch<4>(row, counts, offsets, s, k, e, rows, zero_fill, x, X, row_bytes, status, di, st);
   if (k <= 8) return launch<8>(row, counts, offsets, s, k, e, rows, zero_fill, x, X, row_bytes, status, di, st);

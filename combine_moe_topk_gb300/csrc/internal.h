@@ -102,11 +102,11 @@ int noalloc_lookback_words();
 cudaError_t launch_layout_noalloc(const int32_t* topk_idx, int s, int e, int k, int capacity, int R,
                                   const LayoutOut& out, int* words_needed, cudaStream_t st);
 
-// --- dispatch (bulk-copy gather) -----------------------------------------
+// --- dispatch (register-staged gather) -----------------------------------
 // zero_fill: X has rows no route owns (capacity slots past the count,
 // per-expert padding); they are written with zeros.
 cudaError_t launch_dispatch(const int32_t* row, const int32_t* counts, const int32_t* offsets, int s,
-                            int k, int e, int capacity, long long rows, int zero_fill, const void* x,
+                            int k, int e, long long rows, int zero_fill, const void* x,
                             void* X, long long row_bytes, int32_t* status, const DeviceInfo& di,
                             cudaStream_t st);
 
