@@ -48,7 +48,15 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int kTmemCols = 2 * BN;     // two fp32 accumulators of 128 lanes x 256 columns
 constexpr int kThreads = 256;        // tile-fed form
-constexpr int kGatherThreads = 384;  // fused form: + 4 warps gathering the A rows
+// Warps gathering the fused form's A rows: 8 (16 rows each) measured 1-4 %
+// faster than 4 and 3 % faster than 16 (fewer registers per thread at 768
+// threads); 2 were 20-30 % slower.
+#ifndef MOE_GEMM_GATHER_WARPS
+#define MOE_GEMM_GATHER_WARPS 8
+#endif
+constexpr int kGatherThreads = kThreads + 32 * MOE_GEMM_GATHER_WARPS;  // fused form: + warps gathering A
+constexpr int kGatherRows = BM / MOE_GEMM_GATHER_WARPS;  // A rows per gathering warp
+static_assert(kGatherRows % 4 == 0 && kGatherRows >= 4, "a gathering warp copies 4 rows per instruction");
 constexpr int kMaxE = 256;
 // epilogue staging: per epilogue warp 32 rows x 64 bf16 columns, rows padded
 // to 144 bytes (conflict-free 16-byte writes by row and reads by column)
@@ -199,7 +207,7 @@ __device__ __forceinline__ Unit decode_unit(int u, int ntn, const int* s_blk, co
 //   both ranks, warp 2: one collective TMEM allocation for the pair;
 //   both ranks, warps 4..7: epilogue of its own rows, then an arrival on
 //     rank 0's tempty barrier (remote for rank 1);
-//   fused form, both ranks, warps 8..11: gather the CTA's 128 A rows, each
+//   fused form, both ranks, warps 8..15: gather the CTA's 128 A rows, each
 //     thread's copies arriving through cp.async.mbarrier.arrive.noinc;
 //   fused form, rank 1, warp 1 lane 0: forwards each gathered stage to
 //     rank 0's full barrier.
@@ -426,7 +434,7 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
     if (!ok) atomicOr(&s_err, 1);
   } else if (kGather && warp >= kThreads / 32) {
     // ---- A gather (fused form, both ranks): this CTA's 128 rows ------------
-    // Each lane copies 16 bytes of 8 rows per K block (8 lanes per 128-byte
+    // Each lane copies 16 bytes of kGatherRows / 4 rows per K block (8 lanes per 128-byte
     // row, the swizzle as in the one-SM form), then hands its copies of the
     // stage to the stage's barrier (cp.async.mbarrier.arrive.noinc: one
     // arrival once they land) and runs on to the next free stage; waiting
@@ -439,15 +447,15 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    // token of each of this lane's 8 rows in unit u; -1 for rows no route owns
+    // token of each of this lane's kGatherRows / 4 rows in unit u; -1 for rows no route owns
     auto unit_tokens = [&](int u, int* tok) {
       const Unit t = decode_unit(u, ntn, s_blk, s_off, s_cnt, p.e);
       const int i = u / ntn - s_blk[t.x];
       const int r0 = s_off[t.x] + BM2 * i + BM * (int)rank;
       const int left = s_cnt[t.x] - BM2 * i - BM * (int)rank;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int rr = 32 * gw + 4 * j + (lane >> 3);
+      for (int j = 0; j < kGatherRows / 4; ++j) {
+        const int rr = kGatherRows * gw + 4 * j + (lane >> 3);
         tok[j] = -1;
         if (rr < left) {
           const int v = __ldg(p.inv_row + r0 + rr);
@@ -455,15 +463,15 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
         }
       }
     };
-    int tok[8], ntok[8];
+    int tok[kGatherRows / 4], ntok[kGatherRows / 4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) ntok[j] = -1;  // after the last unit: nothing
+    for (int j = 0; j < kGatherRows / 4; ++j) ntok[j] = -1;  // after the last unit: nothing
     if (pair < nunits) unit_tokens(pair, tok);
     for (int u = pair; u < nunits && ok; u += npairs) {
       if (u + npairs < nunits) unit_tokens(u + npairs, ntok);  // in flight while this unit is gathered
-      const __nv_bfloat16* src[8];
+      const __nv_bfloat16* src[kGatherRows / 4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) src[j] = p.x + (size_t)(tok[j] < 0 ? 0 : tok[j]) * p.K + chunk * 8;
+      for (int j = 0; j < kGatherRows / 4; ++j) src[j] = p.x + (size_t)(tok[j] < 0 ? 0 : tok[j]) * p.K + chunk * 8;
       for (int kb = 0; kb < kblocks; ++kb) {
         bool waited = true;
         if (lane == 0) waited = mbar_wait_bounded(&empty[stage], phase ^ 1u, deadline);
@@ -476,9 +484,9 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
         for (int q = 0; q < kPairKB; ++q) {
           const int kx = (kb * kPairKB + q) * BK;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < kGatherRows / 4; ++j) {
             // rows no route owns are not copied (their results are never stored)
-            const int rr = 32 * gw + 4 * j + (lane >> 3);
+            const int rr = kGatherRows * gw + 4 * j + (lane >> 3);
             if (tok[j] >= 0) {
               // columns past K: zeros, nothing read (the row's end may be the buffer's)
               const bool in_k = kx + chunk * 8 < p.K;
@@ -494,7 +502,7 @@ __global__ void __launch_bounds__(kGather ? kGatherThreads : kThreads, 1)
         }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) tok[j] = ntok[j];
+      for (int j = 0; j < kGatherRows / 4; ++j) tok[j] = ntok[j];
     }
     cp_async_wait_all();  // nothing of this thread's stays in flight
     if (!ok && lane == 0) atomicOr(&s_err, 1);

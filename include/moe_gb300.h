@@ -425,10 +425,11 @@ moe_status moe_grouped_gemm(moe_handle h, int rows, int K, int N, const void* X,
  * [rows, N]; rows no route owns are not written.  Each owned row equals
  * moe_grouped_gemm's bit for bit (same operands, same MMA sequence).  Same
  * limits and errors as moe_grouped_gemm; s must equal the handle's.
- * Each token row is gathered once per 256-column tile of N, from L2 while
- * x fits there: on the measured shapes the fused call beat moe_dispatch
- * followed by moe_grouped_gemm by 7-24 %, except with x larger than the
- * L2 (16384 tokens of 4096) and N = 4096, where it was 6 % slower. */
+ * Each token row is gathered once per 256-column tile of N, mostly from L2
+ * (the column tiles of a row block run on different SM pairs at the same
+ * time): on every measured shape the fused call beat moe_dispatch followed
+ * by moe_grouped_gemm, by 3 % (16384 tokens of 4096, N = 4096) to 26 %
+ * (the GShard-like capacity layout). */
 moe_status moe_dispatch_grouped_gemm(moe_handle h, int s, int rows, int K, int N, const void* x,
                                      const void* W, void* Y, void* stream);
 
