@@ -261,6 +261,7 @@ __device__ __forceinline__ void combine_bwd_body(
   __shared__ SegmentStage seg;
   grid_dependency_wait();
   pdl_trigger_early();
+  if (zero_fill) stage_segments_async(seg, offsets, counts, e);  // read by the zero tail
   // every warp of a block runs the same number of rounds (block-uniform loop)
   for (long long t0 = (long long)blockIdx.x * TPB; t0 < s; t0 += (long long)gridDim.x * TPB) {
     const int t = (int)(t0 + gi);
@@ -349,8 +350,7 @@ __device__ __forceinline__ void combine_bwd_body(
 
   // rows no kept route owns (capacity slots, padding) get zero gradient
   if (zero_fill) {
-    stage_segments(seg, offsets, counts, e);  // one round trip, not a chain per row
-    __syncthreads();
+    segments_wait();  // staged since the kernel began
     const long long warps = (gridDim.x * blockDim.x) >> 5;
     const long long gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -405,6 +405,7 @@ __device__ __forceinline__ void combine_bwd_compact_body(
   __shared__ SegmentStage seg;
   grid_dependency_wait();
   pdl_trigger_early();
+  if (zero_fill) stage_segments_async(seg, offsets, counts, e);  // read by the zero tail
   for (int t = gw; t < s; t += warps) {
     int rl = lane < k ? __ldg(row + (size_t)t * k + lane) : -1;
     if (rl >= rows) rl = -1;  // past the buffer: read nothing
@@ -497,8 +498,7 @@ __device__ __forceinline__ void combine_bwd_compact_body(
 
   // rows no kept route owns (capacity slots, padding) get zero gradient
   if (zero_fill) {
-    stage_segments(seg, offsets, counts, e);  // one round trip, not a chain per row
-    __syncthreads();
+    segments_wait();  // staged since the kernel began
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (long long rr = gw; rr < rows; rr += warps) {
       if (row_is_owned(rr, seg.offsets, seg.counts, e)) continue;

@@ -149,6 +149,25 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// stage_segments with asynchronous 4-byte copies: issued at a kernel's start
+// (after its programmatic-launch wait), so the loads travel while the kernel
+// does its main work; segments_wait() (every thread) before reading them.
+__device__ __forceinline__ void stage_segments_async(SegmentStage& st, const int32_t* offsets,
+                                                     const int32_t* counts, int e) {
+  for (int x = threadIdx.x; x <= e; x += blockDim.x) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(&st.offsets[x])), "l"(offsets + x)
+                 : "memory");
+    if (x < e)
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(&st.counts[x])), "l"(counts + x)
+                   : "memory");
+  }
+}
+
+__device__ __forceinline__ void segments_wait() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
                : "memory");

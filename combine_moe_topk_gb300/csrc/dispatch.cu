@@ -17,7 +17,7 @@
 // The routes are read by lanes 0..k-1 and broadcast by shuffle; a token
 // with no kept route reads nothing.  Rows no route owns (capacity slots
 // past the counts, per-expert padding) are zeroed afterwards, a warp per
-// row, against the segments the block stages in shared memory first.
+// row, against the segments the block stages in shared memory meanwhile.
 // Nothing waits on anything but the previous kernel (the programmatic
 // launch dependency), so the kernel has no time-out path.
 //
@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
   __shared__ SegmentStage seg;
   grid_dependency_wait();
   pdl_trigger_early();
+  if (zero_fill) stage_segments_async(seg, offsets, counts, e);  // read by the zero tail
   bool bad = false;
   for (long long u = gw; u < units; u += warps) {
     const int t = (int)(u / nchunks);
@@ -94,8 +95,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
   pdl_trigger_late();
   if (bad) raise_status(status, MOE_DEV_BAD_ROUTE);
   if (zero_fill) {
-    stage_segments(seg, offsets, counts, e);  // one round trip, not a chain per row
-    __syncthreads();
+    segments_wait();  // staged since the kernel began
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (long long rr = gw; rr < rows; rr += warps) {
       if (row_is_owned(rr, seg.offsets, seg.counts, e)) continue;
