@@ -18,7 +18,8 @@
 //   A. histogram: per-expert route count of the tile in shared memory
 //      (integer atomics: the total does not depend on their order);
 //   B. decoupled look-back over tiles: each tile publishes its aggregate
-//      (flag and value in one 64-bit word) as soon as its histogram is done,
+//      (per expert a 32-bit word: the count, and the published flag in its
+//      top bit) as soon as its histogram is done,
 //      then reads the aggregates of all its predecessors at once -- groups of
 //      threads per expert, eight independent loads in flight each -- instead
 //      of walking back one tile at a time, so the look-back costs a few L2
@@ -286,18 +287,21 @@ __device__ void lookback(const Params& p, int tile, int nread, const int* s_agg,
   }
 }
 
-// Per-expert exclusive scan of the counts (e <= 256: eight per lane of warp
-// 0, then a warp scan) into s_off[0..e]; the tile that holds the totals of
+// Per-expert exclusive scan of the counts (e <= 256: up to eight per lane of
+// warp 0, then a warp scan) into s_off[0..e]; the tile that holds the totals of
 // record also writes raw_counts, counts and offsets to the handle.
 __device__ void expert_offsets(const Params& p, const int* s_tot, int* s_off, bool write_out) {
   const int lane = threadIdx.x & 31;
   if ((threadIdx.x >> 5) != 0) return;
+  // lane l takes experts l*ipl .. l*ipl+ipl-1 (ipl = 1 for e <= 32, so a
+  // small router's scan is one item per lane, not eight on lane 0)
+  const int ipl = (p.e + 31) >> 5;
   int raw[8], v[8];
   int sum = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int x = lane * 8 + i;
-    raw[i] = x < p.e ? s_tot[x] : 0;
+    const int x = lane * ipl + i;
+    raw[i] = (i < ipl && x < p.e) ? s_tot[x] : 0;
     v[i] = p.capacity > 0 ? min(raw[i], p.capacity) : raw[i];
     sum += p.pad > 1 ? (v[i] + p.pad - 1) / p.pad * p.pad : v[i];  // rows of the expert's segment
   }
@@ -310,8 +314,8 @@ __device__ void expert_offsets(const Params& p, const int* s_tot, int* s_off, bo
   int run = incl - sum;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int x = lane * 8 + i;
-    if (x < p.e) {
+    const int x = lane * ipl + i;
+    if (i < ipl && x < p.e) {
       const int off = p.capacity > 0 ? x * p.capacity : run;
       s_off[x] = off;
       if (write_out) {
@@ -569,7 +573,8 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   bool timed_out = false;
   lookback(p, tile, nread, s_agg, s_excl, s_tot, s_pub, deadline, &timed_out);
   if (timed_out) atomicOr(&s_flags, 2);
-  __syncthreads();
+  // the look-back's shared atomics (none when it read no other tile)
+  if (nread > (tile < nread ? 1 : 0)) __syncthreads();
   if (p.capacity == 0 || last) {
     expert_offsets(p, s_tot, s_off, last);
     __syncthreads();
