@@ -132,6 +132,12 @@ __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
   return v;
 }
 
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void st_relaxed_u32(unsigned* p, unsigned v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -209,9 +215,11 @@ __device__ void lookback(const Params& p, int tile, int nread, const int* s_agg,
   const int tid = threadIdx.x, lane = tid & 31;
   const int e4 = padded_e(p.e);
   unsigned* rows = reinterpret_cast<unsigned*>(p.out.lookback);
-  // release: tile 0's cleared status word and rank counts before its
-  // published row (no other tile publishes anything another tile reads, and
-  // a lone tile's clears and atomics are the same thread's, same address)
+  // release: each of tile 0's threads fences its own clears (rank_counts[tid],
+  // the status word for tid 0) before storing word tid of the row, which the
+  // other tiles acquire before their atomics on the same index (no other
+  // tile publishes anything another tile reads, and a lone tile's clears and
+  // atomics are the same thread's, same address)
   if (tile == 0 && p.clear_status && p.tiles > 1) __threadfence();
   if (tile != p.hold_tile)
     for (int x = tid; x < e4; x += kThreads)
@@ -627,10 +635,14 @@ __global__ void __launch_bounds__(kThreads) layout_kernel(const Params p) {
   if (over) atomicOr(&s_flags, 8);
   __syncthreads();
   pdl_trigger_late();
-  // acquire: tile 0's row, read in the look-back, before this tile's atomics
-  // on what tile 0 cleared (tile 0's own atomics follow its own clears)
+  // acquire, before an atomic on what tile 0 cleared in this build: word tid
+  // of tile 0's published row, which tile 0's thread tid stored after
+  // clearing rank_counts[tid] (and, for tid 0, the status word) and a fence.
+  // The look-back already saw it published, so this load returns at once;
+  // tile 0's own atomics follow its own clears.
   const bool rank_add = p.R > 0 && tid < p.R && s_rank[tid];
-  if (tile != 0 && (rank_add || (tid == 0 && s_flags))) __threadfence();
+  if (tile != 0 && p.clear_status && (rank_add || (tid == 0 && s_flags)))
+    (void)ld_acquire_u32(reinterpret_cast<const unsigned*>(p.out.lookback) + tid);
   if (rank_add) atomicAdd(&p.out.rank_counts[tid], s_rank[tid]);
   if (tid == 0 && s_flags) {
     int bits = 0;
