@@ -602,12 +602,23 @@ cudaError_t combine_t(const int32_t* row, const float* gate, int s, int k, long 
                     static_cast<const uint4*>(y), static_cast<uint4*>(out));
 }
 
+// y loads in flight per lane in the combine backward: half the budget with
+// at most two routes or one warp per token, the full budget where several
+// warps split a row of up to 8 routes (measured: the Mixtral-like backward
+// 59.4 -> 56.2 us and the fine-grained one 368.8 -> 366.4 us with half, the
+// stacked-replay one 51.4 -> 52.5 us).
+template <int KMAX, int G>
+constexpr int cbwd_unr() {
+  constexpr int loads = (KMAX <= 2 || G == 1) ? MOE_CMB_BWD_LOADS / 2 : MOE_CMB_BWD_LOADS;
+  return loads / KMAX > 1 ? loads / KMAX : 1;
+}
+
 template <typename T, int KMAX, int G, bool RG>
 cudaError_t combine_bwd_g(const int32_t* row, const int32_t* counts, const int32_t* offsets,
                           long long rows, int zero_fill, const float* gate, int s, int k, int e,
                           int nvec, const void* dout, const void* y, void* dY, float* dgate,
                           const RouterGrad& rg, const DeviceInfo& di, int bps, cudaStream_t st) {
-  constexpr int UNR = MOE_CMB_BWD_LOADS / KMAX > 1 ? MOE_CMB_BWD_LOADS / KMAX : 1;
+  constexpr int UNR = cbwd_unr<KMAX, G>();
   auto kern = cbwd_kernel<T, KMAX, UNR, G, RG>();
   const int chunk = G == 1 ? nvec : ((nvec + G - 1) / G + 31) / 32 * 32;
   long long warps = (long long)s * G;
@@ -624,7 +635,7 @@ cudaError_t combine_bwd_t(const int32_t* row, const int32_t* counts, const int32
                           long long rows, int zero_fill, const float* gate, int s, int k, int e,
                           int m, const void* dout, const void* y, void* dY, float* dgate, int sparse,
                           const RouterGrad& rg, const DeviceInfo& di, cudaStream_t st) {
-  constexpr int UNR = MOE_CMB_BWD_LOADS / KMAX > 1 ? MOE_CMB_BWD_LOADS / KMAX : 1;
+  constexpr int UNR = cbwd_unr<KMAX, 1>();
   const int nvec = m / Vec<T>::N;
   // the split below is chosen on the plain kernel's occupancy, so the fused
   // form splits the same way and computes the same dgate bits
