@@ -424,7 +424,14 @@ __device__ __forceinline__ unsigned long long write_routes(const Params& p, int 
   }
   if (p.R > 0) {
     uint8_t* tir = p.out.token_in_rank + (size_t)t * p.R;
-    for (int r = 0; r < p.R; ++r) tir[r] = (uint8_t)((ranks >> r) & 1ull);
+    if ((p.R & 3) == 0) {  // four ranks' bytes per 4-byte store (t * R is a multiple of 4)
+      for (int r = 0; r < p.R; r += 4) {
+        const uint32_t b = (uint32_t)(ranks >> r) & 0xfu;
+        *reinterpret_cast<uint32_t*>(tir + r) = (b & 1u) | ((b & 2u) << 7) | ((b & 4u) << 14) | ((b & 8u) << 21);
+      }
+    } else {
+      for (int r = 0; r < p.R; ++r) tir[r] = (uint8_t)((ranks >> r) & 1ull);
+    }
   }
   return ranks;
 }
